@@ -1,0 +1,389 @@
+"""KDA benchmark: prefill head-tokens/s (H*T per second) and decode GB/s at
+D=128, each against the GB300 roofline.
+
+A step is one chunked prefill of the mid-size workload (B=1, H=32,
+T=8192, D=128, bf16 q/k/v/beta, fp32 g and state, chunk 64) with its inputs
+resident in HBM (they total ~400 MB, larger than the 129 MB L2, so no L2
+flush is needed between steps). The decode workload (B=256 sequences x 96
+heads, 64 single-token steps on a 1.6 GB fp32 state, replayed from a CUDA
+graph) is measured alongside and reported under "decode".
+
+Prints ONE JSON line (rank 0). With --impl reference it times the fp64 CPU
+oracle instead, on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+D = 128
+C = 64
+PREFILL = dict(H=32, T=8192, seed=1001)
+DECODE = dict(B=256, H=96, steps=64, seed=1002)
+WORKLOAD = "prefill_mid_bf16: B=1, H=32, T=8192, D=128, chunk=64, bf16 q/k/v/beta, fp32 g/state"
+METRIC = "KDA prefill Mtok/s (H*T per s) at D=128"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def prefill_bytes_per_head_token(io_bytes=2):
+    """Minimal fused HBM traffic per head-token: q, k, v, out in the I/O type,
+    g in fp32, beta in the I/O type."""
+    return 4 * D * io_bytes + 4 * D + io_bytes
+
+
+def prefill_flops_per_chunk(c=C, d=D):
+    """12 C^3 + 8 C^2 D + 6 C D^2 per chunk and head ("Kimi K3: The Manos, The
+    Mythos, The Legendos", section 复杂度分析)."""
+    return 12 * c ** 3 + 8 * c * c * d + 6 * c * d * d
+
+
+def decode_bytes_per_head_token(d=D):
+    """~8 D^2 bytes per head and token: fp32 state read + write (same section)."""
+    return 8 * d * d
+
+
+def decode_flops_per_head_token(d=D):
+    return 7 * d * d
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            with open(p) as f:
+                d = json.load(f)
+            out = {}
+            for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+                for k2, v in d.items():
+                    if k2 == key or k2.startswith(key):
+                        if isinstance(v, (int, float)):
+                            out[key] = float(v)
+                            break
+            if "hbm_gbs" in out:
+                return out, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index=0):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or self.path is None:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, world, rank):
+    """The oracle as it stands on the host cores, on bounded samples."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from kimi_delta_attention_rule_gb300 import inputs
+    oracle.build()
+    heads, toks = PREFILL["H"], 1024
+    x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"])
+    f = lambda t: t[:toks].float().numpy()
+    q, k, v, g, b = f(x.q), f(x.k), f(x.v), f(x.g), x.beta[:toks].float().numpy()
+    cores = oracle.default_threads()
+    for _ in range(args.warmup):
+        oracle.prefill(q, k, v, g, b, x.scale)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill(q, k, v, g, b, x.scale)
+        times.append(time.perf_counter() - t0)
+    units = heads * toks
+    sec = sum(times) / len(times)
+    val = units / sec / 1e6
+    sample = "first %d tokens x %d heads of the workload per step (fp64 oracle)" % (toks, heads)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "Mtok/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": val, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "Mtok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def cpu_baseline(budget_s=12.0):
+    """Time the oracle as it stands on a bounded sample of the prefill
+    workload (all 32 heads, a prefix of the tokens)."""
+    import oracle
+    from kimi_delta_attention_rule_gb300 import inputs
+    oracle.build()
+    x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"])
+    cores = oracle.default_threads()
+    toks = 256
+    while True:
+        f = lambda t: t[:toks].float().numpy()
+        t0 = time.perf_counter()
+        oracle.prefill(f(x.q), f(x.k), f(x.v), f(x.g), x.beta[:toks].float().numpy(), x.scale)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or toks >= PREFILL["T"]:
+            break
+        toks = min(PREFILL["T"], toks * 4)
+    units = toks * PREFILL["H"]
+    return {"value": units / dt / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+            "sample": "first %d tokens x %d heads of the prefill workload, %.1f s" % (
+                toks, PREFILL["H"], dt)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import kimi_delta_attention_rule_gb300 as kda
+    from kimi_delta_attention_rule_gb300 import build as kbuild, inputs
+
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0 or world == 1:
+        kbuild.build()
+    if world > 1:
+        dist.barrier()
+    kda.load()
+    stream = torch.cuda.current_stream()
+
+    # ---- prefill workload (each rank: its own independent batch) -----------
+    x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16",
+                              seed=PREFILL["seed"] + 7919 * rank, device=dev)
+    H, T = PREFILL["H"], PREFILL["T"]
+    out = torch.empty_like(x.q)
+    fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
+    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, cu_seqlens=None, chunk=C, out=out,
+                        final_state=fin, workspace=ws, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    assert kda.kda_workspace_status(ws) == kda.KDA_OK
+    units = H * T * world
+    value = units / (ms * 1e-3) / 1e6
+    clocks = clk.summary()
+
+    peaks, peak_src = load_peaks()
+    bpt = prefill_bytes_per_head_token()
+    bytes_per_launch = bpt * H * T + fin.numel() * 4
+    achieved_gbs = bytes_per_launch / (ms * 1e-3) / 1e9
+    flops = prefill_flops_per_chunk() * H * (T // C)
+    tflops = flops / (ms * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers ---------------
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, hg, hb = pin(x.q), pin(x.k), pin(x.v), pin(x.g), pin(x.beta)
+    hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv, dg, db = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb)):
+            d_.copy_(h_, non_blocking=True)
+        kda.kda_prefill(dq, dk, dv, dg, db, x.scale, chunk=C, out=out, final_state=fin,
+                        workspace=ws, stream=stream)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_steps = max(3, min(args.steps, 20))
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_val = units / (e2e_ms * 1e-3) / 1e6
+    del dq, dk, dv, dg, db, hq, hk, hv, hg, hb, hout
+
+    # ---- decode: 64 steps replayed from a CUDA graph -----------------------
+    decode = None
+    if not args.no_decode:
+        B, Hd, S = DECODE["B"], DECODE["H"], DECODE["steps"]
+        dqq, dkk, dvv, dgg, dbb, state, dscale = inputs.decode_inputs(
+            B=B, H=Hd, steps=S, seed=DECODE["seed"] + 7919 * rank, device=dev)
+        dout = torch.empty((S, B, Hd, D), dtype=torch.bfloat16, device=dev)
+        g_stream = torch.cuda.Stream()
+        g_stream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(g_stream):
+            kda.kda_decode_step(dqq[0], dkk[0], dvv[0], dgg[0], dbb[0], dscale, state,
+                                out=dout[0], stream=g_stream)  # warm-up launch
+            g_stream.synchronize()
+            with torch.cuda.graph(graph, stream=g_stream):
+                for s in range(S):
+                    kda.kda_decode_step(dqq[s], dkk[s], dvv[s], dgg[s], dbb[s], dscale, state,
+                                        out=dout[s], stream=g_stream)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        reps = 5
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(g_stream)
+        with torch.cuda.stream(g_stream):
+            for _ in range(reps):
+                graph.replay()
+        e1.record(g_stream)
+        torch.cuda.synchronize()
+        dms = e0.elapsed_time(e1) / (reps * S)
+        state_bytes = decode_bytes_per_head_token() * B * Hd
+        gbs = state_bytes / (dms * 1e-3) / 1e9
+        decode = {
+            "workload": "decode_b256_h96: B=256, H=96, D=128, 64 steps per graph, fp32 state "
+                        "1.61 GB, bf16 q/k/v/beta",
+            "value": gbs, "unit": "GB/s", "ms_per_step": dms,
+            "tokens_per_s": B * Hd / (dms * 1e-3),
+            "gflops": decode_flops_per_head_token() * B * Hd / (dms * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": peak_src,
+                         "algorithmic_bytes_per_launch": state_bytes},
+            "gpu_launches": reps * S,
+        }
+        del graph, dqq, dkk, dvv, dgg, dbb, state, dout
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline()
+    line = {
+        "metric": METRIC, "value": value, "unit": "Mtok/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta sigmoid(N), "
+                "g -5*sigmoid(N))",
+        "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T, "heads": H,
+                   "parallelism": "dp%d" % world,
+                   "l2": "inputs (%.0f MB) larger than L2; no flush" % (
+                       (bpt - 2 * D) * H * T / 1e6)},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peak_src, "kernel": "prefill_bf16_kernel",
+                     "algorithmic_bytes_per_launch": bytes_per_launch},
+        "tensor": {"tflops_pages_count": tflops, "peak": peaks["bf16_tflops"],
+                   "frac": tflops / peaks["bf16_tflops"],
+                   "flops_per_launch": flops},
+        "e2e": {"value": e2e_val, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "decode": decode,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,169 @@
+"""KDA (Kimi Delta Attention) operator for NVIDIA GB300, behind a C ABI.
+
+The compute runs in ``libkda.so`` (hand-written CUDA for sm_103a, declared
+in ``include/kda.h``). This package is a thin ctypes binding with the same
+entry-point names; PyTorch only supplies device memory and streams. There is
+no CPU fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK = 0
+KDA_ERR_INVALID_ARG = 1
+KDA_ERR_UNSUPPORTED = 2
+KDA_ERR_CUDA = 3
+KDA_ERR_TIMEOUT = 4
+KDA_ERR_DEVICE = 5
+KDA_BF16 = 0
+KDA_F32 = 1
+
+EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size", "kda_prefill",
+            "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KDAError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__("%s failed: %s (%d)" % (what, status_string(code), code))
+
+
+def load() -> ctypes.CDLL:
+    """Load libkda.so (built by ``build.build()``); raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libkda.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+        lib = ctypes.CDLL(LIB_PATH)
+        P, I32, F32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_abi_version.argtypes = []
+        lib.kda_abi_version.restype = ctypes.c_int
+        lib.kda_prefill_workspace_size.argtypes = [I32] * 6
+        lib.kda_prefill_workspace_size.restype = SZ
+        lib.kda_prefill.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32, P, P,
+                                    P, SZ, P]
+        lib.kda_prefill.restype = ctypes.c_int
+        lib.kda_decode_step.argtypes = [P, P, P, P, P, F32, I32, I32, I32, I32, P, P, P]
+        lib.kda_decode_step.restype = ctypes.c_int
+        lib.kda_workspace_status.argtypes = [P, P]
+        lib.kda_workspace_status.restype = ctypes.c_int
+        lib.kda_check_cu_seqlens.argtypes = [P, I32, I32]
+        lib.kda_check_cu_seqlens.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return load().kda_status_string(int(code)).decode()
+
+
+def kda_status_string(code: int) -> str:
+    return status_string(code)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _io_code(dt: torch.dtype) -> int:
+    if dt == torch.bfloat16:
+        return KDA_BF16
+    if dt == torch.float32:
+        return KDA_F32
+    raise KDAError(KDA_ERR_UNSUPPORTED, "dtype %s" % dt)
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("KDA tensors must be CUDA tensors")
+            if not t.is_contiguous():
+                raise ValueError("KDA tensors must be contiguous")
+
+
+def kda_prefill_workspace_size(N: int, T: int, H: int, D: int, chunk: int, io: int) -> int:
+    return int(load().kda_prefill_workspace_size(N, T, H, D, chunk, io))
+
+
+def kda_prefill(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk=64, out=None,
+                final_state=None, workspace=None, stream=None, N=None, T=None,
+                output_final_state=True):
+    """Chunked KDA prefill (C entry point ``kda_prefill``).
+
+    q, k, v: [T_total, H, D] (bf16 or fp32); g: fp32 [T_total, H, D];
+    beta: [T_total, H]; init_state: fp32 [N, H, D, D] or None;
+    cu_seqlens: device int32 [N+1] or None (then N sequences of length T,
+    default N=1). Returns (out, final_state)."""
+    lib = load()
+    io = _io_code(q.dtype)
+    T_total, H, D = q.shape
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+        T = T_total
+    else:
+        N = 1 if N is None else N
+        T = T_total // N if T is None else T
+    _check_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, workspace)
+    if out is None:
+        out = torch.empty_like(q) if io != KDA_F32 else torch.empty_like(q)
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    ws_bytes = kda_prefill_workspace_size(N, T, H, D, chunk, io)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+    rc = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                         _ptr(init_state), _ptr(cu_seqlens), N, T, H, D, chunk, io, _ptr(out),
+                         _ptr(final_state), _ptr(workspace), workspace.numel(),
+                         _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_prefill")
+    return out, final_state
+
+
+def kda_decode_step(q, k, v, g, beta, scale, state, out=None, stream=None):
+    """One decode step (C entry point ``kda_decode_step``): q, k, v, g
+    [B, H, D]; beta [B, H]; state fp32 [B, H, D, D] updated in place.
+    Returns out [B, H, D]."""
+    lib = load()
+    io = _io_code(q.dtype)
+    B, H, D = q.shape
+    _check_cuda(q, k, v, g, beta, state, out)
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), B, H,
+                             D, io, _ptr(state), _ptr(out), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_decode_step")
+    return out
+
+
+def kda_workspace_status(workspace, stream=None) -> int:
+    return int(load().kda_workspace_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def kda_check_cu_seqlens(cu_host, T_total: int) -> int:
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(cu_host, dtype=np.int32))
+    return int(load().kda_check_cu_seqlens(a.ctypes.data, a.shape[0] - 1, int(T_total)))

@@ -1,0 +1,151 @@
+// C ABI of libkda (declared in include/kda.h): argument validation and
+// kernel dispatch. No allocation, no host synchronisation except in
+// kda_workspace_status().
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+template <typename IO>
+cudaError_t launch_decode_step(const void *q, const void *k, const void *v, const float *g,
+                               const void *beta, float scale, int B, int H, float *state,
+                               void *out, cudaStream_t stream);
+cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *g,
+                               const float *beta, float scale, const float *init,
+                               const int32_t *cu, int N, int T, int T_total, int H, int chunk,
+                               float *out, float *fin, uint32_t *status, cudaStream_t stream);
+cudaError_t launch_prefill_bf16(const void *q, const void *k, const void *v, const float *g,
+                                const void *beta, float scale, const float *init,
+                                const int32_t *cu, int N, int T, int T_total, int H, void *out,
+                                float *fin, uint32_t *status, cudaStream_t stream);
+}  // namespace kda
+
+namespace {
+
+constexpr size_t kWorkspaceBytes = 256;  // device status word, padded to 256 B
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates the prefill sizes; writes T_total on success.
+int check_prefill_dims(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
+                       bool varlen, long long *T_total) {
+    if (N < 0 || T < 0 || H <= 0 || D <= 0) return KDA_ERR_INVALID_ARG;
+    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (D != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if (io == KDA_BF16 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    if (io == KDA_F32 && chunk != 16 && chunk != 64) return KDA_ERR_UNSUPPORTED;
+    const long long tt = varlen ? (long long)T : (long long)N * T;
+    // element offsets (t * H + h) * D must fit in 64 bits and grid sizes in 32 bits
+    if (tt > (1LL << 31) - 1 || tt * H > (1LL << 40)) return KDA_ERR_INVALID_ARG;
+    if ((long long)N * H * 4 > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    *T_total = tt;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *kda_status_string(int status) {
+    switch (status) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+int kda_abi_version(void) { return 100; }
+
+size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
+                                  int32_t io) {
+    long long tt = 0;
+    if (check_prefill_dims(N, T, H, D, chunk, io, false, &tt) != KDA_OK &&
+        check_prefill_dims(N, T, H, D, chunk, io, true, &tt) != KDA_OK)
+        return 0;
+    return kWorkspaceBytes;
+}
+
+int kda_check_cu_seqlens(const int32_t *cu, int32_t N, int32_t T_total) {
+    if (cu == nullptr || N < 0 || T_total < 0) return KDA_ERR_INVALID_ARG;
+    if (cu[0] != 0 || cu[N] != T_total) return KDA_ERR_INVALID_ARG;
+    for (int32_t n = 0; n < N; ++n)
+        if (cu[n + 1] < cu[n]) return KDA_ERR_INVALID_ARG;
+    return KDA_OK;
+}
+
+int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,
+                float scale, const float *init_state, const int32_t *cu_seqlens, int32_t N,
+                int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io, void *out,
+                float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+    long long T_total = 0;
+    const int rc = check_prefill_dims(N, T, H, D, chunk, io, cu_seqlens != nullptr, &T_total);
+    if (rc != KDA_OK) return rc;
+    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (N == 0) return KDA_OK;
+    if (T_total > 0) {
+        if (!q || !k || !v || !g || !beta || !out) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(g) || !aligned16(out))
+            return KDA_ERR_INVALID_ARG;
+    }
+    if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
+        return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t *status = static_cast<uint32_t *>(workspace);
+    // the status word reports this call only
+    cudaError_t e = cudaMemsetAsync(status, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (io == KDA_F32) {
+        e = kda::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
+                                    static_cast<const float *>(v), g,
+                                    static_cast<const float *>(beta), scale, init_state,
+                                    cu_seqlens, N, T, (int)T_total, H, chunk,
+                                    static_cast<float *>(out), final_state, status, st);
+    } else {
+        e = kda::launch_prefill_bf16(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T,
+                                     (int)T_total, H, out, final_state, status, st);
+    }
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
+                    const void *beta, float scale, int32_t B, int32_t H, int32_t D, int32_t io,
+                    float *state_inout, void *out, void *stream) {
+    if (B < 0 || H <= 0 || D <= 0) return KDA_ERR_INVALID_ARG;
+    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (D != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (B == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state_inout || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_inout)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = io == KDA_F32
+                        ? kda::launch_decode_step<float>(q, k, v, g, beta, scale, B, H,
+                                                         state_inout, out, st)
+                        : kda::launch_decode_step<__nv_bfloat16>(q, k, v, g, beta, scale, B, H,
+                                                                 state_inout, out, st);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_workspace_status(void *workspace, void *stream) {
+    if (workspace == nullptr) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), st) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
+    if (word & kda::kStatusTimeout) return KDA_ERR_TIMEOUT;
+    if (word & kda::kStatusBadSeqlens) return KDA_ERR_DEVICE;
+    return KDA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,106 @@
+"""Host-side checks of the C ABI: the library loads, exports every function
+that include/kda.h declares, and rejects bad arguments before any launch
+(no device memory is touched: every pointer here is NULL or a host array)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import kimi_delta_attention_rule_gb300 as kda
+from kimi_delta_attention_rule_gb300 import build as kbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    kbuild.build()
+    return kda.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = header_functions()
+    assert len(names) >= 7
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(kda.EXPORTED) <= set(names)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARG"), (2, "KDA_ERR_UNSUPPORTED"),
+                       (3, "KDA_ERR_CUDA"), (4, "KDA_ERR_TIMEOUT"), (5, "KDA_ERR_DEVICE")]:
+        assert kda.status_string(code) == name
+    assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
+    assert lib.kda_abi_version() == 100
+
+
+def test_workspace_size(lib):
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 256
+    assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_F32) >= 256
+    assert kda.kda_prefill_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16) == 0      # D != 128
+    assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_BF16) == 0     # chunk
+    assert kda.kda_prefill_workspace_size(-1, 64, 2, 128, 64, kda.KDA_BF16) == 0
+
+
+def _prefill(lib, **kw):
+    a = dict(q=None, k=None, v=None, g=None, beta=None, scale=1.0, init=None, cu=None, N=1, T=64,
+             H=2, D=128, chunk=64, io=0, out=None, fin=None, ws=None, ws_bytes=0, stream=None)
+    a.update(kw)
+    return lib.kda_prefill(a["q"], a["k"], a["v"], a["g"], a["beta"], a["scale"], a["init"],
+                           a["cu"], a["N"], a["T"], a["H"], a["D"], a["chunk"], a["io"], a["out"],
+                           a["fin"], a["ws"], a["ws_bytes"], a["stream"])
+
+
+def test_prefill_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: validation fails first
+    assert _prefill(lib, D=64) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, chunk=32) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, io=7) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(lib, N=-1) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, H=0) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib) == kda.KDA_ERR_INVALID_ARG                      # no workspace
+    assert _prefill(lib, ws=fake, ws_bytes=16) == kda.KDA_ERR_INVALID_ARG  # too small
+    assert _prefill(lib, ws=ctypes.c_void_p(0x100010), ws_bytes=256) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(lib, ws=fake, ws_bytes=256) == kda.KDA_ERR_INVALID_ARG  # null tensors
+    mis = ctypes.c_void_p(0x100002)
+    assert _prefill(lib, q=mis, k=fake, v=fake, g=fake, beta=fake, out=fake, ws=fake,
+                    ws_bytes=256) == kda.KDA_ERR_INVALID_ARG             # misaligned q
+    assert _prefill(lib, N=1, T=1 << 31 - 1, H=1 << 12, ws=fake, ws_bytes=256) \
+        == kda.KDA_ERR_INVALID_ARG                                       # size overflow
+    # N = 0 is a valid empty call: nothing is launched
+    assert _prefill(lib, N=0, ws=fake, ws_bytes=256) == kda.KDA_OK
+
+
+def test_decode_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)
+    f = lib.kda_decode_step
+    assert f(None, None, None, None, None, 1.0, 4, 2, 64, 0, None, None, None) == kda.KDA_ERR_UNSUPPORTED
+    assert f(None, None, None, None, None, 1.0, 4, 2, 128, 3, None, None, None) == kda.KDA_ERR_UNSUPPORTED
+    assert f(None, None, None, None, None, 1.0, -1, 2, 128, 0, None, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(None, None, None, None, None, 1.0, 4, 2, 128, 0, None, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(fake, fake, fake, fake, fake, 1.0, 4, 2, 128, 0, ctypes.c_void_p(0x100004), fake,
+             None) == kda.KDA_ERR_INVALID_ARG                            # misaligned state
+    assert f(None, None, None, None, None, 1.0, 0, 2, 128, 0, None, None, None) == kda.KDA_OK
+
+
+def test_host_cu_seqlens_check(lib):
+    assert kda.kda_check_cu_seqlens([0, 5, 5, 9], 9) == kda.KDA_OK
+    assert kda.kda_check_cu_seqlens([0, 5, 3, 9], 9) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_check_cu_seqlens([1, 5, 9], 9) == kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_check_cu_seqlens([0, 5, 8], 9) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_product_path_has_no_cpu_fallback():
+    """The binding never imports the oracle and raises without the library."""
+    import kimi_delta_attention_rule_gb300 as pkg
+    src = open(pkg.__file__).read()
+    assert "oracle" not in src.replace("no CPU fallback", "")
+    for f in os.listdir(os.path.join(ROOT, "kimi_delta_attention_rule_gb300", "csrc")):
+        assert "oracle" not in open(os.path.join(ROOT, "kimi_delta_attention_rule_gb300", "csrc", f)).read()

@@ -1,0 +1,292 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
+element by element on the same seeded inputs.
+
+Error metric (per compared tensor): max |gpu - oracle| / rms(oracle).
+Bars: 2e-2 for bf16 I/O, 1e-4 for fp32 I/O (outputs and final states);
+sequence indexing is exact (outputs outside a sequence are untouched).
+Full-size workloads are checked on sampled (sequence, head) chains that the
+oracle recomputes one by one from the same inputs.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import kimi_delta_attention_rule_gb300 as kda
+from kimi_delta_attention_rule_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+TOL_F32 = 1e-4
+DEV = "cuda:0"
+
+
+def rel_err(got, ref):
+    ref = np.asarray(ref, dtype=np.float64)
+    got = np.asarray(got, dtype=np.float64)
+    assert np.all(np.isfinite(got)), "non-finite GPU output"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    if rms == 0.0:
+        return float(np.max(np.abs(got)))
+    return float(np.max(np.abs(got - ref))) / rms
+
+
+def np32(t):
+    return t.detach().float().cpu().numpy()
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from kimi_delta_attention_rule_gb300 import build as kbuild
+    kbuild.build()
+    kda.load()
+
+
+def run_gpu_prefill(x, chunk, with_init=True):
+    cu = x.cu_seqlens.to(DEV) if x.cu_seqlens is not None else None
+    init = x.init_state.to(DEV) if (with_init and x.init_state is not None) else None
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
+                               x.beta.to(DEV), x.scale, init_state=init, cu_seqlens=cu,
+                               chunk=chunk, workspace=ws)
+    assert kda.kda_workspace_status(ws) == kda.KDA_OK
+    torch.cuda.synchronize()
+    return out, fin
+
+
+def oracle_prefill(x, with_init=True):
+    init = x.init_state.double().numpy() if (with_init and x.init_state is not None) else None
+    return oracle.prefill(np32(x.q), np32(x.k), np32(x.v), np32(x.g), np32(x.beta), x.scale,
+                          init_state=init, cu_seqlens=x.cu_seqlens.numpy())
+
+
+def check_prefill(x, chunk, tol, with_init=True):
+    out, fin = run_gpu_prefill(x, chunk, with_init)
+    ro, rf = oracle_prefill(x, with_init)
+    eo, ef = rel_err(np32(out), ro), rel_err(fin.cpu().numpy(), rf)
+    assert eo <= tol and ef <= tol, (eo, ef)
+    return eo, ef
+
+
+# ---------------------------------------------------------------- fp32 I/O
+def test_tiny_f32_chunk16():
+    """B=1, H=2, T=64, fp32 I/O, chunk 16, zero initial state."""
+    w = inputs.WORKLOADS["tiny_f32"]
+    x = inputs.prefill_inputs(w["lens"], H=w["H"], io="f32", seed=w["seed"])
+    check_prefill(x, 16, TOL_F32)
+
+
+@pytest.mark.parametrize("lens,chunk", [([1], 16), ([17, 64, 3], 16), ([200], 64),
+                                        ([0, 65, 130], 64)])
+def test_f32_ragged(lens, chunk):
+    x = inputs.prefill_inputs(lens, H=2, io="f32", seed=3, init="normal")
+    check_prefill(x, chunk, TOL_F32)
+
+
+# ---------------------------------------------------------------- bf16 I/O
+@pytest.mark.parametrize("lens", [[1], [63], [64], [65], [130], [1000], [64, 64], [5, 0, 129, 1]])
+def test_bf16_prefill_ragged(lens):
+    x = inputs.prefill_inputs(lens, H=3, io="bf16", seed=11, init="normal")
+    check_prefill(x, 64, TOL_BF16)
+
+
+def test_bf16_zero_initial_state():
+    x = inputs.prefill_inputs([300], H=2, io="bf16", seed=12, init="normal")
+    check_prefill(x, 64, TOL_BF16, with_init=False)
+
+
+def test_bf16_equal_length_batch_without_cu_seqlens():
+    x = inputs.prefill_inputs([192, 192, 192], H=2, io="bf16", seed=13, init="normal")
+    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
+                               x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV), N=3,
+                               T=192, chunk=64)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(x)
+    assert rel_err(np32(out), ro) <= TOL_BF16
+    assert rel_err(fin.cpu().numpy(), rf) <= TOL_BF16
+
+
+def test_bf16_decay_floor_and_special_cases():
+    """g at the floor (every channel -5 after clamping, incl. values below -5),
+    g = 0 (DeltaNet), beta = 0 (pure decay)."""
+    base = inputs.prefill_inputs([257], H=2, io="bf16", seed=14, init="normal")
+    for name in ("floor", "zero_g", "beta0", "positive_g"):
+        x = inputs.prefill_inputs([257], H=2, io="bf16", seed=14, init="normal")
+        if name == "floor":
+            x.g = torch.full_like(base.g, -7.0)
+        elif name == "zero_g":
+            x.g = torch.zeros_like(base.g)
+        elif name == "beta0":
+            x.beta = torch.zeros_like(base.beta)
+        else:
+            x.g = torch.full_like(base.g, 0.5)
+        out, fin = run_gpu_prefill(x, 64)
+        ro, rf = oracle_prefill(x)
+        eo, ef = rel_err(np32(out), ro), rel_err(fin.cpu().numpy(), rf)
+        assert eo <= TOL_BF16 and ef <= TOL_BF16, (name, eo, ef)
+
+
+def test_bf16_varlen_floor_mix():
+    x = inputs.prefill_inputs([700, 1, 64, 333], H=4, io="bf16", seed=15, g_mode="floor",
+                              init="normal")
+    check_prefill(x, 64, TOL_BF16)
+
+
+def test_varlen_rows_all_written():
+    """Every row of every packed sequence is written (sentinel-filled output)."""
+    x = inputs.prefill_inputs([100], H=2, io="bf16", seed=16)
+    cu = torch.tensor([0, 40, 90], dtype=torch.int32, device=DEV)
+    out = torch.full((90, 2, 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    kda.kda_prefill(x.q[:90].to(DEV), x.k[:90].to(DEV), x.v[:90].to(DEV), x.g[:90].to(DEV),
+                    x.beta[:90].to(DEV), x.scale, cu_seqlens=cu, chunk=64, out=out)
+    torch.cuda.synchronize()
+    assert not torch.any(out == 7.0)
+    ro, _ = oracle.prefill(np32(x.q[:90]), np32(x.k[:90]), np32(x.v[:90]), np32(x.g[:90]),
+                           np32(x.beta[:90]), x.scale, cu_seqlens=[0, 40, 90])
+    assert rel_err(np32(out), ro) <= TOL_BF16
+
+
+def test_bad_cu_seqlens_flagged_on_device():
+    x = inputs.prefill_inputs([64, 64], H=1, io="bf16", seed=17)
+    cu = torch.tensor([0, 100, 64], dtype=torch.int32, device=DEV)  # decreasing
+    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV), x.beta.to(DEV), x.scale,
+                    cu_seqlens=cu, chunk=64, workspace=ws)
+    assert kda.kda_workspace_status(ws) == kda.KDA_ERR_DEVICE
+    assert kda.kda_workspace_status(ws) == kda.KDA_OK  # read clears it
+
+
+# ---------------------------------------------------------------- decode
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+def test_decode_chain(io, tol):
+    steps = 12
+    q, k, v, g, beta, state, scale = inputs.decode_inputs(B=5, H=3, steps=steps, io=io, seed=21)
+    st = state.to(DEV).contiguous()
+    ref = state.double().numpy()
+    for s in range(steps):
+        o = kda.kda_decode_step(q[s].to(DEV), k[s].to(DEV), v[s].to(DEV), g[s].to(DEV),
+                                beta[s].to(DEV), scale, st)
+        ro, ref = oracle.decode_step(np32(q[s]), np32(k[s]), np32(v[s]), np32(g[s]),
+                                     np32(beta[s]), scale, ref)
+        assert rel_err(np32(o), ro) <= tol, s
+    assert rel_err(st.cpu().numpy(), ref) <= tol
+
+
+def test_decode_equals_prefill_path():
+    """T decode steps and one T-token prefill reach the same state (both
+    within tolerance of the oracle, and of each other)."""
+    B, H, T = 2, 2, 70
+    x = inputs.prefill_inputs([T] * B, H=H, io="bf16", seed=22, init="normal")
+    out_p, fin_p = run_gpu_prefill(x, 64)
+    st = x.init_state.to(DEV).clone()
+    outs = []
+    for t in range(T):
+        rows = [n * T + t for n in range(B)]
+        o = kda.kda_decode_step(x.q[rows].to(DEV), x.k[rows].to(DEV), x.v[rows].to(DEV),
+                                x.g[rows].to(DEV), x.beta[rows].to(DEV), x.scale, st)
+        outs.append(o)
+    torch.cuda.synchronize()
+    dec = torch.stack(outs, 1).reshape(B * T, H, 128)
+    assert rel_err(np32(dec), np32(out_p)) <= 2 * TOL_BF16
+    assert rel_err(st.cpu().numpy(), fin_p.cpu().numpy()) <= 2 * TOL_BF16
+
+
+# ------------------------------------------------- full-size workloads (sampled)
+def sampled_chain_check(x_dev, out, fin, lens, chains, init_cpu, tol):
+    """Recompute sampled (sequence, head) chains with the oracle from the
+    device inputs (copied back) and compare. Chains of one sequence run in one
+    oracle call (its threads take one head each); sequences run concurrently."""
+    from concurrent.futures import ThreadPoolExecutor
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    by_seq = {}
+    for n, h in chains:
+        by_seq.setdefault(n, []).append(h)
+
+    def one(item):
+        n, heads = item
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        sl = lambda t: np32(t[t0:t1][:, heads])
+        init = None if init_cpu is None else init_cpu[n:n + 1][:, heads].double().numpy()
+        ro, rf = oracle.prefill(sl(x_dev.q), sl(x_dev.k), sl(x_dev.v), sl(x_dev.g),
+                                sl(x_dev.beta), x_dev.scale, init_state=init)
+        eo = rel_err(np32(out[t0:t1][:, heads]), ro)
+        ef = rel_err(fin[n:n + 1][:, heads].cpu().numpy(), rf)
+        return (n, heads, eo, ef)
+
+    with ThreadPoolExecutor(max_workers=8) as ex:
+        res = list(ex.map(one, sorted(by_seq.items())))
+    for n, heads, eo, ef in res:
+        assert eo <= tol and ef <= tol, ((n, heads), eo, ef)
+    return max(max(r[2], r[3]) for r in res)
+
+
+@pytest.mark.slow
+def test_prefill_mid_full_size():
+    """H=32, T=8192, bf16, chunk 64: the benchmark's launch; 6 heads sampled."""
+    w = inputs.WORKLOADS["prefill_mid_bf16"]
+    x = inputs.prefill_inputs(w["lens"], H=w["H"], io="bf16", seed=w["seed"], device=DEV)
+    out, fin = kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, cu_seqlens=x.cu_seqlens,
+                               chunk=64)
+    torch.cuda.synchronize()
+    sampled_chain_check(x, out, fin, w["lens"], [(0, h) for h in (0, 5, 13, 22, 30, 31)], None,
+                        TOL_BF16)
+
+
+@pytest.mark.slow
+def test_decode_full_size_64_steps():
+    """B=256, H=96, 64 steps on the resident 1.6 GB state; 6 (b, h) sampled."""
+    w = inputs.WORKLOADS["decode_b256_h96"]
+    q, k, v, g, beta, state, scale = inputs.decode_inputs(B=w["B"], H=w["H"], steps=w["steps"],
+                                                          seed=w["seed"], device=DEV)
+    picks = [(0, 0), (17, 95), (100, 40), (255, 3), (128, 64), (200, 77)]
+    ref = {p: state[p[0], p[1]].double().cpu().numpy()[None, None] for p in picks}
+    st = state.clone()
+    for s in range(w["steps"]):
+        o = kda.kda_decode_step(q[s], k[s], v[s], g[s], beta[s], scale, st)
+        for (b, h) in picks:
+            ro, ref[(b, h)] = oracle.decode_step(
+                np32(q[s, b:b + 1, h:h + 1]), np32(k[s, b:b + 1, h:h + 1]),
+                np32(v[s, b:b + 1, h:h + 1]), np32(g[s, b:b + 1, h:h + 1]),
+                np32(beta[s, b:b + 1, h:h + 1]), scale, ref[(b, h)])
+            assert rel_err(np32(o[b:b + 1, h:h + 1]), ro) <= TOL_BF16, (s, b, h)
+    for (b, h) in picks:
+        assert rel_err(st[b, h].cpu().numpy(), ref[(b, h)][0, 0]) <= TOL_BF16
+
+
+@pytest.mark.slow
+def test_append_prefill_full_size():
+    """H=96: a 32768-token prefill, then 65536 appended tokens starting from
+    its fp32 final state (both on the GPU); 3 heads sampled, the oracle runs
+    the whole 98304-token stream for each."""
+    w = inputs.WORKLOADS["append_h96"]
+    P, T, H = w["prior"], w["T"], w["H"]
+    x = inputs.prefill_inputs([P + T], H=H, io="bf16", seed=w["seed"], device=DEV)
+    _, s_prior = kda.kda_prefill(x.q[:P], x.k[:P], x.v[:P], x.g[:P], x.beta[:P], x.scale,
+                                 chunk=64)
+    out, fin = kda.kda_prefill(x.q[P:], x.k[P:], x.v[P:], x.g[P:], x.beta[P:], x.scale,
+                               init_state=s_prior, chunk=64)
+    torch.cuda.synchronize()
+    heads = [0, 47, 95]
+    sl = lambda t: np32(t[:, heads])
+    ro, rf = oracle.prefill(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), x.scale)
+    eo = rel_err(np32(out[:, heads]), ro[P:])
+    ef = rel_err(fin[:, heads].cpu().numpy(), rf)
+    assert eo <= TOL_BF16 and ef <= TOL_BF16, (eo, ef)
+
+
+@pytest.mark.slow
+def test_varlen_full_size():
+    """64 sequences, lengths ~U[1024, 32768], H=32, g near the floor, random
+    initial states; 6 chains sampled (incl. the longest and shortest)."""
+    w = inputs.WORKLOADS["varlen64_h32_floor"]
+    lens = inputs.varlen_lengths(w["n_seqs"], w["lo"], w["hi"], seed=w["seed"])
+    x = inputs.prefill_inputs(lens, H=w["H"], io="bf16", seed=w["seed"], g_mode="floor",
+                              init="normal", device=DEV)
+    out, fin = kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, init_state=x.init_state,
+                               cu_seqlens=x.cu_seqlens, chunk=64)
+    torch.cuda.synchronize()
+    order = np.argsort(lens)
+    chains = [(int(order[-1]), 3), (int(order[0]), 31), (int(order[32]), 0), (7, 17), (40, 9),
+              (63, 20)]
+    sampled_chain_check(x, out, fin, lens, chains, x.init_state.cpu(), TOL_BF16)
