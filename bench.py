@@ -195,16 +195,43 @@ def cpu_baseline(budget_s=12.0):
                 toks, PREFILL["H"], dt)}
 
 
+def ncu_case(args):
+    """A single kernel launched warmup + 1 times: the target of ncu captures."""
+    import torch
+    import kimi_delta_attention_rule_gb300 as kda
+    from kimi_delta_attention_rule_gb300 import build as kbuild, inputs
+    kbuild.build()
+    kda.load()
+    dev = torch.device("cuda", 0)
+    if args.ncu_case == "prefill":
+        x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"],
+                                  device=dev)
+        for _ in range(args.warmup + 1):
+            kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, chunk=C)
+    else:
+        q, k, v, g, beta, state, scale = inputs.decode_inputs(
+            B=args.decode_batch, H=DECODE["H"], steps=1, seed=DECODE["seed"], device=dev)
+        for _ in range(args.warmup + 1):
+            kda.kda_decode_step(q[0], k[0], v[0], g[0], beta[0], scale, state)
+    torch.cuda.synchronize()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--ncu-case", choices=["prefill", "decode"], default=None,
+                    help="run only `warmup` + 1 launches of one kernel (for ncu captures)")
+    ap.add_argument("--decode-batch", type=int, default=DECODE["B"])
     args = ap.parse_args()
     world, rank, local = dist_setup()
+    if args.ncu_case:
+        ncu_case(args)
+        return
 
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -21,13 +21,21 @@
 //
 // Per chunk, with S0 the state at the chunk start (fp32, in registers):
 //   A = beta * strict_lower(Gram(k, k)),  M = lower(Gram(q, k))        [bf16 MMA]
+//   (the diagonal of M, which carries no decay, is recomputed in fp32)
 //   T = (I + A)^{-1}                 16x16 diagonal blocks by forward
 //                                    substitution, then blocks below by
 //                                    block products                     [fp32]
-//   W = T (beta k e^{a}),  U~ = T (beta v)                             [bf16 MMA]
+//   W = T (beta k e^{a}),  U~ = T (beta v)                             [fp16 MMA]
 //   U = U~ - W S0
 //   O = scale ((q e^{a}) S0 + M U)
-//   S = Diag(e^{a_C}) S0 + (k e^{a_C - a})^T U                          [bf16 MMA, fp32 acc]
+//   S = Diag(e^{a_C}) S0 + (k e^{a_C - a})^T U                          [fp16 MMA, fp32 acc]
+//
+// Precision: only the Gram operands need bf16's exponent range (factors up
+// to e^80). Every operand of the state path (T, W, U~, U, M, the state copy,
+// q e^{a}, k e^{a_C - a}, beta k e^{a}, beta v) is bounded in magnitude and
+// is carried in fp16, whose 11-bit significand keeps the outputs well inside
+// a 2e-2 max-error / RMS bar on long sequences (bf16 there does not). Values
+// of the state, of v and of U are assumed to stay below 6e4 in magnitude.
 //
 // Grid: one CTA (8 warps) per (sequence, head, 32-column value slab): the
 // value columns of S evolve independently, so slabs need no exchange.
@@ -84,21 +92,21 @@ __global__ void __launch_bounds__(kBfThreads, 1)
     if (!seq_bounds(cu, n, T, T_total, t0, t1, status)) return;
 
     extern __shared__ __align__(128) unsigned char smem[];
-    __nv_bfloat16 *sQt = reinterpret_cast<__nv_bfloat16 *>(smem + kOffQt);
-    __nv_bfloat16 *sKb = reinterpret_cast<__nv_bfloat16 *>(smem + kOffKb);
-    __nv_bfloat16 *sKtb = reinterpret_cast<__nv_bfloat16 *>(smem + kOffKtb);
+    __half *sQt = reinterpret_cast<__half *>(smem + kOffQt);
+    __half *sKb = reinterpret_cast<__half *>(smem + kOffKb);
+    __half *sKtb = reinterpret_cast<__half *>(smem + kOffKtb);
     __nv_bfloat16 *sXq = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXq);
     __nv_bfloat16 *sXk = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXk);
     __nv_bfloat16 *sKh = reinterpret_cast<__nv_bfloat16 *>(smem + kOffKh);
-    __nv_bfloat16 *sW = sXq;
-    __nv_bfloat16 *sTb = sXk;
+    __half *sW = reinterpret_cast<__half *>(smem + kOffXq);
+    __half *sTb = reinterpret_cast<__half *>(smem + kOffXk);
     float *sA = reinterpret_cast<float *>(smem + kOffA);
     float *sT = reinterpret_cast<float *>(smem + kOffT);
     float *sX = reinterpret_cast<float *>(smem + kOffX);
-    __nv_bfloat16 *sM = reinterpret_cast<__nv_bfloat16 *>(smem + kOffM);
-    __nv_bfloat16 *sVb = reinterpret_cast<__nv_bfloat16 *>(smem + kOffVb);
-    __nv_bfloat16 *sU = reinterpret_cast<__nv_bfloat16 *>(smem + kOffU);
-    __nv_bfloat16 *sS = reinterpret_cast<__nv_bfloat16 *>(smem + kOffS);
+    __half *sM = reinterpret_cast<__half *>(smem + kOffM);
+    __half *sVb = reinterpret_cast<__half *>(smem + kOffVb);
+    __half *sU = reinterpret_cast<__half *>(smem + kOffU);
+    __half *sS = reinterpret_cast<__half *>(smem + kOffS);
     float *sGam = reinterpret_cast<float *>(smem + kOffGam);
     float *sBeta = reinterpret_cast<float *>(smem + kOffBeta);
     float *sTile = reinterpret_cast<float *>(smem + kOffTile);
@@ -126,8 +134,8 @@ __global__ void __launch_bounds__(kBfThreads, 1)
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
         const int col = nt * 8 + cq;
-        *reinterpret_cast<uint32_t *>(&sS[r0 * kLDV + col]) = pack_bf16(Sf[nt][0], Sf[nt][1]);
-        *reinterpret_cast<uint32_t *>(&sS[(r0 + 8) * kLDV + col]) = pack_bf16(Sf[nt][2], Sf[nt][3]);
+        *reinterpret_cast<uint32_t *>(&sS[r0 * kLDV + col]) = pack_f16(Sf[nt][0], Sf[nt][1]);
+        *reinterpret_cast<uint32_t *>(&sS[(r0 + 8) * kLDV + col]) = pack_f16(Sf[nt][2], Sf[nt][3]);
     }
 
     const int ch = tid & (kD - 1);  // key channel handled in the preparation phase
@@ -185,9 +193,9 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                     const float bt = sBeta[t];
                     sXq[t * kLDK + ch] = __float2bfloat16_rn(qv * x);
                     sXk[t * kLDK + ch] = __float2bfloat16_rn(kv * x);
-                    sQt[t * kLDK + ch] = __float2bfloat16_rn(qv * (er * x));
-                    sKtb[t * kLDK + ch] = __float2bfloat16_rn(bt * kv * (er * x));
-                    sKb[t * kLDK + ch] = __float2bfloat16_rn(kv * (eC * ix));
+                    sQt[t * kLDK + ch] = __float2half_rn(qv * (er * x));
+                    sKtb[t * kLDK + ch] = __float2half_rn(bt * kv * (er * x));
+                    sKb[t * kLDK + ch] = __float2half_rn(kv * (eC * ix));
                     sKh[(kh_slot(i, i) * 16 + r) * kLDK + ch] = __float2bfloat16_rn(kv * ix);
 #pragma unroll
                     for (int i2 = 0; i2 < 4; ++i2)
@@ -207,7 +215,7 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                     v1 = __high2float(vv);
                 }
                 const float bt = sBeta[t];
-                *reinterpret_cast<uint32_t *>(&sVb[t * kLDV + j]) = pack_bf16(bt * v0, bt * v1);
+                *reinterpret_cast<uint32_t *>(&sVb[t * kLDV + j]) = pack_f16(bt * v0, bt * v1);
             }
         }
         __syncthreads();
@@ -236,7 +244,7 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                     const int t = 16 * i + (lane >> 2) + (e >= 2 ? 8 : 0);
                     const int s = 16 * j + nt * 8 + cq + (e & 1);
                     if (m == 0) sA[t * kLDA + s] = s < t ? sBeta[t] * acc[nt][e] : 0.f;
-                    else sM[t * kLDC + s] = __float2bfloat16_rn(s <= t ? acc[nt][e] : 0.f);
+                    else sM[t * kLDC + s] = __float2half_rn(s <= t ? acc[nt][e] : 0.f);
                 }
         }
         // zero the blocks above the diagonal of A and M
@@ -246,7 +254,7 @@ __global__ void __launch_bounds__(kBfThreads, 1)
             const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
             const int t = 16 * bi + (e >> 4), s = 16 * bj + (e & 15);
             sA[t * kLDA + s] = 0.f;
-            sM[t * kLDC + s] = __float2bfloat16_rn(0.f);
+            sM[t * kLDC + s] = __float2half_rn(0.f);
         }
         __syncthreads();
 
@@ -269,6 +277,20 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                 const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
                 const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
                 sT[(16 * bi + (e >> 4)) * kLDA + 16 * bj + (e & 15)] = 0.f;
+            }
+            // The diagonal of M carries no decay (e^0 = 1): take it in fp32
+            // from the stored q and k instead of from the rounded factors.
+            for (int t = warp - 2; t < L; t += kBfThreads / 32 - 2) {
+                const size_t off = ((size_t)(tc + t) * H + h) * kD + 4 * lane;
+                const uint2 qq = *reinterpret_cast<const uint2 *>(&q[off]);
+                const uint2 kk = *reinterpret_cast<const uint2 *>(&k[off]);
+                const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qq);
+                const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kk);
+                float d = __low2float(q2[0]) * __low2float(k2[0]) + __high2float(q2[0]) * __high2float(k2[0]) +
+                          __low2float(q2[1]) * __low2float(k2[1]) + __high2float(q2[1]) * __high2float(k2[1]);
+#pragma unroll
+                for (int off2 = 16; off2 > 0; off2 >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off2);
+                if (lane == 0) sM[t * kLDC + t] = __float2half_rn(d);
             }
         }
         __syncthreads();
@@ -298,7 +320,7 @@ __global__ void __launch_bounds__(kBfThreads, 1)
         for (int idx = tid; idx < kC * kC / 2; idx += kBfThreads) {
             const int t = idx / (kC / 2), s = 2 * (idx % (kC / 2));
             *reinterpret_cast<uint32_t *>(&sTb[t * kLDC + s]) =
-                pack_bf16(sT[t * kLDA + s], sT[t * kLDA + s + 1]);
+                pack_f16(sT[t * kLDA + s], sT[t * kLDA + s + 1]);
         }
         __syncthreads();
 
@@ -317,21 +339,21 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                 for (int np = 0; np < 4; ++np) {
                     uint32_t b[4];
                     frag_b_kn(b, aKtb, kLDK, 64 * nh + 16 * np, 16 * ks, lane);
-                    mma_bf16_16816(wacc[2 * np], a, b[0], b[1]);
-                    mma_bf16_16816(wacc[2 * np + 1], a, b[2], b[3]);
+                    mma_f16_16816(wacc[2 * np], a, b[0], b[1]);
+                    mma_f16_16816(wacc[2 * np + 1], a, b[2], b[3]);
                 }
                 uint32_t bv[4];
                 frag_b_kn(bv, aVb, kLDV, 16 * nh, 16 * ks, lane);
-                mma_bf16_16816(uacc[0], a, bv[0], bv[1]);
-                mma_bf16_16816(uacc[1], a, bv[2], bv[3]);
+                mma_f16_16816(uacc[0], a, bv[0], bv[1]);
+                mma_f16_16816(uacc[1], a, bv[2], bv[3]);
             }
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const int t = 16 * ti + (lane >> 2);
                 const int c = 64 * nh + nt * 8 + cq;
-                *reinterpret_cast<uint32_t *>(&sW[t * kLDK + c]) = pack_bf16(wacc[nt][0], wacc[nt][1]);
+                *reinterpret_cast<uint32_t *>(&sW[t * kLDK + c]) = pack_f16(wacc[nt][0], wacc[nt][1]);
                 *reinterpret_cast<uint32_t *>(&sW[(t + 8) * kLDK + c]) =
-                    pack_bf16(wacc[nt][2], wacc[nt][3]);
+                    pack_f16(wacc[nt][2], wacc[nt][3]);
             }
         }
         __syncthreads();
@@ -346,19 +368,19 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                 frag_b_kn(b, aS, kLDV, 16 * nh, 16 * ks, lane);
                 frag_a_rowmajor(aw, aW, kLDK, 16 * ti, 16 * ks, lane);
                 frag_a_rowmajor(aq, aQt, kLDK, 16 * ti, 16 * ks, lane);
-                mma_bf16_16816(wsacc[0], aw, b[0], b[1]);
-                mma_bf16_16816(wsacc[1], aw, b[2], b[3]);
-                mma_bf16_16816(oacc[0], aq, b[0], b[1]);
-                mma_bf16_16816(oacc[1], aq, b[2], b[3]);
+                mma_f16_16816(wsacc[0], aw, b[0], b[1]);
+                mma_f16_16816(wsacc[1], aw, b[2], b[3]);
+                mma_f16_16816(oacc[0], aq, b[0], b[1]);
+                mma_f16_16816(oacc[1], aq, b[2], b[3]);
             }
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int t = 16 * ti + (lane >> 2);
                 const int j = 16 * nh + nt * 8 + cq;
                 *reinterpret_cast<uint32_t *>(&sU[t * kLDV + j]) =
-                    pack_bf16(uacc[nt][0] - wsacc[nt][0], uacc[nt][1] - wsacc[nt][1]);
+                    pack_f16(uacc[nt][0] - wsacc[nt][0], uacc[nt][1] - wsacc[nt][1]);
                 *reinterpret_cast<uint32_t *>(&sU[(t + 8) * kLDV + j]) =
-                    pack_bf16(uacc[nt][2] - wsacc[nt][2], uacc[nt][3] - wsacc[nt][3]);
+                    pack_f16(uacc[nt][2] - wsacc[nt][2], uacc[nt][3] - wsacc[nt][3]);
             }
         }
         __syncthreads();
@@ -370,8 +392,8 @@ __global__ void __launch_bounds__(kBfThreads, 1)
             uint32_t a[4], b[4];
             frag_a_rowmajor(a, aM, kLDC, 16 * ti, 16 * ks, lane);
             frag_b_kn(b, aU, kLDV, 16 * nh, 16 * ks, lane);
-            mma_bf16_16816(oacc[0], a, b[0], b[1]);
-            mma_bf16_16816(oacc[1], a, b[2], b[3]);
+            mma_f16_16816(oacc[0], a, b[0], b[1]);
+            mma_f16_16816(oacc[1], a, b[2], b[3]);
         }
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -381,7 +403,7 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                 if (t < L) {
                     const int j = sb * kDV + 16 * nh + nt * 8 + cq;
                     *reinterpret_cast<uint32_t *>(&out[((size_t)(tc + t) * H + h) * kD + j]) =
-                        pack_bf16(scale * oacc[nt][2 * hh], scale * oacc[nt][2 * hh + 1]);
+                        pack_f16(scale * oacc[nt][2 * hh], scale * oacc[nt][2 * hh + 1]);
                 }
             }
 
@@ -401,16 +423,16 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                 for (int np = 0; np < 2; ++np) {
                     uint32_t b[4];
                     frag_b_kn(b, aU, kLDV, 16 * np, 16 * ks, lane);
-                    mma_bf16_16816(Sf[2 * np], a, b[0], b[1]);
-                    mma_bf16_16816(Sf[2 * np + 1], a, b[2], b[3]);
+                    mma_f16_16816(Sf[2 * np], a, b[0], b[1]);
+                    mma_f16_16816(Sf[2 * np + 1], a, b[2], b[3]);
                 }
             }
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int col = nt * 8 + cq;
-                *reinterpret_cast<uint32_t *>(&sS[r0 * kLDV + col]) = pack_bf16(Sf[nt][0], Sf[nt][1]);
+                *reinterpret_cast<uint32_t *>(&sS[r0 * kLDV + col]) = pack_f16(Sf[nt][0], Sf[nt][1]);
                 *reinterpret_cast<uint32_t *>(&sS[(r0 + 8) * kLDV + col]) =
-                    pack_bf16(Sf[nt][2], Sf[nt][3]);
+                    pack_f16(Sf[nt][2], Sf[nt][3]);
             }
         }
     }
