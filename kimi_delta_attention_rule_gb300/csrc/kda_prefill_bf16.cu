@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kBfThreads, 1)
                 if (t < L) {
                     const int j = sb * kDV + 16 * nh + nt * 8 + cq;
                     *reinterpret_cast<uint32_t *>(&out[((size_t)(tc + t) * H + h) * kD + j]) =
-                        pack_f16(scale * oacc[nt][2 * hh], scale * oacc[nt][2 * hh + 1]);
+                        pack_bf16(scale * oacc[nt][2 * hh], scale * oacc[nt][2 * hh + 1]);
                 }
             }
 
