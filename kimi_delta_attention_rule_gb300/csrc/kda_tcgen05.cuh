@@ -4,11 +4,14 @@
 //
 // Layout conventions used with these helpers (no swizzle, 16-bit elements):
 // an operand tile is stored as 8x8 "core matrices" of 128 contiguous bytes
-// (8 rows of 16 bytes).
-//   K-major tile (rows = M or N, K contiguous inside a core matrix):
+// (8 rows of 16 bytes). In the descriptor, LBO is the byte distance between
+// core matrices adjacent along K and SBO the distance between core matrices
+// adjacent along M (or N), for both majors (checked on the GPU by
+// tests/test_tcgen05_layouts.py):
+//   K-major tile (rows = M or N, K contiguous inside a core-matrix row):
 //     byte(r, k) = (r / 8) * SBO + (k / 8) * LBO + (r % 8) * 16 + (k % 8) * 2
-//   MN-major tile (MN contiguous inside a core matrix):
-//     byte(k, x) = (x / 8) * LBO + (k / 8) * SBO + (k % 8) * 16 + (x % 8) * 2
+//   MN-major tile (M or N contiguous inside a core-matrix row):
+//     byte(k, x) = (x / 8) * SBO + (k / 8) * LBO + (k % 8) * 16 + (x % 8) * 2
 #pragma once
 
 #include <stdint.h>
@@ -126,7 +129,7 @@ __host__ __device__ constexpr uint32_t kmajor_off(int r, int k, uint32_t lbo, ui
 }
 // Byte offset of element (k, x) in an MN-major no-swizzle tile (x = M or N index).
 __host__ __device__ constexpr uint32_t mnmajor_off(int k, int x, uint32_t lbo, uint32_t sbo) {
-    return (uint32_t)(x >> 3) * lbo + (uint32_t)(k >> 3) * sbo + (uint32_t)(k & 7) * 16u +
+    return (uint32_t)(x >> 3) * sbo + (uint32_t)(k >> 3) * lbo + (uint32_t)(k & 7) * 16u +
            (uint32_t)(x & 7) * 2u;
 }
 

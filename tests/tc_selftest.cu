@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(128, 1)
 
     const uint32_t lboA = 128, sboA = (uint32_t)(K / 8) * 128;
     uint32_t lboB = 128, sboB = (uint32_t)(K / 8) * 128;     // K-major B (N x K)
-    if (b_mn) { lboB = 128; sboB = (uint32_t)(N / 8) * 128; } // MN-major: N groups adjacent
+    if (b_mn) { lboB = (uint32_t)(N / 8) * 128; sboB = 128; } // MN-major: N groups adjacent
     for (int i = tid; i < M * K; i += blockDim.x) {
         const int r = i / K, k = i % K;
         *reinterpret_cast<uint16_t *>(sA + kmajor_off(r, k, lboA, sboA)) = A[i];
@@ -56,13 +56,13 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t tm = tmem_base;
     if (tid == 0) {
         const uint32_t idesc = idesc_f16(M, N, f16, 0, b_mn);
-        // descriptor fields for B: in the MN-major case the test can swap the
-        // roles of the two byte offsets to check which field is which
+        // descriptor fields for B; mn_swap = 1 passes them in the opposite
+        // order (the test shows that order is wrong)
         const uint32_t dlbo = (b_mn && mn_swap) ? sboB : lboB;
         const uint32_t dsbo = (b_mn && mn_swap) ? lboB : sboB;
         for (int ks = 0; ks < K / 16; ++ks) {
             const uint64_t da = smem_desc(smem_u32(sA) + ks * 2 * lboA, lboA, sboA);
-            const uint32_t bstep = b_mn ? 2 * sboB : 2 * lboB;
+            const uint32_t bstep = 2 * lboB;  // two core matrices along K
             const uint64_t db = smem_desc(smem_u32(sB) + ks * bstep, dlbo, dsbo);
             mma_f16(tm, da, db, idesc, ks > 0 ? 1u : 0u);
         }
@@ -90,7 +90,7 @@ extern "C" int tc_selftest(const void *A, const void *B, float *D, int N, int K,
     if (N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16) return 1;
     // The whole 227 KB window is allocated so that a descriptor read with the
     // byte-offset fields in either order stays inside this CTA's shared memory.
-    const int smem = 227 * 1024;
+    const int smem = 220 * 1024;
     if (cudaFuncSetAttribute(tc_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              smem) != cudaSuccess)
         return 2;

@@ -1,9 +1,14 @@
 """GPU parity: the CUDA path (through the C ABI) against the fp64 oracle,
 element by element on the same seeded inputs.
 
-Error metric (per compared tensor): max |gpu - oracle| / rms(oracle).
-Bars: 2e-2 for bf16 I/O, 1e-4 for fp32 I/O (outputs and final states);
-sequence indexing is exact (outputs outside a sequence are untouched).
+Error metric (per compared tensor): max |gpu - oracle| / rms(oracle), with
+bars 2e-2 for bf16 I/O and 1e-4 for fp32 I/O (outputs and final states).
+A bf16 output cannot be closer to the exact value than half a bf16 spacing,
+and on these heavy-tailed outputs (max|o| / rms(o) ~ 13) that storage
+rounding alone is ~2.6e-2 of the RMS; so for bf16-stored tensors the bar
+applies to the error in excess of half a bf16 spacing at the oracle value:
+    max_i max(0, |gpu_i - ref_i| - ulp_bf16(ref_i) / 2) / rms(ref).
+fp32 tensors (final states, fp32 I/O) use the plain metric.
 Full-size workloads are checked on sampled (sequence, head) chains that the
 oracle recomputes one by one from the same inputs.
 """
@@ -22,14 +27,31 @@ TOL_F32 = 1e-4
 DEV = "cuda:0"
 
 
-def rel_err(got, ref):
+def bf16_half_spacing(ref):
+    """Half the distance between adjacent bf16 numbers at |ref| (8-bit
+    significand: spacing 2^(e - 7) in the binade [2^e, 2^(e+1)))."""
+    _, e = np.frexp(np.abs(ref))
+    e = np.maximum(e, -125)  # bf16 subnormal spacing floor
+    return np.ldexp(1.0, e - 9)
+
+
+def rel_err(got, ref, stored_bf16=False, ulps=0.5):
     ref = np.asarray(ref, dtype=np.float64)
     got = np.asarray(got, dtype=np.float64)
+    assert got.shape == ref.shape
     assert np.all(np.isfinite(got)), "non-finite GPU output"
+    diff = np.abs(got - ref)
+    if stored_bf16:
+        diff = np.maximum(diff - 2 * ulps * bf16_half_spacing(ref), 0.0)
     rms = float(np.sqrt(np.mean(ref ** 2)))
     if rms == 0.0:
-        return float(np.max(np.abs(got)))
-    return float(np.max(np.abs(got - ref))) / rms
+        return float(np.max(diff))
+    return float(np.max(diff)) / rms
+
+
+def out_err(out, ref):
+    """Error of an output tensor against the oracle (storage-aware)."""
+    return rel_err(np32(out), ref, stored_bf16=(out.dtype == torch.bfloat16))
 
 
 def np32(t):
@@ -64,7 +86,7 @@ def oracle_prefill(x, with_init=True):
 def check_prefill(x, chunk, tol, with_init=True):
     out, fin = run_gpu_prefill(x, chunk, with_init)
     ro, rf = oracle_prefill(x, with_init)
-    eo, ef = rel_err(np32(out), ro), rel_err(fin.cpu().numpy(), rf)
+    eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
     assert eo <= tol and ef <= tol, (eo, ef)
     return eo, ef
 
@@ -103,7 +125,7 @@ def test_bf16_equal_length_batch_without_cu_seqlens():
                                T=192, chunk=64)
     torch.cuda.synchronize()
     ro, rf = oracle_prefill(x)
-    assert rel_err(np32(out), ro) <= TOL_BF16
+    assert out_err(out, ro) <= TOL_BF16
     assert rel_err(fin.cpu().numpy(), rf) <= TOL_BF16
 
 
@@ -123,7 +145,7 @@ def test_bf16_decay_floor_and_special_cases():
             x.g = torch.full_like(base.g, 0.5)
         out, fin = run_gpu_prefill(x, 64)
         ro, rf = oracle_prefill(x)
-        eo, ef = rel_err(np32(out), ro), rel_err(fin.cpu().numpy(), rf)
+        eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
         assert eo <= TOL_BF16 and ef <= TOL_BF16, (name, eo, ef)
 
 
@@ -144,7 +166,7 @@ def test_varlen_rows_all_written():
     assert not torch.any(out == 7.0)
     ro, _ = oracle.prefill(np32(x.q[:90]), np32(x.k[:90]), np32(x.v[:90]), np32(x.g[:90]),
                            np32(x.beta[:90]), x.scale, cu_seqlens=[0, 40, 90])
-    assert rel_err(np32(out), ro) <= TOL_BF16
+    assert out_err(out, ro) <= TOL_BF16
 
 
 def test_bad_cu_seqlens_flagged_on_device():
@@ -169,7 +191,7 @@ def test_decode_chain(io, tol):
                                 beta[s].to(DEV), scale, st)
         ro, ref = oracle.decode_step(np32(q[s]), np32(k[s]), np32(v[s]), np32(g[s]),
                                      np32(beta[s]), scale, ref)
-        assert rel_err(np32(o), ro) <= tol, s
+        assert out_err(o, ro) <= tol, s
     assert rel_err(st.cpu().numpy(), ref) <= tol
 
 
@@ -188,7 +210,8 @@ def test_decode_equals_prefill_path():
         outs.append(o)
     torch.cuda.synchronize()
     dec = torch.stack(outs, 1).reshape(B * T, H, 128)
-    assert rel_err(np32(dec), np32(out_p)) <= 2 * TOL_BF16
+    # both are bf16-rounded: allow one bf16 spacing between them
+    assert rel_err(np32(dec), np32(out_p), stored_bf16=True, ulps=1.0) <= 2 * TOL_BF16
     assert rel_err(st.cpu().numpy(), fin_p.cpu().numpy()) <= 2 * TOL_BF16
 
 
@@ -210,7 +233,7 @@ def sampled_chain_check(x_dev, out, fin, lens, chains, init_cpu, tol):
         init = None if init_cpu is None else init_cpu[n:n + 1][:, heads].double().numpy()
         ro, rf = oracle.prefill(sl(x_dev.q), sl(x_dev.k), sl(x_dev.v), sl(x_dev.g),
                                 sl(x_dev.beta), x_dev.scale, init_state=init)
-        eo = rel_err(np32(out[t0:t1][:, heads]), ro)
+        eo = out_err(out[t0:t1][:, heads], ro)
         ef = rel_err(fin[n:n + 1][:, heads].cpu().numpy(), rf)
         return (n, heads, eo, ef)
 
@@ -249,7 +272,7 @@ def test_decode_full_size_64_steps():
                 np32(q[s, b:b + 1, h:h + 1]), np32(k[s, b:b + 1, h:h + 1]),
                 np32(v[s, b:b + 1, h:h + 1]), np32(g[s, b:b + 1, h:h + 1]),
                 np32(beta[s, b:b + 1, h:h + 1]), scale, ref[(b, h)])
-            assert rel_err(np32(o[b:b + 1, h:h + 1]), ro) <= TOL_BF16, (s, b, h)
+            assert out_err(o[b:b + 1, h:h + 1], ro) <= TOL_BF16, (s, b, h)
     for (b, h) in picks:
         assert rel_err(st[b, h].cpu().numpy(), ref[(b, h)][0, 0]) <= TOL_BF16
 
@@ -270,7 +293,7 @@ def test_append_prefill_full_size():
     heads = [0, 47, 95]
     sl = lambda t: np32(t[:, heads])
     ro, rf = oracle.prefill(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), x.scale)
-    eo = rel_err(np32(out[:, heads]), ro[P:])
+    eo = out_err(out[:, heads], ro[P:])
     ef = rel_err(fin[:, heads].cpu().numpy(), rf)
     assert eo <= TOL_BF16 and ef <= TOL_BF16, (eo, ef)
 

@@ -50,6 +50,7 @@ def test_kmajor(lib, N, K, f16):
 
 @pytest.mark.parametrize("N,K", [(64, 64), (128, 128)])
 def test_mnmajor_b(lib, N, K):
-    errs = {swap: run(lib, N, K, 1, 1, swap) for swap in (0, 1)}
-    print("MN-major B errors by descriptor field order:", errs)
-    assert min(errs.values()) < 1e-5, errs
+    """LBO = stride along K, SBO = stride along N, as for K-major tiles."""
+    errs = {swap: run(lib, N, K, 1, f16, swap) for swap in (0, 1) for f16 in (0, 1)}
+    assert run(lib, N, K, 1, 0, 0) < 1e-5 and run(lib, N, K, 1, 1, 0) < 1e-5
+    assert run(lib, N, K, 1, 1, 1) > 1e-2  # the other field order reads other data
