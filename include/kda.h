@@ -50,7 +50,9 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2, /* D != 128, unsupported chunk or dtype */
     KDA_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
     KDA_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out */
-    KDA_ERR_DEVICE = 5       /* the device flagged bad input (e.g. cu_seqlens) */
+    KDA_ERR_DEVICE = 5,      /* the device flagged bad input (e.g. cu_seqlens) */
+    KDA_ERR_TOO_LARGE = 6    /* kda_prefill_noalloc: the sizes need more scratch than its
+                                static array holds */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -130,6 +132,31 @@ int kda_workspace_status(void *workspace, void *stream);
  * non-decreasing, cu[N] = T_total. Returns KDA_OK or KDA_ERR_INVALID_ARG.
  */
 int kda_check_cu_seqlens(const int32_t *cu_seqlens_host, int32_t N, int32_t T_total);
+
+/*
+ * kda_prefill_noalloc -- the same prefill as kda_prefill, for callers that
+ * cannot allocate device memory (no access to cudaMalloc or to the host
+ * framework's allocator, or code that must not allocate at the point of the
+ * call). It takes no workspace: its scratch is a static device array inside
+ * the library, 1 MiB on every GPU that loads the library, held until the
+ * process exits. The pages have no counterpart to this entry point; it exists
+ * for such callers only.
+ *  - Arguments, layouts, stream semantics and results are those of
+ *    kda_prefill without the workspace arguments.
+ *  - Sizes whose kda_prefill_workspace_size() exceeds 1 MiB are rejected
+ *    with KDA_ERR_TOO_LARGE; nothing is launched.
+ *  - The first call on a device (with that device current) looks up the
+ *    array's device address; make that first call before any stream capture.
+ *  - All calls share the one array and each call clears its status word
+ *    first: calls that overlap on the GPU race on it, so the caller must
+ *    serialise them (one stream, or events between streams).
+ *  - It allocates nothing (no cudaMalloc / cudaFree, no allocating library
+ *    routine).
+ */
+int kda_prefill_noalloc(const void *q, const void *k, const void *v, const float *g,
+                        const void *beta, float scale, const float *init_state,
+                        const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
+                        int32_t chunk, int32_t io, void *out, float *final_state, void *stream);
 
 #ifdef __cplusplus
 }

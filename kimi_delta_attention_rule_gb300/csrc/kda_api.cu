@@ -57,6 +57,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
         case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE";
+        case KDA_ERR_TOO_LARGE: return "KDA_ERR_TOO_LARGE";
         default: return "KDA_ERR_UNKNOWN";
     }
 }
