@@ -259,7 +259,7 @@ def main():
     H, T = PREFILL["H"], PREFILL["T"]
     out = torch.empty_like(x.q)
     fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
-    ws = torch.zeros(256, dtype=torch.uint8, device=dev)
+    ws = kda.prefill_workspace(x.q, None, N=1, T=T, chunk=C)
 
     def step():
         kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, cu_seqlens=None, chunk=C, out=out,

@@ -65,13 +65,14 @@ int kda_abi_version(void);
 
 /*
  * Bytes of device workspace that kda_prefill needs for these sizes (same
- * meaning as in kda_prefill). Returns 0 when the sizes are invalid. The
- * workspace holds a device status word and per-call schedule data; it must
- * be 256-byte aligned and must not be shared by calls in flight at the same
- * time.
+ * meaning as in kda_prefill; varlen != 0 when cu_seqlens will be passed, and
+ * then T is the packed total). Returns 0 when the sizes are invalid. The
+ * workspace holds the device status word, the chunk schedule and, for bf16
+ * I/O, one 76,288-byte prepared block per (chunk, head). It must be 256-byte
+ * aligned and must not be shared by calls in flight at the same time.
  */
 size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
-                                  int32_t io);
+                                  int32_t io, int32_t varlen);
 
 /*
  * Chunked-parallel KDA prefill over N sequences.
@@ -138,12 +139,12 @@ int kda_check_cu_seqlens(const int32_t *cu_seqlens_host, int32_t N, int32_t T_to
  * cannot allocate device memory (no access to cudaMalloc or to the host
  * framework's allocator, or code that must not allocate at the point of the
  * call). It takes no workspace: its scratch is a static device array inside
- * the library, 1 MiB on every GPU that loads the library, held until the
+ * the library, 16 MiB on every GPU that loads the library, held until the
  * process exits. The pages have no counterpart to this entry point; it exists
  * for such callers only.
  *  - Arguments, layouts, stream semantics and results are those of
  *    kda_prefill without the workspace arguments.
- *  - Sizes whose kda_prefill_workspace_size() exceeds 1 MiB are rejected
+ *  - Sizes whose kda_prefill_workspace_size() exceeds 16 MiB are rejected
  *    with KDA_ERR_TOO_LARGE; nothing is launched.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.

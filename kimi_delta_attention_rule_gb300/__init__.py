@@ -23,6 +23,7 @@ KDA_ERR_UNSUPPORTED = 2
 KDA_ERR_CUDA = 3
 KDA_ERR_TIMEOUT = 4
 KDA_ERR_DEVICE = 5
+KDA_ERR_TOO_LARGE = 6
 KDA_BF16 = 0
 KDA_F32 = 1
 
@@ -53,7 +54,7 @@ def load() -> ctypes.CDLL:
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_abi_version.argtypes = []
         lib.kda_abi_version.restype = ctypes.c_int
-        lib.kda_prefill_workspace_size.argtypes = [I32] * 6
+        lib.kda_prefill_workspace_size.argtypes = [I32] * 7
         lib.kda_prefill_workspace_size.restype = SZ
         lib.kda_prefill.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32, P, P,
                                     P, SZ, P]
@@ -103,8 +104,23 @@ def _check_cuda(*ts):
                 raise ValueError("KDA tensors must be contiguous")
 
 
-def kda_prefill_workspace_size(N: int, T: int, H: int, D: int, chunk: int, io: int) -> int:
-    return int(load().kda_prefill_workspace_size(N, T, H, D, chunk, io))
+def kda_prefill_workspace_size(N: int, T: int, H: int, D: int, chunk: int, io: int,
+                               varlen: bool = False) -> int:
+    return int(load().kda_prefill_workspace_size(N, T, H, D, chunk, io, int(bool(varlen))))
+
+
+def prefill_workspace(q, cu_seqlens=None, N=None, T=None, chunk=64):
+    """A device workspace of kda_prefill_workspace_size() bytes for these
+    inputs (torch allocates it; the library never does)."""
+    T_total, H, D = q.shape
+    if cu_seqlens is not None:
+        N, T = cu_seqlens.numel() - 1, T_total
+    else:
+        N = 1 if N is None else N
+        T = T_total // N if T is None else T
+    nbytes = kda_prefill_workspace_size(N, T, H, D, chunk, _io_code(q.dtype),
+                                        cu_seqlens is not None)
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
 
 
 def kda_prefill(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk=64, out=None,
@@ -130,9 +146,8 @@ def kda_prefill(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk
         out = torch.empty_like(q) if io != KDA_F32 else torch.empty_like(q)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
-    ws_bytes = kda_prefill_workspace_size(N, T, H, D, chunk, io)
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device=q.device)
+        workspace = prefill_workspace(q, cu_seqlens, N, T, chunk)
     rc = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
                          _ptr(init_state), _ptr(cu_seqlens), N, T, H, D, chunk, io, _ptr(out),
                          _ptr(final_state), _ptr(workspace), workspace.numel(),

@@ -17,15 +17,23 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                const float *beta, float scale, const float *init,
                                const int32_t *cu, int N, int T, int T_total, int H, int chunk,
                                float *out, float *fin, uint32_t *status, cudaStream_t stream);
-cudaError_t launch_prefill_bf16(const void *q, const void *k, const void *v, const float *g,
-                                const void *beta, float scale, const float *init,
-                                const int32_t *cu, int N, int T, int T_total, int H, void *out,
-                                float *fin, uint32_t *status, cudaStream_t stream);
+size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen);
+cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
+                              const void *beta, float scale, const float *init,
+                              const int32_t *cu, int N, int T, int T_total, int H, void *out,
+                              float *fin, unsigned char *ws, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
 
 constexpr size_t kWorkspaceBytes = 256;  // device status word, padded to 256 B
+
+// Workspace of one call: status word, plus (bf16 path) the chunk schedule and
+// one 76 KiB prepared block per (chunk, head).
+size_t workspace_bytes_for(int32_t N, int32_t T, int32_t H, int32_t io, bool varlen) {
+    if (io == KDA_F32) return kWorkspaceBytes;
+    return kda::prefill_tc_workspace(N, T, T, H, varlen);
+}
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -65,12 +73,10 @@ const char *kda_status_string(int status) {
 int kda_abi_version(void) { return 100; }
 
 size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
-                                  int32_t io) {
+                                  int32_t io, int32_t varlen) {
     long long tt = 0;
-    if (check_prefill_dims(N, T, H, D, chunk, io, false, &tt) != KDA_OK &&
-        check_prefill_dims(N, T, H, D, chunk, io, true, &tt) != KDA_OK)
-        return 0;
-    return kWorkspaceBytes;
+    if (check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt) != KDA_OK) return 0;
+    return workspace_bytes_for(N, T, H, io, varlen != 0);
 }
 
 int kda_check_cu_seqlens(const int32_t *cu, int32_t N, int32_t T_total) {
@@ -88,7 +94,8 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
     long long T_total = 0;
     const int rc = check_prefill_dims(N, T, H, D, chunk, io, cu_seqlens != nullptr, &T_total);
     if (rc != KDA_OK) return rc;
-    if (workspace == nullptr || workspace_bytes < kWorkspaceBytes ||
+    if (workspace == nullptr ||
+        workspace_bytes < workspace_bytes_for(N, T, H, io, cu_seqlens != nullptr) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return KDA_ERR_INVALID_ARG;
     if (N == 0) return KDA_OK;
@@ -111,8 +118,9 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
                                     cu_seqlens, N, T, (int)T_total, H, chunk,
                                     static_cast<float *>(out), final_state, status, st);
     } else {
-        e = kda::launch_prefill_bf16(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T,
-                                     (int)T_total, H, out, final_state, status, st);
+        e = kda::launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T,
+                                   (int)T_total, H, out, final_state,
+                                   static_cast<unsigned char *>(workspace), st);
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -26,7 +26,7 @@
 
 namespace {
 
-constexpr size_t kNoallocScratchBytes = 1u << 20;  // 1 MiB
+constexpr size_t kNoallocScratchBytes = 16u << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
@@ -57,7 +57,8 @@ int kda_prefill_noalloc(const void *q, const void *k, const void *v, const float
                         const void *beta, float scale, const float *init_state,
                         const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
                         int32_t chunk, int32_t io, void *out, float *final_state, void *stream) {
-    const size_t need = kda_prefill_workspace_size(N, T, H, D, chunk, io);
+    const size_t need =
+        kda_prefill_workspace_size(N, T, H, D, chunk, io, cu_seqlens != nullptr ? 1 : 0);
     if (need == 0) {
         // same validation (and error code) as kda_prefill
         return kda_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk,

@@ -42,7 +42,12 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 256
+    # bf16: status word + one 76288-byte prepared block per (chunk, head)
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 128 * 32 * 76288
+    assert kda.kda_prefill_workspace_size(4, 100, 2, 128, 64, kda.KDA_BF16) >= 4 * 2 * 2 * 76288
+    # packed: T is the total; one spare chunk slot per sequence at most
+    vl = kda.kda_prefill_workspace_size(64, 1 << 20, 32, 128, 64, kda.KDA_BF16, varlen=True)
+    assert ((1 << 20) // 64) * 32 * 76288 <= vl <= ((1 << 20) // 64 + 64) * 32 * 76288 + 4096
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_F32) >= 256
     assert kda.kda_prefill_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16) == 0      # D != 128
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_BF16) == 0     # chunk
@@ -68,10 +73,12 @@ def test_prefill_argument_validation(lib):
     assert _prefill(lib) == kda.KDA_ERR_INVALID_ARG                      # no workspace
     assert _prefill(lib, ws=fake, ws_bytes=16) == kda.KDA_ERR_INVALID_ARG  # too small
     assert _prefill(lib, ws=ctypes.c_void_p(0x100010), ws_bytes=256) == kda.KDA_ERR_INVALID_ARG
-    assert _prefill(lib, ws=fake, ws_bytes=256) == kda.KDA_ERR_INVALID_ARG  # null tensors
+    big = 1 << 40
+    assert _prefill(lib, ws=fake, ws_bytes=256) == kda.KDA_ERR_INVALID_ARG  # workspace too small
+    assert _prefill(lib, ws=fake, ws_bytes=big) == kda.KDA_ERR_INVALID_ARG  # null tensors
     mis = ctypes.c_void_p(0x100002)
     assert _prefill(lib, q=mis, k=fake, v=fake, g=fake, beta=fake, out=fake, ws=fake,
-                    ws_bytes=256) == kda.KDA_ERR_INVALID_ARG             # misaligned q
+                    ws_bytes=big) == kda.KDA_ERR_INVALID_ARG             # misaligned q
     assert _prefill(lib, N=1, T=1 << 31 - 1, H=1 << 12, ws=fake, ws_bytes=256) \
         == kda.KDA_ERR_INVALID_ARG                                       # size overflow
     # N = 0 is a valid empty call: nothing is launched

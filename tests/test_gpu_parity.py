@@ -68,7 +68,8 @@ def _lib():
 def run_gpu_prefill(x, chunk, with_init=True):
     cu = x.cu_seqlens.to(DEV) if x.cu_seqlens is not None else None
     init = x.init_state.to(DEV) if (with_init and x.init_state is not None) else None
-    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    q = x.q.to(DEV)
+    ws = kda.prefill_workspace(q, cu, chunk=chunk)
     out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
                                x.beta.to(DEV), x.scale, init_state=init, cu_seqlens=cu,
                                chunk=chunk, workspace=ws)
@@ -172,7 +173,7 @@ def test_varlen_rows_all_written():
 def test_bad_cu_seqlens_flagged_on_device():
     x = inputs.prefill_inputs([64, 64], H=1, io="bf16", seed=17)
     cu = torch.tensor([0, 100, 64], dtype=torch.int32, device=DEV)  # decreasing
-    ws = torch.zeros(256, dtype=torch.uint8, device=DEV)
+    ws = kda.prefill_workspace(x.q.to(DEV), cu, chunk=64)
     kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV), x.beta.to(DEV), x.scale,
                     cu_seqlens=cu, chunk=64, workspace=ws)
     assert kda.kda_workspace_status(ws) == kda.KDA_ERR_DEVICE

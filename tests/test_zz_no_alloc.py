@@ -64,3 +64,13 @@ def test_noalloc_rejects_bad_arguments_like_kda_prefill():
     rc = f(None, None, None, None, None, 1.0, None, None, 1, 64, 2, 64, 64, kda.KDA_BF16, None,
            None, None)
     assert rc == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_noalloc_rejects_sizes_beyond_its_static_scratch():
+    f = _noalloc_fn()
+    # H=32, T=8192 needs ~312 MB of prepared chunk blocks: far beyond 16 MiB
+    need = kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16, False)
+    assert need > 16 << 20
+    rc = f(None, None, None, None, None, 1.0, None, None, 1, 8192, 32, 128, 64, kda.KDA_BF16,
+           None, None, None)
+    assert rc == kda.KDA_ERR_TOO_LARGE
