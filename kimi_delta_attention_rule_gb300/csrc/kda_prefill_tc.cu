@@ -33,6 +33,9 @@
 //                    columns; per chunk: one bulk TMA load of the block
 //                    (double-buffered), three tcgen05.mma groups with fp32
 //                    accumulators in TMEM and the fp32 state resident in TMEM.
+//                    Warps 0-3 run the serial chain (P -> U, state -> fp16
+//                    operand); warps 4-7 rescale the state and write the
+//                    outputs; hand-offs are mbarriers.
 //
 // In K2 everything is transposed so that the TMEM lane is the value column
 // j (128 lanes):
@@ -104,25 +107,34 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
 // ============================================================================
 // K1: chunk preparation
 // ============================================================================
+// One CTA (8 warps) per (chunk, head), two CTAs per SM. The cumulative decay
+// a of the chunk is kept in shared memory; q, k, v are read with coalesced
+// 16-byte loads where they are used; every output goes straight to the
+// chunk block in global memory, already in the core-matrix layout K2 reads.
 constexpr int kPrepThreads = 256;
-constexpr int kLDK = 136;  // bf16/fp16 pitch of C x 128 tiles
+constexpr int kLDK = 136;  // bf16/fp16 pitch of 128-wide tiles (conflict-free ldmatrix)
 constexpr int kLDC = 72;   // fp16 pitch of C x C tiles
 constexpr int kLDA = 68;   // fp32 pitch of C x C matrices
-constexpr int kOffXq = 0;
-constexpr int kOffXk = kOffXq + C * kLDK * 2;
-constexpr int kOffKh = kOffXk + C * kLDK * 2;
-constexpr int kOffKtb = kOffKh + 160 * kLDK * 2;
-constexpr int kOffVb = kOffKtb + C * kLDK * 2;
-constexpr int kOffA = kOffVb + C * kLDK * 2;
-constexpr int kOffOut = kOffA + C * kLDA * 4;
-constexpr int kOffBeta = kOffOut + (int)kBlock;
-constexpr int kOffTile = kOffBeta + C * 4;
-constexpr int kPrepSmem = kOffTile + 4 * 128 * 4;
-constexpr int kOffT = kOffKh;                 // fp32 [64][68] (aliases the column tiles)
-constexpr int kOffX = kOffT + C * kLDA * 4;   // fp32 [3][16][16]
-static_assert(kOffX + 3 * 256 * 4 <= kOffKtb, "T scratch inside the column-tile region");
-static_assert(kOffOut % 128 == 0, "bulk store source alignment");
-static_assert(kPrepSmem <= 227 * 1024, "shared memory budget");
+constexpr int kOffAcum = 0;                          // fp32 [64][128] a
+constexpr int kOffRef = kOffAcum + C * 128 * 4;      // fp32 [4][128] r_i
+constexpr int kOffEr = kOffRef + 4 * 128 * 4;        // fp32 [4][128] e^{r_i}
+constexpr int kOffAc = kOffEr + 4 * 128 * 4;         // fp32 [128] a_C
+constexpr int kOffHalf = kOffAc + 128 * 4;           // fp32 [128] a at token 31
+constexpr int kOffBeta = kOffHalf + 128 * 4;         // fp32 [64]
+constexpr int kOffMd = kOffBeta + C * 4;             // fp32 [64] q_t . k_t
+constexpr int kOffA = kOffMd + C * 4;                // fp32 [64][68] A
+constexpr int kOffG = kOffA + C * kLDA * 4;          // phase-dependent region:
+//   Gram:  Xq16 bf16 [16][136] | Xk16 bf16 [16][136] | Kh bf16 [64][136]
+//   T:     Tb fp16 [64][72] | Ah fp16 [64][72] | Xh fp16 [3][16][24]
+//   W, U~: Tb fp16 [64][72] | Ktb fp16 [64][136] | Vb fp16 [64][136]
+constexpr int kGXq = 0, kGXk = kGXq + 16 * kLDK * 2, kGKh = kGXk + 16 * kLDK * 2;
+constexpr int kGTb = 0, kGAh = kGTb + C * kLDC * 2, kGXh = kGAh + C * kLDC * 2;
+constexpr int kGKtb = kGTb + C * kLDC * 2, kGVb = kGKtb + C * kLDK * 2;
+constexpr int kGBytes = kGVb + C * kLDK * 2;
+static_assert(kGKh + C * kLDK * 2 <= kGBytes, "Gram operands fit the region");
+static_assert(kGXh + 3 * 16 * 24 * 2 <= kGBytes, "T scratch fits the region");
+constexpr int kPrepSmem = kOffG + kGBytes;
+static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
 
 __device__ __forceinline__ int kh_slot(int i, int j) { return (i * (i + 1)) / 2 + j; }
 
@@ -149,12 +161,44 @@ __device__ __forceinline__ bool slot_to_chunk(int slot, const int32_t *cu,
     return true;
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 1)
+__device__ __forceinline__ uint4 pack8_bf16(const float *x) {
+    uint4 r;
+    r.x = pack_bf16(x[0], x[1]); r.y = pack_bf16(x[2], x[3]);
+    r.z = pack_bf16(x[4], x[5]); r.w = pack_bf16(x[6], x[7]);
+    return r;
+}
+__device__ __forceinline__ uint4 pack8_f16(const float *x) {
+    uint4 r;
+    r.x = pack_f16(x[0], x[1]); r.y = pack_f16(x[2], x[3]);
+    r.z = pack_f16(x[4], x[5]); r.w = pack_f16(x[6], x[7]);
+    return r;
+}
+__device__ __forceinline__ void unpack8_bf16(uint4 u, float *x) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __low2float(h[e]);
+        x[2 * e + 1] = __high2float(h[e]);
+    }
+}
+// 8 consecutive channels of row t (zeros for padding rows)
+__device__ __forceinline__ void load8(const __nv_bfloat16 *__restrict__ p, int tc, int t, int L,
+                                      int H, int h, int c0, float *x) {
+    uint4 u = make_uint4(0, 0, 0, 0);
+    if (t < L) u = __ldg(reinterpret_cast<const uint4 *>(p + ((size_t)(tc + t) * H + h) * 128 + c0));
+    unpack8_bf16(u, x);
+}
+__device__ __forceinline__ void lds8(const float *s, float *x) {
+    *reinterpret_cast<float4 *>(x) = *reinterpret_cast<const float4 *>(s);
+    *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(s + 4);
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 2)
     prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
                 const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu,
                 const int32_t *__restrict__ first_chunk, int N, int T, int H,
-                unsigned char *__restrict__ blocks) {
+                unsigned char *__restrict__ blocks, uint32_t *status) {
     const int slot = blockIdx.x, h = blockIdx.y;
     int n, c;
     if (!slot_to_chunk(slot, cu, first_chunk, N, T, n, c)) return;
@@ -164,146 +208,175 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     if (t1 < t0 || tc >= t1) return;  // malformed offsets are flagged by K2
     const int L = min(C, t1 - tc);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cq = 2 * (lane & 3);
+    unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
 
     extern __shared__ __align__(1024) unsigned char smem[];
-    __nv_bfloat16 *sXq = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXq);
-    __nv_bfloat16 *sXk = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXk);
-    __nv_bfloat16 *sKh = reinterpret_cast<__nv_bfloat16 *>(smem + kOffKh);
-    __half *sKtb = reinterpret_cast<__half *>(smem + kOffKtb);
-    __half *sVb = reinterpret_cast<__half *>(smem + kOffVb);
-    __half *sTb = reinterpret_cast<__half *>(smem + kOffXq);
-    float *sA = reinterpret_cast<float *>(smem + kOffA);
-    float *sT = reinterpret_cast<float *>(smem + kOffT);
-    float *sX = reinterpret_cast<float *>(smem + kOffX);
-    unsigned char *sOut = smem + kOffOut;
+    const uint32_t sbase = smem_u32(smem);
+    float *sAc_ = reinterpret_cast<float *>(smem + kOffAcum);
+    float *sRef = reinterpret_cast<float *>(smem + kOffRef);
+    float *sEr = reinterpret_cast<float *>(smem + kOffEr);
+    float *sAcT = reinterpret_cast<float *>(smem + kOffAc);
+    float *sHalf = reinterpret_cast<float *>(smem + kOffHalf);
     float *sBeta = reinterpret_cast<float *>(smem + kOffBeta);
-    float *sTile = reinterpret_cast<float *>(smem + kOffTile);
-    float *sGam = reinterpret_cast<float *>(sOut + kGam);
-    const int cq = 2 * (lane & 3);
+    float *sMd = reinterpret_cast<float *>(smem + kOffMd);
+    float *sA = reinterpret_cast<float *>(smem + kOffA);
+    unsigned char *sG = smem + kOffG;
 
-    // ---- loads, all issued up front -------------------------------------------
-    const int ch = tid & 127, ih = tid >> 7;  // channel; this thread prepares tiles ih, ih + 2
-    float gv[2][16], qv[2][16], kv[2][16];
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii)
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int t = 16 * (ih + 2 * ii) + r;
-            const bool ok = t < L;
-            const size_t off = ((size_t)(tc + (ok ? t : 0)) * H + h) * 128 + ch;
-            gv[ii][r] = ok ? clamp_g(g[off]) : 0.f;
-            qv[ii][r] = ok ? __bfloat162float(q[off]) : 0.f;
-            kv[ii][r] = ok ? __bfloat162float(k[off]) : 0.f;
-        }
-    __nv_bfloat162 vv[16];
-#pragma unroll
-    for (int m = 0; m < 16; ++m) {
-        const int p = tid + kPrepThreads * m, t = p >> 6, j = 2 * (p & 63);
-        const int ts = t < L ? t : 0;  // in-bounds address for padding rows
-        const __nv_bfloat162 w =
-            *reinterpret_cast<const __nv_bfloat162 *>(&v[((size_t)(tc + ts) * H + h) * 128 + j]);
-        vv[m] = t < L ? w : __floats2bfloat162_rn(0.f, 0.f);
-    }
-    if (tid < C) {
-        const float bt = __bfloat162float(beta[(size_t)(tc + (tid < L ? tid : 0)) * H + h]);
-        sBeta[tid] = tid < L ? bt : 0.f;
-    }
-#pragma unroll
-    for (int ii = 0; ii < 2; ++ii) {
-        float s = 0.f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r) s += gv[ii][r];
-        sTile[(ih + 2 * ii) * 128 + ch] = s;
-    }
-    __syncthreads();
-
-    // ---- decay-scaled operands --------------------------------------------------
+    // ---- cumulative decay: thread = (channel, half of the chunk) ---------------------
+    if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(size_t)(tc + tid) * H + h]) : 0.f;
     {
-        float ref[4];
-        ref[0] = 0.f;
-        ref[1] = sTile[ch];
-        ref[2] = ref[1] + sTile[128 + ch];
-        ref[3] = ref[2] + sTile[256 + ch];
-        const float aC = ref[3] + sTile[384 + ch];
-        if (ih == 0) sGam[ch] = __expf(aC);
+        const int ch = tid & 127, hf = tid >> 7;
+        float a[32];
 #pragma unroll
-        for (int ii = 0; ii < 2; ++ii) {
-            const int i = ih + 2 * ii;
-            const float er = __expf(ref[i]);       // e^{r_i}       <= 1
-            const float eC = __expf(aC - ref[i]);  // e^{a_C - r_i} <= 1
-            float eR[4];
-#pragma unroll
-            for (int i2 = 0; i2 < 4; ++i2) eR[i2] = i2 > i ? __expf(ref[i2] - ref[i]) : 0.f;
-            float p = 0.f;  // a_t - r_i
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                const int t = 16 * i + r;
-                p += gv[ii][r];
-                const float x = __expf(p);   // e^{a_t - r_i} in [e^-80, 1]
-                const float ix = __expf(-p); // e^{r_i - a_t} in [1, e^80]
-                const float qq = qv[ii][r], kk = kv[ii][r], bt = sBeta[t];
-                sXq[t * kLDK + ch] = __float2bfloat16_rn(qq * x);
-                sXk[t * kLDK + ch] = __float2bfloat16_rn(kk * x);
-                sKh[(kh_slot(i, i) * 16 + r) * kLDK + ch] = __float2bfloat16_rn(kk * ix);
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2)
-                    if (i2 > i)
-                        sKh[(kh_slot(i2, i) * 16 + r) * kLDK + ch] =
-                            __float2bfloat16_rn(kk * (eR[i2] * ix));
-                sKtb[t * kLDK + ch] = __float2half_rn(bt * kk * (er * x));
-                store_h(sOut + kB12, off_k128(t, ch), qq * (er * x));  // q e^{a}
-                store_h(sOut + kB2, off_k64(ch, t), kk * (eC * ix));   // (k e^{a_C - a})^T
-            }
+        for (int r = 0; r < 32; ++r) {
+            const int t = 32 * hf + r;
+            a[r] = t < L ? clamp_g(__ldg(&g[((size_t)(tc + t) * H + h) * 128 + ch])) : 0.f;
         }
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-            const int p = tid + kPrepThreads * m, t = p >> 6, j = 2 * (p & 63);
-            const float bt = sBeta[t];
-            *reinterpret_cast<uint32_t *>(&sVb[t * kLDK + j]) =
-                pack_f16(bt * __low2float(vv[m]), bt * __high2float(vv[m]));
+        for (int r = 1; r < 32; ++r) a[r] += a[r - 1];
+        if (hf == 0) sHalf[ch] = a[31];
+        __syncthreads();
+        const float off = hf ? sHalf[ch] : 0.f;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) sAc_[(32 * hf + r) * 128 + ch] = a[r] + off;
+        // references: exclusive prefix at tiles 2 hf and 2 hf + 1
+        const float r0 = off, r1 = a[15] + off;
+        sRef[(2 * hf) * 128 + ch] = r0;
+        sRef[(2 * hf + 1) * 128 + ch] = r1;
+        sEr[(2 * hf) * 128 + ch] = __expf(r0);
+        sEr[(2 * hf + 1) * 128 + ch] = __expf(r1);
+        if (hf == 1) {
+            sAcT[ch] = a[31] + off;
+            reinterpret_cast<float *>(blk + kGam)[ch] = __expf(a[31] + off);
         }
     }
     __syncthreads();
 
-    // ---- Gram matrices A (beta, strictly lower) and M (lower) -------------------
-    const uint32_t aXq = smem_u32(sXq), aXk = smem_u32(sXk), aKh = smem_u32(sKh);
-    for (int task = warp; task < 20; task += kPrepThreads / 32) {
-        const int m = task / 10;
-        int tt = task % 10, i = 0;
-        while (tt > i) { tt -= i + 1; ++i; }
-        const int j = tt;
-        float acc[2][4] = {};
-        const uint32_t aX = m == 0 ? aXk : aXq;
-        const uint32_t aB = aKh + (uint32_t)(kh_slot(i, j) * 16 * kLDK) * 2u;
+    // ---- q e^{a} -> block; diagonal of M (q_t . k_t, no decay) -------------------
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+        const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8;
+        float qq[8], kk[8], a[8], o[8];
+        load8(q, tc, t, L, H, h, c0, qq);
+        load8(k, tc, t, L, H, h, c0, kk);
+        lds8(&sAc_[t * 128 + c0], a);
+        float md = 0.f;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-            uint32_t a[4], b[4];
-            frag_a_rowmajor(a, aX, kLDK, 16 * i, 16 * ks, lane);
-            frag_b_nk(b, aB, kLDK, 0, 16 * ks, lane);
-            mma_bf16_16816(acc[0], a, b[0], b[1]);
-            mma_bf16_16816(acc[1], a, b[2], b[3]);
+        for (int e = 0; e < 8; ++e) {
+            o[e] = qq[e] * __expf(a[e]);
+            md += qq[e] * kk[e];
         }
+        *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(t, c0)) = pack8_f16(o);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int t = 16 * i + (lane >> 2) + (e >= 2 ? 8 : 0);
-                const int s = 16 * j + nt * 8 + cq + (e & 1);
-                if (m == 0) sA[t * kLDA + s] = s < t ? sBeta[t] * acc[nt][e] : 0.f;
-                else store_h(sOut + kB3, off_k64(t, s), s <= t ? acc[nt][e] : 0.f);
-            }
+        for (int off2 = 8; off2 > 0; off2 >>= 1) md += __shfl_xor_sync(0xffffffffu, md, off2);
+        if ((lane & 15) == 0) sMd[t] = md;
     }
-    for (int idx = tid; idx < 6 * 256; idx += kPrepThreads) {  // blocks above the diagonal
-        const int blk = idx >> 8, e = idx & 255;
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        const int t = 16 * bi + (e >> 4), s = 16 * bj + (e & 15);
-        sA[t * kLDA + s] = 0.f;
-        store_h(sOut + kB3, off_k64(t, s), 0.f);
+    // ---- (k e^{a_C - a})^T -> block: item = (key channel, 8 tokens) ----------------
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+        const int id = tid + kPrepThreads * m, key = id & 127, tg = id >> 7;
+        const float ac = sAcT[key];
+        float o[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int t = 8 * tg + e;
+            const float kv = t < L ? __bfloat162float(__ldg(&k[((size_t)(tc + t) * H + h) * 128 + key])) : 0.f;
+            o[e] = kv * __expf(ac - sAc_[t * 128 + key]);
+        }
+        *reinterpret_cast<uint4 *>(blk + kB2 + off_k64(key, 8 * tg)) = pack8_f16(o);
+    }
+
+    // ---- Gram matrices, one row tile (reference r_i) at a time -------------------------
+    {
+        __nv_bfloat16 *sXq = reinterpret_cast<__nv_bfloat16 *>(sG + kGXq);
+        __nv_bfloat16 *sXk = reinterpret_cast<__nv_bfloat16 *>(sG + kGXk);
+        __nv_bfloat16 *sKh = reinterpret_cast<__nv_bfloat16 *>(sG + kGKh);
+        const uint32_t aXq = sbase + kOffG + kGXq, aXk = sbase + kOffG + kGXk;
+        const uint32_t aKh = sbase + kOffG + kGKh;
+#pragma unroll 1
+        for (int i = 0; i < 4; ++i) {
+            __syncthreads();  // previous round's operands fully consumed
+            // row operands (tile i) and column operands (tokens 0 .. 16 i + 15)
+            const int nitems = 16 * 16 + 16 * (i + 1) * 16;
+            for (int id = tid; id < nitems; id += kPrepThreads) {
+                float r[8], a[8], x[8], o[8];
+                if (id < 256) {
+                    const int rr = id >> 4, c0 = (id & 15) * 8, t = 16 * i + rr;
+                    float qq[8], kk[8];
+                    load8(q, tc, t, L, H, h, c0, qq);
+                    load8(k, tc, t, L, H, h, c0, kk);
+                    lds8(&sRef[i * 128 + c0], r);
+                    lds8(&sAc_[t * 128 + c0], a);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = __expf(a[e] - r[e]);  // <= 1
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = qq[e] * x[e];
+                    *reinterpret_cast<uint4 *>(&sXq[rr * kLDK + c0]) = pack8_bf16(o);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = kk[e] * x[e];
+                    *reinterpret_cast<uint4 *>(&sXk[rr * kLDK + c0]) = pack8_bf16(o);
+                } else {
+                    const int i2 = id - 256, s = i2 >> 4, c0 = (i2 & 15) * 8;
+                    float kk[8];
+                    load8(k, tc, s, L, H, h, c0, kk);
+                    lds8(&sRef[i * 128 + c0], r);
+                    lds8(&sAc_[s * 128 + c0], a);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) o[e] = kk[e] * __expf(r[e] - a[e]);  // <= e^80
+                    *reinterpret_cast<uint4 *>(&sKh[s * kLDK + c0]) = pack8_bf16(o);
+                }
+            }
+            __syncthreads();
+            // tasks: (matrix A or M, column tile j <= i)
+            for (int task = warp; task < 2 * (i + 1); task += kPrepThreads / 32) {
+                const int mm = task & 1, j = task >> 1;
+                float acc[2][4] = {};
+                const uint32_t aX = mm == 0 ? aXk : aXq;
+                const uint32_t aB = aKh + (uint32_t)(16 * j * kLDK) * 2u;
+#pragma unroll
+                for (int ks = 0; ks < 8; ++ks) {
+                    uint32_t af[4], bf[4];
+                    frag_a_rowmajor(af, aX, kLDK, 0, 16 * ks, lane);
+                    frag_b_nk(bf, aB, kLDK, 0, 16 * ks, lane);
+                    mma_bf16_16816(acc[0], af, bf[0], bf[1]);
+                    mma_bf16_16816(acc[1], af, bf[2], bf[3]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int t = 16 * i + (lane >> 2) + 8 * hh;
+                        const int s = 16 * j + nt * 8 + cq;
+                        float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
+                        if (mm == 0) {
+                            sA[t * kLDA + s] = s < t ? sBeta[t] * v0 : 0.f;
+                            sA[t * kLDA + s + 1] = s + 1 < t ? sBeta[t] * v1 : 0.f;
+                        } else {
+                            v0 = s < t ? v0 : (s == t ? sMd[t] : 0.f);
+                            v1 = s + 1 < t ? v1 : (s + 1 == t ? sMd[t] : 0.f);
+                            *reinterpret_cast<uint32_t *>(blk + kB3 + off_k64(t, s)) = pack_f16(v0, v1);
+                        }
+                    }
+            }
+        }
+        // blocks above the diagonal: zero in A (shared) and in M (the block)
+        for (int idx = tid; idx < 6 * 128; idx += kPrepThreads) {
+            const int b_ = idx >> 7, e = idx & 127;
+            const int bi = b_ < 3 ? 0 : (b_ < 5 ? 1 : 2);
+            const int bj = b_ < 3 ? b_ + 1 : (b_ < 5 ? b_ - 1 : 3);
+            const int t = 16 * bi + (e >> 3), s = 16 * bj + 2 * (e & 7);
+            sA[t * kLDA + s] = 0.f;
+            sA[t * kLDA + s + 1] = 0.f;
+            *reinterpret_cast<uint32_t *>(blk + kB3 + off_k64(t, s)) = 0u;
+        }
     }
     __syncthreads();
 
-    // ---- T = (I + A)^{-1} in fp32; exact diagonal of M ----------------------------
+    // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
+    __half *sAh = reinterpret_cast<__half *>(sG + kGAh);
+    __half *sTb = reinterpret_cast<__half *>(sG + kGTb);
+    const uint32_t aTb = sbase + kOffG + kGTb;
     if (tid < 64) {
         const int b = tid >> 4, cc = tid & 15;
         float x[16];
@@ -315,78 +388,96 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sT[(16 * b + r) * kLDA + 16 * b + cc] = x[r];
+        for (int r = 0; r < 16; ++r) sTb[(16 * b + r) * kLDC + 16 * b + cc] = __float2half_rn(x[r]);
     } else {
-        for (int idx = tid - 64; idx < 6 * 256; idx += kPrepThreads - 64) {
-            const int blk = idx >> 8, e = idx & 255;
-            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            sT[(16 * bi + (e >> 4)) * kLDA + 16 * bj + (e & 15)] = 0.f;
-        }
-        // diag(M) carries no decay: q_t . k_t in fp32 from the stored inputs
-        for (int t = warp - 2; t < L; t += kPrepThreads / 32 - 2) {
-            const size_t off = ((size_t)(tc + t) * H + h) * 128 + 4 * lane;
-            const uint2 qq = *reinterpret_cast<const uint2 *>(&q[off]);
-            const uint2 kk = *reinterpret_cast<const uint2 *>(&k[off]);
-            const __nv_bfloat162 *q2 = reinterpret_cast<const __nv_bfloat162 *>(&qq);
-            const __nv_bfloat162 *k2 = reinterpret_cast<const __nv_bfloat162 *>(&kk);
-            float d = __low2float(q2[0]) * __low2float(k2[0]) +
-                      __high2float(q2[0]) * __high2float(k2[0]) +
-                      __low2float(q2[1]) * __low2float(k2[1]) +
-                      __high2float(q2[1]) * __high2float(k2[1]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-            if (lane == 0) store_h(sOut + kB3, off_k64(t, t), d);
+        for (int idx = tid - 64; idx < C * C / 2; idx += kPrepThreads - 64) {
+            const int t = idx >> 5, s = 2 * (idx & 31);
+            *reinterpret_cast<uint32_t *>(&sAh[t * kLDC + s]) =
+                pack_f16(sA[t * kLDA + s], sA[t * kLDA + s + 1]);
+            if ((s >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(&sTb[t * kLDC + s]) = 0u;
         }
     }
     __syncthreads();
+    {
+        // level d: T_ij = -T_ii * sum_{kk = 16j}^{16i - 1} A[16i.., kk] T[kk, 16j..]
+        const uint32_t aAh = sbase + kOffG + kGAh;
+        __half *sXh = reinterpret_cast<__half *>(sG + kGXh);
 #pragma unroll 1
-    for (int d = 1; d < 4; ++d) {
-        const int nb = 4 - d;
-        for (int idx = tid; idx < nb * 256; idx += kPrepThreads) {
-            const int i = d + (idx >> 8), j = i - d, r = (idx >> 4) & 15, cc = idx & 15;
-            float acc = 0.f;
-            for (int kk = 16 * j; kk < 16 * i; ++kk)
-                acc += sA[(16 * i + r) * kLDA + kk] * sT[kk * kLDA + 16 * j + cc];
-            sX[(idx >> 8) * 256 + r * 16 + cc] = acc;
-        }
-        __syncthreads();
-        for (int idx = tid; idx < nb * 256; idx += kPrepThreads) {
-            const int i = d + (idx >> 8), j = i - d, r = (idx >> 4) & 15, cc = idx & 15;
-            float acc = 0.f;
+        for (int d = 1; d < 4; ++d) {
+            if (warp < 4 - d) {
+                const int i = d + warp, j = i - d;
+                float xacc[2][4] = {};
+#pragma unroll 1
+                for (int ks = j; ks < i; ++ks) {
+                    uint32_t af[4], bf[4];
+                    frag_a_rowmajor(af, aAh, kLDC, 16 * i, 16 * ks, lane);
+                    frag_b_kn(bf, aTb, kLDC, 16 * j, 16 * ks, lane);
+                    mma_f16_16816(xacc[0], af, bf[0], bf[1]);
+                    mma_f16_16816(xacc[1], af, bf[2], bf[3]);
+                }
+                __half *xs = sXh + warp * 16 * 24;
 #pragma unroll
-            for (int s = 0; s < 16; ++s)
-                acc += sT[(16 * i + r) * kLDA + 16 * i + s] * sX[(idx >> 8) * 256 + s * 16 + cc];
-            sT[(16 * i + r) * kLDA + 16 * j + cc] = -acc;
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int rr = lane >> 2, cc2 = nt * 8 + cq;
+                    *reinterpret_cast<uint32_t *>(&xs[rr * 24 + cc2]) = pack_f16(xacc[nt][0], xacc[nt][1]);
+                    *reinterpret_cast<uint32_t *>(&xs[(rr + 8) * 24 + cc2]) = pack_f16(xacc[nt][2], xacc[nt][3]);
+                }
+                __syncwarp();
+                float tacc[2][4] = {};
+                uint32_t af[4], bf[4];
+                frag_a_rowmajor(af, aTb, kLDC, 16 * i, 16 * i, lane);
+                frag_b_kn(bf, smem_u32(xs), 24, 0, 0, lane);
+                mma_f16_16816(tacc[0], af, bf[0], bf[1]);
+                mma_f16_16816(tacc[1], af, bf[2], bf[3]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int rr = 16 * i + (lane >> 2), cc2 = 16 * j + nt * 8 + cq;
+                    *reinterpret_cast<uint32_t *>(&sTb[rr * kLDC + cc2]) = pack_f16(-tacc[nt][0], -tacc[nt][1]);
+                    *reinterpret_cast<uint32_t *>(&sTb[(rr + 8) * kLDC + cc2]) = pack_f16(-tacc[nt][2], -tacc[nt][3]);
+                }
+            }
+            __syncthreads();
         }
-        __syncthreads();
     }
-    for (int idx = tid; idx < C * C / 2; idx += kPrepThreads) {
-        const int t = idx / (C / 2), s = 2 * (idx % (C / 2));
-        *reinterpret_cast<uint32_t *>(&sTb[t * kLDC + s]) =
-            pack_f16(sT[t * kLDA + s], sT[t * kLDA + s + 1]);
+
+    // ---- operands beta k e^{a}, beta v (into the region freed by A and the scratch) --
+    {
+        __half *sKtb = reinterpret_cast<__half *>(sG + kGKtb);
+        __half *sVb = reinterpret_cast<__half *>(sG + kGVb);
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+            const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8;
+            float kk[8], vv[8], a[8], o[8];
+            load8(k, tc, t, L, H, h, c0, kk);
+            load8(v, tc, t, L, H, h, c0, vv);
+            lds8(&sAc_[t * 128 + c0], a);
+            const float bt = sBeta[t];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * __expf(a[e]);
+            *reinterpret_cast<uint4 *>(&sKtb[t * kLDK + c0]) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];
+            *reinterpret_cast<uint4 *>(&sVb[t * kLDK + c0]) = pack8_f16(o);
+        }
     }
     __syncthreads();
 
-    // ---- W = T (beta k e^{a}),  U~ = T (beta v) -----------------------------------
+    // ---- W = T (beta k e^{a})  and  U~^T = (beta v)^T T^T -------------------------
     {
+        const uint32_t aKtb = sbase + kOffG + kGKtb, aVb = sbase + kOffG + kGVb;
         const int ti = warp & 3, nh = warp >> 2;
-        const uint32_t aTb = smem_u32(sTb), aKtb = smem_u32(sKtb), aVb = smem_u32(sVb);
-        float wacc[8][4] = {}, uacc[8][4] = {};
+        float wacc[8][4] = {};
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
             if (ks > ti) break;
-            uint32_t a[4];
-            frag_a_rowmajor(a, aTb, kLDC, 16 * ti, 16 * ks, lane);
+            uint32_t af[4];
+            frag_a_rowmajor(af, aTb, kLDC, 16 * ti, 16 * ks, lane);
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
-                uint32_t b[4], bv[4];
-                frag_b_kn(b, aKtb, kLDK, 64 * nh + 16 * np, 16 * ks, lane);
-                mma_f16_16816(wacc[2 * np], a, b[0], b[1]);
-                mma_f16_16816(wacc[2 * np + 1], a, b[2], b[3]);
-                frag_b_kn(bv, aVb, kLDK, 64 * nh + 16 * np, 16 * ks, lane);
-                mma_f16_16816(uacc[2 * np], a, bv[0], bv[1]);
-                mma_f16_16816(uacc[2 * np + 1], a, bv[2], bv[3]);
+                uint32_t bf[4];
+                frag_b_kn(bf, aKtb, kLDK, 64 * nh + 16 * np, 16 * ks, lane);
+                mma_f16_16816(wacc[2 * np], af, bf[0], bf[1]);
+                mma_f16_16816(wacc[2 * np + 1], af, bf[2], bf[3]);
             }
         }
 #pragma unroll
@@ -395,34 +486,57 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             for (int hh = 0; hh < 2; ++hh) {
                 const int t = 16 * ti + (lane >> 2) + 8 * hh;
                 const int col = 64 * nh + nt * 8 + cq;
-                *reinterpret_cast<uint32_t *>(sOut + kB12 + off_k128(64 + t, col)) =
+                *reinterpret_cast<uint32_t *>(blk + kB12 + off_k128(64 + t, col)) =
                     pack_f16(wacc[nt][2 * hh], wacc[nt][2 * hh + 1]);
-                store_h(sOut + kUt, (uint32_t)col * kUtPitch + 2u * t, uacc[nt][2 * hh]);
-                store_h(sOut + kUt, (uint32_t)(col + 1) * kUtPitch + 2u * t, uacc[nt][2 * hh + 1]);
             }
-    }
-    tc::fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-        tc::bulk_s2g(blocks + ((size_t)slot * H + h) * kBlock, smem_u32(sOut), kBlock);
-        tc::bulk_commit();
-        tc::bulk_wait_read();
+        // U~^T rows j in [16 warp, 16 warp + 16), all 64 t; T is lower triangular
+        float uacc[8][4] = {};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            uint32_t af[4];
+            frag_a_colmajor(af, aVb, kLDK, 16 * warp, 16 * ks, lane);
+#pragma unroll
+            for (int np = 0; np < 4; ++np) {
+                if (np < ks) continue;  // T[t][s] = 0 for s > t
+                uint32_t bf[4];
+                frag_b_nk(bf, aTb, kLDC, 16 * np, 16 * ks, lane);
+                mma_f16_16816(uacc[2 * np], af, bf[0], bf[1]);
+                mma_f16_16816(uacc[2 * np + 1], af, bf[2], bf[3]);
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int jj = 16 * warp + (lane >> 2) + 8 * hh;
+                const int t = nt * 8 + cq;
+                *reinterpret_cast<uint32_t *>(blk + kUt + (uint32_t)jj * kUtPitch + 2u * t) =
+                    pack_f16(uacc[nt][2 * hh], uacc[nt][2 * hh + 1]);
+            }
     }
 }
 
 // ============================================================================
 // K2: chunk recurrence on tcgen05
 // ============================================================================
-constexpr int kRecThreads = 128;
+constexpr int kRecThreads = 256;  // warps 0-3: recurrence chain; warps 4-7: state rescale, output
 constexpr uint32_t kOffBuf0 = 0;
 constexpr uint32_t kOffBuf1 = kBlock;
-constexpr uint32_t kOffSA = 2 * kBlock;          // fp16 K-major [j][key]: S^T (A operand)
+constexpr uint32_t kOffSA = 2 * kBlock;              // fp16 K-major [j][key]: S^T (A operand)
 constexpr uint32_t kOffUA = kOffSA + 128 * 128 * 2;  // fp16 K-major [j][t]: U^T (A operand)
-constexpr uint32_t kRecSmem = kOffUA + 128 * 64 * 2;
+constexpr uint32_t kOffO = kOffUA + 128 * 64 * 2;    // bf16 [t][j] output staging
+constexpr uint32_t kRecSmem = kOffO + 64 * 128 * 2;
 static_assert(kRecSmem <= 227 * 1024, "shared memory budget");
-constexpr uint32_t kTmemCols = 256;   // [0,64) O~^T | [64,128) P^T | [128,256) S^T (fp32)
-constexpr uint32_t kColO = 0, kColP = 64, kColS = 128;
-constexpr uint32_t kWaitLimit = 1u << 26;  // bounded mbarrier polls
+// TMEM columns: chunk parity p uses [R_p, R_p + 64) for O~^T and [R_p + 64, R_p + 128)
+// for P^T (R_0 = 0, R_1 = 256); the fp32 state S^T lives in [128, 256).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 128;
+constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s bound on any mbarrier wait
+
+__device__ __forceinline__ uint32_t region_col(int c) { return (c & 1) ? 256u : 0u; }
+__device__ __forceinline__ void named_sync(int id) {
+    asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory");
+}
 
 __global__ void __launch_bounds__(kRecThreads, 1)
     recur_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ first_chunk, int N,
@@ -435,164 +549,107 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (!seq_bounds(cu, n, T, T_total, t0, t1, status)) return;
     const int nchunks = (t1 - t0 + C - 1) / C;
     const int fc = cu ? first_chunk[n] : n * ((T + C - 1) / C);
+    const bool grpA = tid < 128;
+    const int j = tid & 127;  // value column = TMEM lane (warps w and w + 4 share lanes)
 
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t bar_load[2], bar_mma1, bar_mma2;
+    // mbarriers: loads (2), P done, S done, O done (2), state rescaled (128 arrivals),
+    // state read for SA (128), O region consumed (2 x 128)
+    __shared__ __align__(8) uint64_t bars[10];
     __shared__ uint32_t tmem_slot;
+    __shared__ volatile int abort_flag;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t uSA = sbase + kOffSA, uUA = sbase + kOffUA;
-    const uint32_t bl0 = smem_u32(&bar_load[0]), bl1 = smem_u32(&bar_load[1]);
-    const uint32_t bm1 = smem_u32(&bar_mma1), bm2 = smem_u32(&bar_mma2);
+    const uint32_t bL0 = smem_u32(&bars[0]), bL1 = smem_u32(&bars[1]);
+    const uint32_t bP = smem_u32(&bars[2]), bS = smem_u32(&bars[3]);
+    const uint32_t bO0 = smem_u32(&bars[4]), bO1 = smem_u32(&bars[5]);
+    const uint32_t bR = smem_u32(&bars[6]), bSA = smem_u32(&bars[7]);
+    const uint32_t bF0 = smem_u32(&bars[8]), bF1 = smem_u32(&bars[9]);
+    auto bL = [&](int c) { return (c & 1) ? bL1 : bL0; };
+    auto bO = [&](int c) { return (c & 1) ? bO1 : bO0; };
+    auto bF = [&](int c) { return (c & 1) ? bF1 : bF0; };
+    auto buf_off = [](int c) -> uint32_t { return (c & 1) ? kOffBuf1 : kOffBuf0; };
 
     if (warp == 0) {
         tc::tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        tc::mbar_init(bl0, 1);
-        tc::mbar_init(bl1, 1);
-        tc::mbar_init(bm1, 1);
-        tc::mbar_init(bm2, 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(smem_u32(&bars[i]), 1);
+        for (int i = 6; i < 10; ++i) tc::mbar_init(smem_u32(&bars[i]), 128);
+        abort_flag = 0;
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tm = tmem_slot;
-    const uint32_t tlane = tm + ((uint32_t)(32 * warp) << 16);  // this warp's TMEM lanes
-    const int j = tid;                                           // value column = TMEM lane
+    const uint32_t tlane = tm + ((uint32_t)(32 * (warp & 3)) << 16);
 
     const size_t head_state = ((size_t)n * H + h) * 128 * 128;
     const unsigned char *blk0 = blocks + ((size_t)fc * H + h) * kBlock;
     const size_t blk_stride = (size_t)H * kBlock;
 
-    // prologue: first two chunk blocks in flight
-    if (tid == 0) {
-        for (int c = 0; c < 2 && c < nchunks; ++c) {
-            const uint32_t bar = c == 0 ? bl0 : bl1;
-            tc::mbar_arrive_expect_tx(bar, kBlock);
-            tc::bulk_g2s(sbase + (c ? kOffBuf1 : kOffBuf0), blk0 + (size_t)c * blk_stride, kBlock, bar);
-        }
-    }
-    // initial state column j -> TMEM (fp32) and S^T row j -> shared (fp16)
-#pragma unroll 1
-    for (int k0 = 0; k0 < 128; k0 += 16) {
-        float s[16];
+    // Bounded wait; after any timeout every later wait returns at once, so all
+    // threads still pass the same barriers and the kernel ends.
+    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (abort_flag) return false;
+        if (tc::mbar_wait(bar, parity, kWaitLimit)) return true;
+        abort_flag = 1;
+        atomicOr(status, kStatusTimeout);
+        return false;
+    };
+    auto arrive = [&](uint32_t bar) {
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+    };
+    auto issue_load = [&](int c) {
+        tc::mbar_arrive_expect_tx(bL(c), kBlock);
+        tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
+    };
+    // descriptors: no swizzle; +16 in the address field per 256-byte K step
+    const uint64_t dSA = tc::smem_desc(uSA, 128, 2048), dUA = tc::smem_desc(uUA, 128, 1024);
+    const uint32_t id_n128 = tc::idesc_f16(128, 128, 1, 0, 0);
+    const uint32_t id_n64 = tc::idesc_f16(128, 64, 1, 0, 0);
+    auto issue_mma12 = [&](int c) {
+        const uint32_t ub = sbase + buf_off(c) + kB12, rc = tm + region_col(c);
+        const uint64_t dP = tc::smem_desc(ub + 8 * 2048, 128, 2048), dQ = tc::smem_desc(ub, 128, 2048);
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-            s[e] = init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f;
-        tc::tmem_st16(tlane + kColS + k0, s);
-        uint4 pk;
-        pk.x = pack_f16(s[0], s[1]); pk.y = pack_f16(s[2], s[3]);
-        pk.z = pack_f16(s[4], s[5]); pk.w = pack_f16(s[6], s[7]);
-        *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0)) = pk;
-        pk.x = pack_f16(s[8], s[9]); pk.y = pack_f16(s[10], s[11]);
-        pk.z = pack_f16(s[12], s[13]); pk.w = pack_f16(s[14], s[15]);
-        *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0 + 8)) = pk;
-    }
-    tc::tmem_wait_st();
-    tc::fence_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
+        for (int ks = 0; ks < 8; ++ks)  // P^T = S^T W^T
+            tc::mma_f16(rc + 64, dSA + 16 * ks, dP + 16 * ks, id_n64, ks > 0);
+        tc::mma_commit(bP);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)  // O~^T = S^T (q e^a)^T
+            tc::mma_f16(rc, dSA + 16 * ks, dQ + 16 * ks, id_n64, ks > 0);
+    };
+    auto issue_mma23 = [&](int c) {
+        const uint32_t ub = sbase + buf_off(c);
+        const uint64_t d2 = tc::smem_desc(ub + kB2, 128, 1024), d3 = tc::smem_desc(ub + kB3, 128, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // S^T += U^T Kb
+            tc::mma_f16(tm + kColS, dUA + 16 * ks, d2 + 16 * ks, id_n128, 1u);
+        tc::mma_commit(bS);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // O~^T += U^T M^T
+            tc::mma_f16(tm + region_col(c), dUA + 16 * ks, d3 + 16 * ks, id_n64, 1u);
+        tc::mma_commit(bO(c));
+    };
 
-    const uint32_t id12 = tc::idesc_f16(128, 128, 1, 0, 0);
-    const uint32_t id2 = tc::idesc_f16(128, 128, 1, 0, 0);
-    const uint32_t id3 = tc::idesc_f16(128, 64, 1, 0, 0);
-    bool failed = false;
-
-#pragma unroll 1
-    for (int c = 0; c < nchunks; ++c) {
-        const int b = c & 1;
-        const uint32_t bar_l = b ? bl1 : bl0;
-        const unsigned char *buf = smem + (b ? kOffBuf1 : kOffBuf0);
-        const int tc_ = t0 + c * C;
-        const int L = min(C, t1 - tc_);
-
-        bool ok = tc::mbar_wait(bar_l, (uint32_t)((c >> 1) & 1), kWaitLimit);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        tc::fence_after_sync();
-
-        // [O~^T | P^T] = S^T [q e^a ; W]^T
+    if (nchunks == 0) {
+        if (grpA && fin)
+            for (int k0 = 0; k0 < 128; ++k0)
+                fin[head_state + (size_t)k0 * 128 + j] = init ? init[head_state + (size_t)k0 * 128 + j] : 0.f;
+    } else if (grpA) {
+        // ======================= warps 0-3: the recurrence chain =======================
         if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_f16(tm + kColO, tc::smem_desc(uSA + ks * 256, 128, 2048),
-                            tc::smem_desc(sbase + (b ? kOffBuf1 : kOffBuf0) + kB12 + ks * 256, 128, 2048), id12,
-                            ks > 0 ? 1u : 0u);
-            tc::mma_commit(bm1);
+            issue_load(0);
+            if (nchunks > 1) issue_load(1);
         }
-        // meanwhile: S^T <- S^T Diag(e^{a_C}) in TMEM
-        {
-            const float *gam = reinterpret_cast<const float *>(buf + kGam);
 #pragma unroll 1
-            for (int k0 = 0; k0 < 128; k0 += 16) {
-                float s[16];
-                tc::tmem_ld16(tlane + kColS + k0, s);
-                tc::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) s[e] *= gam[k0 + e];
-                tc::tmem_st16(tlane + kColS + k0, s);
-            }
-            tc::tmem_wait_st();
-        }
-        ok = tc::mbar_wait(bm1, (uint32_t)(c & 1), kWaitLimit);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        tc::fence_after_sync();
-
-        // U^T = U~^T - P^T  -> shared (fp16, K-major [j][t])
-        {
-            const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch;
-#pragma unroll 1
-            for (int t0_ = 0; t0_ < 64; t0_ += 16) {
-                float p[16];
-                tc::tmem_ld16(tlane + kColP + t0_, p);
-                const uint4 u0 = *reinterpret_cast<const uint4 *>(ut + 2 * t0_);
-                const uint4 u1 = *reinterpret_cast<const uint4 *>(ut + 2 * t0_ + 16);
-                tc::tmem_wait_ld();
-                const __half2 *h0 = reinterpret_cast<const __half2 *>(&u0);
-                const __half2 *h1 = reinterpret_cast<const __half2 *>(&u1);
-                uint4 pk0, pk1;
-                uint32_t *w0 = reinterpret_cast<uint32_t *>(&pk0);
-                uint32_t *w1 = reinterpret_cast<uint32_t *>(&pk1);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 a = __half22float2(h0[e]);
-                    const float2 bq = __half22float2(h1[e]);
-                    w0[e] = pack_f16(a.x - p[2 * e], a.y - p[2 * e + 1]);
-                    w1[e] = pack_f16(bq.x - p[8 + 2 * e], bq.y - p[8 + 2 * e + 1]);
-                }
-                *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, t0_)) = pk0;
-                *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, t0_ + 8)) = pk1;
-            }
-        }
-        tc::fence_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        tc::fence_after_sync();
-
-        // S^T += U^T Kb ;  O~^T += U^T M^T
-        if (tid == 0) {
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16(tm + kColS, tc::smem_desc(uUA + ks * 256, 128, 1024),
-                            tc::smem_desc(sbase + (b ? kOffBuf1 : kOffBuf0) + kB2 + ks * 256, 128, 1024), id2, 1u);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16(tm + kColO, tc::smem_desc(uUA + ks * 256, 128, 1024),
-                            tc::smem_desc(sbase + (b ? kOffBuf1 : kOffBuf0) + kB3 + ks * 256, 128, 1024), id3, 1u);
-            tc::mma_commit(bm2);
-        }
-        ok = tc::mbar_wait(bm2, (uint32_t)(c & 1), kWaitLimit);
-        if (__syncthreads_or(!ok)) { failed = true; break; }
-        tc::fence_after_sync();
-
-        // S^T (fp32, TMEM) -> fp16 A operand for the next chunk
-#pragma unroll 1
-        for (int k0 = 0; k0 < 128; k0 += 16) {
+        for (int k0 = 0; k0 < 128; k0 += 16) {  // S^T row j (fp16) from the initial state
             float s[16];
-            tc::tmem_ld16(tlane + kColS + k0, s);
-            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                s[e] = init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f;
             uint4 pk;
             pk.x = pack_f16(s[0], s[1]); pk.y = pack_f16(s[2], s[3]);
             pk.z = pack_f16(s[4], s[5]); pk.w = pack_f16(s[6], s[7]);
@@ -601,43 +658,161 @@ __global__ void __launch_bounds__(kRecThreads, 1)
             pk.z = pack_f16(s[12], s[13]); pk.w = pack_f16(s[14], s[15]);
             *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0 + 8)) = pk;
         }
-        // O^T -> out[t][j] (bf16); one 256-byte row per token across the CTA
-#pragma unroll 1
-        for (int o0 = 0; o0 < 64; o0 += 16) {
-            float o[16];
-            tc::tmem_ld16(tlane + kColO + o0, o);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int t = o0 + e;
-                if (t < L) out[((size_t)(tc_ + t) * H + h) * 128 + j] = __float2bfloat16_rn(scale * o[e]);
-            }
-        }
         tc::fence_async_smem();
         tc::fence_before_sync();
-        __syncthreads();
+        named_sync(1);
         tc::fence_after_sync();
-        // buffer b is free again: fetch chunk c + 2 into it
-        if (tid == 0 && c + 2 < nchunks) {
-            tc::mbar_arrive_expect_tx(bar_l, kBlock);
-            tc::bulk_g2s(sbase + (b ? kOffBuf1 : kOffBuf0), blk0 + (size_t)(c + 2) * blk_stride, kBlock, bar_l);
+        if (tid == 0 && wait(bL(0), 0)) issue_mma12(0);
+
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const unsigned char *buf = smem + buf_off(c);
+            // U^T = U~^T - P^T  -> shared (fp16, K-major [j][t])
+            wait(bL(c), (uint32_t)((c >> 1) & 1));
+            wait(bP, (uint32_t)(c & 1));
+            tc::fence_after_sync();
+            {
+                uint32_t pr[4][16];
+                tc::tmem_ld_cols<4>(tlane + region_col(c) + 64, pr);
+                const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch;
+#pragma unroll
+                for (int gi = 0; gi < 8; ++gi) {
+                    const uint4 u = *reinterpret_cast<const uint4 *>(ut + 16 * gi);
+                    const __half2 *hu = reinterpret_cast<const __half2 *>(&u);
+                    uint4 pk;
+                    uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 a = __half22float2(hu[e]);
+                        const int t = 8 * gi + 2 * e;
+                        w[e] = pack_f16(a.x - __uint_as_float(pr[t >> 4][t & 15]),
+                                        a.y - __uint_as_float(pr[(t + 1) >> 4][(t + 1) & 15]));
+                    }
+                    *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, 8 * gi)) = pk;
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            named_sync(1);
+            tc::fence_after_sync();
+            if (tid == 0 && wait(bR, (uint32_t)(c & 1))) {
+                tc::fence_after_sync();
+                issue_mma23(c);
+            }
+            // new state: fp16 copy -> A operand of the next chunk
+            wait(bS, (uint32_t)(c & 1));
+            tc::fence_after_sync();
+            {
+                uint32_t sr[8][16];
+                tc::tmem_ld_cols<8>(tlane + kColS, sr);
+                tc::fence_before_sync();
+                arrive(bSA);  // group B may now overwrite the state with its rescaled copy
+                if (c + 1 < nchunks) {
+#pragma unroll
+                    for (int gi = 0; gi < 16; ++gi) {
+                        const uint32_t *x = &sr[gi >> 1][(gi & 1) * 8];
+                        uint4 pk;
+                        pk.x = pack_f16(__uint_as_float(x[0]), __uint_as_float(x[1]));
+                        pk.y = pack_f16(__uint_as_float(x[2]), __uint_as_float(x[3]));
+                        pk.z = pack_f16(__uint_as_float(x[4]), __uint_as_float(x[5]));
+                        pk.w = pack_f16(__uint_as_float(x[6]), __uint_as_float(x[7]));
+                        *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 8 * gi)) = pk;
+                    }
+                } else if (fin) {
+#pragma unroll
+                    for (int k0 = 0; k0 < 128; ++k0)
+                        fin[head_state + (size_t)k0 * 128 + j] = __uint_as_float(sr[k0 >> 4][k0 & 15]);
+                }
+            }
+            if (c + 1 < nchunks) {
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                named_sync(1);
+                tc::fence_after_sync();
+                if (tid == 0) {
+                    bool ok = wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
+                    if (ok && c + 1 >= 2) ok = wait(bF(c + 1), (uint32_t)(((c - 1) >> 1) & 1));
+                    if (ok) {
+                        tc::fence_after_sync();
+                        issue_mma12(c + 1);
+                    }
+                }
+            }
+        }
+    } else {
+        // ================ warps 4-7: state rescale and the output rows ================
+        // state for chunk 0: Diag(e^{a_C}) S0 -> TMEM
+        if (wait(bL(0), 0)) {
+            const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam);
+#pragma unroll 1
+            for (int k0 = 0; k0 < 128; k0 += 16) {
+                float s[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    s[e] = (init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f) * gam0[k0 + e];
+                tc::tmem_st16(tlane + kColS + k0, s);
+            }
+            tc::tmem_wait_st();
+        }
+        tc::fence_before_sync();
+        arrive(bR);
+#pragma unroll 1
+        for (int c = 0; c < nchunks; ++c) {
+            const int tcc = t0 + c * C, L = min(C, t1 - tcc);
+            if (c + 1 < nchunks) {
+                // Diag(e^{a_C} of chunk c + 1) S_c -> TMEM, once group A has read S_c
+                wait(bS, (uint32_t)(c & 1));
+                tc::fence_after_sync();
+                uint32_t sr[8][16];
+                tc::tmem_ld_cols<8>(tlane + kColS, sr);
+                wait(bSA, (uint32_t)(c & 1));
+                wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
+                tc::fence_after_sync();
+                const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam);
+#pragma unroll
+                for (int gi = 0; gi < 8; ++gi) {
+                    float vv[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) vv[e] = __uint_as_float(sr[gi][e]) * gam[16 * gi + e];
+                    tc::tmem_st16(tlane + kColS + 16 * gi, vv);
+                }
+                tc::tmem_wait_st();
+                tc::fence_before_sync();
+                arrive(bR);
+            }
+            // O^T of chunk c -> out rows, via shared memory (16-byte coalesced stores)
+            wait(bO(c), (uint32_t)((c >> 1) & 1));
+            tc::fence_after_sync();
+            {
+                uint32_t orr[4][16];
+                tc::tmem_ld_cols<4>(tlane + region_col(c), orr);
+                tc::fence_before_sync();
+                arrive(bF(c));  // the O region may be reused two chunks later
+                __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO);
+#pragma unroll
+                for (int t = 0; t < 64; ++t)
+                    sO[t * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[t >> 4][t & 15]));
+                named_sync(2);
+#pragma unroll
+                for (int m = 0; m < 8; ++m) {
+                    const int qd = j + 128 * m, t = qd >> 4, c8 = (qd & 15) * 8;
+                    if (t < L)
+                        *reinterpret_cast<uint4 *>(&out[((size_t)(tcc + t) * H + h) * 128 + c8]) =
+                            *reinterpret_cast<const uint4 *>(&sO[t * 128 + c8]);
+                }
+                named_sync(2);
+            }
+            // buffer of chunk c is no longer read (its MMAs are done): fetch chunk c + 2
+            if (tid == 128 && c + 2 < nchunks && !abort_flag) issue_load(c + 2);
         }
     }
 
-    if (failed) {
-        if (tid == 0) atomicOr(status, kStatusTimeout);
+    if (abort_flag) {
         // let any copy or MMA still in flight land before the TMEM is released
-        tc::mbar_wait(bm1, 0, 1u << 20);
-        tc::mbar_wait(bm2, 0, 1u << 20);
-    } else if (fin) {
-#pragma unroll 1
-        for (int k0 = 0; k0 < 128; k0 += 16) {
-            float s[16];
-            tc::tmem_ld16(tlane + kColS + k0, s);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 16; ++e) fin[head_state + (size_t)(k0 + e) * 128 + j] = s[e];
-        }
+        tc::mbar_wait(bP, 0, 10000000ull);
+        tc::mbar_wait(bS, 0, 10000000ull);
+        tc::mbar_wait(bO0, 0, 10000000ull);
+        tc::mbar_wait(bO1, 0, 10000000ull);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -662,6 +837,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          pf::kPrepSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(pf::prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100);  // two CTAs per SM
+    if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(pf::recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)pf::kRecSmem);
     if (e != cudaSuccess) return e;
@@ -682,7 +860,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         pf::prep_kernel<<<grid, pf::kPrepThreads, pf::kPrepSmem, stream>>>(
             static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
             static_cast<const __nv_bfloat16 *>(v), g, static_cast<const __nv_bfloat16 *>(beta),
-            cu, first_chunk, N, T, H, blocks);
+            cu, first_chunk, N, T, H, blocks, status);
     }
     pf::recur_kernel<<<(unsigned)((long long)N * H), pf::kRecThreads, pf::kRecSmem, stream>>>(
         cu, first_chunk, N, T, T_total, H, scale, init, blocks,

@@ -36,11 +36,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Bounded wait: returns false if the phase did not complete in `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint32_t limit) {
-    for (uint32_t i = 0; i < limit; ++i)
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+// Bounded wait: returns false if the phase did not complete within
+// `limit_ns` nanoseconds (wall clock of the GPU's global timer).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-    return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
 }
 
 // ---- fences -----------------------------------------------------------------
@@ -106,8 +115,9 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
 }
 
 // ---- TMEM -> registers (warp w reads lanes [32 (w % 4), +32)) -------------
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
-    uint32_t r[16];
+// Raw load: the registers are valid only after tmem_wait_ld() followed by
+// reg_fence16() on them (which keeps their uses below the wait).
+__device__ __forceinline__ void tmem_ld16_raw(uint32_t taddr, uint32_t r[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
         "%14,%15}, [%16];\n"
@@ -115,11 +125,33 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void reg_fence16(uint32_t r[16]) {
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
 }
 __device__ __forceinline__ void tmem_wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+// Load 16 columns and wait for them.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16]) {
+    uint32_t r[16];
+    tmem_ld16_raw(taddr, r);
+    tmem_wait_ld();
+    reg_fence16(r);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Load NG groups of 16 columns (starting at taddr) with a single wait.
+template <int NG>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t r[NG][16]) {
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) tmem_ld16_raw(taddr + 16u * gi, r[gi]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) reg_fence16(r[gi]);
 }
 // registers -> TMEM (same lane mapping as tmem_ld16)
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float v[16]) {

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(128, 1)
         }
         mma_commit(smem_u32(&bar));
     }
-    const bool ok = mbar_wait(smem_u32(&bar), 0, 1u << 22);
+    const bool ok = mbar_wait(smem_u32(&bar), 0, 1000000000ull);
     if (!ok && lane == 0) atomicOr(err, 1);
     fence_after_sync();
     if (ok) {
