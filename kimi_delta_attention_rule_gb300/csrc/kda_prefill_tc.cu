@@ -33,16 +33,17 @@
 //                    columns; per chunk: one bulk TMA load of the block
 //                    (double-buffered), three tcgen05.mma groups with fp32
 //                    accumulators in TMEM and the fp32 state resident in TMEM.
-//                    Warps 0-3 run the serial chain (P -> U, state -> fp16
-//                    operand); warps 4-7 rescale the state and write the
-//                    outputs; hand-offs are mbarriers.
+//                    All 8 warps take part in each step (each thread a half
+//                    of its TMEM lane's columns); the state rescale and the
+//                    output rows overlap the next chunk's first product.
 //
 // In K2 everything is transposed so that the TMEM lane is the value column
 // j (128 lanes):
-//   [O~^T | P^T] = S^T [ (q e^a)^T | W^T ]          (M=128, N=128, K=128)
+//   [P^T | O~^T] = S^T [ W ; q e^a ]^T              (M=128, N=128, K=128)
 //   U^T          = U~^T - P^T
-//   S^T          = (S^T Diag(e^{a_C})) + U^T Kb      (M=128, N=128, K=64)
-//   O^T          = O~^T + U^T M^T                    (M=128, N=64,  K=64)
+//   [O^T | S^T] += U^T [ M ; (k e^{a_C - a})^T ]^T   (M=128, N=192, K=64)
+// where the state columns of TMEM were pre-scaled by Diag(e^{a_C}) while the
+// first product ran.
 #include "kda_common.cuh"
 #include "kda_tcgen05.cuh"
 
@@ -52,10 +53,10 @@ namespace pf {
 constexpr int C = 64;
 
 // ---- chunk block written by K1, read by K2 (byte offsets) ------------------
-constexpr uint32_t kB12 = 0;                      // fp16 K-major [n = t' (q~ 0..63 | W 64..127)][k = key]
-constexpr uint32_t kB2 = kB12 + 128 * 128 * 2;    // fp16 K-major [n = key][k = t]: k e^{a_C - a}
-constexpr uint32_t kB3 = kB2 + 128 * 64 * 2;      // fp16 K-major [n = t][k = t']: M
-constexpr uint32_t kUt = kB3 + 64 * 64 * 2;       // fp16 [j][t], pitch 144 B: U~^T
+constexpr uint32_t kB12 = 0;                      // fp16 K-major [n = (W rows 0..63 | q e^a rows 64..127)][k = key]
+constexpr uint32_t kB3 = kB12 + 128 * 128 * 2;    // fp16 K-major [n = t][k = t']: M
+constexpr uint32_t kB2 = kB3 + 64 * 64 * 2;       // fp16 K-major [n = key][k = t]: k e^{a_C - a}
+constexpr uint32_t kUt = kB2 + 128 * 64 * 2;      // fp16 [j][t], pitch 144 B: U~^T
 constexpr uint32_t kUtPitch = 144;
 constexpr uint32_t kGam = kUt + 128 * kUtPitch;   // fp32 [128] e^{a_C}
 constexpr uint32_t kBlock = kGam + 128 * 4;       // 76288 B
@@ -267,7 +268,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             o[e] = qq[e] * __expf(a[e]);
             md += qq[e] * kk[e];
         }
-        *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(t, c0)) = pack8_f16(o);
+        *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(64 + t, c0)) = pack8_f16(o);
 #pragma unroll
         for (int off2 = 8; off2 > 0; off2 >>= 1) md += __shfl_xor_sync(0xffffffffu, md, off2);
         if ((lane & 15) == 0) sMd[t] = md;
@@ -486,7 +487,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
             for (int hh = 0; hh < 2; ++hh) {
                 const int t = 16 * ti + (lane >> 2) + 8 * hh;
                 const int col = 64 * nh + nt * 8 + cq;
-                *reinterpret_cast<uint32_t *>(blk + kB12 + off_k128(64 + t, col)) =
+                *reinterpret_cast<uint32_t *>(blk + kB12 + off_k128(t, col)) =
                     pack_f16(wacc[nt][2 * hh], wacc[nt][2 * hh + 1]);
             }
         // U~^T rows j in [16 warp, 16 warp + 16), all 64 t; T is lower triangular
@@ -519,7 +520,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
 // ============================================================================
 // K2: chunk recurrence on tcgen05
 // ============================================================================
-constexpr int kRecThreads = 256;  // warps 0-3: recurrence chain; warps 4-7: state rescale, output
+constexpr int kRecThreads = 256;  // thread = (value column j, half); all warps on every step
 constexpr uint32_t kOffBuf0 = 0;
 constexpr uint32_t kOffBuf1 = kBlock;
 constexpr uint32_t kOffSA = 2 * kBlock;              // fp16 K-major [j][key]: S^T (A operand)
@@ -527,16 +528,10 @@ constexpr uint32_t kOffUA = kOffSA + 128 * 128 * 2;  // fp16 K-major [j][t]: U^T
 constexpr uint32_t kOffO = kOffUA + 128 * 64 * 2;    // bf16 [t][j] output staging
 constexpr uint32_t kRecSmem = kOffO + 64 * 128 * 2;
 static_assert(kRecSmem <= 227 * 1024, "shared memory budget");
-// TMEM columns: chunk parity p uses [R_p, R_p + 64) for O~^T and [R_p + 64, R_p + 128)
-// for P^T (R_0 = 0, R_1 = 256); the fp32 state S^T lives in [128, 256).
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 128;
+// TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T.
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kColP = 0, kColO = 64, kColS = 128;
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s bound on any mbarrier wait
-
-__device__ __forceinline__ uint32_t region_col(int c) { return (c & 1) ? 256u : 0u; }
-__device__ __forceinline__ void named_sync(int id) {
-    asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory");
-}
 
 __global__ void __launch_bounds__(kRecThreads, 1)
     recur_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ first_chunk, int N,
@@ -549,25 +544,18 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (!seq_bounds(cu, n, T, T_total, t0, t1, status)) return;
     const int nchunks = (t1 - t0 + C - 1) / C;
     const int fc = cu ? first_chunk[n] : n * ((T + C - 1) / C);
-    const bool grpA = tid < 128;
-    const int j = tid & 127;  // value column = TMEM lane (warps w and w + 4 share lanes)
+    const int j = tid & 127;   // value column = TMEM lane (warps w and w + 4 share lanes)
+    const int hf = tid >> 7;   // which half of the columns this thread handles
 
     extern __shared__ __align__(1024) unsigned char smem[];
-    // mbarriers: loads (2), P done, S done, O done (2), state rescaled (128 arrivals),
-    // state read for SA (128), O region consumed (2 x 128)
-    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ __align__(8) uint64_t bars[4];  // loads (2), MMA group 1, MMA group 2
     __shared__ uint32_t tmem_slot;
-    __shared__ volatile int abort_flag;
+    __shared__ int abort_flag;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t uSA = sbase + kOffSA, uUA = sbase + kOffUA;
     const uint32_t bL0 = smem_u32(&bars[0]), bL1 = smem_u32(&bars[1]);
-    const uint32_t bP = smem_u32(&bars[2]), bS = smem_u32(&bars[3]);
-    const uint32_t bO0 = smem_u32(&bars[4]), bO1 = smem_u32(&bars[5]);
-    const uint32_t bR = smem_u32(&bars[6]), bSA = smem_u32(&bars[7]);
-    const uint32_t bF0 = smem_u32(&bars[8]), bF1 = smem_u32(&bars[9]);
+    const uint32_t bM1 = smem_u32(&bars[2]), bM2 = smem_u32(&bars[3]);
     auto bL = [&](int c) { return (c & 1) ? bL1 : bL0; };
-    auto bO = [&](int c) { return (c & 1) ? bO1 : bO0; };
-    auto bF = [&](int c) { return (c & 1) ? bF1 : bF0; };
     auto buf_off = [](int c) -> uint32_t { return (c & 1) ? kOffBuf1 : kOffBuf0; };
 
     if (warp == 0) {
@@ -575,8 +563,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         tc::tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) tc::mbar_init(smem_u32(&bars[i]), 1);
-        for (int i = 6; i < 10; ++i) tc::mbar_init(smem_u32(&bars[i]), 128);
+        for (int i = 0; i < 4; ++i) tc::mbar_init(smem_u32(&bars[i]), 1);
         abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -590,93 +577,92 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     const unsigned char *blk0 = blocks + ((size_t)fc * H + h) * kBlock;
     const size_t blk_stride = (size_t)H * kBlock;
 
-    // Bounded wait; after any timeout every later wait returns at once, so all
-    // threads still pass the same barriers and the kernel ends.
-    auto wait = [&](uint32_t bar, uint32_t parity) -> bool {
-        if (abort_flag) return false;
-        if (tc::mbar_wait(bar, parity, kWaitLimit)) return true;
-        abort_flag = 1;
-        atomicOr(status, kStatusTimeout);
-        return false;
+    // Bounded wait; a timeout is recorded and turns every later wait into a
+    // no-op, so all threads still pass the same barriers and the kernel ends.
+    bool failed = false;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!failed && !tc::mbar_wait(bar, parity, kWaitLimit)) failed = true;
     };
-    auto arrive = [&](uint32_t bar) {
-        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+    auto sync_check = [&]() {  // CTA barrier that also agrees on the failure state
+        tc::fence_before_sync();
+        failed = __syncthreads_or(failed) != 0;
+        tc::fence_after_sync();
     };
     auto issue_load = [&](int c) {
         tc::mbar_arrive_expect_tx(bL(c), kBlock);
         tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
     };
-    // descriptors: no swizzle; +16 in the address field per 256-byte K step
+    // descriptors (no swizzle); +16 in the address field per 256-byte K step
     const uint64_t dSA = tc::smem_desc(uSA, 128, 2048), dUA = tc::smem_desc(uUA, 128, 1024);
     const uint32_t id_n128 = tc::idesc_f16(128, 128, 1, 0, 0);
-    const uint32_t id_n64 = tc::idesc_f16(128, 64, 1, 0, 0);
-    auto issue_mma12 = [&](int c) {
-        const uint32_t ub = sbase + buf_off(c) + kB12, rc = tm + region_col(c);
-        const uint64_t dP = tc::smem_desc(ub + 8 * 2048, 128, 2048), dQ = tc::smem_desc(ub, 128, 2048);
+    const uint32_t id_n192 = tc::idesc_f16(128, 192, 1, 0, 0);
+    auto issue_mma1 = [&](int c) {  // [P^T | O~^T] = S^T [W ; q e^a]^T
+        const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB12, 128, 2048);
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // P^T = S^T W^T
-            tc::mma_f16(rc + 64, dSA + 16 * ks, dP + 16 * ks, id_n64, ks > 0);
-        tc::mma_commit(bP);
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)  // O~^T = S^T (q e^a)^T
-            tc::mma_f16(rc, dSA + 16 * ks, dQ + 16 * ks, id_n64, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_f16(tm + kColP, dSA + 16 * ks, dB + 16 * ks, id_n128, ks > 0);
+        tc::mma_commit(bM1);
     };
-    auto issue_mma23 = [&](int c) {
-        const uint32_t ub = sbase + buf_off(c);
-        const uint64_t d2 = tc::smem_desc(ub + kB2, 128, 1024), d3 = tc::smem_desc(ub + kB3, 128, 1024);
+    auto issue_mma2 = [&](int c) {  // [O^T | S^T] += U^T [M ; Kb^T]^T
+        const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB3, 128, 1024);
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // S^T += U^T Kb
-            tc::mma_f16(tm + kColS, dUA + 16 * ks, d2 + 16 * ks, id_n128, 1u);
-        tc::mma_commit(bS);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // O~^T += U^T M^T
-            tc::mma_f16(tm + region_col(c), dUA + 16 * ks, d3 + 16 * ks, id_n64, 1u);
-        tc::mma_commit(bO(c));
+        for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16(tm + kColO, dUA + 16 * ks, dB + 16 * ks, id_n192, 1u);
+        tc::mma_commit(bM2);
     };
 
     if (nchunks == 0) {
-        if (grpA && fin)
-            for (int k0 = 0; k0 < 128; ++k0)
+        if (fin)
+            for (int k0 = 64 * hf; k0 < 64 * hf + 64; ++k0)
                 fin[head_state + (size_t)k0 * 128 + j] = init ? init[head_state + (size_t)k0 * 128 + j] : 0.f;
-    } else if (grpA) {
-        // ======================= warps 0-3: the recurrence chain =======================
+    } else {
         if (tid == 0) {
             issue_load(0);
             if (nchunks > 1) issue_load(1);
         }
+        // initial state, keys [64 hf, 64 hf + 64) of column j: fp16 copy -> S^T,
+        // and Diag(e^{a_C}) S0 (the first chunk's decay) -> TMEM
+        wait(bL0, 0);
+        {
+            const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam);
 #pragma unroll 1
-        for (int k0 = 0; k0 < 128; k0 += 16) {  // S^T row j (fp16) from the initial state
-            float s[16];
+            for (int k0 = 64 * hf; k0 < 64 * hf + 64; k0 += 16) {
+                float s[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-                s[e] = init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f;
-            uint4 pk;
-            pk.x = pack_f16(s[0], s[1]); pk.y = pack_f16(s[2], s[3]);
-            pk.z = pack_f16(s[4], s[5]); pk.w = pack_f16(s[6], s[7]);
-            *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0)) = pk;
-            pk.x = pack_f16(s[8], s[9]); pk.y = pack_f16(s[10], s[11]);
-            pk.z = pack_f16(s[12], s[13]); pk.w = pack_f16(s[14], s[15]);
-            *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0 + 8)) = pk;
+                for (int e = 0; e < 16; ++e)
+                    s[e] = init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f;
+                uint4 pk;
+                pk.x = pack_f16(s[0], s[1]); pk.y = pack_f16(s[2], s[3]);
+                pk.z = pack_f16(s[4], s[5]); pk.w = pack_f16(s[6], s[7]);
+                *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0)) = pk;
+                pk.x = pack_f16(s[8], s[9]); pk.y = pack_f16(s[10], s[11]);
+                pk.z = pack_f16(s[12], s[13]); pk.w = pack_f16(s[14], s[15]);
+                *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0 + 8)) = pk;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) s[e] *= gam0[k0 + e];
+                tc::tmem_st16(tlane + kColS + k0, s);
+            }
+            tc::tmem_wait_st();
         }
         tc::fence_async_smem();
-        tc::fence_before_sync();
-        named_sync(1);
-        tc::fence_after_sync();
-        if (tid == 0 && wait(bL(0), 0)) issue_mma12(0);
+        sync_check();
+        if (tid == 0 && !failed) issue_mma1(0);
 
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
             const unsigned char *buf = smem + buf_off(c);
-            // U^T = U~^T - P^T  -> shared (fp16, K-major [j][t])
+            const int tcc = t0 + c * C, L = min(C, t1 - tcc);
+
+            // U^T = U~^T - P^T for t in [32 hf, 32 hf + 32) -> shared (fp16)
             wait(bL(c), (uint32_t)((c >> 1) & 1));
-            wait(bP, (uint32_t)(c & 1));
+            wait(bM1, (uint32_t)(c & 1));
             tc::fence_after_sync();
             {
-                uint32_t pr[4][16];
-                tc::tmem_ld_cols<4>(tlane + region_col(c) + 64, pr);
-                const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch;
+                uint32_t pr[2][16];
+                tc::tmem_ld_cols<2>(tlane + kColP + 32 * hf, pr);
+                const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch + 64 * hf;
 #pragma unroll
-                for (int gi = 0; gi < 8; ++gi) {
+                for (int gi = 0; gi < 4; ++gi) {
                     const uint4 u = *reinterpret_cast<const uint4 *>(ut + 16 * gi);
                     const __half2 *hu = reinterpret_cast<const __half2 *>(&u);
                     uint4 pk;
@@ -688,131 +674,75 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                         w[e] = pack_f16(a.x - __uint_as_float(pr[t >> 4][t & 15]),
                                         a.y - __uint_as_float(pr[(t + 1) >> 4][(t + 1) & 15]));
                     }
-                    *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, 8 * gi)) = pk;
+                    *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, 32 * hf + 8 * gi)) = pk;
                 }
             }
             tc::fence_async_smem();
-            tc::fence_before_sync();
-            named_sync(1);
+            sync_check();
+            if (tid == 0 && !failed) issue_mma2(c);
+
+            // new state (keys [64 hf, +64)) and this chunk's O (t in [32 hf, +32))
+            wait(bM2, (uint32_t)(c & 1));
             tc::fence_after_sync();
-            if (tid == 0 && wait(bR, (uint32_t)(c & 1))) {
-                tc::fence_after_sync();
-                issue_mma23(c);
-            }
-            // new state: fp16 copy -> A operand of the next chunk
-            wait(bS, (uint32_t)(c & 1));
-            tc::fence_after_sync();
-            {
-                uint32_t sr[8][16];
-                tc::tmem_ld_cols<8>(tlane + kColS, sr);
-                tc::fence_before_sync();
-                arrive(bSA);  // group B may now overwrite the state with its rescaled copy
-                if (c + 1 < nchunks) {
-#pragma unroll
-                    for (int gi = 0; gi < 16; ++gi) {
-                        const uint32_t *x = &sr[gi >> 1][(gi & 1) * 8];
-                        uint4 pk;
-                        pk.x = pack_f16(__uint_as_float(x[0]), __uint_as_float(x[1]));
-                        pk.y = pack_f16(__uint_as_float(x[2]), __uint_as_float(x[3]));
-                        pk.z = pack_f16(__uint_as_float(x[4]), __uint_as_float(x[5]));
-                        pk.w = pack_f16(__uint_as_float(x[6]), __uint_as_float(x[7]));
-                        *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 8 * gi)) = pk;
-                    }
-                } else if (fin) {
-#pragma unroll
-                    for (int k0 = 0; k0 < 128; ++k0)
-                        fin[head_state + (size_t)k0 * 128 + j] = __uint_as_float(sr[k0 >> 4][k0 & 15]);
-                }
-            }
+            uint32_t sr[4][16], orr[2][16];
+            tc::tmem_ld_cols<4>(tlane + kColS + 64 * hf, sr);
+            tc::tmem_ld_cols<2>(tlane + kColO + 32 * hf, orr);
             if (c + 1 < nchunks) {
-                tc::fence_async_smem();
-                tc::fence_before_sync();
-                named_sync(1);
-                tc::fence_after_sync();
-                if (tid == 0) {
-                    bool ok = wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
-                    if (ok && c + 1 >= 2) ok = wait(bF(c + 1), (uint32_t)(((c - 1) >> 1) & 1));
-                    if (ok) {
-                        tc::fence_after_sync();
-                        issue_mma12(c + 1);
-                    }
-                }
-            }
-        }
-    } else {
-        // ================ warps 4-7: state rescale and the output rows ================
-        // state for chunk 0: Diag(e^{a_C}) S0 -> TMEM
-        if (wait(bL(0), 0)) {
-            const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam);
-#pragma unroll 1
-            for (int k0 = 0; k0 < 128; k0 += 16) {
-                float s[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    s[e] = (init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f) * gam0[k0 + e];
-                tc::tmem_st16(tlane + kColS + k0, s);
-            }
-            tc::tmem_wait_st();
-        }
-        tc::fence_before_sync();
-        arrive(bR);
-#pragma unroll 1
-        for (int c = 0; c < nchunks; ++c) {
-            const int tcc = t0 + c * C, L = min(C, t1 - tcc);
-            if (c + 1 < nchunks) {
-                // Diag(e^{a_C} of chunk c + 1) S_c -> TMEM, once group A has read S_c
-                wait(bS, (uint32_t)(c & 1));
-                tc::fence_after_sync();
-                uint32_t sr[8][16];
-                tc::tmem_ld_cols<8>(tlane + kColS, sr);
-                wait(bSA, (uint32_t)(c & 1));
-                wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
-                tc::fence_after_sync();
-                const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam);
 #pragma unroll
                 for (int gi = 0; gi < 8; ++gi) {
+                    const uint32_t *x = &sr[gi >> 1][(gi & 1) * 8];
+                    uint4 pk;
+                    pk.x = pack_f16(__uint_as_float(x[0]), __uint_as_float(x[1]));
+                    pk.y = pack_f16(__uint_as_float(x[2]), __uint_as_float(x[3]));
+                    pk.z = pack_f16(__uint_as_float(x[4]), __uint_as_float(x[5]));
+                    pk.w = pack_f16(__uint_as_float(x[6]), __uint_as_float(x[7]));
+                    *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 64 * hf + 8 * gi)) = pk;
+                }
+            } else if (fin) {
+#pragma unroll
+                for (int e = 0; e < 64; ++e)
+                    fin[head_state + (size_t)(64 * hf + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
+            }
+            // this chunk's buffer is no longer read: fetch chunk c + 2 into it
+            if (tid == 0 && c + 2 < nchunks && !failed) issue_load(c + 2);
+            if (c + 1 < nchunks) wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
+            tc::fence_async_smem();
+            sync_check();
+            if (tid == 0 && c + 1 < nchunks && !failed) issue_mma1(c + 1);
+
+            // while the next product runs: pre-scale the state by the next chunk's
+            // decay, and write this chunk's output rows
+            if (c + 1 < nchunks) {
+                const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam) + 64 * hf;
+#pragma unroll
+                for (int gi = 0; gi < 4; ++gi) {
                     float vv[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) vv[e] = __uint_as_float(sr[gi][e]) * gam[16 * gi + e];
-                    tc::tmem_st16(tlane + kColS + 16 * gi, vv);
+                    tc::tmem_st16(tlane + kColS + 64 * hf + 16 * gi, vv);
                 }
                 tc::tmem_wait_st();
-                tc::fence_before_sync();
-                arrive(bR);
             }
-            // O^T of chunk c -> out rows, via shared memory (16-byte coalesced stores)
-            wait(bO(c), (uint32_t)((c >> 1) & 1));
-            tc::fence_after_sync();
-            {
-                uint32_t orr[4][16];
-                tc::tmem_ld_cols<4>(tlane + region_col(c), orr);
-                tc::fence_before_sync();
-                arrive(bF(c));  // the O region may be reused two chunks later
-                __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO);
+            __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO);
 #pragma unroll
-                for (int t = 0; t < 64; ++t)
-                    sO[t * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[t >> 4][t & 15]));
-                named_sync(2);
+            for (int e = 0; e < 32; ++e)
+                sO[(32 * hf + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[e >> 4][e & 15]));
+            __syncthreads();
 #pragma unroll
-                for (int m = 0; m < 8; ++m) {
-                    const int qd = j + 128 * m, t = qd >> 4, c8 = (qd & 15) * 8;
-                    if (t < L)
-                        *reinterpret_cast<uint4 *>(&out[((size_t)(tcc + t) * H + h) * 128 + c8]) =
-                            *reinterpret_cast<const uint4 *>(&sO[t * 128 + c8]);
-                }
-                named_sync(2);
+            for (int m = 0; m < 4; ++m) {
+                const int qd = tid + kRecThreads * m, t = qd >> 4, c8 = (qd & 15) * 8;
+                if (t < L)
+                    *reinterpret_cast<uint4 *>(&out[((size_t)(tcc + t) * H + h) * 128 + c8]) =
+                        *reinterpret_cast<const uint4 *>(&sO[t * 128 + c8]);
             }
-            // buffer of chunk c is no longer read (its MMAs are done): fetch chunk c + 2
-            if (tid == 128 && c + 2 < nchunks && !abort_flag) issue_load(c + 2);
         }
     }
 
-    if (abort_flag) {
+    if (failed) {
+        if (tid == 0) atomicOr(status, kStatusTimeout);
         // let any copy or MMA still in flight land before the TMEM is released
-        tc::mbar_wait(bP, 0, 10000000ull);
-        tc::mbar_wait(bS, 0, 10000000ull);
-        tc::mbar_wait(bO0, 0, 10000000ull);
-        tc::mbar_wait(bO1, 0, 10000000ull);
+        tc::mbar_wait(bM1, 0, 10000000ull);
+        tc::mbar_wait(bM2, 0, 10000000ull);
     }
     tc::fence_before_sync();
     __syncthreads();
