@@ -28,7 +28,6 @@
 //   schedule_kernel  first chunk index of each packed sequence
 //   prep_kernel      K1: one CTA per (chunk, head); writes a 76 KiB chunk
 //                    block in the exact shared-memory layout K2 consumes
-//                    (one bulk TMA store)
 //   recur_kernel     K2: one CTA per (sequence, head), all 128 value
 //                    columns; per chunk: one bulk TMA load of the block
 //                    (double-buffered), three tcgen05.mma groups with fp32
@@ -108,34 +107,35 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
 // ============================================================================
 // K1: chunk preparation
 // ============================================================================
-// One CTA (8 warps) per (chunk, head), two CTAs per SM. The cumulative decay
-// a of the chunk is kept in shared memory; q, k, v are read with coalesced
-// 16-byte loads where they are used; every output goes straight to the
-// chunk block in global memory, already in the core-matrix layout K2 reads.
-constexpr int kPrepThreads = 256;
+// One CTA (16 warps) per (chunk, head). One pass over the chunk's tokens
+// builds every operand (q, k, v read once with 16-byte loads); every output
+// goes straight to the chunk block in global memory, already in the
+// core-matrix layout K2 reads.
+constexpr int kPrepThreads = 512;
+constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kLDK = 136;  // bf16/fp16 pitch of 128-wide tiles (conflict-free ldmatrix)
 constexpr int kLDC = 72;   // fp16 pitch of C x C tiles
 constexpr int kLDA = 68;   // fp32 pitch of C x C matrices
 constexpr int kOffAcum = 0;                          // fp32 [64][128] a
 constexpr int kOffRef = kOffAcum + C * 128 * 4;      // fp32 [4][128] r_i
-constexpr int kOffEr = kOffRef + 4 * 128 * 4;        // fp32 [4][128] e^{r_i}
-constexpr int kOffAc = kOffEr + 4 * 128 * 4;         // fp32 [128] a_C
-constexpr int kOffHalf = kOffAc + 128 * 4;           // fp32 [128] a at token 31
-constexpr int kOffBeta = kOffHalf + 128 * 4;         // fp32 [64]
+constexpr int kOffQsum = kOffRef + 4 * 128 * 4;      // fp32 [4][128] sum of g per tile
+constexpr int kOffAc = kOffQsum + 4 * 128 * 4;       // fp32 [128] a_C
+constexpr int kOffBeta = kOffAc + 128 * 4;           // fp32 [64]
 constexpr int kOffMd = kOffBeta + C * 4;             // fp32 [64] q_t . k_t
 constexpr int kOffA = kOffMd + C * 4;                // fp32 [64][68] A
-constexpr int kOffG = kOffA + C * kLDA * 4;          // phase-dependent region:
-//   Gram:  Xq16 bf16 [16][136] | Xk16 bf16 [16][136] | Kh bf16 [64][136]
-//   T:     Tb fp16 [64][72] | Ah fp16 [64][72] | Xh fp16 [3][16][24]
-//   W, U~: Tb fp16 [64][72] | Ktb fp16 [64][136] | Vb fp16 [64][136]
-constexpr int kGXq = 0, kGXk = kGXq + 16 * kLDK * 2, kGKh = kGXk + 16 * kLDK * 2;
-constexpr int kGTb = 0, kGAh = kGTb + C * kLDC * 2, kGXh = kGAh + C * kLDC * 2;
-constexpr int kGKtb = kGTb + C * kLDC * 2, kGVb = kGKtb + C * kLDK * 2;
-constexpr int kGBytes = kGVb + C * kLDK * 2;
-static_assert(kGKh + C * kLDK * 2 <= kGBytes, "Gram operands fit the region");
-static_assert(kGXh + 3 * 16 * 24 * 2 <= kGBytes, "T scratch fits the region");
-constexpr int kPrepSmem = kOffG + kGBytes;
-static_assert(2 * (kPrepSmem + 1024) <= 228 * 1024, "two CTAs per SM");
+constexpr int kOffXq = kOffA + C * kLDA * 4;         // bf16 [64][136] q e^{a - r_i}
+constexpr int kOffXk = kOffXq + C * kLDK * 2;        // bf16 [64][136] k e^{a - r_i}
+constexpr int kOffKh = kOffXk + C * kLDK * 2;        // bf16 [160][136] k e^{r_i - a}, 10 tiles
+constexpr int kOffKtb = kOffKh + 160 * kLDK * 2;     // fp16 [64][136] beta k e^{a}
+constexpr int kOffVb = kOffKtb + C * kLDK * 2;       // fp16 [64][136] beta v
+constexpr int kOffKbS = kOffVb + C * kLDK * 2;       // fp16 [64][136] k e^{a_C - a} (transpose staging)
+constexpr int kPrepSmem = kOffKbS + C * kLDK * 2;
+// after the Gram phase, inside the Xq / Xk region:
+constexpr int kOffTb = kOffXq;                       // fp16 [64][72] T
+constexpr int kOffAh = kOffTb + C * kLDC * 2;        // fp16 [64][72] A
+constexpr int kOffXh = kOffAh + C * kLDC * 2;        // fp16 [3][16][24] level scratch
+static_assert(kOffXh + 3 * 16 * 24 * 2 <= kOffKh, "T scratch inside the row-operand region");
+static_assert(kPrepSmem <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ int kh_slot(int i, int j) { return (i * (i + 1)) / 2 + j; }
 
@@ -182,19 +182,12 @@ __device__ __forceinline__ void unpack8_bf16(uint4 u, float *x) {
         x[2 * e + 1] = __high2float(h[e]);
     }
 }
-// 8 consecutive channels of row t (zeros for padding rows)
-__device__ __forceinline__ void load8(const __nv_bfloat16 *__restrict__ p, int tc, int t, int L,
-                                      int H, int h, int c0, float *x) {
-    uint4 u = make_uint4(0, 0, 0, 0);
-    if (t < L) u = __ldg(reinterpret_cast<const uint4 *>(p + ((size_t)(tc + t) * H + h) * 128 + c0));
-    unpack8_bf16(u, x);
-}
 __device__ __forceinline__ void lds8(const float *s, float *x) {
     *reinterpret_cast<float4 *>(x) = *reinterpret_cast<const float4 *>(s);
     *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(s + 4);
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 2)
+__global__ void __launch_bounds__(kPrepThreads, 1)
     prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
                 const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu,
@@ -211,155 +204,172 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cq = 2 * (lane & 3);
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
+    const size_t row0 = (size_t)tc * H + h;  // row index of token tc, head h
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t sbase = smem_u32(smem);
-    float *sAc_ = reinterpret_cast<float *>(smem + kOffAcum);
+    float *sAcum = reinterpret_cast<float *>(smem + kOffAcum);
     float *sRef = reinterpret_cast<float *>(smem + kOffRef);
-    float *sEr = reinterpret_cast<float *>(smem + kOffEr);
+    float *sQsum = reinterpret_cast<float *>(smem + kOffQsum);
     float *sAcT = reinterpret_cast<float *>(smem + kOffAc);
-    float *sHalf = reinterpret_cast<float *>(smem + kOffHalf);
     float *sBeta = reinterpret_cast<float *>(smem + kOffBeta);
     float *sMd = reinterpret_cast<float *>(smem + kOffMd);
     float *sA = reinterpret_cast<float *>(smem + kOffA);
-    unsigned char *sG = smem + kOffG;
 
-    // ---- cumulative decay: thread = (channel, half of the chunk) ---------------------
-    if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(size_t)(tc + tid) * H + h]) : 0.f;
+    // ---- cumulative decay: thread = (channel, 16-token tile) --------------------------
+    if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(row0 + (size_t)tid * H)]) : 0.f;
     {
-        const int ch = tid & 127, hf = tid >> 7;
-        float a[32];
+        const int ch = tid & 127, i = tid >> 7;
+        float a[16];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-            const int t = 32 * hf + r;
-            a[r] = t < L ? clamp_g(__ldg(&g[((size_t)(tc + t) * H + h) * 128 + ch])) : 0.f;
+        for (int r = 0; r < 16; ++r) {
+            const int t = 16 * i + r;
+            a[r] = t < L ? clamp_g(__ldg(&g[(row0 + (size_t)t * H) * 128 + ch])) : 0.f;
         }
 #pragma unroll
-        for (int r = 1; r < 32; ++r) a[r] += a[r - 1];
-        if (hf == 0) sHalf[ch] = a[31];
+        for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
+        sQsum[i * 128 + ch] = a[15];
         __syncthreads();
-        const float off = hf ? sHalf[ch] : 0.f;
+        float off = 0.f;
+        for (int i2 = 0; i2 < i; ++i2) off += sQsum[i2 * 128 + ch];
+        sRef[i * 128 + ch] = off;  // cumulative decay just before tile i
 #pragma unroll
-        for (int r = 0; r < 32; ++r) sAc_[(32 * hf + r) * 128 + ch] = a[r] + off;
-        // references: exclusive prefix at tiles 2 hf and 2 hf + 1
-        const float r0 = off, r1 = a[15] + off;
-        sRef[(2 * hf) * 128 + ch] = r0;
-        sRef[(2 * hf + 1) * 128 + ch] = r1;
-        sEr[(2 * hf) * 128 + ch] = __expf(r0);
-        sEr[(2 * hf + 1) * 128 + ch] = __expf(r1);
-        if (hf == 1) {
-            sAcT[ch] = a[31] + off;
-            reinterpret_cast<float *>(blk + kGam)[ch] = __expf(a[31] + off);
+        for (int r = 0; r < 16; ++r) sAcum[(16 * i + r) * 128 + ch] = a[r] + off;
+        if (i == 3) {
+            sAcT[ch] = a[15] + off;
+            reinterpret_cast<float *>(blk + kGam)[ch] = __expf(a[15] + off);
         }
     }
     __syncthreads();
 
-    // ---- q e^{a} -> block; diagonal of M (q_t . k_t, no decay) -------------------
+    // ---- all operands, one item = (token t, 8 key channels) ---------------------------
+    {
+        __nv_bfloat16 *sXq = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXq);
+        __nv_bfloat16 *sXk = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXk);
+        __nv_bfloat16 *sKh = reinterpret_cast<__nv_bfloat16 *>(smem + kOffKh);
+        __half *sKtb = reinterpret_cast<__half *>(smem + kOffKtb);
+        __half *sVb = reinterpret_cast<__half *>(smem + kOffVb);
+        __half *sKbS = reinterpret_cast<__half *>(smem + kOffKbS);
 #pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-        const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8;
-        float qq[8], kk[8], a[8], o[8];
-        load8(q, tc, t, L, H, h, c0, qq);
-        load8(k, tc, t, L, H, h, c0, kk);
-        lds8(&sAc_[t * 128 + c0], a);
-        float md = 0.f;
+        for (int m = 0; m < 2; ++m) {
+            const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8, i = t >> 4;
+            float qq[8], kk[8], vv[8], a[8], r[8], ac[8];
+            uint4 uq = make_uint4(0, 0, 0, 0), uk = uq, uv = uq;
+            if (t < L) {
+                const size_t off = (row0 + (size_t)t * H) * 128 + c0;
+                uq = __ldg(reinterpret_cast<const uint4 *>(q + off));
+                uk = __ldg(reinterpret_cast<const uint4 *>(k + off));
+                uv = __ldg(reinterpret_cast<const uint4 *>(v + off));
+            }
+            unpack8_bf16(uq, qq);
+            unpack8_bf16(uk, kk);
+            unpack8_bf16(uv, vv);
+            lds8(&sAcum[t * 128 + c0], a);
+            lds8(&sRef[i * 128 + c0], r);
+            lds8(&sAcT[c0], ac);
+            const float bt = sBeta[t];
+            float x[8], ix[8], o[8], md = 0.f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            o[e] = qq[e] * __expf(a[e]);
-            md += qq[e] * kk[e];
+            for (int e = 0; e < 8; ++e) {
+                const float p = a[e] - r[e];  // a_t - r_i in [-80, 0]
+                x[e] = __expf(p);
+                ix[e] = __expf(-p);
+                md += qq[e] * kk[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = qq[e] * x[e];
+            *reinterpret_cast<uint4 *>(&sXq[t * kLDK + c0]) = pack8_bf16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = kk[e] * x[e];
+            *reinterpret_cast<uint4 *>(&sXk[t * kLDK + c0]) = pack8_bf16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = kk[e] * ix[e];
+            *reinterpret_cast<uint4 *>(&sKh[(kh_slot(i, i) * 16 + (t & 15)) * kLDK + c0]) = pack8_bf16(o);
+#pragma unroll 1
+            for (int i2 = i + 1; i2 < 4; ++i2) {
+                float r2[8];
+                lds8(&sRef[i2 * 128 + c0], r2);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = kk[e] * __expf(r2[e] - a[e]);  // <= 1
+                *reinterpret_cast<uint4 *>(&sKh[(kh_slot(i2, i) * 16 + (t & 15)) * kLDK + c0]) =
+                    pack8_bf16(o);
+            }
+            float ea[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ea[e] = __expf(a[e]);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = qq[e] * ea[e];                    // q e^{a}
+            *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(64 + t, c0)) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * ea[e];               // beta k e^{a}
+            *reinterpret_cast<uint4 *>(&sKtb[t * kLDK + c0]) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                       // beta v
+            *reinterpret_cast<uint4 *>(&sVb[t * kLDK + c0]) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = kk[e] * __expf(ac[e] - a[e]);     // k e^{a_C - a}
+            *reinterpret_cast<uint4 *>(&sKbS[t * kLDK + c0]) = pack8_f16(o);
+            // q_t . k_t (the diagonal of M: no decay) over the 16 lanes of token t
+#pragma unroll
+            for (int o2 = 8; o2 > 0; o2 >>= 1) md += __shfl_xor_sync(0xffffffffu, md, o2);
+            if ((lane & 15) == 0) sMd[t] = md;
         }
-        *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(64 + t, c0)) = pack8_f16(o);
-#pragma unroll
-        for (int off2 = 8; off2 > 0; off2 >>= 1) md += __shfl_xor_sync(0xffffffffu, md, off2);
-        if ((lane & 15) == 0) sMd[t] = md;
     }
-    // ---- (k e^{a_C - a})^T -> block: item = (key channel, 8 tokens) ----------------
+    __syncthreads();
+
+    // ---- (k e^{a_C - a})^T -> block: item = (key channel, 8 tokens) -----------------
+    {
+        const __half *sKbS = reinterpret_cast<const __half *>(smem + kOffKbS);
 #pragma unroll 1
-    for (int m = 0; m < 4; ++m) {
-        const int id = tid + kPrepThreads * m, key = id & 127, tg = id >> 7;
-        const float ac = sAcT[key];
-        float o[8];
+        for (int m = 0; m < 2; ++m) {
+            const int id = tid + kPrepThreads * m, key = id & 127, tg = id >> 7;
+            uint4 pk;
+            uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int t = 8 * tg + e;
-            const float kv = t < L ? __bfloat162float(__ldg(&k[((size_t)(tc + t) * H + h) * 128 + key])) : 0.f;
-            o[e] = kv * __expf(ac - sAc_[t * 128 + key]);
+            for (int e = 0; e < 4; ++e) {
+                const __half lo = sKbS[(8 * tg + 2 * e) * kLDK + key];
+                const __half hi = sKbS[(8 * tg + 2 * e + 1) * kLDK + key];
+                w[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+            }
+            *reinterpret_cast<uint4 *>(blk + kB2 + off_k64(key, 8 * tg)) = pk;
         }
-        *reinterpret_cast<uint4 *>(blk + kB2 + off_k64(key, 8 * tg)) = pack8_f16(o);
     }
 
-    // ---- Gram matrices, one row tile (reference r_i) at a time -------------------------
+    // ---- Gram matrices A (beta, strictly lower) and M (lower) -------------------
     {
-        __nv_bfloat16 *sXq = reinterpret_cast<__nv_bfloat16 *>(sG + kGXq);
-        __nv_bfloat16 *sXk = reinterpret_cast<__nv_bfloat16 *>(sG + kGXk);
-        __nv_bfloat16 *sKh = reinterpret_cast<__nv_bfloat16 *>(sG + kGKh);
-        const uint32_t aXq = sbase + kOffG + kGXq, aXk = sbase + kOffG + kGXk;
-        const uint32_t aKh = sbase + kOffG + kGKh;
-#pragma unroll 1
-        for (int i = 0; i < 4; ++i) {
-            __syncthreads();  // previous round's operands fully consumed
-            // row operands (tile i) and column operands (tokens 0 .. 16 i + 15)
-            const int nitems = 16 * 16 + 16 * (i + 1) * 16;
-            for (int id = tid; id < nitems; id += kPrepThreads) {
-                float r[8], a[8], x[8], o[8];
-                if (id < 256) {
-                    const int rr = id >> 4, c0 = (id & 15) * 8, t = 16 * i + rr;
-                    float qq[8], kk[8];
-                    load8(q, tc, t, L, H, h, c0, qq);
-                    load8(k, tc, t, L, H, h, c0, kk);
-                    lds8(&sRef[i * 128 + c0], r);
-                    lds8(&sAc_[t * 128 + c0], a);
+        const uint32_t aXq = sbase + kOffXq, aXk = sbase + kOffXk, aKh = sbase + kOffKh;
+        for (int task = warp; task < 20; task += kPrepWarps) {
+            const int mm = task / 10;
+            int tt = task % 10, i = 0;
+            while (tt > i) { tt -= i + 1; ++i; }
+            const int j = tt;
+            float acc[2][4] = {};
+            const uint32_t aX = mm == 0 ? aXk : aXq;
+            const uint32_t aB = aKh + (uint32_t)(kh_slot(i, j) * 16 * kLDK) * 2u;
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = __expf(a[e] - r[e]);  // <= 1
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = qq[e] * x[e];
-                    *reinterpret_cast<uint4 *>(&sXq[rr * kLDK + c0]) = pack8_bf16(o);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = kk[e] * x[e];
-                    *reinterpret_cast<uint4 *>(&sXk[rr * kLDK + c0]) = pack8_bf16(o);
-                } else {
-                    const int i2 = id - 256, s = i2 >> 4, c0 = (i2 & 15) * 8;
-                    float kk[8];
-                    load8(k, tc, s, L, H, h, c0, kk);
-                    lds8(&sRef[i * 128 + c0], r);
-                    lds8(&sAc_[s * 128 + c0], a);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = kk[e] * __expf(r[e] - a[e]);  // <= e^80
-                    *reinterpret_cast<uint4 *>(&sKh[s * kLDK + c0]) = pack8_bf16(o);
-                }
+            for (int ks = 0; ks < 8; ++ks) {
+                uint32_t af[4], bf[4];
+                frag_a_rowmajor(af, aX, kLDK, 16 * i, 16 * ks, lane);
+                frag_b_nk(bf, aB, kLDK, 0, 16 * ks, lane);
+                mma_bf16_16816(acc[0], af, bf[0], bf[1]);
+                mma_bf16_16816(acc[1], af, bf[2], bf[3]);
             }
-            __syncthreads();
-            // tasks: (matrix A or M, column tile j <= i)
-            for (int task = warp; task < 2 * (i + 1); task += kPrepThreads / 32) {
-                const int mm = task & 1, j = task >> 1;
-                float acc[2][4] = {};
-                const uint32_t aX = mm == 0 ? aXk : aXq;
-                const uint32_t aB = aKh + (uint32_t)(16 * j * kLDK) * 2u;
 #pragma unroll
-                for (int ks = 0; ks < 8; ++ks) {
-                    uint32_t af[4], bf[4];
-                    frag_a_rowmajor(af, aX, kLDK, 0, 16 * ks, lane);
-                    frag_b_nk(bf, aB, kLDK, 0, 16 * ks, lane);
-                    mma_bf16_16816(acc[0], af, bf[0], bf[1]);
-                    mma_bf16_16816(acc[1], af, bf[2], bf[3]);
-                }
+            for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int t = 16 * i + (lane >> 2) + 8 * hh;
-                        const int s = 16 * j + nt * 8 + cq;
-                        float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
-                        if (mm == 0) {
-                            sA[t * kLDA + s] = s < t ? sBeta[t] * v0 : 0.f;
-                            sA[t * kLDA + s + 1] = s + 1 < t ? sBeta[t] * v1 : 0.f;
-                        } else {
-                            v0 = s < t ? v0 : (s == t ? sMd[t] : 0.f);
-                            v1 = s + 1 < t ? v1 : (s + 1 == t ? sMd[t] : 0.f);
-                            *reinterpret_cast<uint32_t *>(blk + kB3 + off_k64(t, s)) = pack_f16(v0, v1);
-                        }
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = 16 * i + (lane >> 2) + 8 * hh;
+                    const int s = 16 * j + nt * 8 + cq;
+                    float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
+                    if (mm == 0) {
+                        sA[t * kLDA + s] = s < t ? sBeta[t] * v0 : 0.f;
+                        sA[t * kLDA + s + 1] = s + 1 < t ? sBeta[t] * v1 : 0.f;
+                    } else {
+                        v0 = s < t ? v0 : (s == t ? sMd[t] : 0.f);
+                        v1 = s + 1 < t ? v1 : (s + 1 == t ? sMd[t] : 0.f);
+                        *reinterpret_cast<uint32_t *>(blk + kB3 + off_k64(t, s)) = pack_f16(v0, v1);
                     }
-            }
+                }
         }
         // blocks above the diagonal: zero in A (shared) and in M (the block)
         for (int idx = tid; idx < 6 * 128; idx += kPrepThreads) {
@@ -375,9 +385,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     __syncthreads();
 
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
-    __half *sAh = reinterpret_cast<__half *>(sG + kGAh);
-    __half *sTb = reinterpret_cast<__half *>(sG + kGTb);
-    const uint32_t aTb = sbase + kOffG + kGTb;
+    __half *sAh = reinterpret_cast<__half *>(smem + kOffAh);
+    __half *sTb = reinterpret_cast<__half *>(smem + kOffTb);
+    const uint32_t aTb = sbase + kOffTb;
     if (tid < 64) {
         const int b = tid >> 4, cc = tid & 15;
         float x[16];
@@ -401,8 +411,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
     __syncthreads();
     {
         // level d: T_ij = -T_ii * sum_{kk = 16j}^{16i - 1} A[16i.., kk] T[kk, 16j..]
-        const uint32_t aAh = sbase + kOffG + kGAh;
-        __half *sXh = reinterpret_cast<__half *>(sG + kGXh);
+        const uint32_t aAh = sbase + kOffAh;
+        __half *sXh = reinterpret_cast<__half *>(smem + kOffXh);
 #pragma unroll 1
         for (int d = 1; d < 4; ++d) {
             if (warp < 4 - d) {
@@ -441,79 +451,63 @@ __global__ void __launch_bounds__(kPrepThreads, 2)
         }
     }
 
-    // ---- operands beta k e^{a}, beta v (into the region freed by A and the scratch) --
-    {
-        __half *sKtb = reinterpret_cast<__half *>(sG + kGKtb);
-        __half *sVb = reinterpret_cast<__half *>(sG + kGVb);
-#pragma unroll 1
-        for (int m = 0; m < 4; ++m) {
-            const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8;
-            float kk[8], vv[8], a[8], o[8];
-            load8(k, tc, t, L, H, h, c0, kk);
-            load8(v, tc, t, L, H, h, c0, vv);
-            lds8(&sAc_[t * 128 + c0], a);
-            const float bt = sBeta[t];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * __expf(a[e]);
-            *reinterpret_cast<uint4 *>(&sKtb[t * kLDK + c0]) = pack8_f16(o);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];
-            *reinterpret_cast<uint4 *>(&sVb[t * kLDK + c0]) = pack8_f16(o);
-        }
-    }
-    __syncthreads();
-
     // ---- W = T (beta k e^{a})  and  U~^T = (beta v)^T T^T -------------------------
     {
-        const uint32_t aKtb = sbase + kOffG + kGKtb, aVb = sbase + kOffG + kGVb;
-        const int ti = warp & 3, nh = warp >> 2;
-        float wacc[8][4] = {};
+        const uint32_t aKtb = sbase + kOffKtb, aVb = sbase + kOffVb;
+        {   // W: warp = (row tile ti, 32 key columns)
+            const int ti = warp & 3, nq = warp >> 2;
+            float wacc[4][4] = {};
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            if (ks > ti) break;
-            uint32_t af[4];
-            frag_a_rowmajor(af, aTb, kLDC, 16 * ti, 16 * ks, lane);
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks > ti) break;
+                uint32_t af[4];
+                frag_a_rowmajor(af, aTb, kLDC, 16 * ti, 16 * ks, lane);
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t bf[4];
-                frag_b_kn(bf, aKtb, kLDK, 64 * nh + 16 * np, 16 * ks, lane);
-                mma_f16_16816(wacc[2 * np], af, bf[0], bf[1]);
-                mma_f16_16816(wacc[2 * np + 1], af, bf[2], bf[3]);
+                for (int np = 0; np < 2; ++np) {
+                    uint32_t bf[4];
+                    frag_b_kn(bf, aKtb, kLDK, 32 * nq + 16 * np, 16 * ks, lane);
+                    mma_f16_16816(wacc[2 * np], af, bf[0], bf[1]);
+                    mma_f16_16816(wacc[2 * np + 1], af, bf[2], bf[3]);
+                }
             }
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = 16 * ti + (lane >> 2) + 8 * hh;
+                    const int col = 32 * nq + nt * 8 + cq;
+                    *reinterpret_cast<uint32_t *>(blk + kB12 + off_k128(t, col)) =
+                        pack_f16(wacc[nt][2 * hh], wacc[nt][2 * hh + 1]);
+                }
         }
+        {   // U~^T: warp = (16 value rows, 32 tokens); T is lower triangular
+            const int jt = warp & 7, th = warp >> 3;
+            float uacc[4][4] = {};
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+            for (int ks = 0; ks < 4; ++ks) {
+                if (ks > 2 * th + 1) break;  // T[t][s] = 0 for s > t
+                uint32_t af[4];
+                frag_a_colmajor(af, aVb, kLDK, 16 * jt, 16 * ks, lane);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int t = 16 * ti + (lane >> 2) + 8 * hh;
-                const int col = 64 * nh + nt * 8 + cq;
-                *reinterpret_cast<uint32_t *>(blk + kB12 + off_k128(t, col)) =
-                    pack_f16(wacc[nt][2 * hh], wacc[nt][2 * hh + 1]);
+                for (int np = 0; np < 2; ++np) {
+                    const int tt16 = 2 * th + np;  // token tile of these two n8 tiles
+                    if (tt16 < ks) continue;
+                    uint32_t bf[4];
+                    frag_b_nk(bf, aTb, kLDC, 16 * tt16, 16 * ks, lane);
+                    mma_f16_16816(uacc[2 * np], af, bf[0], bf[1]);
+                    mma_f16_16816(uacc[2 * np + 1], af, bf[2], bf[3]);
+                }
             }
-        // U~^T rows j in [16 warp, 16 warp + 16), all 64 t; T is lower triangular
-        float uacc[8][4] = {};
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-            uint32_t af[4];
-            frag_a_colmajor(af, aVb, kLDK, 16 * warp, 16 * ks, lane);
+            for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                if (np < ks) continue;  // T[t][s] = 0 for s > t
-                uint32_t bf[4];
-                frag_b_nk(bf, aTb, kLDC, 16 * np, 16 * ks, lane);
-                mma_f16_16816(uacc[2 * np], af, bf[0], bf[1]);
-                mma_f16_16816(uacc[2 * np + 1], af, bf[2], bf[3]);
-            }
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int jj = 16 * jt + (lane >> 2) + 8 * hh;
+                    const int t = 32 * th + nt * 8 + cq;
+                    *reinterpret_cast<uint32_t *>(blk + kUt + (uint32_t)jj * kUtPitch + 2u * t) =
+                        pack_f16(uacc[nt][2 * hh], uacc[nt][2 * hh + 1]);
+                }
         }
-#pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int jj = 16 * warp + (lane >> 2) + 8 * hh;
-                const int t = nt * 8 + cq;
-                *reinterpret_cast<uint32_t *>(blk + kUt + (uint32_t)jj * kUtPitch + 2u * t) =
-                    pack_f16(uacc[nt][2 * hh], uacc[nt][2 * hh + 1]);
-            }
     }
 }
 
@@ -766,9 +760,6 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     cudaError_t e = cudaFuncSetAttribute(pf::prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          pf::kPrepSmem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(pf::prep_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             100);  // two CTAs per SM
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(pf::recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)pf::kRecSmem);
