@@ -187,24 +187,35 @@ __device__ __forceinline__ void lds8(const float *s, float *x) {
     *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(s + 4);
 }
 
+// Item = (chunk slot, head); false if the item has no tokens (past the end of
+// the packed sequences, or malformed offsets, which K2 flags).
+__device__ __forceinline__ bool item_tokens(int item, int H, const int32_t *cu,
+                                            const int32_t *first_chunk, int N, int T, int &slot,
+                                            int &h, int &tc, int &L) {
+    slot = item / H;
+    h = item - slot * H;
+    int n, c;
+    if (!slot_to_chunk(slot, cu, first_chunk, N, T, n, c)) return false;
+    const int t0 = cu ? cu[n] : n * T;
+    const int t1 = cu ? cu[n + 1] : t0 + T;
+    tc = t0 + c * C;
+    if (t1 < t0 || tc >= t1) return false;
+    L = min(C, t1 - tc);
+    return true;
+}
+
+// Persistent: CTA b handles items b, b + gridDim.x, ... (heads of one chunk are
+// adjacent items). The next item's g is prefetched into registers, and each
+// item's q, k, v loads are issued before its cumulative sum.
 __global__ void __launch_bounds__(kPrepThreads, 1)
     prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
                 const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
                 const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu,
-                const int32_t *__restrict__ first_chunk, int N, int T, int H,
+                const int32_t *__restrict__ first_chunk, int N, int T, int H, int nitems,
                 unsigned char *__restrict__ blocks, uint32_t *status) {
-    const int slot = blockIdx.x, h = blockIdx.y;
-    int n, c;
-    if (!slot_to_chunk(slot, cu, first_chunk, N, T, n, c)) return;
-    const int t0 = cu ? cu[n] : n * T;
-    const int t1 = cu ? cu[n + 1] : t0 + T;
-    const int tc = t0 + c * C;
-    if (t1 < t0 || tc >= t1) return;  // malformed offsets are flagged by K2
-    const int L = min(C, t1 - tc);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cq = 2 * (lane & 3);
-    unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
-    const size_t row0 = (size_t)tc * H + h;  // row index of token tc, head h
+    const int ch = tid & 127, ti4 = tid >> 7;  // cumulative-sum role: (channel, tile)
 
     extern __shared__ __align__(1024) unsigned char smem[];
     const uint32_t sbase = smem_u32(smem);
@@ -216,30 +227,66 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     float *sMd = reinterpret_cast<float *>(smem + kOffMd);
     float *sA = reinterpret_cast<float *>(smem + kOffA);
 
+    auto load_g = [&](int item, float *gr) {
+        int slot_, h_, tc_, L_;
+        const bool ok = item < nitems && item_tokens(item, H, cu, first_chunk, N, T, slot_, h_, tc_, L_);
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            const int t = 16 * ti4 + r;
+            gr[r] = (ok && t < L_) ? __ldg(&g[((size_t)(tc_ + t) * H + h_) * 128 + ch]) : 0.f;
+        }
+    };
+    float gnext[16];
+    load_g(blockIdx.x, gnext);
+
+#pragma unroll 1
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+    float gcur[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) gcur[r] = gnext[r];
+    int slot, h, tc, L;
+    if (!item_tokens(item, H, cu, first_chunk, N, T, slot, h, tc, L)) {
+        load_g(item + gridDim.x, gnext);
+        continue;
+    }
+    unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
+    const size_t row0 = (size_t)tc * H + h;  // row index of token tc, head h
+
+    // this item's q, k, v rows: two items (token, 8 channels) per thread
+    uint4 uq[2], uk[2], uv[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8;
+        uq[m] = uk[m] = uv[m] = make_uint4(0, 0, 0, 0);
+        if (t < L) {
+            const size_t off = (row0 + (size_t)t * H) * 128 + c0;
+            uq[m] = __ldg(reinterpret_cast<const uint4 *>(q + off));
+            uk[m] = __ldg(reinterpret_cast<const uint4 *>(k + off));
+            uv[m] = __ldg(reinterpret_cast<const uint4 *>(v + off));
+        }
+    }
+
     // ---- cumulative decay: thread = (channel, 16-token tile) --------------------------
     if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(row0 + (size_t)tid * H)]) : 0.f;
     {
-        const int ch = tid & 127, i = tid >> 7;
         float a[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int t = 16 * i + r;
-            a[r] = t < L ? clamp_g(__ldg(&g[(row0 + (size_t)t * H) * 128 + ch])) : 0.f;
-        }
+        for (int r = 0; r < 16; ++r) a[r] = clamp_g(gcur[r]);
 #pragma unroll
         for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
-        sQsum[i * 128 + ch] = a[15];
+        sQsum[ti4 * 128 + ch] = a[15];
         __syncthreads();
         float off = 0.f;
-        for (int i2 = 0; i2 < i; ++i2) off += sQsum[i2 * 128 + ch];
-        sRef[i * 128 + ch] = off;  // cumulative decay just before tile i
+        for (int i2 = 0; i2 < ti4; ++i2) off += sQsum[i2 * 128 + ch];
+        sRef[ti4 * 128 + ch] = off;  // cumulative decay just before tile ti4
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sAcum[(16 * i + r) * 128 + ch] = a[r] + off;
-        if (i == 3) {
+        for (int r = 0; r < 16; ++r) sAcum[(16 * ti4 + r) * 128 + ch] = a[r] + off;
+        if (ti4 == 3) {
             sAcT[ch] = a[15] + off;
             reinterpret_cast<float *>(blk + kGam)[ch] = __expf(a[15] + off);
         }
     }
+    load_g(item + gridDim.x, gnext);  // in flight during the rest of this item
     __syncthreads();
 
     // ---- all operands, one item = (token t, 8 key channels) ---------------------------
@@ -250,20 +297,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         __half *sKtb = reinterpret_cast<__half *>(smem + kOffKtb);
         __half *sVb = reinterpret_cast<__half *>(smem + kOffVb);
         __half *sKbS = reinterpret_cast<__half *>(smem + kOffKbS);
-#pragma unroll 1
+#pragma unroll
         for (int m = 0; m < 2; ++m) {
             const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8, i = t >> 4;
             float qq[8], kk[8], vv[8], a[8], r[8], ac[8];
-            uint4 uq = make_uint4(0, 0, 0, 0), uk = uq, uv = uq;
-            if (t < L) {
-                const size_t off = (row0 + (size_t)t * H) * 128 + c0;
-                uq = __ldg(reinterpret_cast<const uint4 *>(q + off));
-                uk = __ldg(reinterpret_cast<const uint4 *>(k + off));
-                uv = __ldg(reinterpret_cast<const uint4 *>(v + off));
-            }
-            unpack8_bf16(uq, qq);
-            unpack8_bf16(uk, kk);
-            unpack8_bf16(uv, vv);
+            unpack8_bf16(uq[m], qq);
+            unpack8_bf16(uk[m], kk);
+            unpack8_bf16(uv[m], vv);
             lds8(&sAcum[t * 128 + c0], a);
             lds8(&sRef[i * 128 + c0], r);
             lds8(&sAcT[c0], ac);
@@ -508,6 +548,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                         pack_f16(uacc[nt][2 * hh], uacc[nt][2 * hh + 1]);
                 }
         }
+    }
+    __syncthreads();  // shared memory is reused by the next item
     }
 }
 
@@ -777,11 +819,16 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         slots = (long long)N * ((T + pf::C - 1) / pf::C);
     }
     if (slots > 0) {
-        dim3 grid((unsigned)slots, (unsigned)H);
+        int dev = 0, nsm = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorUnknown;
+        const long long nitems = slots * H;
+        const int grid = (int)(nitems < nsm ? nitems : nsm);  // one persistent CTA per SM
         pf::prep_kernel<<<grid, pf::kPrepThreads, pf::kPrepSmem, stream>>>(
             static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
             static_cast<const __nv_bfloat16 *>(v), g, static_cast<const __nv_bfloat16 *>(beta),
-            cu, first_chunk, N, T, H, blocks, status);
+            cu, first_chunk, N, T, H, (int)nitems, blocks, status);
     }
     pf::recur_kernel<<<(unsigned)((long long)N * H), pf::kRecThreads, pf::kRecSmem, stream>>>(
         cu, first_chunk, N, T, T_total, H, scale, init, blocks,
