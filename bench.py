@@ -55,6 +55,31 @@ def decode_flops_per_head_token(d=D):
     return 7 * d * d
 
 
+def measured_traffic(key):
+    """DRAM bytes per launch from a committed ncu capture, while the kernel
+    source it was taken from is unchanged (else None)."""
+    import hashlib
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            entry = json.load(f)[key]
+        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != entry["source_sha256_16"]:
+                return None
+        return entry
+    except Exception:
+        return None
+
+
+def decode_traffic(units):
+    """Decode DRAM bytes per launch, scaled by state count from the committed
+    capture (traffic grows in proportion to the number of head states)."""
+    e = measured_traffic("decode_b64_h96")
+    if e is None:
+        return None
+    return e["bytes_per_launch"] * units / e["units_per_launch"]
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -94,7 +119,7 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f,
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
                 stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -172,27 +197,26 @@ def run_reference(args, world, rank):
     }))
 
 
-def cpu_baseline(budget_s=12.0):
-    """Time the oracle as it stands on a bounded sample of the prefill
-    workload (all 32 heads, a prefix of the tokens)."""
+def cpu_baseline(budget_s=10.0, max_reps=20):
+    """Time the oracle as it stands on the prefill workload (all 32 heads x
+    8192 tokens), repeated until about `budget_s` seconds of CPU time."""
     import oracle
     from kimi_delta_attention_rule_gb300 import inputs
     oracle.build()
     x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"])
+    f = lambda t: t.float().numpy()
+    args = (f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta), x.scale)
     cores = oracle.default_threads()
-    toks = 256
-    while True:
-        f = lambda t: t[:toks].float().numpy()
+    reps, total = 0, 0.0
+    while total < budget_s and reps < max_reps:
         t0 = time.perf_counter()
-        oracle.prefill(f(x.q), f(x.k), f(x.v), f(x.g), x.beta[:toks].float().numpy(), x.scale)
-        dt = time.perf_counter() - t0
-        if dt > budget_s / 4 or toks >= PREFILL["T"]:
-            break
-        toks = min(PREFILL["T"], toks * 4)
-    units = toks * PREFILL["H"]
-    return {"value": units / dt / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
-            "sample": "first %d tokens x %d heads of the prefill workload, %.1f s" % (
-                toks, PREFILL["H"], dt)}
+        oracle.prefill(*args)
+        total += time.perf_counter() - t0
+        reps += 1
+    units = reps * PREFILL["T"] * PREFILL["H"]
+    return {"value": units / total / 1e6, "unit": "Mtok/s", "cores": cores, "kind": "oracle",
+            "sample": "the full prefill workload (8192 tokens x 32 heads) %d times, %.1f s"
+                      % (reps, total)}
 
 
 def ncu_case(args):
@@ -219,7 +243,7 @@ def ncu_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -291,6 +315,7 @@ def main():
     clocks = clk.summary()
 
     peaks, peak_src = load_peaks()
+    tr_pf = measured_traffic("prefill_h32_t8192")
     bpt = prefill_bytes_per_head_token()
     bytes_per_launch = bpt * H * T + fin.numel() * 4
     achieved_gbs = bytes_per_launch / (ms * 1e-3) / 1e9
@@ -369,8 +394,9 @@ def main():
             "tokens_per_s": B * Hd / (dms * 1e-3),
             "gflops": decode_flops_per_head_token() * B * Hd / (dms * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"], "traffic": None,
-                         "peak_source": peak_src,
+                         "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                         "traffic": decode_traffic(B * Hd),
+                         "peak_source": peak_src, "kernel": "decode_step_kernel",
                          "algorithmic_bytes_per_launch": state_bytes},
             "gpu_launches": reps * S,
         }
@@ -394,8 +420,10 @@ def main():
                    "l2": "inputs (%.0f MB) larger than L2; no flush" % (
                        (bpt - 2 * D) * H * T / 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
-                     "peak_source": peak_src, "kernel": "prefill_bf16_kernel",
+                     "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
+                     "traffic": (tr_pf or {}).get("bytes_per_launch"),
+                     "peak_source": peak_src,
+                     "kernel": "kda_prefill (prep_kernel + recur_kernel, one call)",
                      "algorithmic_bytes_per_launch": bytes_per_launch},
         "tensor": {"tflops_pages_count": tflops, "peak": peaks["bf16_tflops"],
                    "frac": tflops / peaks["bf16_tflops"],
