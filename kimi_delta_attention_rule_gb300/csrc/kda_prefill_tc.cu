@@ -123,7 +123,13 @@ constexpr int kOffAc = kOffQsum + 4 * 128 * 4;       // fp32 [128] a_C
 constexpr int kOffBeta = kOffAc + 128 * 4;           // fp32 [64]
 constexpr int kOffMd = kOffBeta + C * 4;             // fp32 [64] q_t . k_t
 constexpr int kOffA = kOffMd + C * 4;                // fp32 [64][68] A
-constexpr int kOffXq = kOffA + C * kLDA * 4;         // bf16 [64][136] q e^{a - r_i}
+// per-channel exponential tables (fp32 [k][128] each), so that every operand
+// needs only x = e^{a_t - r_i} and 1/x per element:
+//   kEr[i] = e^{r_i}; kEd[i] = e^{r_{i+1} - r_i}; kEc[i] = e^{a_C - r_{i+1}};
+//   kE21 = e^{r_2 - r_1}, kE31 = e^{r_3 - r_1}, kE32 = e^{r_3 - r_2}  (r_4 = a_C)
+constexpr int kOffTab = kOffA + C * kLDA * 4;
+constexpr int kTabEr = 0, kTabEd = 4, kTabEc = 8, kTabE21 = 12, kTabE31 = 13, kTabE32 = 14;
+constexpr int kOffXq = kOffTab + 16 * 128 * 4;       // bf16 [64][136] q e^{a - r_i}
 constexpr int kOffXk = kOffXq + C * kLDK * 2;        // bf16 [64][136] k e^{a - r_i}
 constexpr int kOffKh = kOffXk + C * kLDK * 2;        // bf16 [160][136] k e^{r_i - a}, 10 tiles
 constexpr int kOffKtb = kOffKh + 160 * kLDK * 2;     // fp16 [64][136] beta k e^{a}
@@ -133,8 +139,8 @@ constexpr int kPrepSmem = kOffKbS + C * kLDK * 2;
 // after the Gram phase, inside the Xq / Xk region:
 constexpr int kOffTb = kOffXq;                       // fp16 [64][72] T
 constexpr int kOffAh = kOffTb + C * kLDC * 2;        // fp16 [64][72] A
-constexpr int kOffXh = kOffAh + C * kLDC * 2;        // fp16 [3][16][24] level scratch
-static_assert(kOffXh + 3 * 16 * 24 * 2 <= kOffKh, "T scratch inside the row-operand region");
+constexpr int kOffXh = kOffAh + C * kLDC * 2;        // fp16 [4][16][24] block-product scratch
+static_assert(kOffXh + 4 * 16 * 24 * 2 <= kOffKh, "T scratch inside the row-operand region");
 static_assert(kPrepSmem <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ int kh_slot(int i, int j) { return (i * (i + 1)) / 2 + j; }
@@ -276,14 +282,29 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
         sQsum[ti4 * 128 + ch] = a[15];
         __syncthreads();
-        float off = 0.f;
-        for (int i2 = 0; i2 < ti4; ++i2) off += sQsum[i2 * 128 + ch];
+        float rr[5];  // r_0 .. r_3, and r_4 = a_C
+        rr[0] = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) rr[i2 + 1] = rr[i2] + sQsum[i2 * 128 + ch];
+        float off = rr[0];
+#pragma unroll
+        for (int i2 = 1; i2 < 4; ++i2) off = ti4 == i2 ? rr[i2] : off;
         sRef[ti4 * 128 + ch] = off;  // cumulative decay just before tile ti4
 #pragma unroll
         for (int r = 0; r < 16; ++r) sAcum[(16 * ti4 + r) * 128 + ch] = a[r] + off;
+        float *tab = reinterpret_cast<float *>(smem + kOffTab);
+        const float rnext = ti4 == 3 ? rr[4] : (ti4 == 2 ? rr[3] : (ti4 == 1 ? rr[2] : rr[1]));
+        tab[(kTabEr + ti4) * 128 + ch] = __expf(off);
+        tab[(kTabEd + ti4) * 128 + ch] = __expf(rnext - off);   // >= e^-80
+        tab[(kTabEc + ti4) * 128 + ch] = __expf(rr[4] - rnext); // <= 1
+        if (ti4 == 0) {
+            tab[kTabE21 * 128 + ch] = __expf(rr[2] - rr[1]);
+            tab[kTabE31 * 128 + ch] = __expf(rr[3] - rr[1]);
+            tab[kTabE32 * 128 + ch] = __expf(rr[3] - rr[2]);
+        }
         if (ti4 == 3) {
-            sAcT[ch] = a[15] + off;
-            reinterpret_cast<float *>(blk + kGam)[ch] = __expf(a[15] + off);
+            sAcT[ch] = rr[4];
+            reinterpret_cast<float *>(blk + kGam)[ch] = __expf(rr[4]);
         }
     }
     load_g(item + gridDim.x, gnext);  // in flight during the rest of this item
@@ -300,20 +321,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
             const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8, i = t >> 4;
-            float qq[8], kk[8], vv[8], a[8], r[8], ac[8];
+            float qq[8], kk[8], vv[8], a[8], r[8];
             unpack8_bf16(uq[m], qq);
             unpack8_bf16(uk[m], kk);
             unpack8_bf16(uv[m], vv);
             lds8(&sAcum[t * 128 + c0], a);
             lds8(&sRef[i * 128 + c0], r);
-            lds8(&sAcT[c0], ac);
+            const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
+            float er[8], ed[8], ec[8];
+            lds8(&tab[(kTabEr + i) * 128 + c0], er);
+            lds8(&tab[(kTabEd + i) * 128 + c0], ed);
+            lds8(&tab[(kTabEc + i) * 128 + c0], ec);
             const float bt = sBeta[t];
-            float x[8], ix[8], o[8], md = 0.f;
+            float x[8], ix[8], y[8], o[8], md = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float p = a[e] - r[e];  // a_t - r_i in [-80, 0]
-                x[e] = __expf(p);
-                ix[e] = __expf(-p);
+                x[e] = __expf(p);             // e^{a_t - r_i}      in [e^-80, 1]
+                ix[e] = __expf(-p);           // e^{r_i - a_t}      in [1, e^80]
+                y[e] = ed[e] * ix[e];         // e^{r_{i+1} - a_t}  in [e^-80, 1]
                 md += qq[e] * kk[e];
             }
 #pragma unroll
@@ -325,29 +351,33 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * ix[e];
             *reinterpret_cast<uint4 *>(&sKh[(kh_slot(i, i) * 16 + (t & 15)) * kLDK + c0]) = pack8_bf16(o);
+            // later reference tiles i2 > i: k e^{r_i2 - a_t} = k e^{r_i2 - r_{i+1}} y
 #pragma unroll 1
             for (int i2 = i + 1; i2 < 4; ++i2) {
-                float r2[8];
-                lds8(&sRef[i2 * 128 + c0], r2);
+                float f[8];
+                if (i2 == i + 1) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = kk[e] * __expf(r2[e] - a[e]);  // <= 1
+                    for (int e = 0; e < 8; ++e) f[e] = 1.f;
+                } else {
+                    const int tb = (i2 == 2) ? kTabE21 : (i == 0 ? kTabE31 : kTabE32);
+                    lds8(&tab[tb * 128 + c0], f);
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = kk[e] * (f[e] * y[e]);
                 *reinterpret_cast<uint4 *>(&sKh[(kh_slot(i2, i) * 16 + (t & 15)) * kLDK + c0]) =
                     pack8_bf16(o);
             }
-            float ea[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) ea[e] = __expf(a[e]);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = qq[e] * ea[e];                    // q e^{a}
+            for (int e = 0; e < 8; ++e) o[e] = qq[e] * (er[e] * x[e]);            // q e^{a}
             *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(64 + t, c0)) = pack8_f16(o);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * ea[e];               // beta k e^{a}
+            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * (er[e] * x[e]);       // beta k e^{a}
             *reinterpret_cast<uint4 *>(&sKtb[t * kLDK + c0]) = pack8_f16(o);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                       // beta v
+            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                        // beta v
             *reinterpret_cast<uint4 *>(&sVb[t * kLDK + c0]) = pack8_f16(o);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = kk[e] * __expf(ac[e] - a[e]);     // k e^{a_C - a}
+            for (int e = 0; e < 8; ++e) o[e] = kk[e] * (ec[e] * y[e]);            // k e^{a_C - a}
             *reinterpret_cast<uint4 *>(&sKbS[t * kLDK + c0]) = pack8_f16(o);
             // q_t . k_t (the diagonal of M: no decay) over the 16 lanes of token t
 #pragma unroll
@@ -450,45 +480,69 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     }
     __syncthreads();
     {
-        // level d: T_ij = -T_ii * sum_{kk = 16j}^{16i - 1} A[16i.., kk] T[kk, 16j..]
+        // Below the diagonal blocks, in two rounds (16x16 tiles, fp16 tensor cores):
+        //  1. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
+        //  2. the lower-left 32x32 block  T_BA = -T_BB (A_BA T_AA),
+        //     T_AA = [[T00, 0], [T10, T11]],  T_BB = [[T22, 0], [T32, T33]].
         const uint32_t aAh = sbase + kOffAh;
         __half *sXh = reinterpret_cast<__half *>(smem + kOffXh);
-#pragma unroll 1
-        for (int d = 1; d < 4; ++d) {
-            if (warp < 4 - d) {
-                const int i = d + warp, j = i - d;
-                float xacc[2][4] = {};
-#pragma unroll 1
-                for (int ks = j; ks < i; ++ks) {
-                    uint32_t af[4], bf[4];
-                    frag_a_rowmajor(af, aAh, kLDC, 16 * i, 16 * ks, lane);
-                    frag_b_kn(bf, aTb, kLDC, 16 * j, 16 * ks, lane);
-                    mma_f16_16816(xacc[0], af, bf[0], bf[1]);
-                    mma_f16_16816(xacc[1], af, bf[2], bf[3]);
-                }
-                __half *xs = sXh + warp * 16 * 24;
+        auto store_tile = [&](__half *dst, int ld, float acc[2][4], float sgn) {
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int rr = lane >> 2, cc2 = nt * 8 + cq;
-                    *reinterpret_cast<uint32_t *>(&xs[rr * 24 + cc2]) = pack_f16(xacc[nt][0], xacc[nt][1]);
-                    *reinterpret_cast<uint32_t *>(&xs[(rr + 8) * 24 + cc2]) = pack_f16(xacc[nt][2], xacc[nt][3]);
-                }
-                __syncwarp();
-                float tacc[2][4] = {};
+            for (int nt = 0; nt < 2; ++nt) {
+                const int rr = lane >> 2, cc2 = nt * 8 + cq;
+                *reinterpret_cast<uint32_t *>(&dst[rr * ld + cc2]) = pack_f16(sgn * acc[nt][0], sgn * acc[nt][1]);
+                *reinterpret_cast<uint32_t *>(&dst[(rr + 8) * ld + cc2]) = pack_f16(sgn * acc[nt][2], sgn * acc[nt][3]);
+            }
+        };
+        if (warp < 2) {
+            const int i = 1 + 2 * warp, j = i - 1;
+            float xacc[2][4] = {};
+            uint32_t af[4], bf[4];
+            frag_a_rowmajor(af, aAh, kLDC, 16 * i, 16 * j, lane);
+            frag_b_kn(bf, aTb, kLDC, 16 * j, 16 * j, lane);
+            mma_f16_16816(xacc[0], af, bf[0], bf[1]);
+            mma_f16_16816(xacc[1], af, bf[2], bf[3]);
+            __half *xs = sXh + warp * 16 * 24;
+            store_tile(xs, 24, xacc, 1.f);
+            __syncwarp();
+            float tacc[2][4] = {};
+            frag_a_rowmajor(af, aTb, kLDC, 16 * i, 16 * i, lane);
+            frag_b_kn(bf, smem_u32(xs), 24, 0, 0, lane);
+            mma_f16_16816(tacc[0], af, bf[0], bf[1]);
+            mma_f16_16816(tacc[1], af, bf[2], bf[3]);
+            store_tile(sTb + (16 * i) * kLDC + 16 * j, kLDC, tacc, -1.f);
+        }
+        __syncthreads();
+        if (warp < 4) {  // X = A_BA T_AA, block (r, c), r in {2, 3}, c in {0, 1}
+            const int r = 2 + (warp >> 1), c = warp & 1;
+            float xacc[2][4] = {};
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                if (kb < c) continue;  // T_01 = 0
                 uint32_t af[4], bf[4];
-                frag_a_rowmajor(af, aTb, kLDC, 16 * i, 16 * i, lane);
-                frag_b_kn(bf, smem_u32(xs), 24, 0, 0, lane);
+                frag_a_rowmajor(af, aAh, kLDC, 16 * r, 16 * kb, lane);
+                frag_b_kn(bf, aTb, kLDC, 16 * c, 16 * kb, lane);
+                mma_f16_16816(xacc[0], af, bf[0], bf[1]);
+                mma_f16_16816(xacc[1], af, bf[2], bf[3]);
+            }
+            store_tile(sXh + warp * 16 * 24, 24, xacc, 1.f);
+        }
+        __syncthreads();
+        if (warp < 4) {  // T_rc = -sum_{k = 2}^{r} T_rk X_kc
+            const int r = 2 + (warp >> 1), c = warp & 1;
+            float tacc[2][4] = {};
+#pragma unroll
+            for (int kb = 2; kb < 4; ++kb) {
+                if (kb > r) continue;  // T_23 = 0
+                uint32_t af[4], bf[4];
+                frag_a_rowmajor(af, aTb, kLDC, 16 * r, 16 * kb, lane);
+                frag_b_kn(bf, smem_u32(sXh + ((kb - 2) * 2 + c) * 16 * 24), 24, 0, 0, lane);
                 mma_f16_16816(tacc[0], af, bf[0], bf[1]);
                 mma_f16_16816(tacc[1], af, bf[2], bf[3]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int rr = 16 * i + (lane >> 2), cc2 = 16 * j + nt * 8 + cq;
-                    *reinterpret_cast<uint32_t *>(&sTb[rr * kLDC + cc2]) = pack_f16(-tacc[nt][0], -tacc[nt][1]);
-                    *reinterpret_cast<uint32_t *>(&sTb[(rr + 8) * kLDC + cc2]) = pack_f16(-tacc[nt][2], -tacc[nt][3]);
-                }
             }
-            __syncthreads();
+            store_tile(sTb + (16 * r) * kLDC + 16 * c, kLDC, tacc, -1.f);
         }
+        __syncthreads();
     }
 
     // ---- W = T (beta k e^{a})  and  U~^T = (beta v)^T T^T -------------------------
