@@ -145,6 +145,14 @@ static_assert(kPrepSmem <= 227 * 1024, "shared memory budget");
 
 __device__ __forceinline__ int kh_slot(int i, int j) { return (i * (i + 1)) / 2 + j; }
 
+// 16-byte global -> shared copy; bytes past `src_bytes` (0 or 16) are zero-filled
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
 // Sequence and chunk of a chunk slot; false if the slot is past the end.
 __device__ __forceinline__ bool slot_to_chunk(int slot, const int32_t *cu,
                                               const int32_t *first_chunk, int N, int T,
@@ -233,51 +241,69 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     float *sMd = reinterpret_cast<float *>(smem + kOffMd);
     float *sA = reinterpret_cast<float *>(smem + kOffA);
 
-    auto load_g = [&](int item, float *gr) {
-        int slot_, h_, tc_, L_;
-        const bool ok = item < nitems && item_tokens(item, H, cu, first_chunk, N, T, slot_, h_, tc_, L_);
+    // Input staging with cp.async (16-byte pieces; padding rows are zero-filled):
+    //   g of an item -> the a buffer (dead after the operand phase),
+    //   q, k -> the column-tile region, v -> the transpose staging (both dead
+    //   after the Gram phase).
+    const uint32_t uG = sbase + kOffAcum, uQ = sbase + kOffKh, uK = sbase + kOffKh + C * 256,
+                   uV = sbase + kOffKbS;
+    auto stage_g = [&](int tc_, int h_, int L_) {
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            const int t = 16 * ti4 + r;
-            gr[r] = (ok && t < L_) ? __ldg(&g[((size_t)(tc_ + t) * H + h_) * 128 + ch]) : 0.f;
+        for (int m = 0; m < 4; ++m) {
+            const int id = tid + kPrepThreads * m, t = id >> 5, c4 = (id & 31) * 4;
+            const int ts = t < L_ ? t : 0;
+            cp_async16(uG + (uint32_t)(t * 512 + c4 * 4), g + ((size_t)(tc_ + ts) * H + h_) * 128 + c4,
+                       t < L_ ? 16u : 0u);
         }
+        cp_async_commit();
     };
-    float gnext[16];
-    load_g(blockIdx.x, gnext);
+    auto stage_qkv = [&](int tc_, int h_, int L_) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int id = tid + kPrepThreads * m, t = id >> 4, c8 = (id & 15) * 8;
+            const int ts = t < L_ ? t : 0;
+            const size_t off = ((size_t)(tc_ + ts) * H + h_) * 128 + c8;
+            const uint32_t so = (uint32_t)(t * 256 + c8 * 2), n = t < L_ ? 16u : 0u;
+            cp_async16(uQ + so, q + off, n);
+            cp_async16(uK + so, k + off, n);
+            cp_async16(uV + so, v + off, n);
+        }
+        cp_async_commit();
+    };
+    // the item that the staged inputs belong to (-1: none)
+    int staged = -1;
+    {
+        int slot_, h_, tc_, L_;
+        if (item_tokens(blockIdx.x, H, cu, first_chunk, N, T, slot_, h_, tc_, L_)) {
+            stage_g(tc_, h_, L_);
+            stage_qkv(tc_, h_, L_);
+            staged = blockIdx.x;
+        }
+    }
 
 #pragma unroll 1
     for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
-    float gcur[16];
-#pragma unroll
-    for (int r = 0; r < 16; ++r) gcur[r] = gnext[r];
     int slot, h, tc, L;
-    if (!item_tokens(item, H, cu, first_chunk, N, T, slot, h, tc, L)) {
-        load_g(item + gridDim.x, gnext);
-        continue;
+    if (!item_tokens(item, H, cu, first_chunk, N, T, slot, h, tc, L)) continue;
+    if (staged != item) {  // the previous item could not prefetch this one
+        stage_g(tc, h, L);
+        stage_qkv(tc, h, L);
     }
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
     const size_t row0 = (size_t)tc * H + h;  // row index of token tc, head h
+    int nslot, nh, ntc, nL;  // the next item of this CTA
+    const int nitem = item + gridDim.x;
+    const bool has_next = nitem < nitems && item_tokens(nitem, H, cu, first_chunk, N, T, nslot, nh, ntc, nL);
 
-    // this item's q, k, v rows: two items (token, 8 channels) per thread
-    uint4 uq[2], uk[2], uv[2];
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-        const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8;
-        uq[m] = uk[m] = uv[m] = make_uint4(0, 0, 0, 0);
-        if (t < L) {
-            const size_t off = (row0 + (size_t)t * H) * 128 + c0;
-            uq[m] = __ldg(reinterpret_cast<const uint4 *>(q + off));
-            uk[m] = __ldg(reinterpret_cast<const uint4 *>(k + off));
-            uv[m] = __ldg(reinterpret_cast<const uint4 *>(v + off));
-        }
-    }
-
-    // ---- cumulative decay: thread = (channel, 16-token tile) --------------------------
     if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(row0 + (size_t)tid * H)]) : 0.f;
+    cp_async_wait_all();
+    __syncthreads();
+
+    // ---- cumulative decay: thread = (channel, 16-token tile), in place over g --------
     {
         float a[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) a[r] = clamp_g(gcur[r]);
+        for (int r = 0; r < 16; ++r) a[r] = clamp_g(sAcum[(16 * ti4 + r) * 128 + ch]);
 #pragma unroll
         for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
         sQsum[ti4 * 128 + ch] = a[15];
@@ -307,7 +333,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             reinterpret_cast<float *>(blk + kGam)[ch] = __expf(rr[4]);
         }
     }
-    load_g(item + gridDim.x, gnext);  // in flight during the rest of this item
+    // this item's q, k, v: out of the staging area before it is overwritten
+    uint4 uq[2], uk[2], uv[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+        const int id = tid + kPrepThreads * m, t = id >> 4, c8 = (id & 15) * 8;
+        const uint32_t so = (uint32_t)(t * 256 + c8 * 2);
+        uq[m] = *reinterpret_cast<const uint4 *>(smem + kOffKh + so);
+        uk[m] = *reinterpret_cast<const uint4 *>(smem + kOffKh + C * 256 + so);
+        uv[m] = *reinterpret_cast<const uint4 *>(smem + kOffKbS + so);
+    }
     __syncthreads();
 
     // ---- all operands, one item = (token t, 8 key channels) ---------------------------
@@ -386,6 +421,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
     }
     __syncthreads();
+    if (has_next) stage_g(ntc, nh, nL);  // the a buffer is free from here on
 
     // ---- (k e^{a_C - a})^T -> block: item = (key channel, 8 tokens) -----------------
     {
@@ -453,6 +489,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
     }
     __syncthreads();
+    if (has_next) {  // column tiles and the transpose staging are free from here on
+        stage_qkv(ntc, nh, nL);
+        staged = nitem;
+    }
 
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
     __half *sAh = reinterpret_cast<__half *>(smem + kOffAh);
