@@ -284,6 +284,12 @@ def main():
     out = torch.empty_like(x.q)
     fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
     ws = kda.prefill_workspace(x.q, None, N=1, T=T, chunk=C)
+    sched = kda.kda_prefill_schedule(1, T, H, D, C, kda.KDA_BF16)
+    fused = sched == kda.KDA_SCHEDULE_FUSED
+    launches_per_step = 1 if fused else 2
+    kernel_label = ("kda_prefill: fused_kernel (chunk preparation and recurrence in one "
+                    "cooperative launch)" if fused else
+                    "kda_prefill: prep_kernel + recur_kernel (one call)")
 
     def step():
         kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, cu_seqlens=None, chunk=C, out=out,
@@ -423,14 +429,14 @@ def main():
                      "unit": "GB/s", "frac": achieved_gbs / peaks["hbm_gbs"],
                      "traffic": (tr_pf or {}).get("bytes_per_launch"),
                      "peak_source": peak_src,
-                     "kernel": "kda_prefill (prep_kernel + recur_kernel, one call)",
+                     "kernel": kernel_label,
                      "algorithmic_bytes_per_launch": bytes_per_launch},
         "tensor": {"tflops_pages_count": tflops, "peak": peaks["bf16_tflops"],
                    "frac": tflops / peaks["bf16_tflops"],
                    "flops_per_launch": flops},
         "e2e": {"value": e2e_val, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "decode": decode,
         "cpu_baseline": cpu,

@@ -57,6 +57,12 @@ typedef enum {
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
 
+typedef enum {
+    KDA_SCHEDULE_SPLIT = 0,  /* bf16: chunk preparation, then the recurrence */
+    KDA_SCHEDULE_FUSED = 1,  /* bf16: both in one cooperative launch */
+    KDA_SCHEDULE_DIRECT = 2  /* fp32 I/O: one kernel */
+} kda_schedule;
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *kda_status_string(int status);
 
@@ -120,6 +126,27 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
 int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                     const void *beta, float scale, int32_t B, int32_t H, int32_t D, int32_t io,
                     float *state_inout, void *out, void *stream);
+
+/*
+ * Kernel schedule that kda_prefill uses for these sizes on the current device
+ * (arguments as in kda_prefill_workspace_size):
+ *   KDA_SCHEDULE_SPLIT  bf16: the chunk-preparation kernel over all
+ *                       (chunk, head) blocks, then the recurrence kernel,
+ *                       one CTA per (sequence, head) chain;
+ *   KDA_SCHEDULE_FUSED  bf16: one cooperative launch in which one CTA per
+ *                       chain runs the recurrence while the other SMs prepare
+ *                       blocks in chunk order, chains waiting (bounded) on a
+ *                       per-block ready flag; chosen when the chains take at
+ *                       most a third of the SMs;
+ *   KDA_SCHEDULE_DIRECT fp32 I/O: one kernel on CUDA cores.
+ * With cu_seqlens a schedule kernel runs first. The environment variable
+ * KDA_PREFILL_SCHEDULE=split|fused overrides the bf16 choice ("fused" needs
+ * fewer chains than SMs). Returns the schedule, or the negated kda_status on
+ * invalid sizes or a failed device query. The result does not depend on the
+ * schedule: both bf16 schedules run the same arithmetic.
+ */
+int kda_prefill_schedule(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
+                         int32_t varlen);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of a

@@ -26,9 +26,13 @@ KDA_ERR_DEVICE = 5
 KDA_ERR_TOO_LARGE = 6
 KDA_BF16 = 0
 KDA_F32 = 1
+KDA_SCHEDULE_SPLIT = 0
+KDA_SCHEDULE_FUSED = 1
+KDA_SCHEDULE_DIRECT = 2
 
 EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size", "kda_prefill",
-            "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens")
+            "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
+            "kda_prefill_schedule")
 
 _lock = threading.Lock()
 _lib = None
@@ -65,6 +69,8 @@ def load() -> ctypes.CDLL:
         lib.kda_workspace_status.restype = ctypes.c_int
         lib.kda_check_cu_seqlens.argtypes = [P, I32, I32]
         lib.kda_check_cu_seqlens.restype = ctypes.c_int
+        lib.kda_prefill_schedule.argtypes = [I32] * 7
+        lib.kda_prefill_schedule.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -107,6 +113,16 @@ def _check_cuda(*ts):
 def kda_prefill_workspace_size(N: int, T: int, H: int, D: int, chunk: int, io: int,
                                varlen: bool = False) -> int:
     return int(load().kda_prefill_workspace_size(N, T, H, D, chunk, io, int(bool(varlen))))
+
+
+def kda_prefill_schedule(N: int, T: int, H: int, D: int, chunk: int, io: int,
+                         varlen: bool = False) -> int:
+    """KDA_SCHEDULE_* that kda_prefill uses for these sizes on the current
+    device (C entry point ``kda_prefill_schedule``); raises on invalid sizes."""
+    s = int(load().kda_prefill_schedule(N, T, H, D, chunk, io, int(bool(varlen))))
+    if s < 0:
+        raise KDAError(-s, "kda_prefill_schedule")
+    return s
 
 
 def prefill_workspace(q, cu_seqlens=None, N=None, T=None, chunk=64):

@@ -22,6 +22,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const void *beta, float scale, const float *init,
                               const int32_t *cu, int N, int T, int T_total, int H, void *out,
                               float *fin, unsigned char *ws, cudaStream_t stream);
+int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen);
 }  // namespace kda
 
 namespace {
@@ -77,6 +78,17 @@ size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, in
     long long tt = 0;
     if (check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt) != KDA_OK) return 0;
     return workspace_bytes_for(N, T, H, io, varlen != 0);
+}
+
+int kda_prefill_schedule(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
+                         int32_t varlen) {
+    long long tt = 0;
+    const int rc = check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt);
+    if (rc != KDA_OK) return -rc;
+    if (io == KDA_F32) return KDA_SCHEDULE_DIRECT;
+    const int s = kda::prefill_tc_schedule(N, T, tt, H, varlen != 0);
+    if (s < 0) return -KDA_ERR_CUDA;
+    return s == 1 ? KDA_SCHEDULE_FUSED : KDA_SCHEDULE_SPLIT;
 }
 
 int kda_check_cu_seqlens(const int32_t *cu, int32_t N, int32_t T_total) {

@@ -46,6 +46,9 @@
 #include "kda_common.cuh"
 #include "kda_tcgen05.cuh"
 
+#include <cstdlib>
+#include <cstring>
+
 namespace kda {
 namespace pf {
 
@@ -75,18 +78,38 @@ __device__ __forceinline__ void store_h(unsigned char *base, uint32_t off, float
     *reinterpret_cast<__half *>(base + off) = __float2half_rn(x);
 }
 
-// chunk slots: first_chunk[n] = sum_{m < n} ceil(L_m / C), first_chunk[N] = total
+// Chunk slots: first_chunk[n] = sum_{m < n} ceil(L_m / C), first_chunk[N] = total,
+// first_chunk[N + 1] = the most chunks of one sequence. The offsets are checked
+// as a whole (cu[0] = 0, non-decreasing, cu[N] <= T_total): the slot count
+// sized on the host only bounds the blocks of offsets that pass. If they do
+// not, the status word is flagged, first_chunk[N] = 0 and first_chunk[N + 1] =
+// -1, and every later kernel of the call skips all sequences.
 __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restrict__ cu, int N,
-                                                        int32_t *__restrict__ first_chunk) {
+                                                        int T_total,
+                                                        int32_t *__restrict__ first_chunk,
+                                                        uint32_t *status) {
     __shared__ int32_t part[1024];
+    __shared__ int32_t maxc_s;
+    __shared__ int bad_s;
     const int tid = threadIdx.x;
+    if (tid == 0) {
+        maxc_s = 0;
+        bad_s = (cu[0] != 0) || (cu[N] > T_total);
+    }
+    __syncthreads();
     const int per = (N + 1023) / 1024;
     const int lo = min(N, tid * per), hi = min(N, lo + per);
-    int32_t s = 0;
+    int32_t s = 0, mc = 0;
+    bool bad = false;
     for (int n = lo; n < hi; ++n) {
         const int32_t L = cu[n + 1] - cu[n];
-        s += L > 0 ? (L + C - 1) / C : 0;
+        bad |= L < 0;
+        const int32_t nc = L > 0 ? (L + C - 1) / C : 0;
+        s += nc;
+        mc = max(mc, nc);
     }
+    if (bad) atomicOr(&bad_s, 1);
+    if (mc > 0) atomicMax(&maxc_s, mc);
     part[tid] = s;
     __syncthreads();
     for (int off = 1; off < 1024; off <<= 1) {
@@ -95,13 +118,18 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
         part[tid] += v;
         __syncthreads();
     }
+    const bool any_bad = bad_s != 0;
     int32_t run = tid > 0 ? part[tid - 1] : 0;
     for (int n = lo; n < hi; ++n) {
-        first_chunk[n] = run;
+        first_chunk[n] = any_bad ? 0 : run;
         const int32_t L = cu[n + 1] - cu[n];
         run += L > 0 ? (L + C - 1) / C : 0;
     }
-    if (tid == 1023) first_chunk[N] = part[1023];
+    if (tid == 1023) {
+        first_chunk[N] = any_bad ? 0 : part[1023];
+        first_chunk[N + 1] = any_bad ? -1 : maxc_s;
+        if (any_bad) atomicOr(status, kStatusBadSeqlens);
+    }
 }
 
 // ============================================================================
@@ -218,15 +246,56 @@ __device__ __forceinline__ bool item_tokens(int item, int H, const int32_t *cu,
     return true;
 }
 
-// Persistent: CTA b handles items b, b + gridDim.x, ... (heads of one chunk are
-// adjacent items). The next item's g is prefetched into registers, and each
-// item's q, k, v loads are issued before its cumulative sum.
-__global__ void __launch_bounds__(kPrepThreads, 1)
-    prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
-                const __nv_bfloat16 *__restrict__ v, const float *__restrict__ g,
-                const __nv_bfloat16 *__restrict__ beta, const int32_t *__restrict__ cu,
-                const int32_t *__restrict__ first_chunk, int N, int T, int H, int nitems,
-                unsigned char *__restrict__ blocks, uint32_t *status) {
+// Item = (chunk c, sequence n, head h) in chunk-major order, idx = (c N + n) H + h,
+// so that a whole wave of items finishes the early chunks of every chain first.
+// Needs offsets that passed the schedule check.
+__device__ __forceinline__ bool item_tokens_cm(int idx, int H, const int32_t *cu,
+                                               const int32_t *first_chunk, int N, int T,
+                                               int &slot, int &h, int &tc, int &L) {
+    const int NH = N * H;
+    const int c = idx / NH, r = idx - c * NH, n = r / H;
+    h = r - n * H;
+    const int t0 = cu ? cu[n] : n * T;
+    const int t1 = cu ? cu[n + 1] : t0 + T;
+    tc = t0 + c * C;
+    if (tc >= t1) return false;
+    slot = (cu ? first_chunk[n] : n * ((T + C - 1) / C)) + c;
+    L = min(C, t1 - tc);
+    return true;
+}
+
+struct PrepArgs {
+    const __nv_bfloat16 *q, *k, *v;
+    const float *g;
+    const __nv_bfloat16 *beta;
+    const int32_t *cu, *first_chunk;
+    int N, T, H;
+    int nitems;  // chunk slots x heads
+    unsigned char *blocks;
+};
+
+// K1 over items first, first + stride, ... (slot-major order, or chunk-major
+// when `ready` is given). The next item's g, q, k, v are staged with cp.async
+// into shared regions that are dead at that point. With `ready`, each finished
+// block is published with a release store of ready[slot H + h] = 1.
+__device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int stride,
+                                          int *ready) {
+    const __nv_bfloat16 *__restrict__ q = pa.q, *__restrict__ k = pa.k, *__restrict__ v = pa.v;
+    const float *__restrict__ g = pa.g;
+    const __nv_bfloat16 *__restrict__ beta = pa.beta;
+    const int32_t *__restrict__ cu = pa.cu, *__restrict__ first_chunk = pa.first_chunk;
+    const int N = pa.N, T = pa.T, H = pa.H;
+    unsigned char *__restrict__ blocks = pa.blocks;
+    const bool chunk_major = ready != nullptr;
+    int nitems = pa.nitems;
+    if (chunk_major) {
+        const int maxc = cu ? first_chunk[N + 1] : (T + C - 1) / C;
+        nitems = maxc > 0 ? maxc * N * H : 0;
+    }
+    auto decode = [&](int idx, int &slot_, int &h_, int &tc_, int &L_) -> bool {
+        return chunk_major ? item_tokens_cm(idx, H, cu, first_chunk, N, T, slot_, h_, tc_, L_)
+                           : item_tokens(idx, H, cu, first_chunk, N, T, slot_, h_, tc_, L_);
+    };
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cq = 2 * (lane & 3);
     const int ch = tid & 127, ti4 = tid >> 7;  // cumulative-sum role: (channel, tile)
@@ -274,17 +343,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     int staged = -1;
     {
         int slot_, h_, tc_, L_;
-        if (item_tokens(blockIdx.x, H, cu, first_chunk, N, T, slot_, h_, tc_, L_)) {
+        if (first < nitems && decode(first, slot_, h_, tc_, L_)) {
             stage_g(tc_, h_, L_);
             stage_qkv(tc_, h_, L_);
-            staged = blockIdx.x;
+            staged = first;
         }
     }
 
 #pragma unroll 1
-    for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+    for (int item = first; item < nitems; item += stride) {
     int slot, h, tc, L;
-    if (!item_tokens(item, H, cu, first_chunk, N, T, slot, h, tc, L)) continue;
+    if (!decode(item, slot, h, tc, L)) continue;
     if (staged != item) {  // the previous item could not prefetch this one
         stage_g(tc, h, L);
         stage_qkv(tc, h, L);
@@ -292,8 +361,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
     const size_t row0 = (size_t)tc * H + h;  // row index of token tc, head h
     int nslot, nh, ntc, nL;  // the next item of this CTA
-    const int nitem = item + gridDim.x;
-    const bool has_next = nitem < nitems && item_tokens(nitem, H, cu, first_chunk, N, T, nslot, nh, ntc, nL);
+    const int nitem = item + stride;
+    const bool has_next = nitem < nitems && decode(nitem, nslot, nh, ntc, nL);
 
     if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(row0 + (size_t)tid * H)]) : 0.f;
     cp_async_wait_all();
@@ -643,14 +712,25 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
                 }
         }
     }
+    if (ready) asm volatile("fence.proxy.async.global;\n" ::: "memory");  // read by bulk copies
     __syncthreads();  // shared memory is reused by the next item
+    if (ready && tid == 0) {
+        __threadfence();
+        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + (size_t)slot * H + h),
+                     "r"(1u)
+                     : "memory");
     }
+    }
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs pa) {
+    prep_loop(pa, blockIdx.x, gridDim.x, nullptr);
 }
 
 // ============================================================================
 // K2: chunk recurrence on tcgen05
 // ============================================================================
-constexpr int kRecThreads = 256;  // thread = (value column j, half); all warps on every step
+constexpr int kRecThreads = 512;  // thread = (value column j, quarter); all warps on every step
 constexpr uint32_t kOffBuf0 = 0;
 constexpr uint32_t kOffBuf1 = kBlock;
 constexpr uint32_t kOffSA = 2 * kBlock;              // fp16 K-major [j][key]: S^T (A operand)
@@ -658,29 +738,51 @@ constexpr uint32_t kOffUA = kOffSA + 128 * 128 * 2;  // fp16 K-major [j][t]: U^T
 constexpr uint32_t kOffO = kOffUA + 128 * 64 * 2;    // bf16 [t][j] output staging
 constexpr uint32_t kRecSmem = kOffO + 64 * 128 * 2;
 static_assert(kRecSmem <= 227 * 1024, "shared memory budget");
+static_assert(kRecThreads == kPrepThreads, "the fused kernel runs both roles");
 // TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColP = 0, kColO = 64, kColS = 128;
-constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s bound on any mbarrier wait
+constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s bound on any wait
 
-__global__ void __launch_bounds__(kRecThreads, 1)
-    recur_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ first_chunk, int N,
-                 int T, int T_total, int H, float scale, const float *__restrict__ init,
-                 const unsigned char *__restrict__ blocks, __nv_bfloat16 *__restrict__ out,
-                 float *__restrict__ fin, uint32_t *status) {
-    const int n = blockIdx.x / H, h = blockIdx.x % H;
+struct RecArgs {
+    const int32_t *cu, *first_chunk;
+    int N, T, T_total, H;
+    float scale;
+    const float *init;
+    const unsigned char *blocks;
+    __nv_bfloat16 *out;
+    float *fin;
+    uint32_t *status;
+};
+
+__device__ __forceinline__ bool flag_set(const int *f) {
+    uint32_t x;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(x) : "l"(f) : "memory");
+    return x != 0;
+}
+
+// K2 for one chain (sequence n, head h). With `ready`, the block of chunk slot
+// s is loaded only after ready[s H + h] is set by its producer.
+__device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const int *ready) {
+    const int32_t *__restrict__ cu = ra.cu;
+    const int N = ra.N, T = ra.T, H = ra.H;
+    const float scale = ra.scale;
+    const float *__restrict__ init = ra.init;
+    __nv_bfloat16 *__restrict__ out = ra.out;
+    float *__restrict__ fin = ra.fin;
+    const int n = chain / H, h = chain % H;
     const int tid = threadIdx.x, warp = tid >> 5;
+    if (cu && ra.first_chunk[N + 1] < 0) return;  // malformed offsets, already flagged
     int t0, t1;
-    if (!seq_bounds(cu, n, T, T_total, t0, t1, status)) return;
+    if (!seq_bounds(cu, n, T, ra.T_total, t0, t1, ra.status)) return;
     const int nchunks = (t1 - t0 + C - 1) / C;
-    const int fc = cu ? first_chunk[n] : n * ((T + C - 1) / C);
-    const int j = tid & 127;   // value column = TMEM lane (warps w and w + 4 share lanes)
-    const int hf = tid >> 7;   // which half of the columns this thread handles
+    const int fc = cu ? ra.first_chunk[n] : n * ((T + C - 1) / C);
+    const int j = tid & 127;   // value column = TMEM lane (warps w, w + 4, ... share lanes)
+    const int qd = tid >> 7;   // which quarter of the columns this thread handles
 
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t bars[4];  // loads (2), MMA group 1, MMA group 2
     __shared__ uint32_t tmem_slot;
-    __shared__ int abort_flag;
     const uint32_t sbase = smem_u32(smem);
     const uint32_t uSA = sbase + kOffSA, uUA = sbase + kOffUA;
     const uint32_t bL0 = smem_u32(&bars[0]), bL1 = smem_u32(&bars[1]);
@@ -694,7 +796,6 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     }
     if (tid == 0) {
         for (int i = 0; i < 4; ++i) tc::mbar_init(smem_u32(&bars[i]), 1);
-        abort_flag = 0;
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -704,7 +805,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     const uint32_t tlane = tm + ((uint32_t)(32 * (warp & 3)) << 16);
 
     const size_t head_state = ((size_t)n * H + h) * 128 * 128;
-    const unsigned char *blk0 = blocks + ((size_t)fc * H + h) * kBlock;
+    const unsigned char *blk0 = ra.blocks + ((size_t)fc * H + h) * kBlock;
     const size_t blk_stride = (size_t)H * kBlock;
 
     // Bounded wait; a timeout is recorded and turns every later wait into a
@@ -718,9 +819,30 @@ __global__ void __launch_bounds__(kRecThreads, 1)
         failed = __syncthreads_or(failed) != 0;
         tc::fence_after_sync();
     };
-    auto issue_load = [&](int c) {
-        tc::mbar_arrive_expect_tx(bL(c), kBlock);
-        tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
+    // Block loads, issued in chunk order by thread 0. Chunk x may be loaded
+    // once chunk x - 2 has left its buffer and (with `ready`) once it exists.
+    int next_load = 0;
+    auto issue_loads = [&](int upto, bool block) {  // chunks [next_load, upto]
+        upto = min(upto, nchunks - 1);
+        while (!failed && next_load <= upto) {
+            if (ready) {
+                const int *f = ready + (size_t)(fc + next_load) * H + h;
+                if (!flag_set(f)) {
+                    if (!block) return;
+                    const uint64_t start = tc::globaltimer_ns();
+                    while (!flag_set(f)) {
+                        if (tc::globaltimer_ns() - start > kWaitLimit) {
+                            failed = true;
+                            return;
+                        }
+                    }
+                }
+                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            }
+            const int c = next_load++;
+            tc::mbar_arrive_expect_tx(bL(c), kBlock);
+            tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
+        }
     };
     // descriptors (no swizzle); +16 in the address field per 256-byte K step
     const uint64_t dSA = tc::smem_desc(uSA, 128, 2048), dUA = tc::smem_desc(uUA, 128, 1024);
@@ -743,35 +865,35 @@ __global__ void __launch_bounds__(kRecThreads, 1)
 
     if (nchunks == 0) {
         if (fin)
-            for (int k0 = 64 * hf; k0 < 64 * hf + 64; ++k0)
+            for (int k0 = 32 * qd; k0 < 32 * qd + 32; ++k0)
                 fin[head_state + (size_t)k0 * 128 + j] = init ? init[head_state + (size_t)k0 * 128 + j] : 0.f;
     } else {
         if (tid == 0) {
-            issue_load(0);
-            if (nchunks > 1) issue_load(1);
+            issue_loads(0, true);
+            issue_loads(1, false);
         }
-        // initial state, keys [64 hf, 64 hf + 64) of column j: fp16 copy -> S^T,
+        // initial state, keys [32 qd, 32 qd + 32) of column j: fp16 copy -> S^T,
         // and Diag(e^{a_C}) S0 (the first chunk's decay) -> TMEM
+        float s0[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            s0[e] = init ? init[head_state + (size_t)(32 * qd + e) * 128 + j] : 0.f;
+        sync_check();  // thread 0's first load was issued (or failed)
         wait(bL0, 0);
         {
-            const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam);
-#pragma unroll 1
-            for (int k0 = 64 * hf; k0 < 64 * hf + 64; k0 += 16) {
-                float s[16];
+            const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam) + 32 * qd;
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    s[e] = init ? init[head_state + (size_t)(k0 + e) * 128 + j] : 0.f;
+            for (int gi = 0; gi < 4; ++gi) {
+                const float *x = &s0[8 * gi];
                 uint4 pk;
-                pk.x = pack_f16(s[0], s[1]); pk.y = pack_f16(s[2], s[3]);
-                pk.z = pack_f16(s[4], s[5]); pk.w = pack_f16(s[6], s[7]);
-                *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0)) = pk;
-                pk.x = pack_f16(s[8], s[9]); pk.y = pack_f16(s[10], s[11]);
-                pk.z = pack_f16(s[12], s[13]); pk.w = pack_f16(s[14], s[15]);
-                *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, k0 + 8)) = pk;
-#pragma unroll
-                for (int e = 0; e < 16; ++e) s[e] *= gam0[k0 + e];
-                tc::tmem_st16(tlane + kColS + k0, s);
+                pk.x = pack_f16(x[0], x[1]); pk.y = pack_f16(x[2], x[3]);
+                pk.z = pack_f16(x[4], x[5]); pk.w = pack_f16(x[6], x[7]);
+                *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 32 * qd + 8 * gi)) = pk;
             }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s0[e] *= gam0[e];
+            tc::tmem_st16(tlane + kColS + 32 * qd, s0);
+            tc::tmem_st16(tlane + kColS + 32 * qd + 16, s0 + 16);
             tc::tmem_wait_st();
         }
         tc::fence_async_smem();
@@ -783,16 +905,16 @@ __global__ void __launch_bounds__(kRecThreads, 1)
             const unsigned char *buf = smem + buf_off(c);
             const int tcc = t0 + c * C, L = min(C, t1 - tcc);
 
-            // U^T = U~^T - P^T for t in [32 hf, 32 hf + 32) -> shared (fp16)
+            // U^T = U~^T - P^T for t in [16 qd, 16 qd + 16) -> shared (fp16)
             wait(bL(c), (uint32_t)((c >> 1) & 1));
             wait(bM1, (uint32_t)(c & 1));
             tc::fence_after_sync();
             {
-                uint32_t pr[2][16];
-                tc::tmem_ld_cols<2>(tlane + kColP + 32 * hf, pr);
-                const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch + 64 * hf;
+                uint32_t pr[1][16];
+                tc::tmem_ld_cols<1>(tlane + kColP + 16 * qd, pr);
+                const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch + 32 * qd;
 #pragma unroll
-                for (int gi = 0; gi < 4; ++gi) {
+                for (int gi = 0; gi < 2; ++gi) {
                     const uint4 u = *reinterpret_cast<const uint4 *>(ut + 16 * gi);
                     const __half2 *hu = reinterpret_cast<const __half2 *>(&u);
                     uint4 pk;
@@ -801,40 +923,47 @@ __global__ void __launch_bounds__(kRecThreads, 1)
                     for (int e = 0; e < 4; ++e) {
                         const float2 a = __half22float2(hu[e]);
                         const int t = 8 * gi + 2 * e;
-                        w[e] = pack_f16(a.x - __uint_as_float(pr[t >> 4][t & 15]),
-                                        a.y - __uint_as_float(pr[(t + 1) >> 4][(t + 1) & 15]));
+                        w[e] = pack_f16(a.x - __uint_as_float(pr[0][t]),
+                                        a.y - __uint_as_float(pr[0][t + 1]));
                     }
-                    *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, 32 * hf + 8 * gi)) = pk;
+                    *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, 16 * qd + 8 * gi)) = pk;
                 }
             }
             tc::fence_async_smem();
             sync_check();
-            if (tid == 0 && !failed) issue_mma2(c);
+            if (tid == 0 && !failed) {
+                issue_mma2(c);
+                issue_loads(c + 1, false);
+            }
 
-            // new state (keys [64 hf, +64)) and this chunk's O (t in [32 hf, +32))
+            // new state (keys [32 qd, +32)) and this chunk's O (t in [16 qd, +16))
             wait(bM2, (uint32_t)(c & 1));
             tc::fence_after_sync();
-            uint32_t sr[4][16], orr[2][16];
-            tc::tmem_ld_cols<4>(tlane + kColS + 64 * hf, sr);
-            tc::tmem_ld_cols<2>(tlane + kColO + 32 * hf, orr);
+            uint32_t sr[2][16], orr[1][16];
+            tc::tmem_ld_cols<2>(tlane + kColS + 32 * qd, sr);
+            tc::tmem_ld_cols<1>(tlane + kColO + 16 * qd, orr);
             if (c + 1 < nchunks) {
 #pragma unroll
-                for (int gi = 0; gi < 8; ++gi) {
+                for (int gi = 0; gi < 4; ++gi) {
                     const uint32_t *x = &sr[gi >> 1][(gi & 1) * 8];
                     uint4 pk;
                     pk.x = pack_f16(__uint_as_float(x[0]), __uint_as_float(x[1]));
                     pk.y = pack_f16(__uint_as_float(x[2]), __uint_as_float(x[3]));
                     pk.z = pack_f16(__uint_as_float(x[4]), __uint_as_float(x[5]));
                     pk.w = pack_f16(__uint_as_float(x[6]), __uint_as_float(x[7]));
-                    *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 64 * hf + 8 * gi)) = pk;
+                    *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 32 * qd + 8 * gi)) = pk;
                 }
             } else if (fin) {
 #pragma unroll
-                for (int e = 0; e < 64; ++e)
-                    fin[head_state + (size_t)(64 * hf + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
+                for (int e = 0; e < 32; ++e)
+                    fin[head_state + (size_t)(32 * qd + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
             }
-            // this chunk's buffer is no longer read: fetch chunk c + 2 into it
-            if (tid == 0 && c + 2 < nchunks && !failed) issue_load(c + 2);
+            // this chunk's buffer is no longer read: chunk c + 2 may use it; chunk
+            // c + 1 must be on its way before anyone waits for it
+            if (tid == 0) {
+                issue_loads(c + 1, true);
+                issue_loads(c + 2, false);
+            }
             if (c + 1 < nchunks) wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
             tc::fence_async_smem();
             sync_check();
@@ -843,24 +972,24 @@ __global__ void __launch_bounds__(kRecThreads, 1)
             // while the next product runs: pre-scale the state by the next chunk's
             // decay, and write this chunk's output rows
             if (c + 1 < nchunks) {
-                const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam) + 64 * hf;
+                const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam) + 32 * qd;
 #pragma unroll
-                for (int gi = 0; gi < 4; ++gi) {
+                for (int gi = 0; gi < 2; ++gi) {
                     float vv[16];
 #pragma unroll
                     for (int e = 0; e < 16; ++e) vv[e] = __uint_as_float(sr[gi][e]) * gam[16 * gi + e];
-                    tc::tmem_st16(tlane + kColS + 64 * hf + 16 * gi, vv);
+                    tc::tmem_st16(tlane + kColS + 32 * qd + 16 * gi, vv);
                 }
                 tc::tmem_wait_st();
             }
             __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO);
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-                sO[(32 * hf + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[e >> 4][e & 15]));
+            for (int e = 0; e < 16; ++e)
+                sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[0][e]));
             __syncthreads();
 #pragma unroll
-            for (int m = 0; m < 4; ++m) {
-                const int qd = tid + kRecThreads * m, t = qd >> 4, c8 = (qd & 15) * 8;
+            for (int m = 0; m < 2; ++m) {
+                const int id = tid + kRecThreads * m, t = id >> 4, c8 = (id & 15) * 8;
                 if (t < L)
                     *reinterpret_cast<uint4 *>(&out[((size_t)(tcc + t) * H + h) * 128 + c8]) =
                         *reinterpret_cast<const uint4 *>(&sO[t * 128 + c8]);
@@ -869,7 +998,7 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     }
 
     if (failed) {
-        if (tid == 0) atomicOr(status, kStatusTimeout);
+        if (tid == 0) atomicOr(ra.status, kStatusTimeout);
         // let any copy or MMA still in flight land before the TMEM is released
         tc::mbar_wait(bM1, 0, 10000000ull);
         tc::mbar_wait(bM2, 0, 10000000ull);
@@ -879,14 +1008,67 @@ __global__ void __launch_bounds__(kRecThreads, 1)
     if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
 }
 
+__global__ void __launch_bounds__(kRecThreads, 1) recur_kernel(RecArgs ra) {
+    recur_chain(ra, blockIdx.x, nullptr);
+}
+
+// K1 and K2 in one cooperative launch (every CTA resident): CTAs [0, nchains)
+// run the chains, the rest prepare blocks in chunk-major order and publish
+// each one through `ready`. Producers never wait, so the chains always make
+// progress; every wait of a chain is bounded.
+constexpr uint32_t kFusedSmem = kRecSmem > (uint32_t)kPrepSmem ? kRecSmem : (uint32_t)kPrepSmem;
+__global__ void __launch_bounds__(kRecThreads, 1)
+    fused_kernel(PrepArgs pa, RecArgs ra, int nchains, int *ready) {
+    if ((int)blockIdx.x < nchains) recur_chain(ra, blockIdx.x, ready);
+    else prep_loop(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
+}
+
 }  // namespace pf
 
-// Workspace: [0, 256) status word | schedule (N + 1 int32, padded) | chunk blocks
+// Workspace: [0, 256) status word | schedule (N + 2 int32, varlen only) |
+// ready flags (one int32 per chunk block) | chunk blocks; each region 256-byte padded.
+namespace {
+size_t pad256(size_t x) { return (x + 255) / 256 * 256; }
+long long prefill_slots(int N, long long T, long long T_total, bool varlen) {
+    return varlen ? (T_total + pf::C - 1) / pf::C + N : (long long)N * ((T + pf::C - 1) / pf::C);
+}
+}  // namespace
+
 size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen) {
-    const long long slots = varlen ? (T_total + pf::C - 1) / pf::C + N
-                                   : (long long)N * ((T + pf::C - 1) / pf::C);
-    const size_t sched = varlen ? (((size_t)(N + 1) * 4 + 255) / 256) * 256 : 0;
-    return 256 + sched + (size_t)slots * H * pf::kBlock;
+    const long long slots = prefill_slots(N, T, T_total, varlen);
+    const size_t sched = varlen ? pad256((size_t)(N + 2) * 4) : 0;
+    return 256 + sched + pad256((size_t)slots * H * 4) + (size_t)slots * H * pf::kBlock;
+}
+
+// Which schedule runs: the fused cooperative kernel when the chains leave most
+// SMs to the producers (N H <= SMs / 3), else K1 then K2. The environment
+// variable KDA_PREFILL_SCHEDULE = "split" or "fused" overrides the choice
+// ("fused" still needs N H < SMs and a cooperative launch).
+// Returns 1 (fused), 0 (K1 then K2) or -1 (the device could not be queried).
+int prefill_tc_schedule(long long nchains, long long nitems) {
+    int dev = 0, nsm = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+        return -1;
+    const char *env = getenv("KDA_PREFILL_SCHEDULE");
+    bool fused = 3 * nchains <= nsm;
+    if (env && strcmp(env, "split") == 0) fused = false;
+    if (env && strcmp(env, "fused") == 0) fused = nchains < nsm;
+    fused = fused && nitems > 0 && coop;
+    if (!fused) return 0;
+    if (cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)pf::kFusedSmem) != cudaSuccess)
+        return -1;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::fused_kernel, pf::kRecThreads,
+                                                      pf::kFusedSmem) != cudaSuccess)
+        return -1;
+    return per_sm >= 1 ? 1 : 0;
+}
+
+int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen) {
+    return prefill_tc_schedule((long long)N * H, prefill_slots(N, T, T_total, varlen) * H);
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
@@ -901,32 +1083,47 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                              (int)pf::kRecSmem);
     if (e != cudaSuccess) return e;
     uint32_t *status = reinterpret_cast<uint32_t *>(ws);
+    const bool varlen = cu != nullptr;
+    const long long slots = prefill_slots(N, T, T_total, varlen);
+    const long long nitems = slots * H;
+    if (nitems > 0x7fffffffLL) return cudaErrorInvalidValue;
+    size_t off = 256;
     int32_t *first_chunk = nullptr;
-    unsigned char *blocks = ws + 256;
-    long long slots;
-    if (cu) {
-        first_chunk = reinterpret_cast<int32_t *>(ws + 256);
-        blocks = ws + 256 + (((size_t)(N + 1) * 4 + 255) / 256) * 256;
-        pf::schedule_kernel<<<1, 1024, 0, stream>>>(cu, N, first_chunk);
-        slots = ((long long)T_total + pf::C - 1) / pf::C + N;
-    } else {
-        slots = (long long)N * ((T + pf::C - 1) / pf::C);
+    if (varlen) {
+        first_chunk = reinterpret_cast<int32_t *>(ws + off);
+        off += pad256((size_t)(N + 2) * 4);
     }
-    if (slots > 0) {
-        int dev = 0, nsm = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return cudaErrorUnknown;
-        const long long nitems = slots * H;
+    int *ready = reinterpret_cast<int *>(ws + off);
+    off += pad256((size_t)nitems * 4);
+    unsigned char *blocks = ws + off;
+    const long long nchains = (long long)N * H;
+    const int sched = prefill_tc_schedule(nchains, nitems);
+    int dev = 0, nsm = 0;
+    if (sched < 0 || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorUnknown;
+    if (varlen) pf::schedule_kernel<<<1, 1024, 0, stream>>>(cu, N, T_total, first_chunk, status);
+    const bool fused = sched == 1;
+
+    pf::PrepArgs pa{static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
+                    static_cast<const __nv_bfloat16 *>(v), g,
+                    static_cast<const __nv_bfloat16 *>(beta), cu, first_chunk, N, T, H,
+                    (int)nitems, blocks};
+    pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
+                   static_cast<__nv_bfloat16 *>(out), fin, status};
+    if (fused) {
+        e = cudaMemsetAsync(ready, 0, (size_t)nitems * 4, stream);
+        if (e != cudaSuccess) return e;
+        int nch = (int)nchains;
+        void *args[] = {&pa, &ra, &nch, &ready};
+        return cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(nsm),
+                                           dim3(pf::kRecThreads), args, pf::kFusedSmem, stream);
+    }
+    if (nitems > 0) {
         const int grid = (int)(nitems < nsm ? nitems : nsm);  // one persistent CTA per SM
-        pf::prep_kernel<<<grid, pf::kPrepThreads, pf::kPrepSmem, stream>>>(
-            static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-            static_cast<const __nv_bfloat16 *>(v), g, static_cast<const __nv_bfloat16 *>(beta),
-            cu, first_chunk, N, T, H, (int)nitems, blocks, status);
+        pf::prep_kernel<<<grid, pf::kPrepThreads, pf::kPrepSmem, stream>>>(pa);
     }
-    pf::recur_kernel<<<(unsigned)((long long)N * H), pf::kRecThreads, pf::kRecSmem, stream>>>(
-        cu, first_chunk, N, T, T_total, H, scale, init, blocks,
-        static_cast<__nv_bfloat16 *>(out), fin, status);
+    pf::recur_kernel<<<(unsigned)nchains, pf::kRecThreads, pf::kRecSmem, stream>>>(ra);
     return cudaGetLastError();
 }
 

@@ -42,12 +42,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # bf16: status word + one 76288-byte prepared block per (chunk, head)
+    # bf16: status word + one 76288-byte prepared block and one 4-byte ready
+    # flag per (chunk, head)
     assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 128 * 32 * 76288
     assert kda.kda_prefill_workspace_size(4, 100, 2, 128, 64, kda.KDA_BF16) >= 4 * 2 * 2 * 76288
     # packed: T is the total; one spare chunk slot per sequence at most
     vl = kda.kda_prefill_workspace_size(64, 1 << 20, 32, 128, 64, kda.KDA_BF16, varlen=True)
-    assert ((1 << 20) // 64) * 32 * 76288 <= vl <= ((1 << 20) // 64 + 64) * 32 * 76288 + 4096
+    assert ((1 << 20) // 64) * 32 * 76288 <= vl <= ((1 << 20) // 64 + 64) * 32 * 76292 + 4096
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_F32) >= 256
     assert kda.kda_prefill_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16) == 0      # D != 128
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_BF16) == 0     # chunk
@@ -83,6 +84,20 @@ def test_prefill_argument_validation(lib):
         == kda.KDA_ERR_INVALID_ARG                                       # size overflow
     # N = 0 is a valid empty call: nothing is launched
     assert _prefill(lib, N=0, ws=fake, ws_bytes=256) == kda.KDA_OK
+
+
+def test_prefill_schedule_query(lib):
+    f = lib.kda_prefill_schedule
+    # invalid sizes: the negated status, no device needed
+    assert f(1, 64, 2, 64, 64, kda.KDA_BF16, 0) == -kda.KDA_ERR_UNSUPPORTED
+    assert f(1, 64, 2, 128, 16, kda.KDA_BF16, 0) == -kda.KDA_ERR_UNSUPPORTED
+    assert f(-1, 64, 2, 128, 64, kda.KDA_BF16, 0) == -kda.KDA_ERR_INVALID_ARG
+    # fp32 I/O has one schedule
+    assert f(1, 64, 2, 128, 16, kda.KDA_F32, 0) == kda.KDA_SCHEDULE_DIRECT
+    assert kda.kda_prefill_schedule(3, 100, 2, 128, 64, kda.KDA_F32, True) == \
+        kda.KDA_SCHEDULE_DIRECT
+    with pytest.raises(kda.KDAError):
+        kda.kda_prefill_schedule(1, 64, 0, 128, 64, kda.KDA_BF16)
 
 
 def test_decode_argument_validation(lib):

@@ -314,3 +314,54 @@ def test_varlen_full_size():
     chains = [(int(order[-1]), 3), (int(order[0]), 31), (int(order[32]), 0), (7, 17), (40, 9),
               (63, 20)]
     sampled_chain_check(x, out, fin, lens, chains, x.init_state.cpu(), TOL_BF16)
+
+
+# ---------------------------------------------------------------- schedules
+@pytest.mark.parametrize("lens,H", [([1000], 3), ([5, 0, 129, 1], 2), ([64] * 40, 2)])
+def test_bf16_split_and_fused_schedules_agree(monkeypatch, lens, H):
+    """The two-kernel schedule and the fused cooperative one run the same
+    arithmetic: both match the oracle and agree bit for bit. ([64] * 40 with
+    H = 2 is 80 chains, over a third of the SMs: the automatic choice there is
+    the two-kernel schedule.)"""
+    x = inputs.prefill_inputs(lens, H=H, io="bf16", seed=21, init="normal")
+    res = {}
+    for mode in ("split", "fused"):
+        monkeypatch.setenv("KDA_PREFILL_SCHEDULE", mode)
+        res[mode] = run_gpu_prefill(x, 64)
+    monkeypatch.delenv("KDA_PREFILL_SCHEDULE")
+    ro, rf = oracle_prefill(x)
+    for mode, (out, fin) in res.items():
+        eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
+        assert eo <= TOL_BF16 and ef <= TOL_BF16, (mode, eo, ef)
+    assert torch.equal(res["split"][0], res["fused"][0])
+    assert torch.equal(res["split"][1], res["fused"][1])
+
+
+def test_bf16_non_monotone_offsets_skip_the_call():
+    """Offsets that go back and forth (each upward sequence in range on its
+    own, but together more chunks than the workspace holds): flagged, and
+    nothing is written."""
+    T_total, N = 129, 9
+    x = inputs.prefill_inputs([T_total], H=1, io="bf16", seed=22)
+    cu = torch.tensor([0 if i % 2 == 0 else T_total for i in range(N + 1)], dtype=torch.int32,
+                      device=DEV)
+    out = torch.full((T_total, 1, 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    fin = torch.full((N, 1, 128, 128), 7.0, dtype=torch.float32, device=DEV)
+    ws = kda.prefill_workspace(x.q.to(DEV), cu, chunk=64)
+    kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV), x.beta.to(DEV), x.scale,
+                    cu_seqlens=cu, chunk=64, out=out, final_state=fin, workspace=ws)
+    assert kda.kda_workspace_status(ws) == kda.KDA_ERR_DEVICE
+    assert torch.all(out == 7.0) and torch.all(fin == 7.0)
+
+
+def test_prefill_schedule_choice(monkeypatch):
+    """Few chains (N H <= SMs / 3): fused; many chains: split; the
+    environment variable overrides."""
+    f = kda.kda_prefill_schedule
+    monkeypatch.delenv("KDA_PREFILL_SCHEDULE", raising=False)
+    assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
+    assert f(64, 1 << 16, 32, 128, 64, kda.KDA_BF16, True) == kda.KDA_SCHEDULE_SPLIT
+    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", "split")
+    assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_SPLIT
+    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", "fused")
+    assert f(40, 64, 2, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
