@@ -339,16 +339,32 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
         cp_async_commit();
     };
-    // the item that the staged inputs belong to (-1: none)
+    // token tid of an item (raw bits: converted only where used, so that the
+    // load does not stall the issuing warp)
+    auto load_beta = [&](int tc_, int h_, int L_) -> unsigned short {
+        return tid < L_ ? __bfloat16_as_ushort(beta[((size_t)tc_ + tid) * H + h_]) : (unsigned short)0;
+    };
+    // the item that the staged inputs belong to (-1: none); its beta (tid < C)
     int staged = -1;
+    unsigned short beta_next = 0;
     {
         int slot_, h_, tc_, L_;
         if (first < nitems && decode(first, slot_, h_, tc_, L_)) {
             stage_g(tc_, h_, L_);
             stage_qkv(tc_, h_, L_);
+            if (tid < C) beta_next = load_beta(tc_, h_, L_);
             staged = first;
         }
     }
+    // With `ready`: the previous item's flag (-1: none) is released by one lane
+    // of the last warp during this item's Gram phase, where that warp would
+    // otherwise wait for the others; the proxy fence that makes the block
+    // visible to bulk copies comes before this item's first barrier.
+    constexpr int kReleaser = kPrepThreads - 32;
+    long long pending = -1;
+    auto release = [&](long long idx) {
+        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + idx), "r"(1u) : "memory");
+    };
 
 #pragma unroll 1
     for (int item = first; item < nitems; item += stride) {
@@ -357,14 +373,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (staged != item) {  // the previous item could not prefetch this one
         stage_g(tc, h, L);
         stage_qkv(tc, h, L);
+        if (tid < C) beta_next = load_beta(tc, h, L);
     }
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
-    const size_t row0 = (size_t)tc * H + h;  // row index of token tc, head h
     int nslot, nh, ntc, nL;  // the next item of this CTA
     const int nitem = item + stride;
     const bool has_next = nitem < nitems && decode(nitem, nslot, nh, ntc, nL);
 
-    if (tid < C) sBeta[tid] = tid < L ? __bfloat162float(beta[(row0 + (size_t)tid * H)]) : 0.f;
+    if (tid < C) sBeta[tid] = __bfloat162float(__ushort_as_bfloat16(beta_next));
+    if (pending >= 0) asm volatile("fence.proxy.async.global;\n" ::: "memory");
     cp_async_wait_all();
     __syncthreads();
 
@@ -403,10 +420,13 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
     }
     // this item's q, k, v: out of the staging area before it is overwritten
+    // operand-phase mapping: tokens 2 (tid / 16) + m (one 16-token tile per
+    // warp), channels 8 (tid % 16) .. + 8
+    const int op_c0 = (tid & 15) * 8, op_t0 = 2 * (tid >> 4), op_i = tid >> 7;
     uint4 uq[2], uk[2], uv[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-        const int id = tid + kPrepThreads * m, t = id >> 4, c8 = (id & 15) * 8;
+        const int t = op_t0 + m, c8 = op_c0;
         const uint32_t so = (uint32_t)(t * 256 + c8 * 2);
         uq[m] = *reinterpret_cast<const uint4 *>(smem + kOffKh + so);
         uk[m] = *reinterpret_cast<const uint4 *>(smem + kOffKh + C * 256 + so);
@@ -422,20 +442,21 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         __half *sKtb = reinterpret_cast<__half *>(smem + kOffKtb);
         __half *sVb = reinterpret_cast<__half *>(smem + kOffVb);
         __half *sKbS = reinterpret_cast<__half *>(smem + kOffKbS);
+        const int c0 = op_c0, i = op_i;
+        const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
+        float r[8], er[8], ed[8], ec[8];  // per-tile values, shared by both tokens
+        lds8(&sRef[i * 128 + c0], r);
+        lds8(&tab[(kTabEr + i) * 128 + c0], er);
+        lds8(&tab[(kTabEd + i) * 128 + c0], ed);
+        lds8(&tab[(kTabEc + i) * 128 + c0], ec);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            const int id = tid + kPrepThreads * m, t = id >> 4, c0 = (id & 15) * 8, i = t >> 4;
-            float qq[8], kk[8], vv[8], a[8], r[8];
+            const int t = op_t0 + m;
+            float qq[8], kk[8], vv[8], a[8];
             unpack8_bf16(uq[m], qq);
             unpack8_bf16(uk[m], kk);
             unpack8_bf16(uv[m], vv);
             lds8(&sAcum[t * 128 + c0], a);
-            lds8(&sRef[i * 128 + c0], r);
-            const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
-            float er[8], ed[8], ec[8];
-            lds8(&tab[(kTabEr + i) * 128 + c0], er);
-            lds8(&tab[(kTabEd + i) * 128 + c0], ed);
-            lds8(&tab[(kTabEc + i) * 128 + c0], ec);
             const float bt = sBeta[t];
             float x[8], ix[8], y[8], o[8], md = 0.f;
 #pragma unroll
@@ -518,17 +539,25 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             int tt = task % 10, i = 0;
             while (tt > i) { tt -= i + 1; ++i; }
             const int j = tt;
-            float acc[2][4] = {};
+            float acc[2][4] = {}, acc2[2][4] = {};  // even / odd k steps: two chains each
             const uint32_t aX = mm == 0 ? aXk : aXq;
             const uint32_t aB = aKh + (uint32_t)(kh_slot(i, j) * 16 * kLDK) * 2u;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t af[4], bf[4];
+            for (int ks = 0; ks < 8; ks += 2) {
+                uint32_t af[4], bf[4], af2[4], bf2[4];
                 frag_a_rowmajor(af, aX, kLDK, 16 * i, 16 * ks, lane);
                 frag_b_nk(bf, aB, kLDK, 0, 16 * ks, lane);
+                frag_a_rowmajor(af2, aX, kLDK, 16 * i, 16 * ks + 16, lane);
+                frag_b_nk(bf2, aB, kLDK, 0, 16 * ks + 16, lane);
                 mma_bf16_16816(acc[0], af, bf[0], bf[1]);
                 mma_bf16_16816(acc[1], af, bf[2], bf[3]);
+                mma_bf16_16816(acc2[0], af2, bf2[0], bf2[1]);
+                mma_bf16_16816(acc2[1], af2, bf2[2], bf2[3]);
             }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -546,6 +575,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                     }
                 }
         }
+        if (pending >= 0 && tid == kReleaser) {
+            release(pending);
+            pending = -1;
+        }
         // blocks above the diagonal: zero in A (shared) and in M (the block)
         for (int idx = tid; idx < 6 * 128; idx += kPrepThreads) {
             const int b_ = idx >> 7, e = idx & 127;
@@ -560,6 +593,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     __syncthreads();
     if (has_next) {  // column tiles and the transpose staging are free from here on
         stage_qkv(ntc, nh, nL);
+        if (tid < C) beta_next = load_beta(ntc, nh, nL);
         staged = nitem;
     }
 
@@ -712,14 +746,13 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 }
         }
     }
-    if (ready) asm volatile("fence.proxy.async.global;\n" ::: "memory");  // read by bulk copies
     __syncthreads();  // shared memory is reused by the next item
-    if (ready && tid == 0) {
-        __threadfence();
-        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + (size_t)slot * H + h),
-                     "r"(1u)
-                     : "memory");
+    if (ready) pending = (long long)slot * H + h;
     }
+    if (pending >= 0) {  // the last item of this CTA
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        __syncthreads();
+        if (tid == kReleaser) release(pending);
     }
 }
 

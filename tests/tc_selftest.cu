@@ -1,7 +1,8 @@
-// Self-test of the tcgen05 helpers (kda_tcgen05.cuh): one CTA issues a
-// 128 x N x K tensor-core MMA from shared-memory tiles in the no-swizzle
-// core-matrix layouts and writes D (fp32) back. Built and called only by
-// tests/test_tcgen05_layouts.py.
+// Self-test of the tcgen05 helpers (kda_tcgen05.cuh): one CTA issues an
+// M x N x K tensor-core MMA (M = 64 or 128) from shared-memory tiles in the
+// no-swizzle core-matrix layouts and writes all 128 TMEM lanes of the first
+// N columns back, so that the test sees where each row of D lands. Built and
+// called only by tests/test_tcgen05_layouts.py.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,22 +14,29 @@ using namespace kda::tc;
 
 __global__ void __launch_bounds__(128, 1)
     tc_selftest_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
-                       float *__restrict__ D, int N, int K, int b_mn, int f16, int mn_swap,
-                       int *err) {
+                       float *__restrict__ D, int M, int N, int K, int a_mn, int b_mn, int f16,
+                       int mn_swap, int *err) {
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t bar;
     __shared__ uint32_t tmem_base;
-    constexpr int M = 128;
     unsigned char *sA = smem;
-    unsigned char *sB = smem + M * K * 2;
+    unsigned char *sB = smem + 128 * 128 * 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    const uint32_t lboA = 128, sboA = (uint32_t)(K / 8) * 128;
+    uint32_t lboA = 128, sboA = (uint32_t)(K / 8) * 128;      // K-major A (M x K)
+    if (a_mn) { lboA = (uint32_t)(M / 8) * 128; sboA = 128; } // MN-major: M groups adjacent
     uint32_t lboB = 128, sboB = (uint32_t)(K / 8) * 128;     // K-major B (N x K)
     if (b_mn) { lboB = (uint32_t)(N / 8) * 128; sboB = 128; } // MN-major: N groups adjacent
-    for (int i = tid; i < M * K; i += blockDim.x) {
-        const int r = i / K, k = i % K;
-        *reinterpret_cast<uint16_t *>(sA + kmajor_off(r, k, lboA, sboA)) = A[i];
+    if (!a_mn) {
+        for (int i = tid; i < M * K; i += blockDim.x) {  // A given as A[M][K]
+            const int r = i / K, k = i % K;
+            *reinterpret_cast<uint16_t *>(sA + kmajor_off(r, k, lboA, sboA)) = A[i];
+        }
+    } else {
+        for (int i = tid; i < K * M; i += blockDim.x) {  // A given as At[K][M]
+            const int k = i / M, r = i % M;
+            *reinterpret_cast<uint16_t *>(sA + mnmajor_off(k, r, lboA, sboA)) = A[i];
+        }
     }
     if (!b_mn) {
         for (int i = tid; i < N * K; i += blockDim.x) {  // B given as Bt[N][K]
@@ -55,13 +63,13 @@ __global__ void __launch_bounds__(128, 1)
     fence_after_sync();
     const uint32_t tm = tmem_base;
     if (tid == 0) {
-        const uint32_t idesc = idesc_f16(M, N, f16, 0, b_mn);
+        const uint32_t idesc = idesc_f16(M, N, f16, a_mn, b_mn);
         // descriptor fields for B; mn_swap = 1 passes them in the opposite
         // order (the test shows that order is wrong)
         const uint32_t dlbo = (b_mn && mn_swap) ? sboB : lboB;
         const uint32_t dsbo = (b_mn && mn_swap) ? lboB : sboB;
         for (int ks = 0; ks < K / 16; ++ks) {
-            const uint64_t da = smem_desc(smem_u32(sA) + ks * 2 * lboA, lboA, sboA);
+            const uint64_t da = smem_desc(smem_u32(sA) + ks * 2 * lboA, lboA, sboA);  // 2 k groups
             const uint32_t bstep = 2 * lboB;  // two core matrices along K
             const uint64_t db = smem_desc(smem_u32(sB) + ks * bstep, dlbo, dsbo);
             mma_f16(tm, da, db, idesc, ks > 0 ? 1u : 0u);
@@ -85,8 +93,9 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tm, 256);
 }
 
-extern "C" int tc_selftest(const void *A, const void *B, float *D, int N, int K, int b_mn,
-                           int f16, int mn_swap, int *err) {
+extern "C" int tc_selftest(const void *A, const void *B, float *D, int M, int N, int K, int a_mn,
+                           int b_mn, int f16, int mn_swap, int *err) {
+    if (M != 64 && M != 128) return 1;
     if (N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16) return 1;
     // The whole 227 KB window is allocated so that a descriptor read with the
     // byte-offset fields in either order stays inside this CTA's shared memory.
@@ -95,8 +104,8 @@ extern "C" int tc_selftest(const void *A, const void *B, float *D, int N, int K,
                              smem) != cudaSuccess)
         return 2;
     tc_selftest_kernel<<<1, 128, smem>>>(static_cast<const uint16_t *>(A),
-                                         static_cast<const uint16_t *>(B), D, N, K, b_mn, f16,
-                                         mn_swap, err);
+                                         static_cast<const uint16_t *>(B), D, M, N, K, a_mn, b_mn,
+                                         f16, mn_swap, err);
     if (cudaGetLastError() != cudaSuccess) return 3;
     return cudaDeviceSynchronize() == cudaSuccess ? 0 : 4;
 }

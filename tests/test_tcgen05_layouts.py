@@ -1,6 +1,8 @@
-"""GPU self-test of the tcgen05 helpers: a 128 x N x K MMA from shared-memory
-tiles in the no-swizzle core-matrix layouts (K-major and MN-major operands,
-bf16 and fp16), compared with a host matmul."""
+"""GPU self-test of the tcgen05 helpers: an M x N x K MMA (M = 128 or 64) from
+shared-memory tiles in the no-swizzle core-matrix layouts (K-major and
+MN-major operands, bf16 and fp16), compared with a host matmul. For M = 64 the
+test also pins which TMEM lanes hold the rows of D: rows 16 w .. 16 w + 15 in
+lanes 32 w .. 32 w + 15 (the first half of each warp's lane quarter)."""
 import ctypes
 import os
 import subprocess
@@ -22,24 +24,36 @@ def lib(tmp_path_factory):
                                           os.path.join(HERE, "tc_selftest.cu"), "-o", out]
     subprocess.check_call(cmd)
     L = ctypes.CDLL(out)
-    L.tc_selftest.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 5 + [ctypes.c_void_p]
+    L.tc_selftest.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 7 + [ctypes.c_void_p]
     L.tc_selftest.restype = ctypes.c_int
     return L
 
 
-def run(lib, N, K, b_mn, f16, mn_swap=0):
+def M64_LANE(m):
+    return 32 * (m // 16) + m % 16
+
+
+def mma_lanes(lib, M, N, K, a_mn, b_mn, f16, mn_swap=0):
+    """(all 128 TMEM lanes x N columns after the MMA, the host product)."""
     dt = torch.float16 if f16 else torch.bfloat16
-    g = torch.Generator().manual_seed(N * 1000 + K)
-    A = torch.randn(128, K, generator=g).to(dt)
+    g = torch.Generator().manual_seed(M * 7 + N * 1000 + K)
+    A = torch.randn(M, K, generator=g).to(dt)
     Bkn = torch.randn(K, N, generator=g).to(dt)
+    Adev = (A.t().contiguous() if a_mn else A).cuda()
     Bdev = (Bkn if b_mn else Bkn.t().contiguous()).cuda()
     D = torch.zeros(128, N, dtype=torch.float32, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    rc = lib.tc_selftest(A.cuda().data_ptr(), Bdev.data_ptr(), D.data_ptr(), N, K, b_mn, f16,
-                         mn_swap, err.data_ptr())
+    rc = lib.tc_selftest(Adev.data_ptr(), Bdev.data_ptr(), D.data_ptr(), M, N, K, a_mn, b_mn,
+                         f16, mn_swap, err.data_ptr())
     assert rc == 0 and int(err.item()) == 0, (rc, int(err.item()))
-    ref = A.float() @ Bkn.float()
-    return (D.cpu() - ref).abs().max().item() / ref.abs().max().item()
+    return D.cpu(), A.float() @ Bkn.float()
+
+
+def run(lib, N, K, b_mn, f16, mn_swap=0, M=128, a_mn=0):
+    D, ref = mma_lanes(lib, M, N, K, a_mn, b_mn, f16, mn_swap)
+    if M == 64:
+        D = D[[M64_LANE(m) for m in range(64)]]
+    return (D - ref).abs().max().item() / ref.abs().max().item()
 
 
 @pytest.mark.parametrize("N,K", [(16, 16), (64, 64), (128, 128), (256, 64)])
@@ -54,3 +68,24 @@ def test_mnmajor_b(lib, N, K):
     errs = {swap: run(lib, N, K, 1, f16, swap) for swap in (0, 1) for f16 in (0, 1)}
     assert run(lib, N, K, 1, 0, 0) < 1e-5 and run(lib, N, K, 1, 1, 0) < 1e-5
     assert run(lib, N, K, 1, 1, 1) > 1e-2  # the other field order reads other data
+
+
+@pytest.mark.parametrize("N,K", [(16, 128), (32, 128), (128, 64)])
+def test_m64_lane_map(lib, N, K):
+    """M = 64: each row of D is found in exactly the lane the kernels read."""
+    D, ref = mma_lanes(lib, 64, N, K, 0, 0, 0)
+    scale = ref.abs().max().item()
+    found = {}
+    for m in range(64):
+        errs = (D - ref[m]).abs().max(dim=1).values / scale
+        found[m] = int(torch.argmin(errs))
+        assert errs[found[m]] < 1e-5, (m, float(errs[found[m]]))
+    assert all(found[m] == M64_LANE(m) for m in range(64)), found
+
+
+@pytest.mark.parametrize("M", [64, 128])
+@pytest.mark.parametrize("f16", [0, 1])
+def test_mnmajor_a(lib, M, f16):
+    """A stored MN-major (K rows of M contiguous elements), same field order."""
+    assert run(lib, 64, 64, 0, f16, M=M, a_mn=1) < 1e-5
+    assert run(lib, 128, 64, 1, f16, M=M, a_mn=1) < 1e-5
