@@ -16,25 +16,29 @@
 //   (<= 1 before the tile, <= e^80 inside it); products are e^{a_t - a_s}.
 //
 // Per chunk, with S0 the state at the chunk start:
-//   A = beta * strict_lower(Gram(k, k)),  M = lower(Gram(q, k))   [bf16 mma.sync]
+//   A = beta * strict_lower(Gram(k, k)),  M = lower(Gram(q, k))   [bf16 tcgen05]
 //       (diag(M) = q_t . k_t, which carries no decay, is taken in fp32)
-//   T = (I + A)^{-1}                            [fp32, 16x16 blocks]
-//   W = T (beta k e^{a}),  U~ = T (beta v)      [fp16 mma.sync]
+//   T = (I + A)^{-1}        [fp32 16x16 diagonal blocks, fp16 mma.sync products]
+//   W = T (beta k e^{a}),  U~ = T (beta v)      [fp16 tcgen05]
 //   U = U~ - W S0
 //   O = scale ((q e^{a}) S0 + M U)
 //   S = Diag(e^{a_C}) S0 + (k e^{a_C - a})^T U
 //
 // Kernels:
-//   schedule_kernel  first chunk index of each packed sequence
-//   prep_kernel      K1: one CTA per (chunk, head); writes a 76 KiB chunk
-//                    block in the exact shared-memory layout K2 consumes
+//   schedule_kernel  first chunk index of each packed sequence (and a check of
+//                    the offsets as a whole)
+//   prep_kernel      K1: persistent, one CTA per SM over (chunk, head) items;
+//                    Gram and pseudo-value products on tcgen05; writes a
+//                    76 KiB chunk block in the exact shared-memory layout K2
+//                    consumes
 //   recur_kernel     K2: one CTA per (sequence, head), all 128 value
 //                    columns; per chunk: one bulk TMA load of the block
-//                    (double-buffered), three tcgen05.mma groups with fp32
+//                    (double-buffered), two tcgen05.mma groups with fp32
 //                    accumulators in TMEM and the fp32 state resident in TMEM.
-//                    All 8 warps take part in each step (each thread a half
-//                    of its TMEM lane's columns); the state rescale and the
-//                    output rows overlap the next chunk's first product.
+//                    All 16 warps take part in each step (each thread a
+//                    quarter of its TMEM lane's columns); the state rescale
+//                    and the output rows overlap the next chunk's first product.
+//   fused_kernel     K1 and K2 in one cooperative launch, for few chains
 //
 // In K2 everything is transposed so that the TMEM lane is the value column
 // j (128 lanes):
@@ -56,9 +60,9 @@ constexpr int C = 64;
 
 // ---- chunk block written by K1, read by K2 (byte offsets) ------------------
 constexpr uint32_t kB12 = 0;                      // fp16 K-major [n = (W rows 0..63 | q e^a rows 64..127)][k = key]
-constexpr uint32_t kB3 = kB12 + 128 * 128 * 2;    // fp16 K-major [n = t][k = t']: M
-constexpr uint32_t kB2 = kB3 + 64 * 64 * 2;       // fp16 K-major [n = key][k = t]: k e^{a_C - a}
-constexpr uint32_t kUt = kB2 + 128 * 64 * 2;      // fp16 [j][t], pitch 144 B: U~^T
+constexpr uint32_t kB3 = kB12 + 128 * 128 * 2;    // fp16 MN-major [k = t'][n]: n = t < 64: M[t][t'],
+                                                  //   n = 64 + key: k_t' e^{a_C - a_t'}
+constexpr uint32_t kUt = kB3 + 64 * 192 * 2;      // fp16 [j][t], pitch 144 B: U~^T
 constexpr uint32_t kUtPitch = 144;
 constexpr uint32_t kGam = kUt + 128 * kUtPitch;   // fp32 [128] e^{a_C}
 constexpr uint32_t kBlock = kGam + 128 * 4;       // 76288 B
@@ -72,6 +76,13 @@ __device__ __forceinline__ uint32_t off_k128(int r, int k) {  // K extent 128: S
 __device__ __forceinline__ uint32_t off_k64(int r, int k) {   // K extent 64: SBO 1024
     return (uint32_t)(r >> 3) * 1024u + (uint32_t)(k >> 3) * 128u + (uint32_t)(r & 7) * 16u +
            (uint32_t)(k & 7) * 2u;
+}
+
+// MN-major offsets of the [M ; k e^{a_C - a}] operand: N extent 192 (K group
+// stride 3072, N group stride 128)
+__device__ __forceinline__ uint32_t off_b3(int k, int x) {
+    return (uint32_t)(x >> 3) * 128u + (uint32_t)(k >> 3) * 3072u + (uint32_t)(k & 7) * 16u +
+           (uint32_t)(x & 7) * 2u;
 }
 
 __device__ __forceinline__ void store_h(unsigned char *base, uint32_t off, float x) {
@@ -135,43 +146,65 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
 // ============================================================================
 // K1: chunk preparation
 // ============================================================================
-// One CTA (16 warps) per (chunk, head). One pass over the chunk's tokens
-// builds every operand (q, k, v read once with 16-byte loads); every output
-// goes straight to the chunk block in global memory, already in the
-// core-matrix layout K2 reads.
+// One CTA (16 warps) per SM, persistent over (chunk, head) items. Per item:
+//   cumulative decay a (thread = channel x 16-token tile);
+//   one pass over the tokens builds every operand (thread = 8 channels x two
+//   tokens of one 16-token tile; 8 consecutive lanes take 8 consecutive
+//   tokens, so that their 16-byte stores into the core-matrix layouts fall in
+//   distinct banks);
+//   the Gram products on tcgen05: per row tile i,
+//     D_i^T = Kh_i [Xk_i ; Xq_i]^T   (M = 64 key rows s, N = 32, K = 128),
+//   where Kh_i are the column tiles k_s e^{r_i - a_s} of row tile i (rows of
+//   later tiles in the 64-row window are read and ignored);
+//   T = (I + A)^{-1}: fp32 diagonal blocks, fp16 mma.sync block products;
+//   W = T (beta k e^{a}) (M = 64, N = 128) and U~^T = (beta v)^T T^T
+//   (M = 128, N = 64) on tcgen05.
+// Every output goes to the chunk block in global memory, already in the
+// layout K2 reads.
 constexpr int kPrepThreads = 512;
 constexpr int kPrepWarps = kPrepThreads / 32;
-constexpr int kLDK = 136;  // bf16/fp16 pitch of 128-wide tiles (conflict-free ldmatrix)
-constexpr int kLDC = 72;   // fp16 pitch of C x C tiles
-constexpr int kLDA = 68;   // fp32 pitch of C x C matrices
-constexpr int kOffAcum = 0;                          // fp32 [64][128] a
-constexpr int kOffRef = kOffAcum + C * 128 * 4;      // fp32 [4][128] r_i
-constexpr int kOffQsum = kOffRef + 4 * 128 * 4;      // fp32 [4][128] sum of g per tile
-constexpr int kOffAc = kOffQsum + 4 * 128 * 4;       // fp32 [128] a_C
-constexpr int kOffBeta = kOffAc + 128 * 4;           // fp32 [64]
-constexpr int kOffMd = kOffBeta + C * 4;             // fp32 [64] q_t . k_t
-constexpr int kOffA = kOffMd + C * 4;                // fp32 [64][68] A
+constexpr int kLDC = 72;   // fp16 pitch of the C x C scratch tiles
+constexpr int kAP = 132;   // fp32 pitch of the a buffer (8 consecutive rows start in distinct banks)
+constexpr int kSP = 136;   // bf16 pitch of the staged q, k, v rows (272 B, same reason)
+__host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
+constexpr uint32_t kOffAcum = 0;                               // fp32 [64][132] a (g staged here)
+constexpr uint32_t kOffRef = align1k(kOffAcum + C * kAP * 4);  // fp32 [4][128] r_i
+constexpr uint32_t kOffQsum = kOffRef + 4 * 128 * 4;           // fp32 [4][128] per-tile sums of g
+constexpr uint32_t kOffAc = kOffQsum + 4 * 128 * 4;            // fp32 [128] a_C
+constexpr uint32_t kOffBeta = kOffAc + 128 * 4;                // fp32 [64]
+constexpr uint32_t kOffMdp = kOffBeta + C * 4;                 // fp32 [4][64] partial q_t . k_t
+constexpr uint32_t kOffAd = kOffMdp + 4 * C * 4;               // fp32 [4][16][16] diagonal blocks of A
 // per-channel exponential tables (fp32 [k][128] each), so that every operand
 // needs only x = e^{a_t - r_i} and 1/x per element:
 //   kEr[i] = e^{r_i}; kEd[i] = e^{r_{i+1} - r_i}; kEc[i] = e^{a_C - r_{i+1}};
 //   kE21 = e^{r_2 - r_1}, kE31 = e^{r_3 - r_1}, kE32 = e^{r_3 - r_2}  (r_4 = a_C)
-constexpr int kOffTab = kOffA + C * kLDA * 4;
+constexpr uint32_t kOffTab = kOffAd + 4 * 256 * 4;
 constexpr int kTabEr = 0, kTabEd = 4, kTabEc = 8, kTabE21 = 12, kTabE31 = 13, kTabE32 = 14;
-constexpr int kOffXq = kOffTab + 16 * 128 * 4;       // bf16 [64][136] q e^{a - r_i}
-constexpr int kOffXk = kOffXq + C * kLDK * 2;        // bf16 [64][136] k e^{a - r_i}
-constexpr int kOffKh = kOffXk + C * kLDK * 2;        // bf16 [160][136] k e^{r_i - a}, 10 tiles
-constexpr int kOffKtb = kOffKh + 160 * kLDK * 2;     // fp16 [64][136] beta k e^{a}
-constexpr int kOffVb = kOffKtb + C * kLDK * 2;       // fp16 [64][136] beta v
-constexpr int kOffKbS = kOffVb + C * kLDK * 2;       // fp16 [64][136] k e^{a_C - a} (transpose staging)
-constexpr int kPrepSmem = kOffKbS + C * kLDK * 2;
-// after the Gram phase, inside the Xq / Xk region:
-constexpr int kOffTb = kOffXq;                       // fp16 [64][72] T
-constexpr int kOffAh = kOffTb + C * kLDC * 2;        // fp16 [64][72] A
-constexpr int kOffXh = kOffAh + C * kLDC * 2;        // fp16 [4][16][24] block-product scratch
-static_assert(kOffXh + 4 * 16 * 24 * 2 <= kOffKh, "T scratch inside the row-operand region");
+constexpr uint32_t kOffX = align1k(kOffTab + 16 * 128 * 4);    // bf16 K-major [128][128]: row 32 i + 16 w + t % 16
+constexpr uint32_t kOffKh = kOffX + 128 * 128 * 2;             // bf16 K-major [160][128]: 10 column tiles
+constexpr uint32_t kOffKtb = kOffKh + 160 * 128 * 2;           // fp16 MN-major [s][c]: beta k e^{a}
+constexpr uint32_t kOffVb = kOffKtb + 64 * 128 * 2;            // fp16 MN-major [s][j]: beta v
+constexpr uint32_t kOffVs = kOffVb + 64 * 128 * 2;             // bf16 [64][136]: staged v
+constexpr uint32_t kPrepSmem = kOffVs + C * kSP * 2;
+// after the Gram products, inside X:
+constexpr uint32_t kOffT = kOffX;                              // fp16 K-major [64][64]: T
+constexpr uint32_t kOffAh = kOffT + 64 * 64 * 2;               // fp16 [64][72]: A below the diagonal blocks
+constexpr uint32_t kOffXh = kOffAh + C * kLDC * 2;             // fp16 [4][16][24]: block-product scratch
+static_assert(kOffXh + 4 * 16 * 24 * 2 <= kOffKh, "T scratch inside X");
+// staged q, k of the next item: inside Kh (free after the Gram products)
+constexpr uint32_t kOffQs = kOffKh, kOffKs = kOffKh + C * kSP * 2;
+static_assert(kOffKs + C * kSP * 2 <= kOffKtb, "q, k staging inside Kh");
 static_assert(kPrepSmem <= 227 * 1024, "shared memory budget");
+constexpr uint32_t kPrepTmemCols = 256;  // Gram [0, 128), then W [0, 128); U~^T [128, 192)
 
 __device__ __forceinline__ int kh_slot(int i, int j) { return (i * (i + 1)) / 2 + j; }
+
+// MN-major no-swizzle offsets of element (k, x), x contiguous in groups of 8:
+// N extent 128 (K group stride 2048, N group stride 128)
+__device__ __forceinline__ uint32_t off_mn128(int k, int x) {
+    return (uint32_t)(x >> 3) * 128u + (uint32_t)(k >> 3) * 2048u + (uint32_t)(k & 7) * 16u +
+           (uint32_t)(x & 7) * 2u;
+}
 
 // 16-byte global -> shared copy; bytes past `src_bytes` (0 or 16) are zero-filled
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
@@ -180,6 +213,21 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+// mma.sync fragments of the fp16 T tile kept in the K-major core-matrix layout
+// (K extent 64) that tcgen05 reads: A (16 x 16) = T[m][k], and B = T[k][n].
+__device__ __forceinline__ void frag_a_k64(uint32_t a[4], uint32_t base, int m0, int k0, int lane) {
+    const int r = m0 + (lane & 15);
+    const int c = k0 + ((lane >> 4) << 3);
+    ldsm_x4(a, base + off_k64(r, c));
+}
+__device__ __forceinline__ void frag_b_kn_k64(uint32_t b[4], uint32_t base, int n0, int k0,
+                                              int lane) {
+    const int idx = lane >> 3;
+    const int r = k0 + (lane & 7) + ((idx & 1) << 3);
+    const int c = n0 + ((idx >> 1) << 3);
+    ldsm_x4_t(b, base + off_k64(r, c));
+}
 
 // Sequence and chunk of a chunk slot; false if the slot is past the end.
 __device__ __forceinline__ bool slot_to_chunk(int slot, const int32_t *cu,
@@ -214,6 +262,14 @@ __device__ __forceinline__ uint4 pack8_f16(const float *x) {
     uint4 r;
     r.x = pack_f16(x[0], x[1]); r.y = pack_f16(x[2], x[3]);
     r.z = pack_f16(x[4], x[5]); r.w = pack_f16(x[6], x[7]);
+    return r;
+}
+__device__ __forceinline__ uint4 pack8_f16_u(const uint32_t *x) {  // fp32 bit patterns
+    uint4 r;
+    r.x = pack_f16(__uint_as_float(x[0]), __uint_as_float(x[1]));
+    r.y = pack_f16(__uint_as_float(x[2]), __uint_as_float(x[3]));
+    r.z = pack_f16(__uint_as_float(x[4]), __uint_as_float(x[5]));
+    r.w = pack_f16(__uint_as_float(x[6]), __uint_as_float(x[7]));
     return r;
 }
 __device__ __forceinline__ void unpack8_bf16(uint4 u, float *x) {
@@ -272,7 +328,10 @@ struct PrepArgs {
     int N, T, H;
     int nitems;  // chunk slots x heads
     unsigned char *blocks;
+    uint32_t *status;
 };
+
+constexpr uint64_t kPrepWaitLimit = 2000000000ull;  // 2 s bound on an MMA completion
 
 // K1 over items first, first + stride, ... (slot-major order, or chunk-major
 // when `ready` is given). The next item's g, q, k, v are staged with cp.async
@@ -296,33 +355,52 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         return chunk_major ? item_tokens_cm(idx, H, cu, first_chunk, N, T, slot_, h_, tc_, L_)
                            : item_tokens(idx, H, cu, first_chunk, N, T, slot_, h_, tc_, L_);
     };
+    if (first >= nitems) return;  // no item: no TMEM either
+
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cq = 2 * (lane & 3);
     const int ch = tid & 127, ti4 = tid >> 7;  // cumulative-sum role: (channel, tile)
 
     extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t pbars[2];  // Gram products, W / U~ products
+    __shared__ uint32_t ptmem_slot;
     const uint32_t sbase = smem_u32(smem);
     float *sAcum = reinterpret_cast<float *>(smem + kOffAcum);
     float *sRef = reinterpret_cast<float *>(smem + kOffRef);
     float *sQsum = reinterpret_cast<float *>(smem + kOffQsum);
     float *sAcT = reinterpret_cast<float *>(smem + kOffAc);
     float *sBeta = reinterpret_cast<float *>(smem + kOffBeta);
-    float *sMd = reinterpret_cast<float *>(smem + kOffMd);
-    float *sA = reinterpret_cast<float *>(smem + kOffA);
+    float *sMdp = reinterpret_cast<float *>(smem + kOffMdp);
+    float *sAd = reinterpret_cast<float *>(smem + kOffAd);
+    const uint32_t bG = smem_u32(&pbars[0]), bW = smem_u32(&pbars[1]);
+
+    if (warp == 0) {
+        tc::tmem_alloc(smem_u32(&ptmem_slot), kPrepTmemCols);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        tc::mbar_init(bG, 1);
+        tc::mbar_init(bW, 1);
+        tc::fence_mbar_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tm = ptmem_slot;
+    const uint32_t tquart = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
 
     // Input staging with cp.async (16-byte pieces; padding rows are zero-filled):
     //   g of an item -> the a buffer (dead after the operand phase),
-    //   q, k -> the column-tile region, v -> the transpose staging (both dead
-    //   after the Gram phase).
-    const uint32_t uG = sbase + kOffAcum, uQ = sbase + kOffKh, uK = sbase + kOffKh + C * 256,
-                   uV = sbase + kOffKbS;
+    //   q, k -> the column-tile region (dead after the Gram products), v -> its own buffer.
+    const uint32_t uG = sbase + kOffAcum, uQ = sbase + kOffQs, uK = sbase + kOffKs,
+                   uV = sbase + kOffVs;
     auto stage_g = [&](int tc_, int h_, int L_) {
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
             const int id = tid + kPrepThreads * m, t = id >> 5, c4 = (id & 31) * 4;
             const int ts = t < L_ ? t : 0;
-            cp_async16(uG + (uint32_t)(t * 512 + c4 * 4), g + ((size_t)(tc_ + ts) * H + h_) * 128 + c4,
-                       t < L_ ? 16u : 0u);
+            cp_async16(uG + (uint32_t)(t * kAP * 4 + c4 * 4),
+                       g + ((size_t)(tc_ + ts) * H + h_) * 128 + c4, t < L_ ? 16u : 0u);
         }
         cp_async_commit();
     };
@@ -332,7 +410,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             const int id = tid + kPrepThreads * m, t = id >> 4, c8 = (id & 15) * 8;
             const int ts = t < L_ ? t : 0;
             const size_t off = ((size_t)(tc_ + ts) * H + h_) * 128 + c8;
-            const uint32_t so = (uint32_t)(t * 256 + c8 * 2), n = t < L_ ? 16u : 0u;
+            const uint32_t so = (uint32_t)(t * kSP * 2 + c8 * 2), n = t < L_ ? 16u : 0u;
             cp_async16(uQ + so, q + off, n);
             cp_async16(uK + so, k + off, n);
             cp_async16(uV + so, v + off, n);
@@ -349,7 +427,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     unsigned short beta_next = 0;
     {
         int slot_, h_, tc_, L_;
-        if (first < nitems && decode(first, slot_, h_, tc_, L_)) {
+        if (decode(first, slot_, h_, tc_, L_)) {
             stage_g(tc_, h_, L_);
             stage_qkv(tc_, h_, L_);
             if (tid < C) beta_next = load_beta(tc_, h_, L_);
@@ -357,15 +435,31 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
     }
     // With `ready`: the previous item's flag (-1: none) is released by one lane
-    // of the last warp during this item's Gram phase, where that warp would
-    // otherwise wait for the others; the proxy fence that makes the block
-    // visible to bulk copies comes before this item's first barrier.
+    // of the last warp while the CTA waits for this item's Gram products; the
+    // proxy fence that makes the block visible to bulk copies comes before
+    // this item's first barrier.
     constexpr int kReleaser = kPrepThreads - 32;
     long long pending = -1;
     auto release = [&](long long idx) {
         asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + idx), "r"(1u) : "memory");
     };
 
+    // operand-phase mapping: 16-token tile op_i = warp % 4, tokens op_t0 and
+    // op_t0 + 8 (op_t0 = 16 op_i + lane % 8), channels op_c0 .. + 8
+    const int op_i = warp & 3;
+    const int op_c0 = 8 * (4 * (warp >> 2) + (lane >> 3));
+    const int op_t0 = 16 * op_i + (lane & 7);
+    // descriptors and instruction descriptors of the tcgen05 products
+    const uint32_t id_gram1 = tc::idesc_f16(128, 128, 0, 0, 0);  // bf16, both K-major
+    const uint32_t id_gram2 = tc::idesc_f16(64, 32, 0, 0, 0);
+    const uint32_t id_w = tc::idesc_f16(64, 128, 1, 0, 1);     // fp16, B MN-major
+    const uint32_t id_u = tc::idesc_f16(128, 64, 1, 1, 0);     // fp16, A MN-major
+    const uint64_t dT = tc::smem_desc(sbase + kOffT, 128, 1024);
+    const uint64_t dKtb = tc::smem_desc(sbase + kOffKtb, 2048, 128);
+    const uint64_t dVb = tc::smem_desc(sbase + kOffVb, 2048, 128);
+
+    bool failed = false;
+    uint32_t it = 0;  // items done by this CTA (mbarrier phase)
 #pragma unroll 1
     for (int item = first; item < nitems; item += stride) {
     int slot, h, tc, L;
@@ -389,7 +483,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     {
         float a[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) a[r] = clamp_g(sAcum[(16 * ti4 + r) * 128 + ch]);
+        for (int r = 0; r < 16; ++r) a[r] = clamp_g(sAcum[(16 * ti4 + r) * kAP + ch]);
 #pragma unroll
         for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
         sQsum[ti4 * 128 + ch] = a[15];
@@ -403,7 +497,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int i2 = 1; i2 < 4; ++i2) off = ti4 == i2 ? rr[i2] : off;
         sRef[ti4 * 128 + ch] = off;  // cumulative decay just before tile ti4
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sAcum[(16 * ti4 + r) * 128 + ch] = a[r] + off;
+        for (int r = 0; r < 16; ++r) sAcum[(16 * ti4 + r) * kAP + ch] = a[r] + off;
         float *tab = reinterpret_cast<float *>(smem + kOffTab);
         const float rnext = ti4 == 3 ? rr[4] : (ti4 == 2 ? rr[3] : (ti4 == 1 ? rr[2] : rr[1]));
         tab[(kTabEr + ti4) * 128 + ch] = __expf(off);
@@ -420,28 +514,18 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
     }
     // this item's q, k, v: out of the staging area before it is overwritten
-    // operand-phase mapping: tokens 2 (tid / 16) + m (one 16-token tile per
-    // warp), channels 8 (tid % 16) .. + 8
-    const int op_c0 = (tid & 15) * 8, op_t0 = 2 * (tid >> 4), op_i = tid >> 7;
     uint4 uq[2], uk[2], uv[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-        const int t = op_t0 + m, c8 = op_c0;
-        const uint32_t so = (uint32_t)(t * 256 + c8 * 2);
-        uq[m] = *reinterpret_cast<const uint4 *>(smem + kOffKh + so);
-        uk[m] = *reinterpret_cast<const uint4 *>(smem + kOffKh + C * 256 + so);
-        uv[m] = *reinterpret_cast<const uint4 *>(smem + kOffKbS + so);
+        const uint32_t so = (uint32_t)((op_t0 + 8 * m) * kSP * 2 + op_c0 * 2);
+        uq[m] = *reinterpret_cast<const uint4 *>(smem + kOffQs + so);
+        uk[m] = *reinterpret_cast<const uint4 *>(smem + kOffKs + so);
+        uv[m] = *reinterpret_cast<const uint4 *>(smem + kOffVs + so);
     }
     __syncthreads();
 
-    // ---- all operands, one item = (token t, 8 key channels) ---------------------------
+    // ---- all operands: thread = (8 channels, tokens op_t0 and op_t0 + 8) ---------------
     {
-        __nv_bfloat16 *sXq = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXq);
-        __nv_bfloat16 *sXk = reinterpret_cast<__nv_bfloat16 *>(smem + kOffXk);
-        __nv_bfloat16 *sKh = reinterpret_cast<__nv_bfloat16 *>(smem + kOffKh);
-        __half *sKtb = reinterpret_cast<__half *>(smem + kOffKtb);
-        __half *sVb = reinterpret_cast<__half *>(smem + kOffVb);
-        __half *sKbS = reinterpret_cast<__half *>(smem + kOffKbS);
         const int c0 = op_c0, i = op_i;
         const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
         float r[8], er[8], ed[8], ec[8];  // per-tile values, shared by both tokens
@@ -451,12 +535,12 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         lds8(&tab[(kTabEc + i) * 128 + c0], ec);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            const int t = op_t0 + m;
+            const int t = op_t0 + 8 * m, tl = t & 15;
             float qq[8], kk[8], vv[8], a[8];
             unpack8_bf16(uq[m], qq);
             unpack8_bf16(uk[m], kk);
             unpack8_bf16(uv[m], vv);
-            lds8(&sAcum[t * 128 + c0], a);
+            lds8(&sAcum[t * kAP + c0], a);
             const float bt = sBeta[t];
             float x[8], ix[8], y[8], o[8], md = 0.f;
 #pragma unroll
@@ -468,14 +552,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 md += qq[e] * kk[e];
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = qq[e] * x[e];
-            *reinterpret_cast<uint4 *>(&sXq[t * kLDK + c0]) = pack8_bf16(o);
-#pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * x[e];
-            *reinterpret_cast<uint4 *>(&sXk[t * kLDK + c0]) = pack8_bf16(o);
+            *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + tl, c0)) = pack8_bf16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = qq[e] * x[e];
+            *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + 16 + tl, c0)) = pack8_bf16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * ix[e];
-            *reinterpret_cast<uint4 *>(&sKh[(kh_slot(i, i) * 16 + (t & 15)) * kLDK + c0]) = pack8_bf16(o);
+            *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i, i) + tl, c0)) =
+                pack8_bf16(o);
             // later reference tiles i2 > i: k e^{r_i2 - a_t} = k e^{r_i2 - r_{i+1}} y
 #pragma unroll 1
             for (int i2 = i + 1; i2 < 4; ++i2) {
@@ -489,7 +574,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) o[e] = kk[e] * (f[e] * y[e]);
-                *reinterpret_cast<uint4 *>(&sKh[(kh_slot(i2, i) * 16 + (t & 15)) * kLDK + c0]) =
+                *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i2, i) + tl, c0)) =
                     pack8_bf16(o);
             }
 #pragma unroll
@@ -497,110 +582,132 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(64 + t, c0)) = pack8_f16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * (er[e] * x[e]);       // beta k e^{a}
-            *reinterpret_cast<uint4 *>(&sKtb[t * kLDK + c0]) = pack8_f16(o);
+            *reinterpret_cast<uint4 *>(smem + kOffKtb + off_mn128(t, c0)) = pack8_f16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                        // beta v
-            *reinterpret_cast<uint4 *>(&sVb[t * kLDK + c0]) = pack8_f16(o);
+            *reinterpret_cast<uint4 *>(smem + kOffVb + off_mn128(t, c0)) = pack8_f16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * (ec[e] * y[e]);            // k e^{a_C - a}
-            *reinterpret_cast<uint4 *>(&sKbS[t * kLDK + c0]) = pack8_f16(o);
-            // q_t . k_t (the diagonal of M: no decay) over the 16 lanes of token t
-#pragma unroll
-            for (int o2 = 8; o2 > 0; o2 >>= 1) md += __shfl_xor_sync(0xffffffffu, md, o2);
-            if ((lane & 15) == 0) sMd[t] = md;
+            *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(t, 64 + c0)) = pack8_f16(o);
+            // q_t . k_t (the diagonal of M: no decay): 32 channels per warp here,
+            // the four warps of the tile are added in the Gram read-back
+            md += __shfl_xor_sync(0xffffffffu, md, 8);
+            md += __shfl_xor_sync(0xffffffffu, md, 16);
+            if (lane < 8) sMdp[(warp >> 2) * C + t] = md;
         }
     }
+    tc::fence_async_smem();  // operands -> tensor core
+    tc::fence_before_sync();
     __syncthreads();
     if (has_next) stage_g(ntc, nh, nL);  // the a buffer is free from here on
 
-    // ---- (k e^{a_C - a})^T -> block: item = (key channel, 8 tokens) -----------------
-    {
-        const __half *sKbS = reinterpret_cast<const __half *>(smem + kOffKbS);
-#pragma unroll 1
-        for (int m = 0; m < 2; ++m) {
-            const int id = tid + kPrepThreads * m, key = id & 127, tg = id >> 7;
-            uint4 pk;
-            uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
+    // ---- Gram products (16 instructions) ---------------------------------------------
+    //   D1 = Kh[0, 128) X^T     -> TMEM [0, 128)   (M = 128: lane = Kh row of slots 0..7)
+    //   D2 = Kh[96, 160) X_3^T  -> TMEM [128, 160) (M = 64: slots 6..9 in the lanes
+    //                                               of quarters 0..3)
+    // Row tile i needs columns [32 i, 32 i + 32) of its slots (i (i + 1) / 2 + j, j <= i);
+    // the other columns are products of unrelated tiles and are not read.
+    if (tid == 0) {
+        tc::fence_after_sync();
+        const uint64_t dA1 = tc::smem_desc(sbase + kOffKh, 128, 2048);
+        const uint64_t dB1 = tc::smem_desc(sbase + kOffX, 128, 2048);
+        const uint64_t dA2 = tc::smem_desc(sbase + kOffKh + 12u * 2048u, 128, 2048);
+        const uint64_t dB2 = tc::smem_desc(sbase + kOffX + 3u * 8192u, 128, 2048);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const __half lo = sKbS[(8 * tg + 2 * e) * kLDK + key];
-                const __half hi = sKbS[(8 * tg + 2 * e + 1) * kLDK + key];
-                w[e] = (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
-            }
-            *reinterpret_cast<uint4 *>(blk + kB2 + off_k64(key, 8 * tg)) = pk;
-        }
+        for (int ks = 0; ks < 8; ++ks) tc::mma_f16(tm, dA1 + 16 * ks, dB1 + 16 * ks, id_gram1, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_f16(tm + 128u, dA2 + 16 * ks, dB2 + 16 * ks, id_gram2, ks > 0);
+        tc::mma_commit(bG);
     }
+    if (pending >= 0 && tid == kReleaser) {
+        release(pending);
+        pending = -1;
+    }
+    if (!failed && !tc::mbar_wait(bG, it & 1u, kPrepWaitLimit)) failed = true;
+    tc::fence_after_sync();
 
-    // ---- Gram matrices A (beta, strictly lower) and M (lower) -------------------
+    // ---- read back: each warp one 16-column slice (part 0: k-Gram, 1: q-Gram) of its
+    // quarter's slots; a lane holds key row s of slot (i, j) and 16 tokens t = 16 i + n
     {
-        const uint32_t aXq = sbase + kOffXq, aXk = sbase + kOffXk, aKh = sbase + kOffKh;
-        for (int task = warp; task < 20; task += kPrepWarps) {
-            const int mm = task / 10;
-            int tt = task % 10, i = 0;
-            while (tt > i) { tt -= i + 1; ++i; }
-            const int j = tt;
-            float acc[2][4] = {}, acc2[2][4] = {};  // even / odd k steps: two chains each
-            const uint32_t aX = mm == 0 ? aXk : aXq;
-            const uint32_t aB = aKh + (uint32_t)(kh_slot(i, j) * 16 * kLDK) * 2u;
+        const int q4 = warp & 3, u = warp >> 2;
+        int i, part, tcol, slot;
+        bool valid;
+        if (q4 <= 1) {  // slots 2 q4 (lanes 0..15) and 2 q4 + 1 (lanes 16..31): row tiles q4, q4 + 1
+            const int sel = u >> 1;
+            i = q4 + sel;
+            part = u & 1;
+            tcol = 32 * i + 16 * part;
+            valid = (lane >> 4) == sel;
+            slot = 2 * q4 + (lane >> 4);
+        } else if (u < 2) {  // slots 4, 5 (row tile 2) or 6, 7 (row tile 3)
+            i = q4 == 2 ? 2 : 3;
+            part = u;
+            tcol = 32 * i + 16 * part;
+            valid = true;
+            slot = 2 * q4 + (lane >> 4);
+        } else {  // D2: slot 8 (quarter 2) or 9 (quarter 3), lanes 0..15
+            i = 3;
+            part = u - 2;
+            tcol = 128 + 16 * part;
+            valid = lane < 16;
+            slot = 6 + q4;
+        }
+        const int j = slot - kh_slot(i, 0), sl = lane & 15, s = 16 * j + sl;
+        // shared inputs first, into registers (the stores below could alias them)
+        float bt[16];
 #pragma unroll
-            for (int ks = 0; ks < 8; ks += 2) {
-                uint32_t af[4], bf[4], af2[4], bf2[4];
-                frag_a_rowmajor(af, aX, kLDK, 16 * i, 16 * ks, lane);
-                frag_b_nk(bf, aB, kLDK, 0, 16 * ks, lane);
-                frag_a_rowmajor(af2, aX, kLDK, 16 * i, 16 * ks + 16, lane);
-                frag_b_nk(bf2, aB, kLDK, 0, 16 * ks + 16, lane);
-                mma_bf16_16816(acc[0], af, bf[0], bf[1]);
-                mma_bf16_16816(acc[1], af, bf[2], bf[3]);
-                mma_bf16_16816(acc2[0], af2, bf2[0], bf2[1]);
-                mma_bf16_16816(acc2[1], af2, bf2[2], bf2[3]);
-            }
+        for (int n4 = 0; n4 < 4; ++n4)
+            *reinterpret_cast<float4 *>(&bt[4 * n4]) =
+                *reinterpret_cast<const float4 *>(&sBeta[16 * i + 4 * n4]);
+        const bool diag = valid && i == j;
+        float md_s = 0.f;
+        if (diag && part == 1) md_s = sMdp[s] + sMdp[C + s] + sMdp[2 * C + s] + sMdp[3 * C + s];
+        uint32_t rv[1][16];
+        tc::tmem_ld_cols<1>(tquart + (uint32_t)tcol, rv);
+        if (valid) {
+            if (part == 0) {
+                if (diag) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
+                    for (int n = 0; n < 16; ++n)
+                        sAd[j * 256 + n * 16 + sl] = sl < n ? bt[n] * __uint_as_float(rv[0][n]) : 0.f;
+                } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
+                    for (int n = 0; n < 16; ++n)
+                        *reinterpret_cast<__half *>(smem + kOffAh + (uint32_t)((16 * i + n) * kLDC + s) * 2u) =
+                            __float2half_rn(bt[n] * __uint_as_float(rv[0][n]));
+                }
+            } else {
+                float mt[16];
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = 16 * i + (lane >> 2) + 8 * hh;
-                    const int s = 16 * j + nt * 8 + cq;
-                    float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
-                    if (mm == 0) {
-                        sA[t * kLDA + s] = s < t ? sBeta[t] * v0 : 0.f;
-                        sA[t * kLDA + s + 1] = s + 1 < t ? sBeta[t] * v1 : 0.f;
-                    } else {
-                        v0 = s < t ? v0 : (s == t ? sMd[t] : 0.f);
-                        v1 = s + 1 < t ? v1 : (s + 1 == t ? sMd[t] : 0.f);
-                        *reinterpret_cast<uint32_t *>(blk + kB3 + off_k64(t, s)) = pack_f16(v0, v1);
+                for (int n = 0; n < 16; ++n) {
+                    const float mv = __uint_as_float(rv[0][n]);
+                    mt[n] = diag ? (sl < n ? mv : (sl == n ? md_s : 0.f)) : mv;
+                }
+                *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i)) = pack8_f16(mt);
+                *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i + 8)) = pack8_f16(mt + 8);
+                if (diag) {  // t in the tiles before s: zero
+#pragma unroll 1
+                    for (int i2 = 0; i2 < j; ++i2) {
+                        *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i2)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i2 + 8)) = make_uint4(0, 0, 0, 0);
                     }
                 }
-        }
-        if (pending >= 0 && tid == kReleaser) {
-            release(pending);
-            pending = -1;
-        }
-        // blocks above the diagonal: zero in A (shared) and in M (the block)
-        for (int idx = tid; idx < 6 * 128; idx += kPrepThreads) {
-            const int b_ = idx >> 7, e = idx & 127;
-            const int bi = b_ < 3 ? 0 : (b_ < 5 ? 1 : 2);
-            const int bj = b_ < 3 ? b_ + 1 : (b_ < 5 ? b_ - 1 : 3);
-            const int t = 16 * bi + (e >> 3), s = 16 * bj + 2 * (e & 7);
-            sA[t * kLDA + s] = 0.f;
-            sA[t * kLDA + s + 1] = 0.f;
-            *reinterpret_cast<uint32_t *>(blk + kB3 + off_k64(t, s)) = 0u;
+            }
         }
     }
-    __syncthreads();
-    if (has_next) {  // column tiles and the transpose staging are free from here on
+    tc::fence_before_sync();
+    failed = __syncthreads_or(failed) != 0;
+    tc::fence_after_sync();
+    if (failed) break;
+    if (has_next) {  // column tiles and the v buffer are free from here on
         stage_qkv(ntc, nh, nL);
         if (tid < C) beta_next = load_beta(ntc, nh, nL);
         staged = nitem;
     }
 
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
-    __half *sAh = reinterpret_cast<__half *>(smem + kOffAh);
-    __half *sTb = reinterpret_cast<__half *>(smem + kOffTb);
-    const uint32_t aTb = sbase + kOffTb;
+    const uint32_t aT = sbase + kOffT, aAh = sbase + kOffAh;
     if (tid < 64) {
         const int b = tid >> 4, cc = tid & 15;
         float x[16];
@@ -608,17 +715,19 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int r = 0; r < 16; ++r) {
             float acc = 0.f;
 #pragma unroll
-            for (int s = 0; s < r; ++s) acc += sA[(16 * b + r) * kLDA + 16 * b + s] * x[s];
+            for (int s2 = 0; s2 < r; ++s2) acc += sAd[b * 256 + r * 16 + s2] * x[s2];
             x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sTb[(16 * b + r) * kLDC + 16 * b + cc] = __float2half_rn(x[r]);
+        for (int r = 0; r < 16; ++r) store_h(smem + kOffT, off_k64(16 * b + r, 16 * b + cc), x[r]);
     } else {
-        for (int idx = tid - 64; idx < C * C / 2; idx += kPrepThreads - 64) {
-            const int t = idx >> 5, s = 2 * (idx & 31);
-            *reinterpret_cast<uint32_t *>(&sAh[t * kLDC + s]) =
-                pack_f16(sA[t * kLDA + s], sA[t * kLDA + s + 1]);
-            if ((s >> 4) > (t >> 4)) *reinterpret_cast<uint32_t *>(&sTb[t * kLDC + s]) = 0u;
+        // blocks above the diagonal of T: zero
+        for (int idx = tid - 64; idx < 6 * 128; idx += kPrepThreads - 64) {
+            const int b_ = idx >> 7, e = idx & 127;
+            const int bi = b_ < 3 ? 0 : (b_ < 5 ? 1 : 2);
+            const int bj = b_ < 3 ? b_ + 1 : (b_ < 5 ? b_ - 1 : 3);
+            const int t = 16 * bi + (e >> 3), s2 = 16 * bj + 2 * (e & 7);
+            *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(t, s2)) = 0u;
         }
     }
     __syncthreads();
@@ -627,7 +736,6 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         //  1. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
         //  2. the lower-left 32x32 block  T_BA = -T_BB (A_BA T_AA),
         //     T_AA = [[T00, 0], [T10, T11]],  T_BB = [[T22, 0], [T32, T33]].
-        const uint32_t aAh = sbase + kOffAh;
         __half *sXh = reinterpret_cast<__half *>(smem + kOffXh);
         auto store_tile = [&](__half *dst, int ld, float acc[2][4], float sgn) {
 #pragma unroll
@@ -637,23 +745,31 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 *reinterpret_cast<uint32_t *>(&dst[(rr + 8) * ld + cc2]) = pack_f16(sgn * acc[nt][2], sgn * acc[nt][3]);
             }
         };
+        auto store_tile_T = [&](int m0, int n0, float acc[2][4]) {  // T block := -acc
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int rr = m0 + (lane >> 2), cc2 = n0 + nt * 8 + cq;
+                *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(rr, cc2)) = pack_f16(-acc[nt][0], -acc[nt][1]);
+                *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(rr + 8, cc2)) = pack_f16(-acc[nt][2], -acc[nt][3]);
+            }
+        };
         if (warp < 2) {
             const int i = 1 + 2 * warp, j = i - 1;
             float xacc[2][4] = {};
             uint32_t af[4], bf[4];
             frag_a_rowmajor(af, aAh, kLDC, 16 * i, 16 * j, lane);
-            frag_b_kn(bf, aTb, kLDC, 16 * j, 16 * j, lane);
+            frag_b_kn_k64(bf, aT, 16 * j, 16 * j, lane);
             mma_f16_16816(xacc[0], af, bf[0], bf[1]);
             mma_f16_16816(xacc[1], af, bf[2], bf[3]);
             __half *xs = sXh + warp * 16 * 24;
             store_tile(xs, 24, xacc, 1.f);
             __syncwarp();
             float tacc[2][4] = {};
-            frag_a_rowmajor(af, aTb, kLDC, 16 * i, 16 * i, lane);
+            frag_a_k64(af, aT, 16 * i, 16 * i, lane);
             frag_b_kn(bf, smem_u32(xs), 24, 0, 0, lane);
             mma_f16_16816(tacc[0], af, bf[0], bf[1]);
             mma_f16_16816(tacc[1], af, bf[2], bf[3]);
-            store_tile(sTb + (16 * i) * kLDC + 16 * j, kLDC, tacc, -1.f);
+            store_tile_T(16 * i, 16 * j, tacc);
         }
         __syncthreads();
         if (warp < 4) {  // X = A_BA T_AA, block (r, c), r in {2, 3}, c in {0, 1}
@@ -664,7 +780,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 if (kb < c) continue;  // T_01 = 0
                 uint32_t af[4], bf[4];
                 frag_a_rowmajor(af, aAh, kLDC, 16 * r, 16 * kb, lane);
-                frag_b_kn(bf, aTb, kLDC, 16 * c, 16 * kb, lane);
+                frag_b_kn_k64(bf, aT, 16 * c, 16 * kb, lane);
                 mma_f16_16816(xacc[0], af, bf[0], bf[1]);
                 mma_f16_16816(xacc[1], af, bf[2], bf[3]);
             }
@@ -678,82 +794,73 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             for (int kb = 2; kb < 4; ++kb) {
                 if (kb > r) continue;  // T_23 = 0
                 uint32_t af[4], bf[4];
-                frag_a_rowmajor(af, aTb, kLDC, 16 * r, 16 * kb, lane);
+                frag_a_k64(af, aT, 16 * r, 16 * kb, lane);
                 frag_b_kn(bf, smem_u32(sXh + ((kb - 2) * 2 + c) * 16 * 24), 24, 0, 0, lane);
                 mma_f16_16816(tacc[0], af, bf[0], bf[1]);
                 mma_f16_16816(tacc[1], af, bf[2], bf[3]);
             }
-            store_tile(sTb + (16 * r) * kLDC + 16 * c, kLDC, tacc, -1.f);
+            store_tile_T(16 * r, 16 * c, tacc);
         }
-        __syncthreads();
     }
+    tc::fence_async_smem();  // T -> tensor core
+    tc::fence_before_sync();
+    __syncthreads();
 
-    // ---- W = T (beta k e^{a})  and  U~^T = (beta v)^T T^T -------------------------
-    {
-        const uint32_t aKtb = sbase + kOffKtb, aVb = sbase + kOffVb;
-        {   // W: warp = (row tile ti, 32 key columns)
-            const int ti = warp & 3, nq = warp >> 2;
-            float wacc[4][4] = {};
+    // ---- W = T (beta k e^{a}) -> TMEM [0, 128);  U~^T = (beta v)^T T^T -> [128, 192) --
+    if (tid == 0) {
+        tc::fence_after_sync();
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                if (ks > ti) break;
-                uint32_t af[4];
-                frag_a_rowmajor(af, aTb, kLDC, 16 * ti, 16 * ks, lane);
+        for (int ks = 0; ks < 4; ++ks)  // K = 16 tokens: 2 core matrices of T, 2 K groups of Ktb
+            tc::mma_f16(tm, dT + 16 * ks, dKtb + 256 * ks, id_w, ks > 0);
 #pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    uint32_t bf[4];
-                    frag_b_kn(bf, aKtb, kLDK, 32 * nq + 16 * np, 16 * ks, lane);
-                    mma_f16_16816(wacc[2 * np], af, bf[0], bf[1]);
-                    mma_f16_16816(wacc[2 * np + 1], af, bf[2], bf[3]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = 16 * ti + (lane >> 2) + 8 * hh;
-                    const int col = 32 * nq + nt * 8 + cq;
-                    *reinterpret_cast<uint32_t *>(blk + kB12 + off_k128(t, col)) =
-                        pack_f16(wacc[nt][2 * hh], wacc[nt][2 * hh + 1]);
-                }
-        }
-        {   // U~^T: warp = (16 value rows, 32 tokens); T is lower triangular
-            const int jt = warp & 7, th = warp >> 3;
-            float uacc[4][4] = {};
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                if (ks > 2 * th + 1) break;  // T[t][s] = 0 for s > t
-                uint32_t af[4];
-                frag_a_colmajor(af, aVb, kLDK, 16 * jt, 16 * ks, lane);
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {
-                    const int tt16 = 2 * th + np;  // token tile of these two n8 tiles
-                    if (tt16 < ks) continue;
-                    uint32_t bf[4];
-                    frag_b_nk(bf, aTb, kLDC, 16 * tt16, 16 * ks, lane);
-                    mma_f16_16816(uacc[2 * np], af, bf[0], bf[1]);
-                    mma_f16_16816(uacc[2 * np + 1], af, bf[2], bf[3]);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int jj = 16 * jt + (lane >> 2) + 8 * hh;
-                    const int t = 32 * th + nt * 8 + cq;
-                    *reinterpret_cast<uint32_t *>(blk + kUt + (uint32_t)jj * kUtPitch + 2u * t) =
-                        pack_f16(uacc[nt][2 * hh], uacc[nt][2 * hh + 1]);
-                }
-        }
+        for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16(tm + 128u, dVb + 256 * ks, dT + 16 * ks, id_u, ks > 0);
+        tc::mma_commit(bW);
     }
-    __syncthreads();  // shared memory is reused by the next item
+    if (!failed && !tc::mbar_wait(bW, it & 1u, kPrepWaitLimit)) failed = true;
+    tc::fence_after_sync();
+    {
+        // W: lanes 0..15 of the quarter hold rows t = 16 (warp % 4) + lane; columns
+        // [32 (warp / 4), +32) of the 128 keys
+        const int cb = 32 * (warp >> 2), t = 16 * (warp & 3) + lane;
+        uint32_t rw[2][16];
+        tc::tmem_ld_cols<2>(tquart + (uint32_t)cb, rw);
+        if (lane < 16) {
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi)
+                *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(t, cb + 8 * gi)) =
+                    pack8_f16_u(&rw[gi >> 1][(gi & 1) * 8]);
+        }
+        // U~^T: lane = value column j = 32 (warp % 4) + lane; tokens [16 (warp / 4), +16)
+        const int jj = 32 * (warp & 3) + lane, t0 = 16 * (warp >> 2);
+        uint32_t ru[1][16];
+        tc::tmem_ld_cols<1>(tquart + 128u + (uint32_t)t0, ru);
+        unsigned char *ut = blk + kUt + (size_t)jj * kUtPitch + 2 * t0;
+        *reinterpret_cast<uint4 *>(ut) = pack8_f16_u(&ru[0][0]);
+        *reinterpret_cast<uint4 *>(ut + 16) = pack8_f16_u(&ru[0][8]);
+    }
+    tc::fence_before_sync();
+    failed = __syncthreads_or(failed) != 0;  // shared memory and TMEM are reused by the next item
+    tc::fence_after_sync();
+    if (failed) break;
+    ++it;
     if (ready) pending = (long long)slot * H + h;
     }
-    if (pending >= 0) {  // the last item of this CTA
+
+    if (failed) {
+        if (tid == 0) atomicOr(pa.status, kStatusTimeout);
+        // let any MMA still in flight land before the TMEM is released
+        tc::mbar_wait(bG, it & 1u, 10000000ull);
+        tc::mbar_wait(bW, it & 1u, 10000000ull);
+    } else if (pending >= 0) {  // the last item of this CTA
         asm volatile("fence.proxy.async.global;\n" ::: "memory");
         __syncthreads();
         if (tid == kReleaser) release(pending);
     }
+    cp_async_wait_all();  // a staged copy still in flight (after a failure)
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tm, kPrepTmemCols);
 }
 
 __global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs pa) {
@@ -880,7 +987,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     // descriptors (no swizzle); +16 in the address field per 256-byte K step
     const uint64_t dSA = tc::smem_desc(uSA, 128, 2048), dUA = tc::smem_desc(uUA, 128, 1024);
     const uint32_t id_n128 = tc::idesc_f16(128, 128, 1, 0, 0);
-    const uint32_t id_n192 = tc::idesc_f16(128, 192, 1, 0, 0);
+    const uint32_t id_n192 = tc::idesc_f16(128, 192, 1, 0, 1);  // B MN-major
     auto issue_mma1 = [&](int c) {  // [P^T | O~^T] = S^T [W ; q e^a]^T
         const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB12, 128, 2048);
 #pragma unroll
@@ -889,10 +996,11 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
         tc::mma_commit(bM1);
     };
     auto issue_mma2 = [&](int c) {  // [O^T | S^T] += U^T [M ; Kb^T]^T
-        const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB3, 128, 1024);
+        // B MN-major: LBO = 3072 (one K group of 8 tokens), SBO = 128; 6144 B per K step
+        const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB3, 3072, 128);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            tc::mma_f16(tm + kColO, dUA + 16 * ks, dB + 16 * ks, id_n192, 1u);
+            tc::mma_f16(tm + kColO, dUA + 16 * ks, dB + 384 * ks, id_n192, 1u);
         tc::mma_commit(bM2);
     };
 
@@ -1110,7 +1218,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               float *fin, unsigned char *ws, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(pf::prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         pf::kPrepSmem);
+                                         (int)pf::kPrepSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(pf::recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)pf::kRecSmem);
@@ -1141,7 +1249,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     pf::PrepArgs pa{static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
                     static_cast<const __nv_bfloat16 *>(v), g,
                     static_cast<const __nv_bfloat16 *>(beta), cu, first_chunk, N, T, H,
-                    (int)nitems, blocks};
+                    (int)nitems, blocks, status};
     pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
                    static_cast<__nv_bfloat16 *>(out), fin, status};
     if (fused) {

@@ -62,7 +62,7 @@ def test_kmajor(lib, N, K, f16):
     assert run(lib, N, K, 0, f16) < 1e-5
 
 
-@pytest.mark.parametrize("N,K", [(64, 64), (128, 128)])
+@pytest.mark.parametrize("N,K", [(64, 64), (128, 128), (192, 64)])
 def test_mnmajor_b(lib, N, K):
     """LBO = stride along K, SBO = stride along N, as for K-major tiles."""
     errs = {swap: run(lib, N, K, 1, f16, swap) for swap in (0, 1) for f16 in (0, 1)}
