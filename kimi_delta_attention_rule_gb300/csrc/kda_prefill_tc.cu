@@ -50,6 +50,8 @@
 #include "kda_common.cuh"
 #include "kda_tcgen05.cuh"
 
+#include <cuda.h>  // CUtensorMap (the encoder is resolved at run time)
+
 #include <cstdlib>
 #include <cstring>
 
@@ -164,11 +166,14 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
 constexpr int kPrepThreads = 512;
 constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kLDC = 72;   // fp16 pitch of the C x C scratch tiles
-constexpr int kAP = 132;   // fp32 pitch of the a buffer (8 consecutive rows start in distinct banks)
-constexpr int kSP = 136;   // bf16 pitch of the staged q, k, v rows (272 B, same reason)
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
-constexpr uint32_t kOffAcum = 0;                               // fp32 [64][132] a (g staged here)
-constexpr uint32_t kOffRef = align1k(kOffAcum + C * kAP * 4);  // fp32 [4][128] r_i
+// Staged inputs arrive by TMA with the 128-byte swizzle: a region holds 64 token
+// rows of 128 B, and the 16-byte chunk c of row t sits at chunk c ^ (t % 8), so
+// that 8 consecutive tokens at the same channels fall in distinct banks.
+//   g: four regions of 32 fp32 channels;  q, k, v: two regions of 64 bf16 channels.
+constexpr uint32_t kRegion = 64 * 128;                         // 8 KiB, 1 KiB aligned
+constexpr uint32_t kOffAcum = 0;                               // fp32 a (g staged here): 4 regions
+constexpr uint32_t kOffRef = align1k(kOffAcum + 4 * kRegion);  // fp32 [4][128] r_i
 constexpr uint32_t kOffQsum = kOffRef + 4 * 128 * 4;           // fp32 [4][128] per-tile sums of g
 constexpr uint32_t kOffAc = kOffQsum + 4 * 128 * 4;            // fp32 [128] a_C
 constexpr uint32_t kOffBeta = kOffAc + 128 * 4;                // fp32 [64]
@@ -184,16 +189,38 @@ constexpr uint32_t kOffX = align1k(kOffTab + 16 * 128 * 4);    // bf16 K-major [
 constexpr uint32_t kOffKh = kOffX + 128 * 128 * 2;             // bf16 K-major [160][128]: 10 column tiles
 constexpr uint32_t kOffKtb = kOffKh + 160 * 128 * 2;           // fp16 MN-major [s][c]: beta k e^{a}
 constexpr uint32_t kOffVb = kOffKtb + 64 * 128 * 2;            // fp16 MN-major [s][j]: beta v
-constexpr uint32_t kOffVs = kOffVb + 64 * 128 * 2;             // bf16 [64][136]: staged v
-constexpr uint32_t kPrepSmem = kOffVs + C * kSP * 2;
+constexpr uint32_t kOffVs = kOffVb + 64 * 128 * 2;             // bf16 staged v: 2 regions
+constexpr uint32_t kPrepSmem = kOffVs + 2 * kRegion;
 // after the Gram products, inside X:
 constexpr uint32_t kOffT = kOffX;                              // fp16 K-major [64][64]: T
 constexpr uint32_t kOffAh = kOffT + 64 * 64 * 2;               // fp16 [64][72]: A below the diagonal blocks
 constexpr uint32_t kOffXh = kOffAh + C * kLDC * 2;             // fp16 [4][16][24]: block-product scratch
 static_assert(kOffXh + 4 * 16 * 24 * 2 <= kOffKh, "T scratch inside X");
 // staged q, k of the next item: inside Kh (free after the Gram products)
-constexpr uint32_t kOffQs = kOffKh, kOffKs = kOffKh + C * kSP * 2;
-static_assert(kOffKs + C * kSP * 2 <= kOffKtb, "q, k staging inside Kh");
+constexpr uint32_t kOffQs = kOffKh, kOffKs = kOffKh + 2 * kRegion;
+static_assert(kOffKs + 2 * kRegion <= kOffKtb, "q, k staging inside Kh");
+static_assert(kOffX % 1024 == 0 && kOffKh % 1024 == 0 && kOffVs % 1024 == 0, "swizzled regions");
+
+// byte offset of 16-byte chunk `chunk` of row t in a 128-byte-swizzled region
+__device__ __forceinline__ uint32_t swz128(int t, int chunk) {
+    return (uint32_t)t * 128u + ((uint32_t)(chunk ^ (t & 7)) << 4);
+}
+// g / a element (t, c): region c / 32, chunk (c % 32) / 4
+__device__ __forceinline__ uint32_t a_off(int t, int c) {
+    return (uint32_t)(c >> 5) * kRegion + swz128(t, (c & 31) >> 2) + (uint32_t)(c & 3) * 4u;
+}
+// q, k, v: the 16 bytes of channels c8 .. c8 + 7 (c8 a multiple of 8) of token t
+__device__ __forceinline__ uint32_t qkv_off(int t, int c8) {
+    return (uint32_t)(c8 >> 6) * kRegion + swz128(t, (c8 & 63) >> 3);
+}
+// 3-D tensor-map load (box of the map) into shared memory, counted on `bar`
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
 static_assert(kPrepSmem <= 227 * 1024, "shared memory budget");
 constexpr uint32_t kPrepTmemCols = 256;  // Gram [0, 128), then W [0, 128); U~^T [128, 192)
 
@@ -205,14 +232,6 @@ __device__ __forceinline__ uint32_t off_mn128(int k, int x) {
     return (uint32_t)(x >> 3) * 128u + (uint32_t)(k >> 3) * 2048u + (uint32_t)(k & 7) * 16u +
            (uint32_t)(x & 7) * 2u;
 }
-
-// 16-byte global -> shared copy; bytes past `src_bytes` (0 or 16) are zero-filled
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // mma.sync fragments of the fp16 T tile kept in the K-major core-matrix layout
 // (K extent 64) that tcgen05 reads: A (16 x 16) = T[m][k], and B = T[k][n].
@@ -321,6 +340,7 @@ __device__ __forceinline__ bool item_tokens_cm(int idx, int H, const int32_t *cu
 }
 
 struct PrepArgs {
+    CUtensorMap tmq, tmk, tmv, tmg;  // [T_total][H][128]: boxes of 64 tokens x 64 (bf16) / 32 (fp32) channels
     const __nv_bfloat16 *q, *k, *v;
     const float *g;
     const __nv_bfloat16 *beta;
@@ -362,10 +382,9 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const int ch = tid & 127, ti4 = tid >> 7;  // cumulative-sum role: (channel, tile)
 
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t pbars[2];  // Gram products, W / U~ products
+    __shared__ __align__(8) uint64_t pbars[4];  // Gram products, W / U~ products, staged g, staged q k v
     __shared__ uint32_t ptmem_slot;
     const uint32_t sbase = smem_u32(smem);
-    float *sAcum = reinterpret_cast<float *>(smem + kOffAcum);
     float *sRef = reinterpret_cast<float *>(smem + kOffRef);
     float *sQsum = reinterpret_cast<float *>(smem + kOffQsum);
     float *sAcT = reinterpret_cast<float *>(smem + kOffAc);
@@ -373,6 +392,11 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     float *sMdp = reinterpret_cast<float *>(smem + kOffMdp);
     float *sAd = reinterpret_cast<float *>(smem + kOffAd);
     const uint32_t bG = smem_u32(&pbars[0]), bW = smem_u32(&pbars[1]);
+    const uint32_t bInG = smem_u32(&pbars[2]), bInQKV = smem_u32(&pbars[3]);
+    if ((sbase & 1023u) != 0) {  // the swizzled TMA regions need 1 KiB alignment
+        if (tid == 0) atomicOr(pa.status, kStatusTimeout);
+        return;
+    }
 
     if (warp == 0) {
         tc::tmem_alloc(smem_u32(&ptmem_slot), kPrepTmemCols);
@@ -381,6 +405,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (tid == 0) {
         tc::mbar_init(bG, 1);
         tc::mbar_init(bW, 1);
+        tc::mbar_init(bInG, 1);
+        tc::mbar_init(bInQKV, 1);
         tc::fence_mbar_init();
     }
     tc::fence_before_sync();
@@ -389,33 +415,32 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const uint32_t tm = ptmem_slot;
     const uint32_t tquart = tm + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
 
-    // Input staging with cp.async (16-byte pieces; padding rows are zero-filled):
+    // Input staging with tensor-map TMA (box = 64 tokens of one head), counted on an
+    // mbarrier; rows past the end of a partial chunk hold other tokens (or the
+    // fill zeros) and are masked where they are read:
     //   g of an item -> the a buffer (dead after the operand phase),
     //   q, k -> the column-tile region (dead after the Gram products), v -> its own buffer.
     const uint32_t uG = sbase + kOffAcum, uQ = sbase + kOffQs, uK = sbase + kOffKs,
                    uV = sbase + kOffVs;
-    auto stage_g = [&](int tc_, int h_, int L_) {
+    uint32_t n_staged = 0;  // stagings issued (each completes one phase of both barriers)
+    auto stage_g = [&](int tc_, int h_) {
+        ++n_staged;
+        if (tid == 32) {
+            tc::mbar_arrive_expect_tx(bInG, 4 * kRegion);
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            const int id = tid + kPrepThreads * m, t = id >> 5, c4 = (id & 31) * 4;
-            const int ts = t < L_ ? t : 0;
-            cp_async16(uG + (uint32_t)(t * kAP * 4 + c4 * 4),
-                       g + ((size_t)(tc_ + ts) * H + h_) * 128 + c4, t < L_ ? 16u : 0u);
+            for (int r = 0; r < 4; ++r) tma_load_3d(uG + r * kRegion, &pa.tmg, 32 * r, h_, tc_, bInG);
         }
-        cp_async_commit();
     };
-    auto stage_qkv = [&](int tc_, int h_, int L_) {
+    auto stage_qkv = [&](int tc_, int h_) {
+        if (tid == 32) {
+            tc::mbar_arrive_expect_tx(bInQKV, 6 * kRegion);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-            const int id = tid + kPrepThreads * m, t = id >> 4, c8 = (id & 15) * 8;
-            const int ts = t < L_ ? t : 0;
-            const size_t off = ((size_t)(tc_ + ts) * H + h_) * 128 + c8;
-            const uint32_t so = (uint32_t)(t * kSP * 2 + c8 * 2), n = t < L_ ? 16u : 0u;
-            cp_async16(uQ + so, q + off, n);
-            cp_async16(uK + so, k + off, n);
-            cp_async16(uV + so, v + off, n);
+            for (int r = 0; r < 2; ++r) {
+                tma_load_3d(uQ + r * kRegion, &pa.tmq, 64 * r, h_, tc_, bInQKV);
+                tma_load_3d(uK + r * kRegion, &pa.tmk, 64 * r, h_, tc_, bInQKV);
+                tma_load_3d(uV + r * kRegion, &pa.tmv, 64 * r, h_, tc_, bInQKV);
+            }
         }
-        cp_async_commit();
     };
     // token tid of an item (raw bits: converted only where used, so that the
     // load does not stall the issuing warp)
@@ -428,8 +453,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     {
         int slot_, h_, tc_, L_;
         if (decode(first, slot_, h_, tc_, L_)) {
-            stage_g(tc_, h_, L_);
-            stage_qkv(tc_, h_, L_);
+            stage_g(tc_, h_);
+            stage_qkv(tc_, h_);
             if (tid < C) beta_next = load_beta(tc_, h_, L_);
             staged = first;
         }
@@ -465,8 +490,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     int slot, h, tc, L;
     if (!decode(item, slot, h, tc, L)) continue;
     if (staged != item) {  // the previous item could not prefetch this one
-        stage_g(tc, h, L);
-        stage_qkv(tc, h, L);
+        stage_g(tc, h);
+        stage_qkv(tc, h);
         if (tid < C) beta_next = load_beta(tc, h, L);
     }
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
@@ -476,14 +501,18 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
 
     if (tid < C) sBeta[tid] = __bfloat162float(__ushort_as_bfloat16(beta_next));
     if (pending >= 0) asm volatile("fence.proxy.async.global;\n" ::: "memory");
-    cp_async_wait_all();
-    __syncthreads();
+    if (!failed && !tc::mbar_wait(bInG, it & 1u, kPrepWaitLimit)) failed = true;
+    if (!failed && !tc::mbar_wait(bInQKV, it & 1u, kPrepWaitLimit)) failed = true;
+    failed = __syncthreads_or(failed) != 0;
+    if (failed) break;
 
     // ---- cumulative decay: thread = (channel, 16-token tile), in place over g --------
     {
         float a[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) a[r] = clamp_g(sAcum[(16 * ti4 + r) * kAP + ch]);
+        for (int r = 0; r < 16; ++r)  // rows past the chunk: g = 0
+            a[r] = 16 * ti4 + r < L ? clamp_g(*reinterpret_cast<const float *>(smem + kOffAcum + a_off(16 * ti4 + r, ch)))
+                                    : 0.f;
 #pragma unroll
         for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
         sQsum[ti4 * 128 + ch] = a[15];
@@ -497,7 +526,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int i2 = 1; i2 < 4; ++i2) off = ti4 == i2 ? rr[i2] : off;
         sRef[ti4 * 128 + ch] = off;  // cumulative decay just before tile ti4
 #pragma unroll
-        for (int r = 0; r < 16; ++r) sAcum[(16 * ti4 + r) * kAP + ch] = a[r] + off;
+        for (int r = 0; r < 16; ++r)
+            *reinterpret_cast<float *>(smem + kOffAcum + a_off(16 * ti4 + r, ch)) = a[r] + off;
         float *tab = reinterpret_cast<float *>(smem + kOffTab);
         const float rnext = ti4 == 3 ? rr[4] : (ti4 == 2 ? rr[3] : (ti4 == 1 ? rr[2] : rr[1]));
         tab[(kTabEr + ti4) * 128 + ch] = __expf(off);
@@ -517,10 +547,12 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     uint4 uq[2], uk[2], uv[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-        const uint32_t so = (uint32_t)((op_t0 + 8 * m) * kSP * 2 + op_c0 * 2);
+        const int t = op_t0 + 8 * m;
+        const uint32_t so = qkv_off(t, op_c0);
         uq[m] = *reinterpret_cast<const uint4 *>(smem + kOffQs + so);
         uk[m] = *reinterpret_cast<const uint4 *>(smem + kOffKs + so);
         uv[m] = *reinterpret_cast<const uint4 *>(smem + kOffVs + so);
+        if (t >= L) uq[m] = uk[m] = uv[m] = make_uint4(0, 0, 0, 0);  // past the chunk
     }
     __syncthreads();
 
@@ -540,7 +572,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             unpack8_bf16(uq[m], qq);
             unpack8_bf16(uk[m], kk);
             unpack8_bf16(uv[m], vv);
-            lds8(&sAcum[t * kAP + c0], a);
+            *reinterpret_cast<float4 *>(a) =
+                *reinterpret_cast<const float4 *>(smem + kOffAcum + a_off(t, c0));
+            *reinterpret_cast<float4 *>(a + 4) =
+                *reinterpret_cast<const float4 *>(smem + kOffAcum + a_off(t, c0 + 4));
             const float bt = sBeta[t];
             float x[8], ix[8], y[8], o[8], md = 0.f;
 #pragma unroll
@@ -599,7 +634,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     tc::fence_async_smem();  // operands -> tensor core
     tc::fence_before_sync();
     __syncthreads();
-    if (has_next) stage_g(ntc, nh, nL);  // the a buffer is free from here on
+    if (has_next) stage_g(ntc, nh);  // the a buffer is free from here on
 
     // ---- Gram products (16 instructions) ---------------------------------------------
     //   D1 = Kh[0, 128) X^T     -> TMEM [0, 128)   (M = 128: lane = Kh row of slots 0..7)
@@ -701,7 +736,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     tc::fence_after_sync();
     if (failed) break;
     if (has_next) {  // column tiles and the v buffer are free from here on
-        stage_qkv(ntc, nh, nL);
+        stage_qkv(ntc, nh);
         if (tid < C) beta_next = load_beta(ntc, nh, nL);
         staged = nitem;
     }
@@ -857,13 +892,16 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         __syncthreads();
         if (tid == kReleaser) release(pending);
     }
-    cp_async_wait_all();  // a staged copy still in flight (after a failure)
+    if (failed && n_staged > 0) {  // staged copies still in flight: the last phase issued
+        tc::mbar_wait(bInG, (n_staged - 1) & 1u, 10000000ull);
+        tc::mbar_wait(bInQKV, (n_staged - 1) & 1u, 10000000ull);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tm, kPrepTmemCols);
 }
 
-__global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(PrepArgs pa) {
+__global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(const __grid_constant__ PrepArgs pa) {
     prep_loop(pa, blockIdx.x, gridDim.x, nullptr);
 }
 
@@ -1159,7 +1197,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) recur_kernel(RecArgs ra) {
 // progress; every wait of a chain is bounded.
 constexpr uint32_t kFusedSmem = kRecSmem > (uint32_t)kPrepSmem ? kRecSmem : (uint32_t)kPrepSmem;
 __global__ void __launch_bounds__(kRecThreads, 1)
-    fused_kernel(PrepArgs pa, RecArgs ra, int nchains, int *ready) {
+    fused_kernel(const __grid_constant__ PrepArgs pa, RecArgs ra, int nchains, int *ready) {
     if ((int)blockIdx.x < nchains) recur_chain(ra, blockIdx.x, ready);
     else prep_loop(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
 }
@@ -1179,6 +1217,40 @@ size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool v
     const long long slots = prefill_slots(N, T, T_total, varlen);
     const size_t sched = varlen ? pad256((size_t)(N + 2) * 4) : 0;
     return 256 + sched + pad256((size_t)slots * H * 4) + (size_t)slots * H * pf::kBlock;
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
+// dependence on the driver library)
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static const EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+// [T_total][H][128] tensor; box = 64 tokens x one head x 128 bytes of channels,
+// 128-byte swizzle, zero fill past the end
+bool make_token_map(CUtensorMap *m, const void *base, bool f32, int H, int T_total) {
+    const EncodeTiledFn fn = encode_tiled();
+    if (fn == nullptr) return false;
+    const cuuint64_t es = f32 ? 4 : 2;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_total};
+    const cuuint64_t strides[2] = {128 * es, (cuuint64_t)H * 128 * es};
+    const cuuint32_t box[3] = {f32 ? 32u : 64u, 1u, 64u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Which schedule runs: the fused cooperative kernel when the chains leave most
@@ -1246,10 +1318,26 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if (varlen) pf::schedule_kernel<<<1, 1024, 0, stream>>>(cu, N, T_total, first_chunk, status);
     const bool fused = sched == 1;
 
-    pf::PrepArgs pa{static_cast<const __nv_bfloat16 *>(q), static_cast<const __nv_bfloat16 *>(k),
-                    static_cast<const __nv_bfloat16 *>(v), g,
-                    static_cast<const __nv_bfloat16 *>(beta), cu, first_chunk, N, T, H,
-                    (int)nitems, blocks, status};
+    pf::PrepArgs pa;
+    memset(&pa, 0, sizeof(pa));
+    if (nitems > 0 && !(make_token_map(&pa.tmq, q, false, H, T_total) &&
+                        make_token_map(&pa.tmk, k, false, H, T_total) &&
+                        make_token_map(&pa.tmv, v, false, H, T_total) &&
+                        make_token_map(&pa.tmg, g, true, H, T_total)))
+        return cudaErrorUnknown;
+    pa.q = static_cast<const __nv_bfloat16 *>(q);
+    pa.k = static_cast<const __nv_bfloat16 *>(k);
+    pa.v = static_cast<const __nv_bfloat16 *>(v);
+    pa.g = g;
+    pa.beta = static_cast<const __nv_bfloat16 *>(beta);
+    pa.cu = cu;
+    pa.first_chunk = first_chunk;
+    pa.N = N;
+    pa.T = T;
+    pa.H = H;
+    pa.nitems = (int)nitems;
+    pa.blocks = blocks;
+    pa.status = status;
     pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
                    static_cast<__nv_bfloat16 *>(out), fin, status};
     if (fused) {
