@@ -74,7 +74,7 @@ int kda_abi_version(void);
  * meaning as in kda_prefill; varlen != 0 when cu_seqlens will be passed, and
  * then T is the packed total). Returns 0 when the sizes are invalid. The
  * workspace holds the device status word, the chunk schedule and, for bf16
- * I/O, one 76,288-byte prepared block per (chunk, head). It must be 256-byte
+ * I/O, one 74,240-byte prepared block per (chunk, head). It must be 256-byte
  * aligned and must not be shared by calls in flight at the same time.
  */
 size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,

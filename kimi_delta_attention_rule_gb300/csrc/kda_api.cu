@@ -30,7 +30,7 @@ namespace {
 constexpr size_t kWorkspaceBytes = 256;  // device status word, padded to 256 B
 
 // Workspace of one call: status word, plus (bf16 path) the chunk schedule and
-// one 76 KiB prepared block per (chunk, head).
+// one 74,240-byte prepared block per (chunk, head).
 size_t workspace_bytes_for(int32_t N, int32_t T, int32_t H, int32_t io, bool varlen) {
     if (io == KDA_F32) return kWorkspaceBytes;
     return kda::prefill_tc_workspace(N, T, T, H, varlen);

@@ -29,7 +29,7 @@
 //                    the offsets as a whole)
 //   prep_kernel      K1: persistent, one CTA per SM over (chunk, head) items;
 //                    Gram and pseudo-value products on tcgen05; writes a
-//                    76 KiB chunk block in the exact shared-memory layout K2
+//                    72.5 KiB chunk block in the exact shared-memory layout K2
 //                    consumes
 //   recur_kernel     K2: one CTA per (sequence, head), all 128 value
 //                    columns; per chunk: one bulk TMA load of the block
@@ -64,11 +64,17 @@ constexpr int C = 64;
 constexpr uint32_t kB12 = 0;                      // fp16 K-major [n = (W rows 0..63 | q e^a rows 64..127)][k = key]
 constexpr uint32_t kB3 = kB12 + 128 * 128 * 2;    // fp16 MN-major [k = t'][n]: n = t < 64: M[t][t'],
                                                   //   n = 64 + key: k_t' e^{a_C - a_t'}
-constexpr uint32_t kUt = kB3 + 64 * 192 * 2;      // fp16 [j][t], pitch 144 B: U~^T
-constexpr uint32_t kUtPitch = 144;
-constexpr uint32_t kGam = kUt + 128 * kUtPitch;   // fp32 [128] e^{a_C}
-constexpr uint32_t kBlock = kGam + 128 * 4;       // 76288 B
+constexpr uint32_t kUt = kB3 + 64 * 192 * 2;      // fp16 [j][t], 128-B rows, chunks swizzled: U~^T
+constexpr uint32_t kGam = kUt + 128 * 128;        // fp32 [128] e^{a_C}
+constexpr uint32_t kBlock = kGam + 128 * 4;       // 74240 B
 static_assert(kBlock % 128 == 0, "block size");
+
+// U~^T row j holds tokens 0..63; its 16-byte chunk c (tokens 8 c .. 8 c + 7) sits at
+// chunk c ^ (j % 8): K1 writes whole 32-byte sectors, and K2's reads of 8 consecutive
+// rows at the same tokens fall in distinct banks
+__device__ __forceinline__ uint32_t ut_off(int j, int chunk) {
+    return kUt + (uint32_t)j * 128u + ((uint32_t)(chunk ^ (j & 7)) << 4);
+}
 
 // K-major core-matrix offsets (LBO = 128: K-adjacent core matrices contiguous)
 __device__ __forceinline__ uint32_t off_k128(int r, int k) {  // K extent 128: SBO 2048
@@ -185,12 +191,19 @@ constexpr uint32_t kOffAd = kOffMdp + 4 * C * 4;               // fp32 [4][16][1
 //   kE21 = e^{r_2 - r_1}, kE31 = e^{r_3 - r_1}, kE32 = e^{r_3 - r_2}  (r_4 = a_C)
 constexpr uint32_t kOffTab = kOffAd + 4 * 256 * 4;
 constexpr int kTabEr = 0, kTabEd = 4, kTabEc = 8, kTabE21 = 12, kTabE31 = 13, kTabE32 = 14;
-constexpr uint32_t kOffX = align1k(kOffTab + 16 * 128 * 4);    // bf16 K-major [128][128]: row 32 i + 16 w + t % 16
+constexpr uint32_t kOffGamS = kOffTab + 16 * 128 * 4;          // fp32 [128] e^{a_C}, until the block is written
+constexpr uint32_t kOffX = align1k(kOffGamS + 128 * 4);        // bf16 K-major [128][128]: row 32 i + 16 w + t % 16
 constexpr uint32_t kOffKh = kOffX + 128 * 128 * 2;             // bf16 K-major [160][128]: 10 column tiles
 constexpr uint32_t kOffKtb = kOffKh + 160 * 128 * 2;           // fp16 MN-major [s][c]: beta k e^{a}
 constexpr uint32_t kOffVb = kOffKtb + 64 * 128 * 2;            // fp16 MN-major [s][j]: beta v
 constexpr uint32_t kOffVs = kOffVb + 64 * 128 * 2;             // bf16 staged v: 2 regions
-constexpr uint32_t kPrepSmem = kOffVs + 2 * kRegion;
+// block pieces staged for TMA bulk stores, in the block's own layout:
+//   Sqe: q e^{a} (block rows 64..127 of [W ; q e^a]), later W (rows 0..63);
+//   Sb3: the [M ; k e^{a_C - a}] operand, later U~^T followed by e^{a_C}
+constexpr uint32_t kOffSqe = kOffVs + 2 * kRegion;
+constexpr uint32_t kOffSb3 = kOffSqe + 64 * 128 * 2;
+constexpr uint32_t kPrepSmem = kOffSb3 + 64 * 192 * 2;
+static_assert(128 * 128 + 128 * 4 <= 64 * 192 * 2, "U~^T and e^{a_C} fit the Sb3 staging");
 // after the Gram products, inside X:
 constexpr uint32_t kOffT = kOffX;                              // fp16 K-major [64][64]: T
 constexpr uint32_t kOffAh = kOffT + 64 * 64 * 2;               // fp16 [64][72]: A below the diagonal blocks
@@ -459,10 +472,11 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             staged = first;
         }
     }
-    // With `ready`: the previous item's flag (-1: none) is released by one lane
-    // of the last warp while the CTA waits for this item's Gram products; the
-    // proxy fence that makes the block visible to bulk copies comes before
-    // this item's first barrier.
+    // Every block byte leaves shared memory by TMA bulk stores issued by thread 0,
+    // which waits for them to complete before the barrier ahead of the next item's
+    // operand phase. With `ready`: the previous item's flag (-1: none) is then
+    // released by one lane of the last warp during this item's T phase, where that
+    // warp is otherwise idle.
     constexpr int kReleaser = kPrepThreads - 32;
     long long pending = -1;
     auto release = [&](long long idx) {
@@ -500,7 +514,6 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const bool has_next = nitem < nitems && decode(nitem, nslot, nh, ntc, nL);
 
     if (tid < C) sBeta[tid] = __bfloat162float(__ushort_as_bfloat16(beta_next));
-    if (pending >= 0) asm volatile("fence.proxy.async.global;\n" ::: "memory");
     if (!failed && !tc::mbar_wait(bInG, it & 1u, kPrepWaitLimit)) failed = true;
     if (!failed && !tc::mbar_wait(bInQKV, it & 1u, kPrepWaitLimit)) failed = true;
     failed = __syncthreads_or(failed) != 0;
@@ -540,7 +553,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
         if (ti4 == 3) {
             sAcT[ch] = rr[4];
-            reinterpret_cast<float *>(blk + kGam)[ch] = __expf(rr[4]);
+            reinterpret_cast<float *>(smem + kOffGamS)[ch] = __expf(rr[4]);
         }
     }
     // this item's q, k, v: out of the staging area before it is overwritten
@@ -554,6 +567,9 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         uv[m] = *reinterpret_cast<const uint4 *>(smem + kOffVs + so);
         if (t >= L) uq[m] = uk[m] = uv[m] = make_uint4(0, 0, 0, 0);  // past the chunk
     }
+    // the previous item's bulk stores are complete: its staging is free, and its
+    // flag may be released after this barrier
+    if (tid == 0) tc::bulk_wait_all();
     __syncthreads();
 
     // ---- all operands: thread = (8 channels, tokens op_t0 and op_t0 + 8) ---------------
@@ -614,7 +630,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = qq[e] * (er[e] * x[e]);            // q e^{a}
-            *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(64 + t, c0)) = pack8_f16(o);
+            *reinterpret_cast<uint4 *>(smem + kOffSqe + off_k128(t, c0)) = pack8_f16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * (er[e] * x[e]);       // beta k e^{a}
             *reinterpret_cast<uint4 *>(smem + kOffKtb + off_mn128(t, c0)) = pack8_f16(o);
@@ -623,7 +639,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             *reinterpret_cast<uint4 *>(smem + kOffVb + off_mn128(t, c0)) = pack8_f16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * (ec[e] * y[e]);            // k e^{a_C - a}
-            *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(t, 64 + c0)) = pack8_f16(o);
+            *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(t, 64 + c0)) = pack8_f16(o);
             // q_t . k_t (the diagonal of M: no decay): 32 channels per warp here,
             // the four warps of the tile are added in the Gram read-back
             md += __shfl_xor_sync(0xffffffffu, md, 8);
@@ -644,6 +660,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // the other columns are products of unrelated tiles and are not read.
     if (tid == 0) {
         tc::fence_after_sync();
+        tc::bulk_s2g(blk + kB12 + 64 * 256, sbase + kOffSqe, 64 * 256);  // q e^{a}
+        tc::bulk_commit();
         const uint64_t dA1 = tc::smem_desc(sbase + kOffKh, 128, 2048);
         const uint64_t dB1 = tc::smem_desc(sbase + kOffX, 128, 2048);
         const uint64_t dA2 = tc::smem_desc(sbase + kOffKh + 12u * 2048u, 128, 2048);
@@ -654,10 +672,6 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int ks = 0; ks < 8; ++ks)
             tc::mma_f16(tm + 128u, dA2 + 16 * ks, dB2 + 16 * ks, id_gram2, ks > 0);
         tc::mma_commit(bG);
-    }
-    if (pending >= 0 && tid == kReleaser) {
-        release(pending);
-        pending = -1;
     }
     if (!failed && !tc::mbar_wait(bG, it & 1u, kPrepWaitLimit)) failed = true;
     tc::fence_after_sync();
@@ -719,22 +733,27 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                     const float mv = __uint_as_float(rv[0][n]);
                     mt[n] = diag ? (sl < n ? mv : (sl == n ? md_s : 0.f)) : mv;
                 }
-                *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i)) = pack8_f16(mt);
-                *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i + 8)) = pack8_f16(mt + 8);
+                *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(s, 16 * i)) = pack8_f16(mt);
+                *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(s, 16 * i + 8)) = pack8_f16(mt + 8);
                 if (diag) {  // t in the tiles before s: zero
 #pragma unroll 1
                     for (int i2 = 0; i2 < j; ++i2) {
-                        *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i2)) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4 *>(blk + kB3 + off_b3(s, 16 * i2 + 8)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(s, 16 * i2)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(s, 16 * i2 + 8)) = make_uint4(0, 0, 0, 0);
                     }
                 }
             }
         }
     }
+    tc::fence_async_smem();  // [M ; k e^{a_C - a}] staging -> bulk store
     tc::fence_before_sync();
     failed = __syncthreads_or(failed) != 0;
     tc::fence_after_sync();
     if (failed) break;
+    if (tid == 0) {
+        tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);
+        tc::bulk_commit();
+    }
     if (has_next) {  // column tiles and the v buffer are free from here on
         stage_qkv(ntc, nh);
         if (tid < C) beta_next = load_beta(ntc, nh, nL);
@@ -744,14 +763,17 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
     const uint32_t aT = sbase + kOffT, aAh = sbase + kOffAh;
     if (tid < 64) {
+        // column cc of the inverse of block b by forward substitution, updating the
+        // remaining rows as each entry is known (one multiply-add per step on the chain)
         const int b = tid >> 4, cc = tid & 15;
-        float x[16];
+        float x[16], acc[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float acc = 0.f;
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-            for (int s2 = 0; s2 < r; ++s2) acc += sAd[b * 256 + r * 16 + s2] * x[s2];
-            x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
+        for (int s2 = 0; s2 < 16; ++s2) {
+            x[s2] = s2 < cc ? 0.f : (s2 == cc ? 1.f : -acc[s2]);
+#pragma unroll
+            for (int r = s2 + 1; r < 16; ++r) acc[r] += sAd[b * 256 + r * 16 + s2] * x[s2];
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) store_h(smem + kOffT, off_k64(16 * b + r, 16 * b + cc), x[r]);
@@ -788,6 +810,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(rr + 8, cc2)) = pack_f16(-acc[nt][2], -acc[nt][3]);
             }
         };
+        if (pending >= 0 && tid == kReleaser) {  // idle here: publish the previous item's block
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            release(pending);
+        }
         if (warp < 2) {
             const int i = 1 + 2 * warp, j = i - 1;
             float xacc[2][4] = {};
@@ -838,6 +864,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
     }
     tc::fence_async_smem();  // T -> tensor core
+    if (tid == 0) tc::bulk_wait_read();  // q e^{a} and [M ; Kb] staging free for W, U~
     tc::fence_before_sync();
     __syncthreads();
 
@@ -863,23 +890,41 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         if (lane < 16) {
 #pragma unroll
             for (int gi = 0; gi < 4; ++gi)
-                *reinterpret_cast<uint4 *>(blk + kB12 + off_k128(t, cb + 8 * gi)) =
+                *reinterpret_cast<uint4 *>(smem + kOffSqe + off_k128(t, cb + 8 * gi)) =
                     pack8_f16_u(&rw[gi >> 1][(gi & 1) * 8]);
         }
         // U~^T: lane = value column j = 32 (warp % 4) + lane; tokens [16 (warp / 4), +16)
         const int jj = 32 * (warp & 3) + lane, t0 = 16 * (warp >> 2);
         uint32_t ru[1][16];
         tc::tmem_ld_cols<1>(tquart + 128u + (uint32_t)t0, ru);
-        unsigned char *ut = blk + kUt + (size_t)jj * kUtPitch + 2 * t0;
-        *reinterpret_cast<uint4 *>(ut) = pack8_f16_u(&ru[0][0]);
-        *reinterpret_cast<uint4 *>(ut + 16) = pack8_f16_u(&ru[0][8]);
+        unsigned char *su = smem + kOffSb3 - kUt;  // U~^T staged at its block offsets
+        *reinterpret_cast<uint4 *>(su + ut_off(jj, t0 >> 3)) = pack8_f16_u(&ru[0][0]);
+        *reinterpret_cast<uint4 *>(su + ut_off(jj, (t0 >> 3) + 1)) = pack8_f16_u(&ru[0][8]);
+        if (tid < 128)
+            reinterpret_cast<float *>(su + kGam)[tid] = reinterpret_cast<const float *>(smem + kOffGamS)[tid];
     }
+    tc::fence_async_smem();  // W, U~^T, e^{a_C} staging -> bulk stores
     tc::fence_before_sync();
     failed = __syncthreads_or(failed) != 0;  // shared memory and TMEM are reused by the next item
     tc::fence_after_sync();
     if (failed) break;
+    if (tid == 0) {
+        tc::bulk_s2g(blk + kB12, sbase + kOffSqe, 64 * 256);             // W
+        tc::bulk_s2g(blk + kUt, sbase + kOffSb3, kBlock - kUt);          // U~^T, e^{a_C}
+        tc::bulk_commit();
+    }
+    if (ready) {
+        if (it == 0) {  // the chains wait for the first blocks: publish this one at once
+            if (tid == 0) {
+                tc::bulk_wait_all();
+                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+                release((long long)slot * H + h);
+            }
+        } else {
+            pending = (long long)slot * H + h;
+        }
+    }
     ++it;
-    if (ready) pending = (long long)slot * H + h;
     }
 
     if (failed) {
@@ -887,10 +932,13 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         // let any MMA still in flight land before the TMEM is released
         tc::mbar_wait(bG, it & 1u, 10000000ull);
         tc::mbar_wait(bW, it & 1u, 10000000ull);
-    } else if (pending >= 0) {  // the last item of this CTA
-        asm volatile("fence.proxy.async.global;\n" ::: "memory");
-        __syncthreads();
-        if (tid == kReleaser) release(pending);
+    }
+    if (tid == 0) {
+        tc::bulk_wait_all();  // every block write of this CTA is done
+        if (!failed && pending >= 0) {  // the last item of this CTA
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            release(pending);
+        }
     }
     if (failed && n_staged > 0) {  // staged copies still in flight: the last phase issued
         tc::mbar_wait(bInG, (n_staged - 1) & 1u, 10000000ull);
@@ -997,31 +1045,44 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
         failed = __syncthreads_or(failed) != 0;
         tc::fence_after_sync();
     };
-    // Block loads, issued in chunk order by thread 0. Chunk x may be loaded
-    // once chunk x - 2 has left its buffer and (with `ready`) once it exists.
+    // Block loads, issued in chunk order by one lane of warp 1 (thread 0 issues the
+    // MMAs). Chunk x may be loaded once chunk x - 2 has left its buffer and (with
+    // `ready`) once its flag is set. The flag of the next chunk is checked where the
+    // CTA waits for the tensor core anyway; only a chunk that is still missing when
+    // it is needed is waited for.
     int next_load = 0;
-    auto issue_loads = [&](int upto, bool block) {  // chunks [next_load, upto]
-        upto = min(upto, nchunks - 1);
-        while (!failed && next_load <= upto) {
+    auto issue_one = [&]() {
+        const int c = next_load++;
+        tc::mbar_arrive_expect_tx(bL(c), kBlock);
+        tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
+    };
+    auto flag_ptr = [&](int x) { return ready + (size_t)(fc + x) * H + h; };
+    auto check_issue = [&](int x) {  // issue chunk x if it is the next one and exists
+        if (failed || next_load != x || x >= nchunks) return;
+        if (ready) {
+            if (!flag_set(flag_ptr(x))) return;
+            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        }
+        issue_one();
+    };
+    auto block_issue = [&](int x) {  // chunks [next_load, x], waiting (bounded) for flags
+        x = min(x, nchunks - 1);
+        while (!failed && next_load <= x) {
             if (ready) {
-                const int *f = ready + (size_t)(fc + next_load) * H + h;
-                if (!flag_set(f)) {
-                    if (!block) return;
-                    const uint64_t start = tc::globaltimer_ns();
-                    while (!flag_set(f)) {
-                        if (tc::globaltimer_ns() - start > kWaitLimit) {
-                            failed = true;
-                            return;
-                        }
+                const int *f = flag_ptr(next_load);
+                const uint64_t start = tc::globaltimer_ns();
+                while (!flag_set(f)) {
+                    if (tc::globaltimer_ns() - start > kWaitLimit) {
+                        failed = true;
+                        return;
                     }
                 }
                 asm volatile("fence.proxy.async.global;\n" ::: "memory");
             }
-            const int c = next_load++;
-            tc::mbar_arrive_expect_tx(bL(c), kBlock);
-            tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
+            issue_one();
         }
     };
+    constexpr int kLoader = 32;
     // descriptors (no swizzle); +16 in the address field per 256-byte K step
     const uint64_t dSA = tc::smem_desc(uSA, 128, 2048), dUA = tc::smem_desc(uUA, 128, 1024);
     const uint32_t id_n128 = tc::idesc_f16(128, 128, 1, 0, 0);
@@ -1047,9 +1108,9 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             for (int k0 = 32 * qd; k0 < 32 * qd + 32; ++k0)
                 fin[head_state + (size_t)k0 * 128 + j] = init ? init[head_state + (size_t)k0 * 128 + j] : 0.f;
     } else {
-        if (tid == 0) {
-            issue_loads(0, true);
-            issue_loads(1, false);
+        if (tid == kLoader) {
+            block_issue(0);
+            check_issue(1);
         }
         // initial state, keys [32 qd, 32 qd + 32) of column j: fp16 copy -> S^T,
         // and Diag(e^{a_C}) S0 (the first chunk's decay) -> TMEM
@@ -1057,7 +1118,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
 #pragma unroll
         for (int e = 0; e < 32; ++e)
             s0[e] = init ? init[head_state + (size_t)(32 * qd + e) * 128 + j] : 0.f;
-        sync_check();  // thread 0's first load was issued (or failed)
+        sync_check();  // the first load was issued (or failed)
         wait(bL0, 0);
         {
             const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam) + 32 * qd;
@@ -1085,16 +1146,16 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             const int tcc = t0 + c * C, L = min(C, t1 - tcc);
 
             // U^T = U~^T - P^T for t in [16 qd, 16 qd + 16) -> shared (fp16)
+            if (tid == kLoader) check_issue(c + 1);  // while the first product runs
             wait(bL(c), (uint32_t)((c >> 1) & 1));
             wait(bM1, (uint32_t)(c & 1));
             tc::fence_after_sync();
             {
                 uint32_t pr[1][16];
                 tc::tmem_ld_cols<1>(tlane + kColP + 16 * qd, pr);
-                const unsigned char *ut = buf + kUt + (size_t)j * kUtPitch + 32 * qd;
 #pragma unroll
                 for (int gi = 0; gi < 2; ++gi) {
-                    const uint4 u = *reinterpret_cast<const uint4 *>(ut + 16 * gi);
+                    const uint4 u = *reinterpret_cast<const uint4 *>(buf + ut_off(j, 2 * qd + gi));
                     const __half2 *hu = reinterpret_cast<const __half2 *>(&u);
                     uint4 pk;
                     uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
@@ -1110,10 +1171,8 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             }
             tc::fence_async_smem();
             sync_check();
-            if (tid == 0 && !failed) {
-                issue_mma2(c);
-                issue_loads(c + 1, false);
-            }
+            if (tid == 0 && !failed) issue_mma2(c);
+            if (tid == kLoader) check_issue(c + 1);  // while the second product runs
 
             // new state (keys [32 qd, +32)) and this chunk's O (t in [16 qd, +16))
             wait(bM2, (uint32_t)(c & 1));
@@ -1139,14 +1198,14 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             }
             // this chunk's buffer is no longer read: chunk c + 2 may use it; chunk
             // c + 1 must be on its way before anyone waits for it
-            if (tid == 0) {
-                issue_loads(c + 1, true);
-                issue_loads(c + 2, false);
-            }
+            if (tid == kLoader) block_issue(c + 1);
             if (c + 1 < nchunks) wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
             tc::fence_async_smem();
             sync_check();
             if (tid == 0 && c + 1 < nchunks && !failed) issue_mma1(c + 1);
+            // this chunk's buffer is free: without flags, fetch chunk c + 2 into it now
+            if (tid == kLoader && !ready) check_issue(c + 2);
+
 
             // while the next product runs: pre-scale the state by the next chunk's
             // decay, and write this chunk's output rows

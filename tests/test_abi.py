@@ -42,13 +42,13 @@ def test_status_strings(lib):
 
 
 def test_workspace_size(lib):
-    # bf16: status word + one 76288-byte prepared block and one 4-byte ready
+    # bf16: status word + one 74240-byte prepared block and one 4-byte ready
     # flag per (chunk, head)
-    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 128 * 32 * 76288
-    assert kda.kda_prefill_workspace_size(4, 100, 2, 128, 64, kda.KDA_BF16) >= 4 * 2 * 2 * 76288
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 128 * 32 * 74240
+    assert kda.kda_prefill_workspace_size(4, 100, 2, 128, 64, kda.KDA_BF16) >= 4 * 2 * 2 * 74240
     # packed: T is the total; one spare chunk slot per sequence at most
     vl = kda.kda_prefill_workspace_size(64, 1 << 20, 32, 128, 64, kda.KDA_BF16, varlen=True)
-    assert ((1 << 20) // 64) * 32 * 76288 <= vl <= ((1 << 20) // 64 + 64) * 32 * 76292 + 4096
+    assert ((1 << 20) // 64) * 32 * 74240 <= vl <= ((1 << 20) // 64 + 64) * 32 * 74244 + 4096
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_F32) >= 256
     assert kda.kda_prefill_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16) == 0      # D != 128
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_BF16) == 0     # chunk
