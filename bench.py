@@ -322,6 +322,12 @@ def main():
 
     peaks, peak_src = load_peaks()
     tr_pf = measured_traffic("prefill_h32_t8192")
+    if tr_pf is not None:  # DRAM bytes of one call under the schedule that ran
+        kern = tr_pf["kernels"]
+        names = ["fused_kernel"] if fused else ["prep_kernel (split schedule)",
+                                                "recur_kernel (split schedule)"]
+        tr_pf = ({"bytes_per_launch": sum(kern[k]["read"] + kern[k]["write"] for k in names)}
+                 if all(k in kern for k in names) else None)
     bpt = prefill_bytes_per_head_token()
     bytes_per_launch = bpt * H * T + fin.numel() * 4
     achieved_gbs = bytes_per_launch / (ms * 1e-3) / 1e9
