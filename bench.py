@@ -408,11 +408,59 @@ def main():
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                          "traffic": decode_traffic(B * Hd),
-                         "peak_source": peak_src, "kernel": "decode_step_kernel",
+                         "peak_source": peak_src, "kernel": "decode_kernel",
                          "algorithmic_bytes_per_launch": state_bytes},
             "gpu_launches": reps * S,
         }
         del graph, dqq, dkk, dvv, dgg, dbb, state, dout
+
+        # multi-token decode through a state pool: T = 4 tokens per sequence,
+        # pool entries addressed by a permutation (16 calls in a CUDA graph)
+        Tm, calls = 4, 16
+        xm = inputs.prefill_inputs([Tm] * B, H=Hd, io="bf16", seed=DECODE["seed"] + 5 + 7919 * rank,
+                                   device=dev)
+        shp = (B, Tm, Hd, D)
+        mq, mk, mv, mg = (t.view(shp) for t in (xm.q, xm.k, xm.v, xm.g))
+        mb = xm.beta.view(B, Tm, Hd)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(DECODE["seed"] + 6)
+        pool = 0.02 * torch.randn((B, Hd, D, D), generator=gen, device=dev)
+        perm = torch.randperm(B, generator=gen, device=dev).to(torch.int32)
+        mout = torch.empty_like(mq)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(g_stream):
+            kda.kda_decode(mq, mk, mv, mg, mb, dscale, pool, state_indices=perm, out=mout,
+                           stream=g_stream)
+            g_stream.synchronize()
+            with torch.cuda.graph(graph, stream=g_stream):
+                for _ in range(calls):
+                    kda.kda_decode(mq, mk, mv, mg, mb, dscale, pool, state_indices=perm, out=mout,
+                                   stream=g_stream)
+        torch.cuda.synchronize()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        e0.record(g_stream)
+        with torch.cuda.stream(g_stream):
+            for _ in range(reps):
+                graph.replay()
+        e1.record(g_stream)
+        torch.cuda.synchronize()
+        mms = e0.elapsed_time(e1) / (reps * calls)
+        mgbs = state_bytes / (mms * 1e-3) / 1e9
+        decode["multi_token_pool"] = {
+            "workload": "B=256, H=96, T=4 tokens per sequence per call, pool entries by a "
+                        "permutation, 16 calls per graph",
+            "value": mgbs, "unit": "GB/s", "ms_per_call": mms,
+            "tokens_per_s": Tm * B * Hd / (mms * 1e-3),
+            "roofline": {"bound": "hbm", "achieved": mgbs, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": mgbs / peaks["hbm_gbs"],
+                         "kernel": "decode_kernel",
+                         "algorithmic_bytes_per_launch": state_bytes},
+            "gpu_launches": reps * calls,
+        }
+        decode["gpu_launches"] += reps * calls
+        del graph, xm, mq, mk, mv, mg, mb, pool, perm, mout
 
     if rank != 0:
         if world > 1:

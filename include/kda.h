@@ -114,8 +114,8 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
                 float *final_state, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * One decode step: B sequences x H heads, one new token each, following the
- * per-token form ("FlashKDA 算法": decode follows the recurrence; its cost
+ * One decode step (kda_decode with T = 1, channel-wise g, no indices): B
+ * sequences x H heads, one new token each, following the per-token form ("FlashKDA 算法": decode follows the recurrence; its cost
  * is dominated by one fp32 read and one fp32 write of the state, ~8 D^2
  * bytes per head and token, "复杂度分析").
  *   q, k, v : io dtype [B, H, D]   g : fp32 [B, H, D]   beta : io dtype [B, H]
@@ -147,6 +147,29 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
  */
 int kda_prefill_schedule(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
                          int32_t varlen);
+
+/*
+ * Decode of T new tokens for each of B sequences (T = 1: one step; T up to 64,
+ * e.g. the drafted tokens of speculative decoding), the per-token recurrence
+ * applied in order, with each head's state read once and written once
+ * ("FlashKDA 算法", "复杂度分析": ~8 D^2 bytes of state traffic per head and step).
+ *   q, k, v : io dtype [B, T, H, D]   beta : io dtype [B, T, H]
+ *   g       : fp32 [B, T, H, D] when g_per_channel = 1 (KDA), or fp32 [B, T, H]
+ *             when g_per_channel = 0 (one decay per token and head: the Gated
+ *             DeltaNet form; clamped to [-5, 0] like the channel-wise one)
+ *   state_pool : fp32 [pool_size, H, D, D], updated in place
+ *   state_indices : DEVICE int32 [B], the pool entry of each sequence, or NULL
+ *             (sequence b uses entry b; then pool_size >= B). An index < 0 or
+ *             >= pool_size skips its sequence (no output, no state change).
+ *             Indices must be distinct among the sequences of one call.
+ *   out : io dtype [B, T, H, D]
+ * Pointer alignment: 16 bytes. Needs no workspace. T = 0 or B = 0 is a no-op.
+ * Returns KDA_ERR_UNSUPPORTED for T > 64, D != 128 or an unknown io.
+ */
+int kda_decode(const void *q, const void *k, const void *v, const float *g, const void *beta,
+               float scale, int32_t B, int32_t T, int32_t H, int32_t D, int32_t io,
+               int32_t g_per_channel, float *state_pool, int32_t pool_size,
+               const int32_t *state_indices, void *out, void *stream);
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of a

@@ -32,7 +32,7 @@ KDA_SCHEDULE_DIRECT = 2
 
 EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size", "kda_prefill",
             "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
-            "kda_prefill_schedule")
+            "kda_prefill_schedule", "kda_decode")
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,9 @@ def load() -> ctypes.CDLL:
         lib.kda_check_cu_seqlens.restype = ctypes.c_int
         lib.kda_prefill_schedule.argtypes = [I32] * 7
         lib.kda_prefill_schedule.restype = ctypes.c_int
+        lib.kda_decode.argtypes = [P, P, P, P, P, F32, I32, I32, I32, I32, I32, I32, P, I32, P, P,
+                                   P]
+        lib.kda_decode.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -187,6 +190,29 @@ def kda_decode_step(q, k, v, g, beta, scale, state, out=None, stream=None):
                              D, io, _ptr(state), _ptr(out), _stream_ptr(stream))
     if rc != KDA_OK:
         raise KDAError(rc, "kda_decode_step")
+    return out
+
+
+def kda_decode(q, k, v, g, beta, scale, state_pool, state_indices=None, out=None, stream=None):
+    """Decode of T tokens per sequence (C entry point ``kda_decode``):
+    q, k, v [B, T, H, D]; g [B, T, H, D] (per channel) or [B, T, H] (one
+    decay per token and head); beta [B, T, H]; state_pool fp32
+    [P, H, D, D] updated in place; state_indices device int32 [B] or None
+    (sequence b uses pool entry b). Returns out [B, T, H, D]."""
+    lib = load()
+    io = _io_code(q.dtype)
+    B, T, H, D = q.shape
+    g_per_channel = 1 if g.dim() == 4 else 0
+    _check_cuda(q, k, v, g, beta, state_pool, state_indices, out)
+    if state_indices is not None and state_indices.dtype != torch.int32:
+        raise ValueError("state_indices must be int32")
+    if out is None:
+        out = torch.empty_like(q)
+    rc = lib.kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale), B, T, H, D,
+                        io, g_per_channel, _ptr(state_pool), state_pool.shape[0],
+                        _ptr(state_indices), _ptr(out), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_decode")
     return out
 
 

@@ -10,9 +10,10 @@
 
 namespace kda {
 template <typename IO>
-cudaError_t launch_decode_step(const void *q, const void *k, const void *v, const float *g,
-                               const void *beta, float scale, int B, int H, float *state,
-                               void *out, cudaStream_t stream);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
+                          const void *beta, float scale, int B, int T, int H, int g_per_channel,
+                          float *pool, int pool_size, const int32_t *idx, void *out,
+                          cudaStream_t stream);
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *g,
                                const float *beta, float scale, const float *init,
                                const int32_t *cu, int N, int T, int T_total, int H, int chunk,
@@ -28,6 +29,7 @@ int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varle
 namespace {
 
 constexpr size_t kWorkspaceBytes = 256;  // device status word, padded to 256 B
+constexpr int32_t kMaxDecodeTokens = 64;  // beyond a chunk, the prefill path is the better one
 
 // Workspace of one call: status word, plus (bf16 path) the chunk schedule and
 // one 74,240-byte prepared block per (chunk, head).
@@ -137,23 +139,36 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+int kda_decode(const void *q, const void *k, const void *v, const float *g, const void *beta,
+               float scale, int32_t B, int32_t T, int32_t H, int32_t D, int32_t io,
+               int32_t g_per_channel, float *state_pool, int32_t pool_size,
+               const int32_t *state_indices, void *out, void *stream) {
+    if (B < 0 || T < 0 || H <= 0 || D <= 0 || pool_size < 0) return KDA_ERR_INVALID_ARG;
+    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (D != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if (T > kMaxDecodeTokens) return KDA_ERR_UNSUPPORTED;
+    if (g_per_channel != 0 && g_per_channel != 1) return KDA_ERR_INVALID_ARG;
+    if ((long long)B * H > 0x7fffffffLL || (long long)B * T * H > (1LL << 40))
+        return KDA_ERR_INVALID_ARG;
+    if (state_indices == nullptr && pool_size < B) return KDA_ERR_INVALID_ARG;
+    if (B == 0 || T == 0) return KDA_OK;
+    if (!q || !k || !v || !g || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e =
+        io == KDA_F32
+            ? kda::launch_decode<float>(q, k, v, g, beta, scale, B, T, H, g_per_channel,
+                                        state_pool, pool_size, state_indices, out, st)
+            : kda::launch_decode<__nv_bfloat16>(q, k, v, g, beta, scale, B, T, H, g_per_channel,
+                                                state_pool, pool_size, state_indices, out, st);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                     const void *beta, float scale, int32_t B, int32_t H, int32_t D, int32_t io,
                     float *state_inout, void *out, void *stream) {
-    if (B < 0 || H <= 0 || D <= 0) return KDA_ERR_INVALID_ARG;
-    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
-    if (D != kda::kD) return KDA_ERR_UNSUPPORTED;
-    if ((long long)B * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    if (B == 0) return KDA_OK;
-    if (!q || !k || !v || !g || !beta || !state_inout || !out) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(state_inout)) return KDA_ERR_INVALID_ARG;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = io == KDA_F32
-                        ? kda::launch_decode_step<float>(q, k, v, g, beta, scale, B, H,
-                                                         state_inout, out, st)
-                        : kda::launch_decode_step<__nv_bfloat16>(q, k, v, g, beta, scale, B, H,
-                                                                 state_inout, out, st);
-    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return kda_decode(q, k, v, g, beta, scale, B, 1, H, D, io, 1, state_inout, B, nullptr, out,
+                      stream);
 }
 
 int kda_workspace_status(void *workspace, void *stream) {

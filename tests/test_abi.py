@@ -112,6 +112,24 @@ def test_decode_argument_validation(lib):
     assert f(None, None, None, None, None, 1.0, 0, 2, 128, 0, None, None, None) == kda.KDA_OK
 
 
+def test_decode_multi_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)
+    f = lib.kda_decode
+    args = lambda **kw: dict(dict(q=fake, k=fake, v=fake, g=fake, beta=fake, B=4, T=2, H=2, D=128,
+                                  io=0, gpc=1, pool=fake, P=4, idx=None, out=fake), **kw)
+    call = lambda a: f(a["q"], a["k"], a["v"], a["g"], a["beta"], 1.0, a["B"], a["T"], a["H"],
+                       a["D"], a["io"], a["gpc"], a["pool"], a["P"], a["idx"], a["out"], None)
+    assert call(args(T=65)) == kda.KDA_ERR_UNSUPPORTED        # beyond a chunk
+    assert call(args(D=64)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(args(io=5)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(args(gpc=2)) == kda.KDA_ERR_INVALID_ARG
+    assert call(args(P=3)) == kda.KDA_ERR_INVALID_ARG         # pool smaller than B, no indices
+    assert call(args(T=-1)) == kda.KDA_ERR_INVALID_ARG
+    assert call(args(pool=ctypes.c_void_p(0x100004))) == kda.KDA_ERR_INVALID_ARG  # misaligned
+    assert call(args(q=None)) == kda.KDA_ERR_INVALID_ARG
+    assert call(args(B=0)) == kda.KDA_OK and call(args(T=0)) == kda.KDA_OK  # nothing to do
+
+
 def test_host_cu_seqlens_check(lib):
     assert kda.kda_check_cu_seqlens([0, 5, 5, 9], 9) == kda.KDA_OK
     assert kda.kda_check_cu_seqlens([0, 5, 3, 9], 9) == kda.KDA_ERR_INVALID_ARG

@@ -216,6 +216,89 @@ def test_decode_equals_prefill_path():
     assert rel_err(st.cpu().numpy(), fin_p.cpu().numpy()) <= 2 * TOL_BF16
 
 
+# ------------------------------------------------ multi-token / pooled decode
+def multi_decode_case(B, T, H, io, seed, scalar_g=False, P=None, idx=None):
+    """Inputs [B, T, H, ...] of B sequences of T tokens, a state pool of P
+    entries (N(0, 0.02^2)), and the oracle's result for the sequences that run:
+    each is a T-token prefill from its pool entry."""
+    x = inputs.prefill_inputs([T] * B, H=H, io=io, seed=seed)
+    shp = (B, T, H, 128)
+    q, k, v = x.q.view(shp), x.k.view(shp), x.v.view(shp)
+    g = x.g.view(shp)
+    if scalar_g:  # one decay per token and head: channel 0 of the channel-wise draw
+        g = g[..., 0].contiguous()
+    beta = x.beta.view(B, T, H)
+    P = B if P is None else P
+    gen = torch.Generator().manual_seed(seed + 1)
+    pool = 0.02 * torch.randn(P, H, 128, 128, generator=gen)
+    run = [b for b in range(B) if idx is None or 0 <= idx[b] < P]
+    slot = [b if idx is None else idx[b] for b in run]
+    g_full = g if not scalar_g else g[..., None].expand(B, T, H, 128)
+    cu = np.arange(0, len(run) * T + 1, T, dtype=np.int32)
+    pick = lambda t: np32(t[run].reshape(len(run) * T, *t.shape[2:]))
+    ro, rf = oracle.prefill(pick(q), pick(k), pick(v), pick(g_full.contiguous()), pick(beta),
+                            x.scale, init_state=pool[slot].double().numpy(), cu_seqlens=cu)
+    return (q, k, v, g, beta, x.scale, pool, run, slot, ro.reshape(len(run), T, H, 128), rf)
+
+
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_multi_token_decode(io, tol, T):
+    """T tokens per sequence in one call (state read and written once) equal
+    T steps of the recurrence."""
+    q, k, v, g, beta, scale, pool, run, slot, ro, rf = multi_decode_case(6, T, 3, io, 31 + T)
+    st = pool.to(DEV)
+    out = kda.kda_decode(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), scale, st)
+    torch.cuda.synchronize()
+    assert out_err(out, ro) <= tol
+    assert rel_err(st.cpu().numpy(), rf) <= tol
+
+
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+def test_decode_scalar_decay(io, tol):
+    """One decay per (token, head) (g of shape [B, T, H]) equals the
+    channel-wise recurrence with that decay on every channel."""
+    q, k, v, g, beta, scale, pool, run, slot, ro, rf = multi_decode_case(4, 3, 2, io, 41,
+                                                                         scalar_g=True)
+    assert g.dim() == 3
+    st = pool.to(DEV)
+    out = kda.kda_decode(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), scale, st)
+    torch.cuda.synchronize()
+    assert out_err(out, ro) <= tol
+    assert rel_err(st.cpu().numpy(), rf) <= tol
+
+
+def test_decode_state_pool_indices():
+    """Sequences address pool entries through indices; a negative index is a
+    padding entry (skipped); entries no sequence uses stay bit-identical."""
+    B, T, H, P = 4, 2, 2, 7
+    idx = [5, 0, -1, 3]
+    q, k, v, g, beta, scale, pool, run, slot, ro, rf = multi_decode_case(B, T, H, "bf16", 51,
+                                                                         P=P, idx=idx)
+    st = pool.to(DEV)
+    out = torch.full((B, T, H, 128), 7.0, dtype=torch.bfloat16, device=DEV)
+    kda.kda_decode(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), scale, st,
+                   state_indices=torch.tensor(idx, dtype=torch.int32, device=DEV), out=out)
+    torch.cuda.synchronize()
+    assert out_err(out[run], ro) <= TOL_BF16
+    assert rel_err(st[slot].cpu().numpy(), rf) <= TOL_BF16
+    assert torch.all(out[2] == 7.0)  # the padding entry wrote nothing
+    unused = [p for p in range(P) if p not in slot]
+    assert torch.equal(st[unused].cpu(), pool[unused])
+
+
+def test_decode_t1_matches_decode_step():
+    """kda_decode with T = 1 is the single-step entry point, bit for bit."""
+    q, k, v, g, beta, state, scale = inputs.decode_inputs(B=3, H=2, steps=1, seed=61)
+    s1, s2 = state.to(DEV), state.to(DEV)
+    o1 = kda.kda_decode_step(q[0].to(DEV), k[0].to(DEV), v[0].to(DEV), g[0].to(DEV),
+                             beta[0].to(DEV), scale, s1)
+    o2 = kda.kda_decode(q[0, :, None].to(DEV), k[0, :, None].to(DEV), v[0, :, None].to(DEV),
+                        g[0, :, None].to(DEV), beta[0, :, None].to(DEV), scale, s2)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2[:, 0]) and torch.equal(s1, s2)
+
+
 # ------------------------------------------------- full-size workloads (sampled)
 def sampled_chain_check(x_dev, out, fin, lens, chains, init_cpu, tol):
     """Recompute sampled (sequence, head) chains with the oracle from the
