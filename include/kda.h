@@ -114,6 +114,30 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
                 float *final_state, void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_prefill with two options (kda_prefill is this with g_per_channel = 1 and
+ * snapshot_interval = 0):
+ *   g_per_channel : 1 = g fp32 [T_total, H, D] (KDA's channel-wise decay);
+ *                   0 = g fp32 [T_total, H], one decay per token and head (the
+ *                   Gated DeltaNet form, "K3 vs DSV4 architecture divergence",
+ *                   section KDA), clamped to [-5, 0] like the channel-wise one.
+ *   snapshot_interval : 0 = none; else a positive multiple of `chunk`: the state
+ *                   after every snapshot_interval tokens of each sequence (for
+ *                   prefix caching of long prompts) is written to
+ *                   snapshots fp32 [N, max_snapshots, H, D, D] (16-byte aligned):
+ *                   entry [n][s] = the state after (s + 1) * snapshot_interval
+ *                   tokens of sequence n, for s < max_snapshots; entries past a
+ *                   sequence's end are not written. The final state of each
+ *                   sequence still goes to final_state.
+ * Returns KDA_ERR_UNSUPPORTED when snapshot_interval is not a multiple of chunk.
+ */
+int kda_prefill_ex(const void *q, const void *k, const void *v, const float *g,
+                   const void *beta, float scale, const float *init_state,
+                   const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
+                   int32_t chunk, int32_t io, int32_t g_per_channel, int32_t snapshot_interval,
+                   int32_t max_snapshots, float *snapshots, void *out, float *final_state,
+                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * One decode step (kda_decode with T = 1, channel-wise g, no indices): B
  * sequences x H heads, one new token each, following the per-token form ("FlashKDA 算法": decode follows the recurrence; its cost
  * is dominated by one fp32 read and one fp32 write of the state, ~8 D^2

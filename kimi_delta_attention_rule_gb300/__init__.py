@@ -32,7 +32,7 @@ KDA_SCHEDULE_DIRECT = 2
 
 EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size", "kda_prefill",
             "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
-            "kda_prefill_schedule", "kda_decode")
+            "kda_prefill_schedule", "kda_decode", "kda_prefill_ex")
 
 _lock = threading.Lock()
 _lib = None
@@ -74,6 +74,9 @@ def load() -> ctypes.CDLL:
         lib.kda_decode.argtypes = [P, P, P, P, P, F32, I32, I32, I32, I32, I32, I32, P, I32, P, P,
                                    P]
         lib.kda_decode.restype = ctypes.c_int
+        lib.kda_prefill_ex.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32, I32,
+                                       I32, I32, P, P, P, P, SZ, P]
+        lib.kda_prefill_ex.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -144,13 +147,16 @@ def prefill_workspace(q, cu_seqlens=None, N=None, T=None, chunk=64):
 
 def kda_prefill(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk=64, out=None,
                 final_state=None, workspace=None, stream=None, N=None, T=None,
-                output_final_state=True):
-    """Chunked KDA prefill (C entry point ``kda_prefill``).
+                output_final_state=True, snapshot_interval=0, snapshots=None):
+    """Chunked KDA prefill (C entry points ``kda_prefill`` / ``kda_prefill_ex``).
 
-    q, k, v: [T_total, H, D] (bf16 or fp32); g: fp32 [T_total, H, D];
-    beta: [T_total, H]; init_state: fp32 [N, H, D, D] or None;
-    cu_seqlens: device int32 [N+1] or None (then N sequences of length T,
-    default N=1). Returns (out, final_state)."""
+    q, k, v: [T_total, H, D] (bf16 or fp32); g: fp32 [T_total, H, D], or
+    [T_total, H] for one decay per token and head; beta: [T_total, H];
+    init_state: fp32 [N, H, D, D] or None; cu_seqlens: device int32 [N+1] or
+    None (then N sequences of length T, default N=1). With snapshot_interval
+    > 0, snapshots: fp32 [N, S, H, D, D] receives the state after every
+    snapshot_interval tokens of each sequence (S entries at most).
+    Returns (out, final_state)."""
     lib = load()
     io = _io_code(q.dtype)
     T_total, H, D = q.shape
@@ -160,17 +166,26 @@ def kda_prefill(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk
     else:
         N = 1 if N is None else N
         T = T_total // N if T is None else T
-    _check_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, workspace)
+    g_per_channel = 0 if g.dim() == 2 else 1
+    _check_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, workspace, snapshots)
     if out is None:
-        out = torch.empty_like(q) if io != KDA_F32 else torch.empty_like(q)
+        out = torch.empty_like(q)
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = prefill_workspace(q, cu_seqlens, N, T, chunk)
-    rc = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
-                         _ptr(init_state), _ptr(cu_seqlens), N, T, H, D, chunk, io, _ptr(out),
-                         _ptr(final_state), _ptr(workspace), workspace.numel(),
-                         _stream_ptr(stream))
+    max_snaps = 0 if snapshots is None else snapshots.shape[1]
+    if g_per_channel == 1 and not snapshot_interval:
+        rc = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                             _ptr(init_state), _ptr(cu_seqlens), N, T, H, D, chunk, io, _ptr(out),
+                             _ptr(final_state), _ptr(workspace), workspace.numel(),
+                             _stream_ptr(stream))
+    else:
+        rc = lib.kda_prefill_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                _ptr(init_state), _ptr(cu_seqlens), N, T, H, D, chunk, io,
+                                g_per_channel, int(snapshot_interval), max_snaps, _ptr(snapshots),
+                                _ptr(out), _ptr(final_state), _ptr(workspace), workspace.numel(),
+                                _stream_ptr(stream))
     if rc != KDA_OK:
         raise KDAError(rc, "kda_prefill")
     return out, final_state

@@ -17,12 +17,14 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *g,
                                const float *beta, float scale, const float *init,
                                const int32_t *cu, int N, int T, int T_total, int H, int chunk,
+                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
                                float *out, float *fin, uint32_t *status, cudaStream_t stream);
 size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen);
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const void *beta, float scale, const float *init,
-                              const int32_t *cu, int N, int T, int T_total, int H, void *out,
-                              float *fin, unsigned char *ws, cudaStream_t stream);
+                              const int32_t *cu, int N, int T, int T_total, int H,
+                              int g_per_channel, int snap_interval, int snap_max, float *snaps,
+                              void *out, float *fin, unsigned char *ws, cudaStream_t stream);
 int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen);
 }  // namespace kda
 
@@ -101,13 +103,23 @@ int kda_check_cu_seqlens(const int32_t *cu, int32_t N, int32_t T_total) {
     return KDA_OK;
 }
 
-int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,
-                float scale, const float *init_state, const int32_t *cu_seqlens, int32_t N,
-                int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io, void *out,
-                float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+int kda_prefill_ex(const void *q, const void *k, const void *v, const float *g,
+                   const void *beta, float scale, const float *init_state,
+                   const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
+                   int32_t chunk, int32_t io, int32_t g_per_channel, int32_t snapshot_interval,
+                   int32_t max_snapshots, float *snapshots, void *out, float *final_state,
+                   void *workspace, size_t workspace_bytes, void *stream) {
     long long T_total = 0;
     const int rc = check_prefill_dims(N, T, H, D, chunk, io, cu_seqlens != nullptr, &T_total);
     if (rc != KDA_OK) return rc;
+    if (g_per_channel != 0 && g_per_channel != 1) return KDA_ERR_INVALID_ARG;
+    if (snapshot_interval < 0) return KDA_ERR_INVALID_ARG;
+    if (snapshot_interval > 0) {
+        if (snapshot_interval % chunk != 0) return KDA_ERR_UNSUPPORTED;
+        if (snapshots == nullptr || max_snapshots <= 0 || !aligned16(snapshots))
+            return KDA_ERR_INVALID_ARG;
+        if ((long long)N * max_snapshots * H > (1LL << 40)) return KDA_ERR_INVALID_ARG;
+    }
     if (workspace == nullptr ||
         workspace_bytes < workspace_bytes_for(N, T, H, io, cu_seqlens != nullptr) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -120,6 +132,7 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
     }
     if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
         return KDA_ERR_INVALID_ARG;
+    const int si = snapshot_interval, sm = snapshot_interval > 0 ? max_snapshots : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
     // the status word reports this call only
@@ -129,14 +142,23 @@ int kda_prefill(const void *q, const void *k, const void *v, const float *g, con
         e = kda::launch_prefill_f32(static_cast<const float *>(q), static_cast<const float *>(k),
                                     static_cast<const float *>(v), g,
                                     static_cast<const float *>(beta), scale, init_state,
-                                    cu_seqlens, N, T, (int)T_total, H, chunk,
-                                    static_cast<float *>(out), final_state, status, st);
+                                    cu_seqlens, N, T, (int)T_total, H, chunk, g_per_channel, si,
+                                    sm, snapshots, static_cast<float *>(out), final_state,
+                                    status, st);
     } else {
         e = kda::launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T,
-                                   (int)T_total, H, out, final_state,
-                                   static_cast<unsigned char *>(workspace), st);
+                                   (int)T_total, H, g_per_channel, si, sm, snapshots, out,
+                                   final_state, static_cast<unsigned char *>(workspace), st);
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,
+                float scale, const float *init_state, const int32_t *cu_seqlens, int32_t N,
+                int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io, void *out,
+                float *final_state, void *workspace, size_t workspace_bytes, void *stream) {
+    return kda_prefill_ex(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk, io,
+                          1, 0, 0, nullptr, out, final_state, workspace, workspace_bytes, stream);
 }
 
 int kda_decode(const void *q, const void *k, const void *v, const float *g, const void *beta,

@@ -38,8 +38,9 @@ __global__ void __launch_bounds__(kF32Threads, 1)
                        const float *__restrict__ v, const float *__restrict__ g,
                        const float *__restrict__ beta, float scale,
                        const float *__restrict__ init, const int32_t *__restrict__ cu, int T,
-                       int T_total, int H, float *__restrict__ out, float *__restrict__ fin,
-                       uint32_t *status) {
+                       int T_total, int H, int g_per_channel, int snap_interval, int snap_max,
+                       float *__restrict__ snaps, float *__restrict__ out,
+                       float *__restrict__ fin, uint32_t *status) {
     constexpr int DV = kF32Slab;
     constexpr int NSLAB = kD / DV;
     const int sb = blockIdx.x % NSLAB;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(kF32Threads, 1)
             const size_t off = ((size_t)(tc + t) * H + h) * kD + c;
             sQ[idx] = ok ? q[off] : 0.f;
             sK[idx] = ok ? k[off] : 0.f;
-            sA[idx] = ok ? clamp_g(g[off]) : 0.f;
+            sA[idx] = ok ? clamp_g(g_per_channel ? g[off] : g[(size_t)(tc + t) * H + h]) : 0.f;
         }
         for (int idx = tid; idx < C * DV; idx += kF32Threads) {
             const int t = idx / DV, j = idx % DV;
@@ -179,11 +180,16 @@ __global__ void __launch_bounds__(kF32Threads, 1)
         __syncthreads();
 
         // S <- Diag(e^{a_C}) S + (k e^{a_C - a})^T U
+        const int done = tc + L - t0;  // tokens of the sequence done after this chunk
+        float *snap = nullptr;          // the state after every snap_interval tokens
+        if (snaps && done % snap_interval == 0 && done / snap_interval - 1 < snap_max)
+            snap = snaps + (((size_t)n * snap_max + done / snap_interval - 1) * H + h) * kD * kD;
         for (int idx = tid; idx < kD * DV; idx += kF32Threads) {
             const int c = idx / DV, j = idx % DV;
             float acc = sGam[c] * sS[idx];
             for (int t = 0; t < C; ++t) acc += sK[t * kD + c] * sU[t * DV + j];
             sS[idx] = acc;
+            if (snap) snap[(size_t)c * kD + sb * DV + j] = acc;
         }
     }
     __syncthreads();
@@ -199,7 +205,8 @@ template <int C>
 static cudaError_t launch_f32_impl(const float *q, const float *k, const float *v,
                                    const float *g, const float *beta, float scale,
                                    const float *init, const int32_t *cu, int N, int T,
-                                   int T_total, int H, float *out, float *fin, uint32_t *status,
+                                   int T_total, int H, int gpc, int si, int sm_, float *snaps,
+                                   float *out, float *fin, uint32_t *status,
                                    cudaStream_t stream) {
     const size_t smem = f32_smem_floats<C>() * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(prefill_f32_kernel<C>,
@@ -208,19 +215,23 @@ static cudaError_t launch_f32_impl(const float *q, const float *k, const float *
     const long long grid = (long long)N * H * (kD / kF32Slab);
     if (grid == 0) return cudaSuccess;
     prefill_f32_kernel<C><<<(unsigned)grid, kF32Threads, smem, stream>>>(
-        q, k, v, g, beta, scale, init, cu, T, T_total, H, out, fin, status);
+        q, k, v, g, beta, scale, init, cu, T, T_total, H, gpc, si > 0 ? si : 1, sm_,
+        si > 0 ? snaps : nullptr, out, fin, status);
     return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, const float *g,
                                const float *beta, float scale, const float *init,
                                const int32_t *cu, int N, int T, int T_total, int H, int chunk,
+                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
                                float *out, float *fin, uint32_t *status, cudaStream_t stream) {
     if (chunk == 16)
-        return launch_f32_impl<16>(q, k, v, g, beta, scale, init, cu, N, T, T_total, H, out, fin,
+        return launch_f32_impl<16>(q, k, v, g, beta, scale, init, cu, N, T, T_total, H,
+                                   g_per_channel, snap_interval, snap_max, snaps, out, fin,
                                    status, stream);
-    return launch_f32_impl<64>(q, k, v, g, beta, scale, init, cu, N, T, T_total, H, out, fin,
-                               status, stream);
+    return launch_f32_impl<64>(q, k, v, g, beta, scale, init, cu, N, T, T_total, H,
+                               g_per_channel, snap_interval, snap_max, snaps, out, fin, status,
+                               stream);
 }
 
 }  // namespace kda

@@ -192,7 +192,8 @@ constexpr uint32_t kOffAd = kOffMdp + 4 * C * 4;               // fp32 [4][16][1
 constexpr uint32_t kOffTab = kOffAd + 4 * 256 * 4;
 constexpr int kTabEr = 0, kTabEd = 4, kTabEc = 8, kTabE21 = 12, kTabE31 = 13, kTabE32 = 14;
 constexpr uint32_t kOffGamS = kOffTab + 16 * 128 * 4;          // fp32 [128] e^{a_C}, until the block is written
-constexpr uint32_t kOffX = align1k(kOffGamS + 128 * 4);        // bf16 K-major [128][128]: row 32 i + 16 w + t % 16
+constexpr uint32_t kOffGs = kOffGamS + 128 * 4;                // fp32 [64] one decay per token (scalar mode)
+constexpr uint32_t kOffX = align1k(kOffGs + C * 4);            // bf16 K-major [128][128]: row 32 i + 16 w + t % 16
 constexpr uint32_t kOffKh = kOffX + 128 * 128 * 2;             // bf16 K-major [160][128]: 10 column tiles
 constexpr uint32_t kOffKtb = kOffKh + 160 * 128 * 2;           // fp16 MN-major [s][c]: beta k e^{a}
 constexpr uint32_t kOffVb = kOffKtb + 64 * 128 * 2;            // fp16 MN-major [s][j]: beta v
@@ -360,6 +361,7 @@ struct PrepArgs {
     const int32_t *cu, *first_chunk;
     int N, T, H;
     int nitems;  // chunk slots x heads
+    int g_per_channel;  // 0: g is [T_total][H], one decay per token and head
     unsigned char *blocks;
     uint32_t *status;
 };
@@ -436,12 +438,19 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const uint32_t uG = sbase + kOffAcum, uQ = sbase + kOffQs, uK = sbase + kOffKs,
                    uV = sbase + kOffVs;
     uint32_t n_staged = 0;  // stagings issued (each completes one phase of both barriers)
-    auto stage_g = [&](int tc_, int h_) {
+    const bool gpc = pa.g_per_channel != 0;
+    float gs_next = 0.f;  // scalar mode: the decay of token tid of the staged item
+    auto stage_g = [&](int tc_, int h_, int L_) {
         ++n_staged;
-        if (tid == 32) {
-            tc::mbar_arrive_expect_tx(bInG, 4 * kRegion);
+        if (gpc) {
+            if (tid == 32) {
+                tc::mbar_arrive_expect_tx(bInG, 4 * kRegion);
 #pragma unroll
-            for (int r = 0; r < 4; ++r) tma_load_3d(uG + r * kRegion, &pa.tmg, 32 * r, h_, tc_, bInG);
+                for (int r = 0; r < 4; ++r) tma_load_3d(uG + r * kRegion, &pa.tmg, 32 * r, h_, tc_, bInG);
+            }
+        } else {
+            if (tid == 32) tc::mbar_arrive_expect_tx(bInG, 0);  // nothing in flight: the phase completes
+            if (tid < C) gs_next = tid < L_ ? g[((size_t)tc_ + tid) * H + h_] : 0.f;
         }
     };
     auto stage_qkv = [&](int tc_, int h_) {
@@ -466,7 +475,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     {
         int slot_, h_, tc_, L_;
         if (decode(first, slot_, h_, tc_, L_)) {
-            stage_g(tc_, h_);
+            stage_g(tc_, h_, L_);
             stage_qkv(tc_, h_);
             if (tid < C) beta_next = load_beta(tc_, h_, L_);
             staged = first;
@@ -504,7 +513,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     int slot, h, tc, L;
     if (!decode(item, slot, h, tc, L)) continue;
     if (staged != item) {  // the previous item could not prefetch this one
-        stage_g(tc, h);
+        stage_g(tc, h, L);
         stage_qkv(tc, h);
         if (tid < C) beta_next = load_beta(tc, h, L);
     }
@@ -514,6 +523,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const bool has_next = nitem < nitems && decode(nitem, nslot, nh, ntc, nL);
 
     if (tid < C) sBeta[tid] = __bfloat162float(__ushort_as_bfloat16(beta_next));
+    if (!gpc && tid < C) reinterpret_cast<float *>(smem + kOffGs)[tid] = gs_next;
     if (!failed && !tc::mbar_wait(bInG, it & 1u, kPrepWaitLimit)) failed = true;
     if (!failed && !tc::mbar_wait(bInQKV, it & 1u, kPrepWaitLimit)) failed = true;
     failed = __syncthreads_or(failed) != 0;
@@ -523,9 +533,12 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     {
         float a[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r)  // rows past the chunk: g = 0
-            a[r] = 16 * ti4 + r < L ? clamp_g(*reinterpret_cast<const float *>(smem + kOffAcum + a_off(16 * ti4 + r, ch)))
-                                    : 0.f;
+        for (int r = 0; r < 16; ++r) {  // rows past the chunk: g = 0
+            const int t = 16 * ti4 + r;
+            const float gv = gpc ? *reinterpret_cast<const float *>(smem + kOffAcum + a_off(t, ch))
+                                 : reinterpret_cast<const float *>(smem + kOffGs)[t];
+            a[r] = t < L ? clamp_g(gv) : 0.f;
+        }
 #pragma unroll
         for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
         sQsum[ti4 * 128 + ch] = a[15];
@@ -650,7 +663,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     tc::fence_async_smem();  // operands -> tensor core
     tc::fence_before_sync();
     __syncthreads();
-    if (has_next) stage_g(ntc, nh);  // the a buffer is free from here on
+    if (has_next) stage_g(ntc, nh, nL);  // the a buffer is free from here on
 
     // ---- Gram products (16 instructions) ---------------------------------------------
     //   D1 = Kh[0, 128) X^T     -> TMEM [0, 128)   (M = 128: lane = Kh row of slots 0..7)
@@ -978,6 +991,8 @@ struct RecArgs {
     const unsigned char *blocks;
     __nv_bfloat16 *out;
     float *fin;
+    float *snaps;  // [N][snap_max][H][128][128], or null
+    int snap_interval, snap_max;
     uint32_t *status;
 };
 
@@ -1196,6 +1211,16 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 for (int e = 0; e < 32; ++e)
                     fin[head_state + (size_t)(32 * qd + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
             }
+            if (ra.snaps) {  // the state after every snap_interval tokens of the sequence
+                const int done = min((c + 1) * C, t1 - t0);
+                const int si = done / ra.snap_interval - 1;
+                if (done % ra.snap_interval == 0 && si < ra.snap_max) {
+                    float *dst = ra.snaps + (((size_t)n * ra.snap_max + si) * H + h) * 128 * 128;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        dst[(size_t)(32 * qd + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
+                }
+            }
             // this chunk's buffer is no longer read: chunk c + 2 may use it; chunk
             // c + 1 must be on its way before anyone waits for it
             if (tid == kLoader) block_issue(c + 1);
@@ -1345,8 +1370,9 @@ int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varle
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const void *beta, float scale, const float *init,
-                              const int32_t *cu, int N, int T, int T_total, int H, void *out,
-                              float *fin, unsigned char *ws, cudaStream_t stream) {
+                              const int32_t *cu, int N, int T, int T_total, int H,
+                              int g_per_channel, int snap_interval, int snap_max, float *snaps,
+                              void *out, float *fin, unsigned char *ws, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(pf::prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pf::kPrepSmem);
@@ -1382,7 +1408,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if (nitems > 0 && !(make_token_map(&pa.tmq, q, false, H, T_total) &&
                         make_token_map(&pa.tmk, k, false, H, T_total) &&
                         make_token_map(&pa.tmv, v, false, H, T_total) &&
-                        make_token_map(&pa.tmg, g, true, H, T_total)))
+                        (!g_per_channel || make_token_map(&pa.tmg, g, true, H, T_total))))
         return cudaErrorUnknown;
     pa.q = static_cast<const __nv_bfloat16 *>(q);
     pa.k = static_cast<const __nv_bfloat16 *>(k);
@@ -1395,10 +1421,13 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     pa.T = T;
     pa.H = H;
     pa.nitems = (int)nitems;
+    pa.g_per_channel = g_per_channel;
     pa.blocks = blocks;
     pa.status = status;
     pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
-                   static_cast<__nv_bfloat16 *>(out), fin, status};
+                   static_cast<__nv_bfloat16 *>(out), fin,
+                   snap_interval > 0 ? snaps : nullptr, snap_interval > 0 ? snap_interval : 1,
+                   snap_max, status};
     if (fused) {
         e = cudaMemsetAsync(ready, 0, (size_t)nitems * 4, stream);
         if (e != cudaSuccess) return e;

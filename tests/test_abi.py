@@ -112,6 +112,21 @@ def test_decode_argument_validation(lib):
     assert f(None, None, None, None, None, 1.0, 0, 2, 128, 0, None, None, None) == kda.KDA_OK
 
 
+def test_prefill_ex_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)
+    f = lib.kda_prefill_ex
+    def call(gpc=1, si=0, smax=0, snaps=None, chunk=64, ws_bytes=1 << 40):
+        return f(fake, fake, fake, fake, fake, 1.0, None, None, 1, 128, 2, 128, chunk, 0, gpc, si,
+                 smax, snaps, fake, None, fake, ws_bytes, None)
+    assert call(gpc=2) == kda.KDA_ERR_INVALID_ARG
+    assert call(si=-64) == kda.KDA_ERR_INVALID_ARG
+    assert call(si=96, smax=2, snaps=fake) == kda.KDA_ERR_UNSUPPORTED   # not a multiple of 64
+    assert call(si=64, smax=2, snaps=None) == kda.KDA_ERR_INVALID_ARG   # nowhere to write
+    assert call(si=64, smax=0, snaps=fake) == kda.KDA_ERR_INVALID_ARG
+    assert call(si=64, smax=2, snaps=ctypes.c_void_p(0x100008)) == kda.KDA_ERR_INVALID_ARG
+    assert call(ws_bytes=16) == kda.KDA_ERR_INVALID_ARG                  # workspace too small
+
+
 def test_decode_multi_argument_validation(lib):
     fake = ctypes.c_void_p(0x100000)
     f = lib.kda_decode

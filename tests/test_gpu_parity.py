@@ -216,6 +216,74 @@ def test_decode_equals_prefill_path():
     assert rel_err(st.cpu().numpy(), fin_p.cpu().numpy()) <= 2 * TOL_BF16
 
 
+# ------------------------------------------------ prefill options
+def scalar_decay_inputs(lens, H, io, seed):
+    """Inputs with one decay per (token, head): channel 0 of the channel-wise
+    draw; the oracle gets it on every channel."""
+    x = inputs.prefill_inputs(lens, H=H, io=io, seed=seed, init="normal")
+    gs = x.g[..., 0].contiguous()
+    x_full = inputs.prefill_inputs(lens, H=H, io=io, seed=seed, init="normal")
+    x_full.g = gs[..., None].expand(*gs.shape, 128).contiguous()
+    return x, gs, x_full
+
+
+@pytest.mark.parametrize("mode", ["split", "fused"])
+def test_bf16_prefill_scalar_decay(monkeypatch, mode):
+    """g of shape [T_total, H] (one decay per token and head) equals the
+    channel-wise path with that decay on every channel."""
+    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", mode)
+    x, gs, x_full = scalar_decay_inputs([300, 1, 129], 2, "bf16", 71)
+    cu = x.cu_seqlens.to(DEV)
+    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), gs.to(DEV),
+                               x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
+                               cu_seqlens=cu, chunk=64)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(x_full)
+    assert out_err(out, ro) <= TOL_BF16 and rel_err(fin.cpu().numpy(), rf) <= TOL_BF16
+
+
+def test_f32_prefill_scalar_decay():
+    x, gs, x_full = scalar_decay_inputs([100, 37], 2, "f32", 72)
+    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), gs.to(DEV),
+                               x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
+                               cu_seqlens=x.cu_seqlens.to(DEV), chunk=16)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(x_full)
+    assert out_err(out, ro) <= TOL_F32 and rel_err(fin.cpu().numpy(), rf) <= TOL_F32
+
+
+@pytest.mark.parametrize("io,chunk,tol,mode", [("bf16", 64, TOL_BF16, "split"),
+                                                ("bf16", 64, TOL_BF16, "fused"),
+                                                ("f32", 16, TOL_F32, None)])
+def test_prefill_snapshots(monkeypatch, io, chunk, tol, mode):
+    """The state after every 64 tokens of each sequence equals the oracle's
+    final state of that prefix; slots past a sequence's end stay untouched."""
+    if mode:
+        monkeypatch.setenv("KDA_PREFILL_SCHEDULE", mode)
+    lens, H, S, every = [300, 200], 2, 4, 64
+    x = inputs.prefill_inputs(lens, H=H, io=io, seed=73, init="normal")
+    snaps = torch.full((len(lens), S, H, 128, 128), 7.0, dtype=torch.float32, device=DEV)
+    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
+                               x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
+                               cu_seqlens=x.cu_seqlens.to(DEV), chunk=chunk,
+                               snapshot_interval=every, snapshots=snaps)
+    torch.cuda.synchronize()
+    ro, rf = oracle_prefill(x)
+    assert out_err(out, ro) <= tol and rel_err(fin.cpu().numpy(), rf) <= tol
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    for n, L in enumerate(lens):
+        for si in range(S):
+            got = snaps[n, si].cpu().numpy()
+            P = (si + 1) * every
+            if P > L:
+                assert np.all(got == 7.0), (n, si)
+                continue
+            sl = lambda t: np32(t[cu[n]:cu[n] + P])
+            _, rs = oracle.prefill(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), x.scale,
+                                   init_state=x.init_state[n:n + 1].double().numpy())
+            assert rel_err(got, rs[0]) <= tol, (n, si)
+
+
 # ------------------------------------------------ multi-token / pooled decode
 def multi_decode_case(B, T, H, io, seed, scalar_g=False, P=None, idx=None):
     """Inputs [B, T, H, ...] of B sequences of T tokens, a state pool of P
