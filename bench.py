@@ -366,6 +366,48 @@ def main():
     e2e_val = units / (e2e_ms * 1e-3) / 1e6
     del dq, dk, dv, dg, db, hq, hk, hv, hg, hb, hout
 
+    # ---- layer prologue / epilogue on the same rows (HBM streams) ----------
+    layer = None
+    if not args.no_decode:
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(PREFILL["seed"] + 11)
+        raw = [torch.randn((T, H, D), generator=gen, device=dev).to(torch.bfloat16)
+               for _ in range(5)]
+        braw = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
+        convs = [0.5 * torch.randn((H, D, 4), generator=gen, device=dev) for _ in range(3)]
+        nw = torch.ones(D, device=dev)
+        for _ in range(3):
+            lq, lk, lv, lg, lb = kda.kda_layer_prologue(*raw[:4], braw, *convs, stream=stream)
+            ly = kda.kda_layer_epilogue(raw[0], raw[4], nw, stream=stream)
+        torch.cuda.synchronize()
+        reps_l = 50
+        ev0.record(stream)
+        for _ in range(reps_l):
+            kda.kda_layer_prologue(*raw[:4], braw, *convs, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        pro_ms = ev0.elapsed_time(ev1) / reps_l
+        ev0.record(stream)
+        for _ in range(reps_l):
+            kda.kda_layer_epilogue(raw[0], raw[4], nw, y=ly, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        epi_ms = ev0.elapsed_time(ev1) / reps_l
+        rows = T * H
+        pro_bytes = rows * (4 * 2 * D + 2 + 3 * 2 * D + 4 * D + 2)  # bf16 rows in, q k v g beta out
+        epi_bytes = rows * 3 * 2 * D
+        layer = {
+            "workload": "rows of the prefill workload (T=8192, H=32, D=128), bf16, conv width 4",
+            "prologue": {"ms": pro_ms, "GB/s": pro_bytes / (pro_ms * 1e-3) / 1e9,
+                         "frac_hbm": pro_bytes / (pro_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         "bytes_per_launch": pro_bytes, "kernel": "layer_prologue_kernel"},
+            "epilogue": {"ms": epi_ms, "GB/s": epi_bytes / (epi_ms * 1e-3) / 1e9,
+                         "frac_hbm": epi_bytes / (epi_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                         "bytes_per_launch": epi_bytes, "kernel": "layer_epilogue_kernel"},
+            "gpu_launches": 2 * reps_l,
+        }
+        del raw, braw, convs, lq, lk, lv, lg, lb, ly
+
     # ---- decode: 64 steps replayed from a CUDA graph -----------------------
     decode = None
     if not args.no_decode:
@@ -493,6 +535,7 @@ def main():
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "decode": decode,
+        "layer": layer,
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -196,6 +196,39 @@ int kda_decode(const void *q, const void *k, const void *v, const float *g, cons
                const int32_t *state_indices, void *out, void *stream);
 
 /*
+ * The layer steps on either side of the operator ("Kimi K3: The Manos, The
+ * Mythos, The Legendos", section "Kimi Linear"); the projections themselves are
+ * plain matrix products done by the caller. Rows are [T_total, H, D], D = 128.
+ *
+ * kda_layer_prologue: from the projected q_raw, k_raw, v_raw, alpha_raw (io
+ * dtype [T_total, H, D]) and beta_raw (io dtype [T_total, H]):
+ *   q = l2(conv(q_raw)), k = l2(conv(k_raw)), v = conv(v_raw),
+ *   g = -5 sigmoid(alpha_raw) (fp32 [T_total, H, D]), beta = sigmoid(beta_raw),
+ * where conv is a depthwise causal convolution of width W (1..4) along each
+ * sequence, left-padded with zeros (weights conv_* fp32 [H, D, W]; tap W - 1
+ * multiplies the current token), with no activation, and l2(x) = x /
+ * sqrt(sum x^2 + 1e-6) over the D channels of a (token, head). cu_seqlens:
+ * DEVICE int32 [N + 1] offsets of packed sequences (NULL: one sequence);
+ * convolutions never cross a sequence start. Outputs may not alias inputs.
+ * Pointer alignment: 8 bytes (bf16) or 16 bytes (fp32) for the [.., D] rows,
+ * 16 bytes for g.
+ *
+ * kda_layer_epilogue: y = o / sqrt(mean(o^2) + 1e-6) * w * sigmoid(gate_raw)
+ * per (token, head) over its D channels: o, gate_raw, y io dtype
+ * [T_total, H, D]; norm_weight fp32 [D] (16-byte aligned).
+ *
+ * Both return KDA_ERR_UNSUPPORTED for D != 128, W outside 1..4 or an unknown
+ * io; T_total = 0 is a no-op.
+ */
+int kda_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
+                       const void *alpha_raw, const void *beta_raw, const float *conv_q,
+                       const float *conv_k, const float *conv_v, int32_t W,
+                       const int32_t *cu_seqlens, int32_t N, int32_t T_total, int32_t H, int32_t D,
+                       int32_t io, void *q, void *k, void *v, float *g, void *beta, void *stream);
+int kda_layer_epilogue(const void *o, const void *gate_raw, const float *norm_weight,
+                       int32_t T_total, int32_t H, int32_t D, int32_t io, void *y, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of a
  * kda_prefill workspace. Returns KDA_OK, KDA_ERR_DEVICE (malformed
  * cu_seqlens were seen), KDA_ERR_TIMEOUT or KDA_ERR_CUDA.

@@ -32,7 +32,8 @@ KDA_SCHEDULE_DIRECT = 2
 
 EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size", "kda_prefill",
             "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
-            "kda_prefill_schedule", "kda_decode", "kda_prefill_ex")
+            "kda_prefill_schedule", "kda_decode", "kda_prefill_ex", "kda_layer_prologue",
+            "kda_layer_epilogue")
 
 _lock = threading.Lock()
 _lib = None
@@ -77,6 +78,10 @@ def load() -> ctypes.CDLL:
         lib.kda_prefill_ex.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32, I32,
                                        I32, I32, P, P, P, P, SZ, P]
         lib.kda_prefill_ex.restype = ctypes.c_int
+        lib.kda_layer_prologue.argtypes = [P] * 8 + [I32, P, I32, I32, I32, I32, I32] + [P] * 6
+        lib.kda_layer_prologue.restype = ctypes.c_int
+        lib.kda_layer_epilogue.argtypes = [P, P, P, I32, I32, I32, I32, P, P]
+        lib.kda_layer_epilogue.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -229,6 +234,46 @@ def kda_decode(q, k, v, g, beta, scale, state_pool, state_indices=None, out=None
     if rc != KDA_OK:
         raise KDAError(rc, "kda_decode")
     return out
+
+
+def kda_layer_prologue(q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q, conv_k, conv_v,
+                       cu_seqlens=None, stream=None):
+    """The layer steps before the operator (C entry point ``kda_layer_prologue``):
+    rows [T_total, H, D] of projected q, k, v, alpha and beta [T_total, H];
+    depthwise causal convolutions conv_* fp32 [H, D, W]. Returns
+    (q, k, v, g, beta) ready for ``kda_prefill``."""
+    lib = load()
+    io = _io_code(q_raw.dtype)
+    T_total, H, D = q_raw.shape
+    W = conv_q.shape[2]
+    N = 0 if cu_seqlens is None else cu_seqlens.numel() - 1
+    _check_cuda(q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q, conv_k, conv_v, cu_seqlens)
+    q, k, v = (torch.empty_like(q_raw) for _ in range(3))
+    g = torch.empty((T_total, H, D), dtype=torch.float32, device=q_raw.device)
+    beta = torch.empty_like(beta_raw)
+    rc = lib.kda_layer_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(alpha_raw),
+                                _ptr(beta_raw), _ptr(conv_q), _ptr(conv_k), _ptr(conv_v), W,
+                                _ptr(cu_seqlens), N, T_total, H, D, io, _ptr(q), _ptr(k), _ptr(v),
+                                _ptr(g), _ptr(beta), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_layer_prologue")
+    return q, k, v, g, beta
+
+
+def kda_layer_epilogue(o, gate_raw, norm_weight, y=None, stream=None):
+    """Per-head RMS norm of the operator output times sigmoid(gate_raw)
+    (C entry point ``kda_layer_epilogue``). Returns y [T_total, H, D]."""
+    lib = load()
+    io = _io_code(o.dtype)
+    T_total, H, D = o.shape
+    _check_cuda(o, gate_raw, norm_weight, y)
+    if y is None:
+        y = torch.empty_like(o)
+    rc = lib.kda_layer_epilogue(_ptr(o), _ptr(gate_raw), _ptr(norm_weight), T_total, H, D, io,
+                                _ptr(y), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_layer_epilogue")
+    return y
 
 
 def kda_workspace_status(workspace, stream=None) -> int:

@@ -26,6 +26,15 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
                               void *out, float *fin, unsigned char *ws, cudaStream_t stream);
 int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen);
+template <typename IO>
+cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
+                                  const void *alpha_raw, const void *beta_raw, const float *wq,
+                                  const float *wk, const float *wv, int W, const int32_t *cu,
+                                  int N, long long T_total, int H, void *q, void *k, void *v,
+                                  float *g, void *beta, cudaStream_t stream);
+template <typename IO>
+cudaError_t launch_layer_epilogue(const void *o, const void *gate_raw, const float *w,
+                                  long long T_total, int H, void *y, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -191,6 +200,56 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
                     float *state_inout, void *out, void *stream) {
     return kda_decode(q, k, v, g, beta, scale, B, 1, H, D, io, 1, state_inout, B, nullptr, out,
                       stream);
+}
+
+int kda_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
+                       const void *alpha_raw, const void *beta_raw, const float *conv_q,
+                       const float *conv_k, const float *conv_v, int32_t W,
+                       const int32_t *cu_seqlens, int32_t N, int32_t T_total, int32_t H, int32_t D,
+                       int32_t io, void *q, void *k, void *v, float *g, void *beta, void *stream) {
+    if (N < 0 || T_total < 0 || H <= 0 || D <= 0) return KDA_ERR_INVALID_ARG;
+    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (D != kda::kD || W < 1 || W > 4) return KDA_ERR_UNSUPPORTED;
+    if ((long long)T_total * H > (1LL << 33)) return KDA_ERR_INVALID_ARG;
+    if (T_total == 0) return KDA_OK;
+    if (!q_raw || !k_raw || !v_raw || !alpha_raw || !beta_raw || !conv_q || !conv_k || !conv_v ||
+        !q || !k || !v || !g || !beta)
+        return KDA_ERR_INVALID_ARG;
+    const unsigned a = io == KDA_F32 ? 15u : 7u;  // row pieces of 4 channels
+    for (const void *p : {q_raw, k_raw, v_raw, alpha_raw, static_cast<const void *>(q),
+                          static_cast<const void *>(k), static_cast<const void *>(v)})
+        if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(g)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        io == KDA_F32
+            ? kda::launch_layer_prologue<float>(q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q,
+                                                conv_k, conv_v, W, cu_seqlens, N, T_total, H, q,
+                                                k, v, g, beta, st)
+            : kda::launch_layer_prologue<__nv_bfloat16>(q_raw, k_raw, v_raw, alpha_raw, beta_raw,
+                                                        conv_q, conv_k, conv_v, W, cu_seqlens, N,
+                                                        T_total, H, q, k, v, g, beta, st);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_layer_epilogue(const void *o, const void *gate_raw, const float *norm_weight,
+                       int32_t T_total, int32_t H, int32_t D, int32_t io, void *y, void *stream) {
+    if (T_total < 0 || H <= 0 || D <= 0) return KDA_ERR_INVALID_ARG;
+    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (D != kda::kD) return KDA_ERR_UNSUPPORTED;
+    if ((long long)T_total * H > (1LL << 33)) return KDA_ERR_INVALID_ARG;
+    if (T_total == 0) return KDA_OK;
+    if (!o || !gate_raw || !norm_weight || !y) return KDA_ERR_INVALID_ARG;
+    const unsigned a = io == KDA_F32 ? 15u : 7u;
+    for (const void *p : {o, gate_raw, static_cast<const void *>(y)})
+        if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(norm_weight)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        io == KDA_F32 ? kda::launch_layer_epilogue<float>(o, gate_raw, norm_weight, T_total, H, y, st)
+                      : kda::launch_layer_epilogue<__nv_bfloat16>(o, gate_raw, norm_weight, T_total,
+                                                                  H, y, st);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 int kda_workspace_status(void *workspace, void *stream) {

@@ -17,6 +17,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import layer as oracle_layer
 import kimi_delta_attention_rule_gb300 as kda
 from kimi_delta_attention_rule_gb300 import inputs
 
@@ -282,6 +283,42 @@ def test_prefill_snapshots(monkeypatch, io, chunk, tol, mode):
             _, rs = oracle.prefill(sl(x.q), sl(x.k), sl(x.v), sl(x.g), sl(x.beta), x.scale,
                                    init_state=x.init_state[n:n + 1].double().numpy())
             assert rel_err(got, rs[0]) <= tol, (n, si)
+
+
+# ------------------------------------------------ layer prologue / epilogue
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_layer_prologue(io, tol, W):
+    """Short causal convolutions (per packed sequence, incl. an empty one and
+    ones shorter than W), L2 norms and gates against the oracle."""
+    lens, H = [5, 0, 70, 2], 3
+    T = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    gen = torch.Generator().manual_seed(81 + W)
+    dt = torch.bfloat16 if io == "bf16" else torch.float32
+    raw = [torch.randn(T, H, 128, generator=gen).to(dt) for _ in range(4)]
+    braw = torch.randn(T, H, generator=gen).to(dt)
+    ws = [0.5 * torch.randn(H, 128, W, generator=gen) for _ in range(3)]
+    dev = lambda t: t.to(DEV)
+    q, k, v, g, beta = kda.kda_layer_prologue(*map(dev, raw), dev(braw), *map(dev, ws),
+                                              cu_seqlens=torch.from_numpy(cu).to(DEV))
+    torch.cuda.synchronize()
+    rq, rk, rv, rg, rb = oracle_layer.prologue(*map(np32, raw), np32(braw), *map(np32, ws), cu)
+    for got, ref in ((q, rq), (k, rk), (v, rv), (beta, rb)):
+        assert out_err(got, ref) <= tol
+    assert rel_err(g.cpu().numpy(), rg) <= 1e-5
+
+
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+def test_layer_epilogue(io, tol):
+    gen = torch.Generator().manual_seed(91)
+    dt = torch.bfloat16 if io == "bf16" else torch.float32
+    o = (3 * torch.randn(37, 4, 128, generator=gen)).to(dt)
+    gr = torch.randn(37, 4, 128, generator=gen).to(dt)
+    w = 1 + 0.1 * torch.randn(128, generator=gen)
+    y = kda.kda_layer_epilogue(o.to(DEV), gr.to(DEV), w.to(DEV))
+    torch.cuda.synchronize()
+    assert out_err(y, oracle_layer.epilogue(np32(o), np32(gr), np32(w))) <= tol
 
 
 # ------------------------------------------------ multi-token / pooled decode
