@@ -227,7 +227,19 @@ def ncu_case(args):
     kbuild.build()
     kda.load()
     dev = torch.device("cuda", 0)
-    if args.ncu_case == "prefill":
+    if args.ncu_case == "layer":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(PREFILL["seed"] + 11)
+        T, H = PREFILL["T"], PREFILL["H"]
+        raw = [torch.randn((T, H, D), generator=gen, device=dev).to(torch.bfloat16)
+               for _ in range(5)]
+        braw = torch.randn((T, H), generator=gen, device=dev).to(torch.bfloat16)
+        convs = [0.5 * torch.randn((H, D, 4), generator=gen, device=dev) for _ in range(3)]
+        nw = torch.ones(D, device=dev)
+        for _ in range(args.warmup + 1):
+            kda.kda_layer_prologue(*raw[:4], braw, *convs)
+            kda.kda_layer_epilogue(raw[0], raw[4], nw)
+    elif args.ncu_case == "prefill":
         x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"],
                                   device=dev)
         for _ in range(args.warmup + 1):
@@ -248,7 +260,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "layer"], default=None,
                     help="run only `warmup` + 1 launches of one kernel (for ncu captures)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"])
     args = ap.parse_args()

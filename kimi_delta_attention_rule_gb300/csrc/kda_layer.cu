@@ -57,29 +57,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One warp per (token, head) row, rows in memory order (lane = 4 channels):
-// the W - 1 earlier rows the convolutions read were loaded by other warps a
-// moment before and come from L2; a lane's 4 channels x W taps of weights are
-// contiguous in [H, D, W] and load as W float4.
-template <typename IO, int W>
-__device__ __forceinline__ void conv_row(const IO *__restrict__ x, const float *__restrict__ w,
-                                         int t, int t_lo, int H, int h, int c0, float *acc) {
-    float wl[4 * W];  // [channel][tap]
-#pragma unroll
-    for (int i = 0; i < W; ++i)
-        *reinterpret_cast<float4 *>(&wl[4 * i]) =
-            *reinterpret_cast<const float4 *>(w + ((size_t)h * kD + c0) * W + 4 * i);
-    acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-#pragma unroll
-    for (int i = 0; i < W; ++i) {  // i steps back: tap W - 1 - i
-        if (t - i < t_lo) break;
-        float xv[4];
-        load4<IO>(x + ((size_t)(t - i) * H + h) * kD + c0, xv);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[e] += wl[e * W + (W - 1 - i)] * xv[e];
-    }
-}
-
+// One warp per (token, head) row, rows in memory order (lane = 4 channels).
+// All loads of a row are issued before any arithmetic (the W taps of q, k and
+// v, alpha, beta): the W - 1 earlier rows were loaded by other warps a moment
+// before and mostly come from L2, and independent loads keep the row's
+// latency to about one memory round trip. A lane's 4 channels x W taps of
+// weights are contiguous in [H, D, W] and load as W float4.
 template <typename IO, int W>
 __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
     layer_prologue_kernel(const IO *__restrict__ q_raw, const IO *__restrict__ k_raw,
@@ -103,25 +86,51 @@ __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
         }
         t_lo = max(0, min(cu[lo], t));
     }
+    const IO *raw3[3] = {q_raw, k_raw, v_raw};
+    const float *w3[3] = {wq, wk, wv};
+    float x[3][W][4];  // [tensor][steps back][channel]
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int i = 0; i < W; ++i) {
+            if (t - i >= t_lo) {
+                load4<IO>(raw3[m] + ((size_t)(t - i) * H + h) * kD + c0, x[m][i]);
+            } else {
+                x[m][i][0] = x[m][i][1] = x[m][i][2] = x[m][i][3] = 0.f;
+            }
+        }
     const size_t o = (size_t)r * kD + c0;
-    float a[4];
-    conv_row<IO, W>(q_raw, wq, t, t_lo, H, h, c0, a);
-    float s = rsqrtf(warp_sum(a[0] * a[0] + a[1] * a[1] + a[2] * a[2] + a[3] * a[3]) + kL2Eps);
+    float al[4];
+    load4<IO>(alpha_raw + o, al);
+    const float braw = lane == 0 ? to_f32(beta_raw[r]) : 0.f;
+    IO *out3[3] = {q, k, v};
 #pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] *= s;
-    store4<IO>(q + o, a);
-    conv_row<IO, W>(k_raw, wk, t, t_lo, H, h, c0, a);
-    s = rsqrtf(warp_sum(a[0] * a[0] + a[1] * a[1] + a[2] * a[2] + a[3] * a[3]) + kL2Eps);
+    for (int m = 0; m < 3; ++m) {
+        float wl[4 * W];  // [channel][tap]
 #pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] *= s;
-    store4<IO>(k + o, a);
-    conv_row<IO, W>(v_raw, wv, t, t_lo, H, h, c0, a);
-    store4<IO>(v + o, a);
-    load4<IO>(alpha_raw + o, a);
+        for (int i = 0; i < W; ++i)
+            *reinterpret_cast<float4 *>(&wl[4 * i]) =
+                *reinterpret_cast<const float4 *>(w3[m] + ((size_t)h * kD + c0) * W + 4 * i);
+        float acc[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc[e] = 0.f;
+#pragma unroll
+            for (int i = 0; i < W; ++i) acc[e] += wl[e * W + (W - 1 - i)] * x[m][i][e];
+        }
+        if (m < 2) {  // q, k: L2 norm over the row
+            const float sc = rsqrtf(
+                warp_sum(acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3]) +
+                kL2Eps);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] *= sc;
+        }
+        store4<IO>(out3[m] + o, acc);
+    }
     *reinterpret_cast<float4 *>(g + o) =
-        make_float4(-5.f * sigmoidf_(a[0]), -5.f * sigmoidf_(a[1]), -5.f * sigmoidf_(a[2]),
-                    -5.f * sigmoidf_(a[3]));
-    if (lane == 0) beta[r] = from_f32<IO>(sigmoidf_(to_f32(beta_raw[r])));
+        make_float4(-5.f * sigmoidf_(al[0]), -5.f * sigmoidf_(al[1]), -5.f * sigmoidf_(al[2]),
+                    -5.f * sigmoidf_(al[3]));
+    if (lane == 0) beta[r] = from_f32<IO>(sigmoidf_(braw));
 }
 
 template <typename IO>
