@@ -381,6 +381,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const int N = pa.N, T = pa.T, H = pa.H;
     unsigned char *__restrict__ blocks = pa.blocks;
     const bool chunk_major = ready != nullptr;
+    const int nslots = pa.nitems / H;  // ready flags are [head][slot]
     int nitems = pa.nitems;
     if (chunk_major) {
         const int maxc = cu ? first_chunk[N + 1] : (T + C - 1) / C;
@@ -931,10 +932,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             if (tid == 0) {
                 tc::bulk_wait_all();
                 asm volatile("fence.proxy.async.global;\n" ::: "memory");
-                release((long long)slot * H + h);
+                release((long long)h * nslots + slot);
             }
         } else {
-            pending = (long long)slot * H + h;
+            pending = (long long)h * nslots + slot;
         }
     }
     ++it;
@@ -993,14 +994,20 @@ struct RecArgs {
     float *fin;
     float *snaps;  // [N][snap_max][H][128][128], or null
     int snap_interval, snap_max;
+    int nslots;  // chunk slots: the ready flags are [head][slot]
     uint32_t *status;
 };
 
-__device__ __forceinline__ bool flag_set(const int *f) {
-    uint32_t x;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(x) : "l"(f) : "memory");
-    return x != 0;
+// Four consecutive ready flags (16-byte aligned group), with acquire semantics.
+__device__ __forceinline__ uint4 flags4_acquire(const int *f) {
+    uint4 x;
+    asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];\n"
+                 : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                 : "l"(f)
+                 : "memory");
+    return x;
 }
+
 
 // K2 for one chain (sequence n, head h). With `ready`, the block of chunk slot
 // s is loaded only after ready[s H + h] is set by its producer.
@@ -1062,39 +1069,56 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     };
     // Block loads, issued in chunk order by one lane of warp 1 (thread 0 issues the
     // MMAs). Chunk x may be loaded once chunk x - 2 has left its buffer and (with
-    // `ready`) once its flag is set. The flag of the next chunk is checked where the
-    // CTA waits for the tensor core anyway; only a chunk that is still missing when
-    // it is needed is waited for.
+    // `ready`) once its flag is set. A chain's flags are consecutive, so one
+    // 16-byte acquire read learns up to four chunks, and one proxy fence covers
+    // every block load they allow. Reads happen where the CTA waits for the tensor
+    // core anyway; only a chunk still missing when it is needed is waited for.
     int next_load = 0;
+    int known_set = -1;  // chunks [0, known_set] are known to exist (acquired)
+    int fenced = -1;     // chunks [0, fenced] are covered by a proxy fence
     auto issue_one = [&]() {
         const int c = next_load++;
         tc::mbar_arrive_expect_tx(bL(c), kBlock);
         tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
     };
-    auto flag_ptr = [&](int x) { return ready + (size_t)(fc + x) * H + h; };
-    auto check_issue = [&](int x) {  // issue chunk x if it is the next one and exists
+    auto refresh = [&]() {  // one read of the aligned group holding the next unknown flag
+        const int x = known_set + 1;
+        if (x >= nchunks) return;
+        const size_t a = (size_t)h * ra.nslots + fc + x, base = a & ~(size_t)3;
+        const uint4 v = flags4_acquire(ready + base);
+        const uint32_t fl[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int y = x + i - (int)(a - base);  // chunk of flag i (this chain's if y >= x)
+            if (y < x) continue;
+            if (y >= nchunks || fl[i] == 0) break;
+            known_set = y;
+        }
+    };
+    auto check_issue = [&](int x) {  // issue chunk x if it is the next one and known to exist
         if (failed || next_load != x || x >= nchunks) return;
         if (ready) {
-            if (!flag_set(flag_ptr(x))) return;
-            asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            if (known_set < x) return;
+            if (fenced < x) {
+                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+                fenced = known_set;
+            }
         }
         issue_one();
     };
     auto block_issue = [&](int x) {  // chunks [next_load, x], waiting (bounded) for flags
         x = min(x, nchunks - 1);
         while (!failed && next_load <= x) {
-            if (ready) {
-                const int *f = flag_ptr(next_load);
+            if (ready && known_set < next_load) {
                 const uint64_t start = tc::globaltimer_ns();
-                while (!flag_set(f)) {
-                    if (tc::globaltimer_ns() - start > kWaitLimit) {
+                while (!failed && known_set < next_load) {
+                    refresh();
+                    if (known_set < next_load && tc::globaltimer_ns() - start > kWaitLimit)
                         failed = true;
-                        return;
-                    }
                 }
-                asm volatile("fence.proxy.async.global;\n" ::: "memory");
+                if (failed) return;
             }
-            issue_one();
+            check_issue(next_load);
         }
     };
     constexpr int kLoader = 32;
@@ -1125,6 +1149,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     } else {
         if (tid == kLoader) {
             block_issue(0);
+            if (ready && known_set < 1) refresh();
             check_issue(1);
         }
         // initial state, keys [32 qd, 32 qd + 32) of column j: fp16 copy -> S^T,
@@ -1161,7 +1186,10 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             const int tcc = t0 + c * C, L = min(C, t1 - tcc);
 
             // U^T = U~^T - P^T for t in [16 qd, 16 qd + 16) -> shared (fp16)
-            if (tid == kLoader) check_issue(c + 1);  // while the first product runs
+            if (tid == kLoader) {  // while the first product runs
+                if (ready && known_set < c + 1) refresh();
+                check_issue(c + 1);
+            }
             wait(bL(c), (uint32_t)((c >> 1) & 1));
             wait(bM1, (uint32_t)(c & 1));
             tc::fence_after_sync();
@@ -1187,7 +1215,10 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             tc::fence_async_smem();
             sync_check();
             if (tid == 0 && !failed) issue_mma2(c);
-            if (tid == kLoader) check_issue(c + 1);  // while the second product runs
+            if (tid == kLoader) {  // while the second product runs
+                if (ready && known_set < c + 2) refresh();
+                check_issue(c + 1);
+            }
 
             // new state (keys [32 qd, +32)) and this chunk's O (t in [16 qd, +16))
             wait(bM2, (uint32_t)(c & 1));
@@ -1229,7 +1260,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             sync_check();
             if (tid == 0 && c + 1 < nchunks && !failed) issue_mma1(c + 1);
             // this chunk's buffer is free: without flags, fetch chunk c + 2 into it now
-            if (tid == kLoader && !ready) check_issue(c + 2);
+            if (tid == kLoader) check_issue(c + 2);  // known to exist (or no flags)
 
 
             // while the next product runs: pre-scale the state by the next chunk's
@@ -1427,7 +1458,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
                    static_cast<__nv_bfloat16 *>(out), fin,
                    snap_interval > 0 ? snaps : nullptr, snap_interval > 0 ? snap_interval : 1,
-                   snap_max, status};
+                   snap_max, (int)slots, status};
     if (fused) {
         e = cudaMemsetAsync(ready, 0, (size_t)nitems * 4, stream);
         if (e != cudaSuccess) return e;
