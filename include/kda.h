@@ -165,7 +165,10 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
  *   KDA_SCHEDULE_DIRECT fp32 I/O: one kernel on CUDA cores.
  * With cu_seqlens a schedule kernel runs first. The environment variable
  * KDA_PREFILL_SCHEDULE=split|fused overrides the bf16 choice ("fused" needs
- * fewer chains than SMs). Returns the schedule, or the negated kda_status on
+ * fewer chains than SMs). Test hook (failure detection, never for production):
+ * with KDA_TEST_FLAG_TIMEOUT_MS=<ms> a fused launch runs its chains without any
+ * producer and with that bound on each wait, so every chain gives up after
+ * <ms> and kda_workspace_status() reports KDA_ERR_TIMEOUT; outputs are garbage. Returns the schedule, or the negated kda_status on
  * invalid sizes or a failed device query. The result does not depend on the
  * schedule: both bf16 schedules run the same arithmetic.
  */

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>  // header-only: ranges are free unless a profiler is attached
+
 #include "kda.h"
 #include "kda_common.cuh"
 
@@ -50,6 +52,12 @@ size_t workspace_bytes_for(int32_t N, int32_t T, int32_t H, int32_t io, bool var
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// An NVTX range around the launches of one call (seen by nsys / ncu --nvtx).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+};
 
 // Validates the prefill sizes; writes T_total on success.
 int check_prefill_dims(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
@@ -142,6 +150,7 @@ int kda_prefill_ex(const void *q, const void *k, const void *v, const float *g,
     if ((init_state && !aligned16(init_state)) || (final_state && !aligned16(final_state)))
         return KDA_ERR_INVALID_ARG;
     const int si = snapshot_interval, sm = snapshot_interval > 0 ? max_snapshots : 0;
+    NvtxRange range(io == KDA_F32 ? "kda_prefill (fp32)" : "kda_prefill");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t *status = static_cast<uint32_t *>(workspace);
     // the status word reports this call only
@@ -185,6 +194,7 @@ int kda_decode(const void *q, const void *k, const void *v, const float *g, cons
     if (B == 0 || T == 0) return KDA_OK;
     if (!q || !k || !v || !g || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
     if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    NvtxRange range("kda_decode");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e =
         io == KDA_F32
@@ -220,6 +230,7 @@ int kda_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
                           static_cast<const void *>(k), static_cast<const void *>(v)})
         if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
     if (!aligned16(g)) return KDA_ERR_INVALID_ARG;
+    NvtxRange range("kda_layer_prologue");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e =
         io == KDA_F32
@@ -244,6 +255,7 @@ int kda_layer_epilogue(const void *o, const void *gate_raw, const float *norm_we
     for (const void *p : {o, gate_raw, static_cast<const void *>(y)})
         if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
     if (!aligned16(norm_weight)) return KDA_ERR_INVALID_ARG;
+    NvtxRange range("kda_layer_epilogue");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e =
         io == KDA_F32 ? kda::launch_layer_epilogue<float>(o, gate_raw, norm_weight, T_total, H, y, st)

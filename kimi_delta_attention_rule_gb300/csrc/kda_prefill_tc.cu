@@ -982,7 +982,7 @@ static_assert(kRecThreads == kPrepThreads, "the fused kernel runs both roles");
 // TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T.
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColP = 0, kColO = 64, kColS = 128;
-constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s bound on any wait
+constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s: the default bound on any wait of a chain
 
 struct RecArgs {
     const int32_t *cu, *first_chunk;
@@ -996,6 +996,7 @@ struct RecArgs {
     int snap_interval, snap_max;
     int nslots;  // chunk slots: the ready flags are [head][slot]
     uint32_t *status;
+    unsigned long long wait_ns;  // bound on every wait of a chain (ns)
 };
 
 // Four consecutive ready flags (16-byte aligned group), with acquire semantics.
@@ -1060,7 +1061,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     // no-op, so all threads still pass the same barriers and the kernel ends.
     bool failed = false;
     auto wait = [&](uint32_t bar, uint32_t parity) {
-        if (!failed && !tc::mbar_wait(bar, parity, kWaitLimit)) failed = true;
+        if (!failed && !tc::mbar_wait(bar, parity, ra.wait_ns)) failed = true;
     };
     auto sync_check = [&]() {  // CTA barrier that also agrees on the failure state
         tc::fence_before_sync();
@@ -1113,7 +1114,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 const uint64_t start = tc::globaltimer_ns();
                 while (!failed && known_set < next_load) {
                     refresh();
-                    if (known_set < next_load && tc::globaltimer_ns() - start > kWaitLimit)
+                    if (known_set < next_load && tc::globaltimer_ns() - start > ra.wait_ns)
                         failed = true;
                 }
                 if (failed) return;
@@ -1458,13 +1459,20 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
                    static_cast<__nv_bfloat16 *>(out), fin,
                    snap_interval > 0 ? snaps : nullptr, snap_interval > 0 ? snap_interval : 1,
-                   snap_max, (int)slots, status};
+                   snap_max, (int)slots, status, pf::kWaitLimit};
     if (fused) {
         e = cudaMemsetAsync(ready, 0, (size_t)nitems * 4, stream);
         if (e != cudaSuccess) return e;
         int nch = (int)nchains;
+        unsigned grid = (unsigned)nsm;
+        // Failure-detection test hook: the chains run with no producer at all and
+        // a short wait bound, so that every wait for a ready flag runs out.
+        if (const char *tt = getenv("KDA_TEST_FLAG_TIMEOUT_MS")) {
+            grid = (unsigned)nch;
+            ra.wait_ns = (unsigned long long)strtoul(tt, nullptr, 10) * 1000000ull;
+        }
         void *args[] = {&pa, &ra, &nch, &ready};
-        return cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(nsm),
+        return cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(grid),
                                            dim3(pf::kRecThreads), args, pf::kFusedSmem, stream);
     }
     if (nitems > 0) {

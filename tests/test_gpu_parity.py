@@ -542,6 +542,24 @@ def test_bf16_non_monotone_offsets_skip_the_call():
     assert torch.all(out == 7.0) and torch.all(fin == 7.0)
 
 
+def test_fused_chain_waits_are_bounded(monkeypatch):
+    """A chain whose producer never comes gives up after its wait bound and
+    reports KDA_ERR_TIMEOUT through the status word; the context stays usable
+    and the next call is correct. (Test hook: chains launched without
+    producers, 50 ms bound; nothing faults or hangs.)"""
+    x = inputs.prefill_inputs([200, 64], H=2, io="bf16", seed=101, init="normal")
+    q = x.q.to(DEV)
+    cu = x.cu_seqlens.to(DEV)
+    ws = kda.prefill_workspace(q, cu, chunk=64)
+    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", "fused")
+    monkeypatch.setenv("KDA_TEST_FLAG_TIMEOUT_MS", "50")
+    kda.kda_prefill(q, x.k.to(DEV), x.v.to(DEV), x.g.to(DEV), x.beta.to(DEV), x.scale,
+                    init_state=x.init_state.to(DEV), cu_seqlens=cu, chunk=64, workspace=ws)
+    assert kda.kda_workspace_status(ws) == kda.KDA_ERR_TIMEOUT
+    monkeypatch.delenv("KDA_TEST_FLAG_TIMEOUT_MS")
+    check_prefill(x, 64, TOL_BF16)
+
+
 def test_prefill_schedule_choice(monkeypatch):
     """Few chains (N H <= SMs / 3): fused; many chains: split; the
     environment variable overrides."""
