@@ -318,41 +318,6 @@ __device__ __forceinline__ void lds8(const float *s, float *x) {
     *reinterpret_cast<float4 *>(x + 4) = *reinterpret_cast<const float4 *>(s + 4);
 }
 
-// Item = (chunk slot, head); false if the item has no tokens (past the end of
-// the packed sequences, or malformed offsets, which K2 flags).
-__device__ __forceinline__ bool item_tokens(int item, int H, const int32_t *cu,
-                                            const int32_t *first_chunk, int N, int T, int &slot,
-                                            int &h, int &tc, int &L) {
-    slot = item / H;
-    h = item - slot * H;
-    int n, c;
-    if (!slot_to_chunk(slot, cu, first_chunk, N, T, n, c)) return false;
-    const int t0 = cu ? cu[n] : n * T;
-    const int t1 = cu ? cu[n + 1] : t0 + T;
-    tc = t0 + c * C;
-    if (t1 < t0 || tc >= t1) return false;
-    L = min(C, t1 - tc);
-    return true;
-}
-
-// Item = (chunk c, sequence n, head h) in chunk-major order, idx = (c N + n) H + h,
-// so that a whole wave of items finishes the early chunks of every chain first.
-// Needs offsets that passed the schedule check.
-__device__ __forceinline__ bool item_tokens_cm(int idx, int H, const int32_t *cu,
-                                               const int32_t *first_chunk, int N, int T,
-                                               int &slot, int &h, int &tc, int &L) {
-    const int NH = N * H;
-    const int c = idx / NH, r = idx - c * NH, n = r / H;
-    h = r - n * H;
-    const int t0 = cu ? cu[n] : n * T;
-    const int t1 = cu ? cu[n + 1] : t0 + T;
-    tc = t0 + c * C;
-    if (tc >= t1) return false;
-    slot = (cu ? first_chunk[n] : n * ((T + C - 1) / C)) + c;
-    L = min(C, t1 - tc);
-    return true;
-}
-
 struct PrepArgs {
     CUtensorMap tmq, tmk, tmv, tmg;  // [T_total][H][128]: boxes of 64 tokens x 64 (bf16) / 32 (fp32) channels
     const __nv_bfloat16 *q, *k, *v;
@@ -387,9 +352,59 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         const int maxc = cu ? first_chunk[N + 1] : (T + C - 1) / C;
         nitems = maxc > 0 ? maxc * N * H : 0;
     }
-    auto decode = [&](int idx, int &slot_, int &h_, int &tc_, int &L_) -> bool {
-        return chunk_major ? item_tokens_cm(idx, H, cu, first_chunk, N, T, slot_, h_, tc_, L_)
-                           : item_tokens(idx, H, cu, first_chunk, N, T, slot_, h_, tc_, L_);
+    // Item cursor: items are visited first, first + stride, ..., so the digits of
+    // an item index advance by carries and the loop needs no division:
+    //   chunk-major: idx = (c N + n) H + h   -> (h, mid = n, top = c), radices H, N;
+    //   slot-major, equal lengths: idx = (n cpn + c) H + h -> (h, mid = c, top = n);
+    //   slot-major, packed: idx = slot H + h -> (h, mid = slot), mid without carry.
+    struct Cur { int h, mid, top; };
+    const int cpn = (T + C - 1) / C;
+    const int R2 = chunk_major ? N : (cu ? 0x7fffffff : cpn);
+    auto split = [&](int x) {
+        Cur r;
+        r.h = x % H;
+        const int q = x / H;
+        r.mid = R2 == 0x7fffffff ? q : q % R2;
+        r.top = R2 == 0x7fffffff ? 0 : q / R2;
+        return r;
+    };
+    const Cur sd = split(stride);
+    auto advance = [&](Cur r) {
+        r.h += sd.h;
+        int carry = 0;
+        if (r.h >= H) {
+            r.h -= H;
+            carry = 1;
+        }
+        r.mid += sd.mid + carry;
+        if (r.mid >= R2) {
+            r.mid -= R2;
+            ++r.top;
+        }
+        r.top += sd.top;
+        return r;
+    };
+    // the tokens of an item; false if it has none (past a sequence's end)
+    auto tokens = [&](Cur r, int &slot_, int &h_, int &tc_, int &L_) -> bool {
+        h_ = r.h;
+        int n, c;
+        if (chunk_major) {
+            n = r.mid;
+            c = r.top;
+        } else if (!cu) {
+            c = r.mid;
+            n = r.top;
+            if (n >= N) return false;
+        } else if (!slot_to_chunk(r.mid, cu, first_chunk, N, T, n, c)) {
+            return false;
+        }
+        const int t0 = cu ? cu[n] : n * T;
+        const int t1 = cu ? cu[n + 1] : t0 + T;
+        tc_ = t0 + c * C;
+        if (t1 < t0 || tc_ >= t1) return false;
+        slot_ = (cu ? (chunk_major ? first_chunk[n] + c : r.mid) : n * cpn + c);
+        L_ = min(C, t1 - tc_);
+        return true;
     };
     if (first >= nitems) return;  // no item: no TMEM either
 
@@ -475,7 +490,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     unsigned short beta_next = 0;
     {
         int slot_, h_, tc_, L_;
-        if (decode(first, slot_, h_, tc_, L_)) {
+        if (tokens(split(first), slot_, h_, tc_, L_)) {
             stage_g(tc_, h_, L_);
             stage_qkv(tc_, h_);
             if (tid < C) beta_next = load_beta(tc_, h_, L_);
@@ -509,10 +524,11 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
 
     bool failed = false;
     uint32_t it = 0;  // items done by this CTA (mbarrier phase)
+    Cur cur = split(first);
 #pragma unroll 1
-    for (int item = first; item < nitems; item += stride) {
+    for (int item = first; item < nitems; item += stride, cur = advance(cur)) {
     int slot, h, tc, L;
-    if (!decode(item, slot, h, tc, L)) continue;
+    if (!tokens(cur, slot, h, tc, L)) continue;
     if (staged != item) {  // the previous item could not prefetch this one
         stage_g(tc, h, L);
         stage_qkv(tc, h);
@@ -521,7 +537,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
     int nslot, nh, ntc, nL;  // the next item of this CTA
     const int nitem = item + stride;
-    const bool has_next = nitem < nitems && decode(nitem, nslot, nh, ntc, nL);
+    const bool has_next = nitem < nitems && tokens(advance(cur), nslot, nh, ntc, nL);
 
     if (tid < C) sBeta[tid] = __bfloat162float(__ushort_as_bfloat16(beta_next));
     if (!gpc && tid < C) reinterpret_cast<float *>(smem + kOffGs)[tid] = gs_next;
