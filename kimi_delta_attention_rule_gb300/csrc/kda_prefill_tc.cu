@@ -453,24 +453,27 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     //   q, k -> the column-tile region (dead after the Gram products), v -> its own buffer.
     const uint32_t uG = sbase + kOffAcum, uQ = sbase + kOffQs, uK = sbase + kOffKs,
                    uV = sbase + kOffVs;
+    // the issuing thread: lane 0 of warp 14, which has no work of its own in the
+    // T phase (where the q, k, v copies are issued)
+    constexpr int kStager = kPrepThreads - 64;
     uint32_t n_staged = 0;  // stagings issued (each completes one phase of both barriers)
     const bool gpc = pa.g_per_channel != 0;
     float gs_next = 0.f;  // scalar mode: the decay of token tid of the staged item
     auto stage_g = [&](int tc_, int h_, int L_) {
         ++n_staged;
         if (gpc) {
-            if (tid == 32) {
+            if (tid == kStager) {
                 tc::mbar_arrive_expect_tx(bInG, 4 * kRegion);
 #pragma unroll
                 for (int r = 0; r < 4; ++r) tma_load_3d(uG + r * kRegion, &pa.tmg, 32 * r, h_, tc_, bInG);
             }
         } else {
-            if (tid == 32) tc::mbar_arrive_expect_tx(bInG, 0);  // nothing in flight: the phase completes
+            if (tid == kStager) tc::mbar_arrive_expect_tx(bInG, 0);  // nothing in flight: the phase completes
             if (tid < C) gs_next = tid < L_ ? g[((size_t)tc_ + tid) * H + h_] : 0.f;
         }
     };
     auto stage_qkv = [&](int tc_, int h_) {
-        if (tid == 32) {
+        if (tid == kStager) {
             tc::mbar_arrive_expect_tx(bInQKV, 6 * kRegion);
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
@@ -497,20 +500,23 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             staged = first;
         }
     }
-    // Every block byte leaves shared memory by TMA bulk stores issued by thread 0,
-    // which waits for them to complete before the barrier ahead of the next item's
-    // operand phase. With `ready`: the previous item's flag (-1: none) is then
-    // released by one lane of the last warp during this item's T phase, where that
-    // warp is otherwise idle.
+    // Every block byte leaves shared memory by TMA bulk stores issued by thread 0.
+    // Before the next item's operand phase it waits only until their sources were
+    // read (the staging is reused there); it waits for their completion once it has
+    // issued that item's Gram products, while the tensor core runs. With `ready`:
+    // the previous item's flag (-1: none) is then released by one lane of the last
+    // warp during this item's T phase, where that warp is otherwise idle.
     constexpr int kReleaser = kPrepThreads - 32;
     long long pending = -1;
     auto release = [&](long long idx) {
         asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + idx), "r"(1u) : "memory");
     };
 
-    // operand-phase mapping: 16-token tile op_i = warp % 4, tokens op_t0 and
-    // op_t0 + 8 (op_t0 = 16 op_i + lane % 8), channels op_c0 .. + 8
-    const int op_i = warp & 3;
+    // operand-phase mapping: 16-token tile op_i, tokens op_t0 and op_t0 + 8
+    // (op_t0 = 16 op_i + lane % 8), channels op_c0 .. + 8. Earlier tiles write more
+    // column tiles of Kh; the tile is rotated by warp / 4 so that each SM
+    // sub-partition (warp % 4) runs one warp of every tile.
+    const int op_i = (warp + (warp >> 2)) & 3;
     const int op_c0 = 8 * (4 * (warp >> 2) + (lane >> 3));
     const int op_t0 = 16 * op_i + (lane & 7);
     // descriptors and instruction descriptors of the tcgen05 products
@@ -597,9 +603,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         uv[m] = *reinterpret_cast<const uint4 *>(smem + kOffVs + so);
         if (t >= L) uq[m] = uk[m] = uv[m] = make_uint4(0, 0, 0, 0);  // past the chunk
     }
-    // the previous item's bulk stores are complete: its staging is free, and its
-    // flag may be released after this barrier
-    if (tid == 0) tc::bulk_wait_all();
+    // the previous item's bulk stores have read their sources: the staging is free
+    if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
 
     // ---- all operands: thread = (8 channels, tokens op_t0 and op_t0 + 8) ---------------
@@ -702,9 +707,16 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int ks = 0; ks < 8; ++ks)
             tc::mma_f16(tm + 128u, dA2 + 16 * ks, dB2 + 16 * ks, id_gram2, ks > 0);
         tc::mma_commit(bG);
+        // the previous item's block is complete in global memory (all groups but
+        // the q e^{a} store above): its flag may be released after the next barrier
+        tc::bulk_wait_all_but<1>();
     }
     if (!failed && !tc::mbar_wait(bG, it & 1u, kPrepWaitLimit)) failed = true;
     tc::fence_after_sync();
+    // the Gram products have read the column tiles, and the v buffer was read before
+    // the operand phase: the next item's q, k, v copies go out now, ahead of the
+    // [M ; k e^{a_C - a}] store below on the same copy engine
+    if (has_next && !failed) stage_qkv(ntc, nh);
 
     // ---- read back: each warp one 16-column slice (part 0: k-Gram, 1: q-Gram) of its
     // quarter's slots; a lane holds key row s of slot (i, j) and 16 tokens t = 16 i + n
@@ -784,8 +796,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);
         tc::bulk_commit();
     }
-    if (has_next) {  // column tiles and the v buffer are free from here on
-        stage_qkv(ntc, nh);
+    if (has_next) {  // the next item's q, k, v are on their way
         if (tid < C) beta_next = load_beta(ntc, nh, nL);
         staged = nitem;
     }
@@ -793,17 +804,25 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
     const uint32_t aT = sbase + kOffT, aAh = sbase + kOffAh;
     if (tid < 64) {
-        // column cc of the inverse of block b by forward substitution, updating the
-        // remaining rows as each entry is known (one multiply-add per step on the chain)
+        // column cc of the inverse of block b by forward substitution: entry r is
+        // -sum_{s < r} A_rs x_s (ascending s), row r of A read 4 entries at a time
+        // (the 16 lanes of a block read the same address); only the last term
+        // waits for x_{r-1}
         const int b = tid >> 4, cc = tid & 15;
-        float x[16], acc[16];
+        const float *Ab = sAd + b * 256;
+        float x[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+        for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
 #pragma unroll
-        for (int s2 = 0; s2 < 16; ++s2) {
-            x[s2] = s2 < cc ? 0.f : (s2 == cc ? 1.f : -acc[s2]);
+            for (int s4 = 0; s4 < r; s4 += 4) {
+                const float4 a4 = *reinterpret_cast<const float4 *>(Ab + r * 16 + s4);
+                const float av[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
-            for (int r = s2 + 1; r < 16; ++r) acc[r] += sAd[b * 256 + r * 16 + s2] * x[s2];
+                for (int e = 0; e < 4; ++e)
+                    if (s4 + e < r) acc += av[e] * x[s4 + e];
+            }
+            x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) store_h(smem + kOffT, off_k64(16 * b + r, 16 * b + cc), x[r]);
