@@ -512,13 +512,12 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + idx), "r"(1u) : "memory");
     };
 
-    // operand-phase mapping: 16-token tile op_i, tokens op_t0 and op_t0 + 8
-    // (op_t0 = 16 op_i + lane % 8), channels op_c0 .. + 8. Earlier tiles write more
-    // column tiles of Kh; the tile is rotated by warp / 4 so that each SM
-    // sub-partition (warp % 4) runs one warp of every tile.
-    const int op_i = (warp + (warp >> 2)) & 3;
+    // operand-phase mapping: channels op_c0 .. + 8 of token op_lt of two 16-token
+    // tiles, op_p and 3 - op_p. A token of tile i writes 3 - i column tiles of Kh
+    // beyond its own, so every thread writes three.
+    const int op_p = warp & 1;
     const int op_c0 = 8 * (4 * (warp >> 2) + (lane >> 3));
-    const int op_t0 = 16 * op_i + (lane & 7);
+    const int op_lt = 8 * ((warp >> 1) & 1) + (lane & 7);
     // descriptors and instruction descriptors of the tcgen05 products
     const uint32_t id_gram1 = tc::idesc_f16(128, 128, 0, 0, 0);  // bf16, both K-major
     const uint32_t id_gram2 = tc::idesc_f16(64, 32, 0, 0, 0);
@@ -596,7 +595,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     uint4 uq[2], uk[2], uv[2];
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
-        const int t = op_t0 + 8 * m;
+        const int t = 16 * (m == 0 ? op_p : 3 - op_p) + op_lt;
         const uint32_t so = qkv_off(t, op_c0);
         uq[m] = *reinterpret_cast<const uint4 *>(smem + kOffQs + so);
         uk[m] = *reinterpret_cast<const uint4 *>(smem + kOffKs + so);
@@ -607,74 +606,69 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (tid == 0) tc::bulk_wait_read();
     __syncthreads();
 
-    // ---- all operands: thread = (8 channels, tokens op_t0 and op_t0 + 8) ---------------
+    // ---- Gram operands: thread = (8 channels, token op_lt of tiles op_p and 3 - op_p) --
+    // x = e^{a_t - r_i} and y = e^{r_{i+1} - a_t} stay in registers for the second
+    // half of the operands, which runs while the tensor core forms the Gram products
+    float xs[2][8], ys[2][8];
     {
-        const int c0 = op_c0, i = op_i;
+        const int c0 = op_c0, tl = op_lt;
         const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
-        float r[8], er[8], ed[8], ec[8];  // per-tile values, shared by both tokens
-        lds8(&sRef[i * 128 + c0], r);
-        lds8(&tab[(kTabEr + i) * 128 + c0], er);
-        lds8(&tab[(kTabEd + i) * 128 + c0], ed);
-        lds8(&tab[(kTabEc + i) * 128 + c0], ec);
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-            const int t = op_t0 + 8 * m, tl = t & 15;
-            float qq[8], kk[8], vv[8], a[8];
+            const int i = m == 0 ? op_p : 3 - op_p, t = 16 * i + tl;
+            float r[8], ed[8];  // per-tile values
+            lds8(&sRef[i * 128 + c0], r);
+            lds8(&tab[(kTabEd + i) * 128 + c0], ed);
+            float qq[8], kk[8], a[8];
             unpack8_bf16(uq[m], qq);
             unpack8_bf16(uk[m], kk);
-            unpack8_bf16(uv[m], vv);
             *reinterpret_cast<float4 *>(a) =
                 *reinterpret_cast<const float4 *>(smem + kOffAcum + a_off(t, c0));
             *reinterpret_cast<float4 *>(a + 4) =
                 *reinterpret_cast<const float4 *>(smem + kOffAcum + a_off(t, c0 + 4));
-            const float bt = sBeta[t];
-            float x[8], ix[8], y[8], o[8], md = 0.f;
+            float ix[8], o[8], md = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float p = a[e] - r[e];  // a_t - r_i in [-80, 0]
-                x[e] = __expf(p);             // e^{a_t - r_i}      in [e^-80, 1]
+                xs[m][e] = __expf(p);         // e^{a_t - r_i}      in [e^-80, 1]
                 ix[e] = __expf(-p);           // e^{r_i - a_t}      in [1, e^80]
-                y[e] = ed[e] * ix[e];         // e^{r_{i+1} - a_t}  in [e^-80, 1]
+                ys[m][e] = ed[e] * ix[e];     // e^{r_{i+1} - a_t}  in [e^-80, 1]
                 md += qq[e] * kk[e];
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = kk[e] * x[e];
+            for (int e = 0; e < 8; ++e) o[e] = kk[e] * xs[m][e];
             *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + tl, c0)) = pack8_bf16(o);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = qq[e] * x[e];
+            for (int e = 0; e < 8; ++e) o[e] = qq[e] * xs[m][e];
             *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + 16 + tl, c0)) = pack8_bf16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * ix[e];
             *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i, i) + tl, c0)) =
                 pack8_bf16(o);
             // later reference tiles i2 > i: k e^{r_i2 - a_t} = k e^{r_i2 - r_{i+1}} y
-#pragma unroll 1
-            for (int i2 = i + 1; i2 < 4; ++i2) {
-                float f[8];
-                if (i2 == i + 1) {
+            // (tile 0: i2 = 1, 2, 3; tile 1: 2, 3; tile 2: 3)
+            if (i < 3) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = 1.f;
-                } else {
-                    const int tb = (i2 == 2) ? kTabE21 : (i == 0 ? kTabE31 : kTabE32);
-                    lds8(&tab[tb * 128 + c0], f);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = kk[e] * (f[e] * y[e]);
-                *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i2, i) + tl, c0)) =
+                for (int e = 0; e < 8; ++e) o[e] = kk[e] * ys[m][e];
+                *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i + 1, i) + tl, c0)) =
                     pack8_bf16(o);
             }
+            if (i < 2) {
+                float f[8];
+                lds8(&tab[(i == 0 ? kTabE21 : kTabE32) * 128 + c0], f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = qq[e] * (er[e] * x[e]);            // q e^{a}
-            *reinterpret_cast<uint4 *>(smem + kOffSqe + off_k128(t, c0)) = pack8_f16(o);
+                for (int e = 0; e < 8; ++e) o[e] = kk[e] * (f[e] * ys[m][e]);
+                *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i + 2, i) + tl, c0)) =
+                    pack8_bf16(o);
+            }
+            if (i == 0) {
+                float f[8];
+                lds8(&tab[kTabE31 * 128 + c0], f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * (er[e] * x[e]);       // beta k e^{a}
-            *reinterpret_cast<uint4 *>(smem + kOffKtb + off_mn128(t, c0)) = pack8_f16(o);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                        // beta v
-            *reinterpret_cast<uint4 *>(smem + kOffVb + off_mn128(t, c0)) = pack8_f16(o);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = kk[e] * (ec[e] * y[e]);            // k e^{a_C - a}
-            *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(t, 64 + c0)) = pack8_f16(o);
+                for (int e = 0; e < 8; ++e) o[e] = kk[e] * (f[e] * ys[m][e]);
+                *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(3, 0) + tl, c0)) =
+                    pack8_bf16(o);
+            }
             // q_t . k_t (the diagonal of M: no decay): 32 channels per warp here,
             // the four warps of the tile are added in the Gram read-back
             md += __shfl_xor_sync(0xffffffffu, md, 8);
@@ -695,8 +689,6 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // the other columns are products of unrelated tiles and are not read.
     if (tid == 0) {
         tc::fence_after_sync();
-        tc::bulk_s2g(blk + kB12 + 64 * 256, sbase + kOffSqe, 64 * 256);  // q e^{a}
-        tc::bulk_commit();
         const uint64_t dA1 = tc::smem_desc(sbase + kOffKh, 128, 2048);
         const uint64_t dB1 = tc::smem_desc(sbase + kOffX, 128, 2048);
         const uint64_t dA2 = tc::smem_desc(sbase + kOffKh + 12u * 2048u, 128, 2048);
@@ -707,9 +699,42 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int ks = 0; ks < 8; ++ks)
             tc::mma_f16(tm + 128u, dA2 + 16 * ks, dB2 + 16 * ks, id_gram2, ks > 0);
         tc::mma_commit(bG);
-        // the previous item's block is complete in global memory (all groups but
-        // the q e^{a} store above): its flag may be released after the next barrier
-        tc::bulk_wait_all_but<1>();
+        // the previous item's block is complete in global memory: its flag may be
+        // released after the next barrier
+        tc::bulk_wait_all();
+    }
+
+    // ---- the other operands, meanwhile (same thread mapping) --------------------------
+    {
+        const int c0 = op_c0;
+        const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int i = m == 0 ? op_p : 3 - op_p, t = 16 * i + op_lt;
+            float er[8], ec[8];
+            lds8(&tab[(kTabEr + i) * 128 + c0], er);
+            lds8(&tab[(kTabEc + i) * 128 + c0], ec);
+            float qq[8], kk[8], vv[8], o[8];
+            unpack8_bf16(uq[m], qq);
+            unpack8_bf16(uk[m], kk);
+            unpack8_bf16(uv[m], vv);
+            const float bt = sBeta[t];
+            float ea[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ea[e] = er[e] * xs[m][e];                 // e^{a_t}
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = qq[e] * ea[e];                     // q e^{a}
+            *reinterpret_cast<uint4 *>(smem + kOffSqe + off_k128(t, c0)) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * ea[e];                // beta k e^{a}
+            *reinterpret_cast<uint4 *>(smem + kOffKtb + off_mn128(t, c0)) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                        // beta v
+            *reinterpret_cast<uint4 *>(smem + kOffVb + off_mn128(t, c0)) = pack8_f16(o);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) o[e] = kk[e] * (ec[e] * ys[m][e]);        // k e^{a_C - a}
+            *reinterpret_cast<uint4 *>(smem + kOffSb3 + off_b3(t, 64 + c0)) = pack8_f16(o);
+        }
     }
     if (!failed && !tc::mbar_wait(bG, it & 1u, kPrepWaitLimit)) failed = true;
     tc::fence_after_sync();
@@ -787,13 +812,14 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             }
         }
     }
-    tc::fence_async_smem();  // [M ; k e^{a_C - a}] staging -> bulk store
+    tc::fence_async_smem();  // q e^{a} and [M ; k e^{a_C - a}] staging -> bulk stores
     tc::fence_before_sync();
     failed = __syncthreads_or(failed) != 0;
     tc::fence_after_sync();
     if (failed) break;
     if (tid == 0) {
-        tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);
+        tc::bulk_s2g(blk + kB12 + 64 * 256, sbase + kOffSqe, 64 * 256);  // q e^{a}
+        tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);          // [M ; k e^{a_C - a}]
         tc::bulk_commit();
     }
     if (has_next) {  // the next item's q, k, v are on their way

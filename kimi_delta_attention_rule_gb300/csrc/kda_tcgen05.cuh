@@ -201,11 +201,6 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
 }
-// wait until all committed bulk stores but the newest N are complete
-template <int N>
-__device__ __forceinline__ void bulk_wait_all_but() {
-    asm volatile("cp.async.bulk.wait_group %0;\n" ::"n"(N) : "memory");
-}
 
 // Byte offset of element (r, k) in a K-major no-swizzle tile.
 __host__ __device__ constexpr uint32_t kmajor_off(int r, int k, uint32_t lbo, uint32_t sbo) {
