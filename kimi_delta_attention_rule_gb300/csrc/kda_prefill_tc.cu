@@ -1036,8 +1036,8 @@ constexpr uint32_t kOffBuf0 = 0;
 constexpr uint32_t kOffBuf1 = kBlock;
 constexpr uint32_t kOffSA = 2 * kBlock;              // fp16 K-major [j][key]: S^T (A operand)
 constexpr uint32_t kOffUA = kOffSA + 128 * 128 * 2;  // fp16 K-major [j][t]: U^T (A operand)
-constexpr uint32_t kOffO = kOffUA + 128 * 64 * 2;    // bf16 [t][j] output staging
-constexpr uint32_t kRecSmem = kOffO + 64 * 128 * 2;
+constexpr uint32_t kOffO = kOffUA + 128 * 64 * 2;    // bf16 [t][j] output staging, 2 chunks
+constexpr uint32_t kRecSmem = kOffO + 2 * 64 * 128 * 2;
 static_assert(kRecSmem <= 227 * 1024, "shared memory budget");
 static_assert(kRecThreads == kPrepThreads, "the fused kernel runs both roles");
 // TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T.
@@ -1204,6 +1204,19 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
         tc::mma_commit(bM2);
     };
 
+    // chunk cw's output rows, staged in shared memory, to global memory
+    auto write_out = [&](int cw) {
+        const __nv_bfloat16 *sO = reinterpret_cast<const __nv_bfloat16 *>(smem + kOffO + (cw & 1) * 16384);
+        const int tcw = t0 + cw * C, Lw = min(C, t1 - tcw);
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+            const int id = tid + kRecThreads * m, t = id >> 4, c8 = (id & 15) * 8;
+            if (t < Lw)
+                *reinterpret_cast<uint4 *>(&out[((size_t)(tcw + t) * H + h) * 128 + c8]) =
+                    *reinterpret_cast<const uint4 *>(&sO[t * 128 + c8]);
+        }
+    };
+
     if (nchunks == 0) {
         if (fin)
             for (int k0 = 32 * qd; k0 < 32 * qd + 32; ++k0)
@@ -1245,7 +1258,6 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
             const unsigned char *buf = smem + buf_off(c);
-            const int tcc = t0 + c * C, L = min(C, t1 - tcc);
 
             // U^T = U~^T - P^T for t in [16 qd, 16 qd + 16) -> shared (fp16)
             if (tid == kLoader) {  // while the first product runs
@@ -1281,6 +1293,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 if (ready && known_set < c + 2) refresh();
                 check_issue(c + 1);
             }
+            if (c > 0) write_out(c - 1);  // meanwhile, the previous chunk's output rows
 
             // new state (keys [32 qd, +32)) and this chunk's O (t in [16 qd, +16))
             wait(bM2, (uint32_t)(c & 1));
@@ -1288,6 +1301,12 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             uint32_t sr[2][16], orr[1][16];
             tc::tmem_ld_cols<2>(tlane + kColS + 32 * qd, sr);
             tc::tmem_ld_cols<1>(tlane + kColO + 16 * qd, orr);
+            {  // this chunk's output rows -> staging, written out during the next chunk
+                __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO + (c & 1) * 16384);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[0][e]));
+            }
             if (c + 1 < nchunks) {
 #pragma unroll
                 for (int gi = 0; gi < 4; ++gi) {
@@ -1325,8 +1344,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             if (tid == kLoader) check_issue(c + 2);  // known to exist (or no flags)
 
 
-            // while the next product runs: pre-scale the state by the next chunk's
-            // decay, and write this chunk's output rows
+            // while the next product runs: pre-scale the state by the next chunk's decay
             if (c + 1 < nchunks) {
                 const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam) + 32 * qd;
 #pragma unroll
@@ -1338,19 +1356,8 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 }
                 tc::tmem_wait_st();
             }
-            __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO);
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-                sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[0][e]));
-            __syncthreads();
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int id = tid + kRecThreads * m, t = id >> 4, c8 = (id & 15) * 8;
-                if (t < L)
-                    *reinterpret_cast<uint4 *>(&out[((size_t)(tcc + t) * H + h) * 128 + c8]) =
-                        *reinterpret_cast<const uint4 *>(&sO[t * 128 + c8]);
-            }
         }
+        write_out(nchunks - 1);  // staged before the last barrier of the loop
     }
 
     if (failed) {
