@@ -12,8 +12,7 @@
 // RMS-normalised over the head's 128 channels (eps 1e-6) with a weight per
 // channel and multiplied by sigmoid(gate).
 //
-// Both kernels are HBM streams over [T_total, H, 128] rows: one warp per
-// (token, head) row, 4 channels per lane, rows in memory order.
+// Both kernels are HBM streams over [T_total, H, 128] rows, 4 channels per lane.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -57,80 +56,188 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
-// One warp per (token, head) row, rows in memory order (lane = 4 channels).
-// All loads of a row are issued before any arithmetic (the W taps of q, k and
-// v, alpha, beta): the W - 1 earlier rows were loaded by other warps a moment
-// before and mostly come from L2, and independent loads keep the row's
-// latency to about one memory round trip. A lane's 4 channels x W taps of
-// weights are contiguous in [H, D, W] and load as W float4.
+// Prologue: one warp per (head, run of kProTokens consecutive tokens), lane = 4
+// channels. The head's conv weights stay in registers for the whole run (a
+// lane's 4 channels x W taps are contiguous in [H, D, W]), and the last W - 1
+// inputs of each tensor slide along in registers, so every input row is read
+// from memory once. The q, k, v and alpha rows of the next tokens are already
+// on their way: each lane copies its own 4 channels with cp.async into a ring of
+// kProRing token slots in shared memory (the copies hold no registers), one
+// commit group per token. Consecutive warps take consecutive heads of the same
+// tokens, so a CTA reads whole [H, D] rows. The window is cleared where a
+// sequence starts.
+constexpr int kProTokens = 32;
+template <typename IO>
+struct ProRing {
+    static constexpr int depth = sizeof(IO) == 2 ? 4 : 2;  // 32 KiB per 8-warp CTA either way
+};
+template <int BYTES>
+__device__ __forceinline__ void cp_async_row(uint32_t dst, const void *src);
+template <>
+__device__ __forceinline__ void cp_async_row<8>(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+}
+template <>
+__device__ __forceinline__ void cp_async_row<16>(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+template <typename IO>
+struct Raw4;  // 4 channels of a row, as stored
+template <>
+struct Raw4<float> {
+    float4 v;
+};
+template <>
+struct Raw4<__nv_bfloat16> {
+    uint2 v;
+};
+template <typename IO>
+__device__ __forceinline__ Raw4<IO> ld_raw4(const IO *p) {
+    Raw4<IO> r;
+    r.v = *reinterpret_cast<const decltype(r.v) *>(p);
+    return r;
+}
+__device__ __forceinline__ void cvt4(const Raw4<float> &r, float *x) {
+    x[0] = r.v.x; x[1] = r.v.y; x[2] = r.v.z; x[3] = r.v.w;
+}
+__device__ __forceinline__ void cvt4(const Raw4<__nv_bfloat16> &r, float *x) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r.v);
+    x[0] = __low2float(h[0]); x[1] = __high2float(h[0]);
+    x[2] = __low2float(h[1]); x[3] = __high2float(h[1]);
+}
+
 template <typename IO, int W>
 __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
     layer_prologue_kernel(const IO *__restrict__ q_raw, const IO *__restrict__ k_raw,
                           const IO *__restrict__ v_raw, const IO *__restrict__ alpha_raw,
                           const IO *__restrict__ beta_raw, const float *__restrict__ wq,
                           const float *__restrict__ wk, const float *__restrict__ wv,
-                          const int32_t *__restrict__ cu, int N, long long rows, int H,
+                          const int32_t *__restrict__ cu, int N, long long T_total, int H,
                           IO *__restrict__ q, IO *__restrict__ k, IO *__restrict__ v,
                           float *__restrict__ g, IO *__restrict__ beta) {
-    const int lane = threadIdx.x & 31;
-    const long long r = (long long)blockIdx.x * kLayerRowsPerCta + (threadIdx.x >> 5);
-    if (r >= rows) return;
-    const int t = (int)(r / H), h = (int)(r - (long long)t * H), c0 = 4 * lane;
-    int t_lo = 0;  // first token of t's sequence: the last n with cu[n] <= t
+    constexpr int WP = W > 1 ? W - 1 : 1;
+    const int lane = threadIdx.x & 31, c0 = 4 * lane;
+    const long long wid = (long long)blockIdx.x * kLayerRowsPerCta + (threadIdx.x >> 5);
+    const long long nruns = (T_total + kProTokens - 1) / kProTokens;
+    if (wid >= nruns * H) return;
+    const int h = (int)(wid % H);
+    const long long t0 = (wid / H) * kProTokens;
+    const long long t1 = t0 + kProTokens < T_total ? t0 + kProTokens : T_total;
+    // the sequence of t0: the last n with cu[n] <= t0; next_start = cu[n + 1]
+    int n = 0;
+    long long seq_lo = 0, next_start = T_total;
     if (cu) {
-        int lo = 0, hi = N;
+        int lo = 0, hi = N - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (cu[mid] <= t) lo = mid;
+            if (cu[mid] <= t0) lo = mid;
             else hi = mid - 1;
         }
-        t_lo = max(0, min(cu[lo], t));
+        n = lo;
+        seq_lo = cu[n];
+        next_start = cu[n + 1];
     }
     const IO *raw3[3] = {q_raw, k_raw, v_raw};
     const float *w3[3] = {wq, wk, wv};
-    float x[3][W][4];  // [tensor][steps back][channel]
+    float wl[3][4 * W];  // [tensor][channel * W + tap]
 #pragma unroll
     for (int m = 0; m < 3; ++m)
 #pragma unroll
-        for (int i = 0; i < W; ++i) {
-            if (t - i >= t_lo) {
-                load4<IO>(raw3[m] + ((size_t)(t - i) * H + h) * kD + c0, x[m][i]);
-            } else {
-                x[m][i][0] = x[m][i][1] = x[m][i][2] = x[m][i][3] = 0.f;
+        for (int i = 0; i < W; ++i)
+            *reinterpret_cast<float4 *>(&wl[m][4 * i]) =
+                *reinterpret_cast<const float4 *>(w3[m] + ((size_t)h * kD + c0) * W + 4 * i);
+    // win[m][i - 1]: the input i tokens back, as stored (zero bits before the sequence)
+    Raw4<IO> win[3][WP], zero;
+    zero.v = {};
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int i = 1; i < W; ++i) {
+            const long long ts = t0 - i;
+            win[m][i - 1] = ts >= seq_lo ? ld_raw4<IO>(raw3[m] + ((size_t)ts * H + h) * kD + c0) : zero;
+        }
+    // the ring: [warp][slot][q, k, v, alpha][lane]
+    constexpr int RD = ProRing<IO>::depth;
+    __shared__ __align__(16) Raw4<IO> ring[kLayerRowsPerCta][RD][4][32];
+    Raw4<IO>(*wr)[4][32] = ring[threadIdx.x >> 5];
+    const IO *src4[4] = {q_raw, k_raw, v_raw, alpha_raw};
+    auto issue = [&](long long t, int slot) {
+        const size_t o = ((size_t)t * H + h) * kD + c0;
+#pragma unroll
+        for (int m = 0; m < 4; ++m)
+            cp_async_row<(int)sizeof(Raw4<IO>)>(
+                static_cast<uint32_t>(__cvta_generic_to_shared(&wr[slot][m][lane])), src4[m] + o);
+    };
+#pragma unroll
+    for (int sl = 0; sl < RD; ++sl) {  // one group per token slot (empty past the run)
+        if (t0 + sl < t1) issue(t0 + sl, sl);
+        cp_async_commit();
+    }
+    IO nb = lane == 0 ? beta_raw[(size_t)t0 * H + h] : IO();  // beta one token ahead
+    IO *out3[3] = {q, k, v};
+    int slot = 0;
+#pragma unroll 1
+    for (long long t = t0; t < t1; ++t) {
+        cp_async_wait<RD - 1>();  // this lane's copies of token t have landed
+        Raw4<IO> cx[3], ca = wr[slot][3][lane];
+#pragma unroll
+        for (int m = 0; m < 3; ++m) cx[m] = wr[slot][m][lane];
+        const IO cb = nb;
+        if (lane == 0 && t + 1 < t1) nb = beta_raw[(size_t)(t + 1) * H + h];
+        if (cu && t >= next_start) {  // a sequence starts here (empty ones are skipped)
+            while (n < N - 1 && cu[n + 1] <= t) ++n;
+            next_start = cu[n + 1];
+#pragma unroll
+            for (int m = 0; m < 3; ++m)
+#pragma unroll
+                for (int i = 0; i < WP; ++i) win[m][i] = zero;
+        }
+        const size_t o = ((size_t)t * H + h) * kD + c0;
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            float x[4], acc[4];
+            cvt4(cx[m], x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = wl[m][e * W + W - 1] * x[e];
+#pragma unroll
+            for (int i = 1; i < W; ++i) {
+                float xp[4];
+                cvt4(win[m][i - 1], xp);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] += wl[m][e * W + W - 1 - i] * xp[e];
+            }
+            if (m < 2) {  // q, k: L2 norm over the row
+                const float sc = rsqrtf(
+                    warp_sum(acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3]) +
+                    kL2Eps);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] *= sc;
+            }
+            store4<IO>(out3[m] + o, acc);
+            if (W > 1) {  // slide the window
+#pragma unroll
+                for (int i = WP - 1; i > 0; --i) win[m][i] = win[m][i - 1];
+                win[m][0] = cx[m];
             }
         }
-    const size_t o = (size_t)r * kD + c0;
-    float al[4];
-    load4<IO>(alpha_raw + o, al);
-    const float braw = lane == 0 ? to_f32(beta_raw[r]) : 0.f;
-    IO *out3[3] = {q, k, v};
-#pragma unroll
-    for (int m = 0; m < 3; ++m) {
-        float wl[4 * W];  // [channel][tap]
-#pragma unroll
-        for (int i = 0; i < W; ++i)
-            *reinterpret_cast<float4 *>(&wl[4 * i]) =
-                *reinterpret_cast<const float4 *>(w3[m] + ((size_t)h * kD + c0) * W + 4 * i);
-        float acc[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            acc[e] = 0.f;
-#pragma unroll
-            for (int i = 0; i < W; ++i) acc[e] += wl[e * W + (W - 1 - i)] * x[m][i][e];
-        }
-        if (m < 2) {  // q, k: L2 norm over the row
-            const float sc = rsqrtf(
-                warp_sum(acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3]) +
-                kL2Eps);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[e] *= sc;
-        }
-        store4<IO>(out3[m] + o, acc);
+        float al[4];
+        cvt4(ca, al);
+        *reinterpret_cast<float4 *>(g + o) =
+            make_float4(-5.f * sigmoidf_(al[0]), -5.f * sigmoidf_(al[1]), -5.f * sigmoidf_(al[2]),
+                        -5.f * sigmoidf_(al[3]));
+        if (lane == 0) beta[(size_t)t * H + h] = from_f32<IO>(sigmoidf_(to_f32(cb)));
+        // the slot was read above (its values are in use): token t + RD goes into it
+        if (t + RD < t1) issue(t + RD, slot);
+        cp_async_commit();
+        slot = slot + 1 == RD ? 0 : slot + 1;
     }
-    *reinterpret_cast<float4 *>(g + o) =
-        make_float4(-5.f * sigmoidf_(al[0]), -5.f * sigmoidf_(al[1]), -5.f * sigmoidf_(al[2]),
-                    -5.f * sigmoidf_(al[3]));
-    if (lane == 0) beta[r] = from_f32<IO>(sigmoidf_(braw));
+    cp_async_wait<0>();
 }
 
 template <typename IO>
@@ -159,14 +266,14 @@ cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const vo
                                   const float *wk, const float *wv, int W, const int32_t *cu,
                                   int N, long long T_total, int H, void *q, void *k, void *v,
                                   float *g, void *beta, cudaStream_t stream) {
-    const long long rows = T_total * H;
-    if (rows == 0) return cudaSuccess;
-    const unsigned grid = (unsigned)((rows + kLayerRowsPerCta - 1) / kLayerRowsPerCta);
+    if (T_total == 0) return cudaSuccess;
+    const long long warps = (T_total + kProTokens - 1) / kProTokens * H;
+    const unsigned grid = (unsigned)((warps + kLayerRowsPerCta - 1) / kLayerRowsPerCta);
 #define KDA_PROLOGUE(WW)                                                                          \
     layer_prologue_kernel<IO, WW><<<grid, 32 * kLayerRowsPerCta, 0, stream>>>(                   \
         static_cast<const IO *>(q_raw), static_cast<const IO *>(k_raw),                           \
         static_cast<const IO *>(v_raw), static_cast<const IO *>(alpha_raw),                       \
-        static_cast<const IO *>(beta_raw), wq, wk, wv, cu, N, rows, H, static_cast<IO *>(q),      \
+        static_cast<const IO *>(beta_raw), wq, wk, wv, cu, N, T_total, H, static_cast<IO *>(q),   \
         static_cast<IO *>(k), static_cast<IO *>(v), g, static_cast<IO *>(beta))
     switch (W) {
         case 1: KDA_PROLOGUE(1); break;

@@ -310,6 +310,30 @@ def test_layer_prologue(io, tol, W):
 
 
 @pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+@pytest.mark.parametrize("lens,W", [(None, 4), ([32, 32, 0, 36, 1, 199], 3), ([64, 64], 2)])
+def test_layer_prologue_runs(io, tol, lens, W):
+    """Several runs of tokens per head: a single sequence with a ragged last run,
+    and sequence starts on and off the run boundaries (incl. an empty one)."""
+    H = 5
+    T = 300 if lens is None else sum(lens)
+    cu = None if lens is None else np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    gen = torch.Generator().manual_seed(97 + W)
+    dt = torch.bfloat16 if io == "bf16" else torch.float32
+    raw = [torch.randn(T, H, 128, generator=gen).to(dt) for _ in range(4)]
+    braw = torch.randn(T, H, generator=gen).to(dt)
+    ws = [0.5 * torch.randn(H, 128, W, generator=gen) for _ in range(3)]
+    dev = lambda t: t.to(DEV)
+    q, k, v, g, beta = kda.kda_layer_prologue(
+        *map(dev, raw), dev(braw), *map(dev, ws),
+        cu_seqlens=None if cu is None else torch.from_numpy(cu).to(DEV))
+    torch.cuda.synchronize()
+    rq, rk, rv, rg, rb = oracle_layer.prologue(*map(np32, raw), np32(braw), *map(np32, ws), cu)
+    for got, ref in ((q, rq), (k, rk), (v, rv), (beta, rb)):
+        assert out_err(got, ref) <= tol
+    assert rel_err(g.cpu().numpy(), rg) <= 1e-5
+
+
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
 def test_layer_epilogue(io, tol):
     gen = torch.Generator().manual_seed(91)
     dt = torch.bfloat16 if io == "bf16" else torch.float32
