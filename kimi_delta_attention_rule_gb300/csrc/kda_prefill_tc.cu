@@ -1034,15 +1034,17 @@ __global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(const __grid_cons
 constexpr int kRecThreads = 512;  // thread = (value column j, quarter); all warps on every step
 constexpr uint32_t kOffBuf0 = 0;
 constexpr uint32_t kOffBuf1 = kBlock;
-constexpr uint32_t kOffSA = 2 * kBlock;              // fp16 K-major [j][key]: S^T (A operand)
-constexpr uint32_t kOffUA = kOffSA + 128 * 128 * 2;  // fp16 K-major [j][t]: U^T (A operand)
-constexpr uint32_t kOffO = kOffUA + 128 * 64 * 2;    // bf16 [t][j] output staging, 2 chunks
+constexpr uint32_t kOffO = 2 * kBlock;               // bf16 [t][j] output staging, 2 chunks
 constexpr uint32_t kRecSmem = kOffO + 2 * 64 * 128 * 2;
 static_assert(kRecSmem <= 227 * 1024, "shared memory budget");
 static_assert(kRecThreads == kPrepThreads, "the fused kernel runs both roles");
-// TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T.
-constexpr uint32_t kTmemCols = 256;
+// TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T,
+// [256, 288) U^T and [288, 352) the fp16 state S^T as pairs of 16-bit values
+// (the A operands of the two products; no shared-memory copy, no proxy fence).
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColP = 0, kColO = 64, kColS = 128;
+constexpr uint32_t kColU = 256;   // U^T (fp16 pairs): the A operand of the second product
+constexpr uint32_t kColSh = 288;  // S^T (fp16 pairs): the A operand of the first product
 constexpr uint64_t kWaitLimit = 2000000000ull;  // 2 s: the default bound on any wait of a chain
 
 struct RecArgs {
@@ -1094,7 +1096,6 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     __shared__ __align__(8) uint64_t bars[4];  // loads (2), MMA group 1, MMA group 2
     __shared__ uint32_t tmem_slot;
     const uint32_t sbase = smem_u32(smem);
-    const uint32_t uSA = sbase + kOffSA, uUA = sbase + kOffUA;
     const uint32_t bL0 = smem_u32(&bars[0]), bL1 = smem_u32(&bars[1]);
     const uint32_t bM1 = smem_u32(&bars[2]), bM2 = smem_u32(&bars[3]);
     auto bL = [&](int c) { return (c & 1) ? bL1 : bL0; };
@@ -1184,15 +1185,14 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
         }
     };
     constexpr int kLoader = 32;
-    // descriptors (no swizzle); +16 in the address field per 256-byte K step
-    const uint64_t dSA = tc::smem_desc(uSA, 128, 2048), dUA = tc::smem_desc(uUA, 128, 1024);
+    // B descriptors (no swizzle); +16 in the address field per 256-byte K step
     const uint32_t id_n128 = tc::idesc_f16(128, 128, 1, 0, 0);
     const uint32_t id_n192 = tc::idesc_f16(128, 192, 1, 0, 1);  // B MN-major
     auto issue_mma1 = [&](int c) {  // [P^T | O~^T] = S^T [W ; q e^a]^T
         const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB12, 128, 2048);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            tc::mma_f16(tm + kColP, dSA + 16 * ks, dB + 16 * ks, id_n128, ks > 0);
+            tc::mma_f16_ta(tm + kColP, tm + kColSh + 8u * ks, dB + 16 * ks, id_n128, ks > 0);
         tc::mma_commit(bM1);
     };
     auto issue_mma2 = [&](int c) {  // [O^T | S^T] += U^T [M ; Kb^T]^T
@@ -1200,7 +1200,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
         const uint64_t dB = tc::smem_desc(sbase + buf_off(c) + kB3, 3072, 128);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-            tc::mma_f16(tm + kColO, dUA + 16 * ks, dB + 384 * ks, id_n192, 1u);
+            tc::mma_f16_ta(tm + kColO, tm + kColU + 8u * ks, dB + 384 * ks, id_n192, 1u);
         tc::mma_commit(bM2);
     };
 
@@ -1237,21 +1237,16 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
         wait(bL0, 0);
         {
             const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam) + 32 * qd;
+            uint32_t w16[16];  // keys 32 qd + 2 c, + 1 -> TMEM column kColSh + 16 qd + c
 #pragma unroll
-            for (int gi = 0; gi < 4; ++gi) {
-                const float *x = &s0[8 * gi];
-                uint4 pk;
-                pk.x = pack_f16(x[0], x[1]); pk.y = pack_f16(x[2], x[3]);
-                pk.z = pack_f16(x[4], x[5]); pk.w = pack_f16(x[6], x[7]);
-                *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 32 * qd + 8 * gi)) = pk;
-            }
+            for (int c2 = 0; c2 < 16; ++c2) w16[c2] = pack_f16(s0[2 * c2], s0[2 * c2 + 1]);
+            tc::tmem_st16u(tlane + kColSh + 16 * qd, w16);
 #pragma unroll
             for (int e = 0; e < 32; ++e) s0[e] *= gam0[e];
             tc::tmem_st16(tlane + kColS + 32 * qd, s0);
             tc::tmem_st16(tlane + kColS + 32 * qd + 16, s0 + 16);
             tc::tmem_wait_st();
         }
-        tc::fence_async_smem();
         sync_check();
         if (tid == 0 && !failed) issue_mma1(0);
 
@@ -1270,23 +1265,22 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             {
                 uint32_t pr[1][16];
                 tc::tmem_ld_cols<1>(tlane + kColP + 16 * qd, pr);
+                uint32_t w8[8];  // tokens 16 qd + 2 c, + 1 -> TMEM column kColU + 8 qd + c
 #pragma unroll
                 for (int gi = 0; gi < 2; ++gi) {
                     const uint4 u = *reinterpret_cast<const uint4 *>(buf + ut_off(j, 2 * qd + gi));
                     const __half2 *hu = reinterpret_cast<const __half2 *>(&u);
-                    uint4 pk;
-                    uint32_t *w = reinterpret_cast<uint32_t *>(&pk);
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float2 a = __half22float2(hu[e]);
                         const int t = 8 * gi + 2 * e;
-                        w[e] = pack_f16(a.x - __uint_as_float(pr[0][t]),
-                                        a.y - __uint_as_float(pr[0][t + 1]));
+                        w8[4 * gi + e] = pack_f16(a.x - __uint_as_float(pr[0][t]),
+                                                  a.y - __uint_as_float(pr[0][t + 1]));
                     }
-                    *reinterpret_cast<uint4 *>(smem + kOffUA + off_k64(j, 16 * qd + 8 * gi)) = pk;
                 }
+                tc::tmem_st8u(tlane + kColU + 8 * qd, w8);
+                tc::tmem_wait_st();
             }
-            tc::fence_async_smem();
             sync_check();
             if (tid == 0 && !failed) issue_mma2(c);
             if (tid == kLoader) {  // while the second product runs
@@ -1307,17 +1301,14 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 for (int e = 0; e < 16; ++e)
                     sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[0][e]));
             }
-            if (c + 1 < nchunks) {
+            if (c + 1 < nchunks) {  // the fp16 copy of the new state: the next first product's A
+                uint32_t w16[16];
 #pragma unroll
-                for (int gi = 0; gi < 4; ++gi) {
-                    const uint32_t *x = &sr[gi >> 1][(gi & 1) * 8];
-                    uint4 pk;
-                    pk.x = pack_f16(__uint_as_float(x[0]), __uint_as_float(x[1]));
-                    pk.y = pack_f16(__uint_as_float(x[2]), __uint_as_float(x[3]));
-                    pk.z = pack_f16(__uint_as_float(x[4]), __uint_as_float(x[5]));
-                    pk.w = pack_f16(__uint_as_float(x[6]), __uint_as_float(x[7]));
-                    *reinterpret_cast<uint4 *>(smem + kOffSA + off_k128(j, 32 * qd + 8 * gi)) = pk;
-                }
+                for (int c2 = 0; c2 < 16; ++c2)
+                    w16[c2] = pack_f16(__uint_as_float(sr[c2 >> 3][(2 * c2) & 15]),
+                                       __uint_as_float(sr[c2 >> 3][(2 * c2 + 1) & 15]));
+                tc::tmem_st16u(tlane + kColSh + 16 * qd, w16);
+                tc::tmem_wait_st();
             } else if (fin) {
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
@@ -1337,7 +1328,8 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             // c + 1 must be on its way before anyone waits for it
             if (tid == kLoader) block_issue(c + 1);
             if (c + 1 < nchunks) wait(bL(c + 1), (uint32_t)(((c + 1) >> 1) & 1));
-            tc::fence_async_smem();
+            // (both operands the tensor core reads from this CTA's writes, U^T and the
+            // fp16 state, are in TMEM: no proxy fence before these barriers)
             sync_check();
             if (tid == 0 && c + 1 < nchunks && !failed) issue_mma1(c + 1);
             // this chunk's buffer is free: without flags, fetch chunk c + 2 into it now
