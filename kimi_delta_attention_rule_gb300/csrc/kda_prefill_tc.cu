@@ -483,12 +483,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             }
         }
     };
-    // token tid of an item (raw bits: converted only where used, so that the
-    // load does not stall the issuing warp)
+    // beta of token tid - 64 of an item, held by warps 2 and 3 (not by the warps of
+    // the T phase's diagonal blocks); raw bits, converted only where used, so that
+    // the load does not stall the issuing warp
+    const bool beta_thr = tid >= 64 && tid < 64 + C;
     auto load_beta = [&](int tc_, int h_, int L_) -> unsigned short {
-        return tid < L_ ? __bfloat16_as_ushort(beta[((size_t)tc_ + tid) * H + h_]) : (unsigned short)0;
+        const int t = tid - 64;
+        return t < L_ ? __bfloat16_as_ushort(beta[((size_t)tc_ + t) * H + h_]) : (unsigned short)0;
     };
-    // the item that the staged inputs belong to (-1: none); its beta (tid < C)
+    // the item that the staged inputs belong to (-1: none); its beta
     int staged = -1;
     unsigned short beta_next = 0;
     {
@@ -496,16 +499,18 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         if (tokens(split(first), slot_, h_, tc_, L_)) {
             stage_g(tc_, h_, L_);
             stage_qkv(tc_, h_);
-            if (tid < C) beta_next = load_beta(tc_, h_, L_);
+            if (beta_thr) beta_next = load_beta(tc_, h_, L_);
             staged = first;
         }
     }
-    // Every block byte leaves shared memory by TMA bulk stores issued by thread 0.
-    // Before the next item's operand phase it waits only until their sources were
-    // read (the staging is reused there); it waits for their completion once it has
-    // issued that item's Gram products, while the tensor core runs. With `ready`:
-    // the previous item's flag (-1: none) is then released by one lane of the last
-    // warp during this item's T phase, where that warp is otherwise idle.
+    // Every block byte leaves shared memory by TMA bulk stores: q e^{a} and
+    // [M ; Kb] from the staging thread (issued as the T phase starts), W, U~^T and
+    // e^{a_C} from thread 0 (at the item's end). Each waits until its sources were
+    // read before that staging is reused, and for completion about one item later:
+    // thread 0 once it has issued the next item's Gram products, the staging thread
+    // before the next item's Gram read-back barrier. With `ready`: the previous
+    // item's flag (-1: none) is then released by one lane of the last warp during
+    // this item's T phase, where that warp is otherwise idle.
     constexpr int kReleaser = kPrepThreads - 32;
     long long pending = -1;
     auto release = [&](long long idx) {
@@ -537,14 +542,14 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (staged != item) {  // the previous item could not prefetch this one
         stage_g(tc, h, L);
         stage_qkv(tc, h);
-        if (tid < C) beta_next = load_beta(tc, h, L);
+        if (beta_thr) beta_next = load_beta(tc, h, L);
     }
     unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
     int nslot, nh, ntc, nL;  // the next item of this CTA
     const int nitem = item + stride;
     const bool has_next = nitem < nitems && tokens(advance(cur), nslot, nh, ntc, nL);
 
-    if (tid < C) sBeta[tid] = __bfloat162float(__ushort_as_bfloat16(beta_next));
+    if (beta_thr) sBeta[tid - 64] = __bfloat162float(__ushort_as_bfloat16(beta_next));
     if (!gpc && tid < C) reinterpret_cast<float *>(smem + kOffGs)[tid] = gs_next;
     if (!failed && !tc::mbar_wait(bInG, it & 1u, kPrepWaitLimit)) failed = true;
     if (!failed && !tc::mbar_wait(bInQKV, it & 1u, kPrepWaitLimit)) failed = true;
@@ -812,18 +817,22 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             }
         }
     }
+    // the staging thread's stores of the previous item are complete (issued about
+    // one item ago): with thread 0's wait above, its flag may be released after
+    // this barrier
+    if (tid == kStager) tc::bulk_wait_all();
     tc::fence_async_smem();  // q e^{a} and [M ; k e^{a_C - a}] staging -> bulk stores
     tc::fence_before_sync();
     failed = __syncthreads_or(failed) != 0;
     tc::fence_after_sync();
     if (failed) break;
-    if (tid == 0) {
+    if (tid == kStager) {  // (thread 0 and the diagonal-block warps go on to the T phase)
         tc::bulk_s2g(blk + kB12 + 64 * 256, sbase + kOffSqe, 64 * 256);  // q e^{a}
         tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);          // [M ; k e^{a_C - a}]
         tc::bulk_commit();
     }
     if (has_next) {  // the next item's q, k, v are on their way
-        if (tid < C) beta_next = load_beta(ntc, nh, nL);
+        if (beta_thr) beta_next = load_beta(ntc, nh, nL);
         staged = nitem;
     }
 
@@ -939,7 +948,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
     }
     tc::fence_async_smem();  // T -> tensor core
-    if (tid == 0) tc::bulk_wait_read();  // q e^{a} and [M ; Kb] staging free for W, U~
+    if (tid == kStager) tc::bulk_wait_read();  // q e^{a} and [M ; Kb] staging free for W, U~
     tc::fence_before_sync();
     __syncthreads();
 
@@ -979,6 +988,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             reinterpret_cast<float *>(su + kGam)[tid] = reinterpret_cast<const float *>(smem + kOffGamS)[tid];
     }
     tc::fence_async_smem();  // W, U~^T, e^{a_C} staging -> bulk stores
+    if (ready && it == 0 && tid == kStager) tc::bulk_wait_all();  // published at once, below
     tc::fence_before_sync();
     failed = __syncthreads_or(failed) != 0;  // shared memory and TMEM are reused by the next item
     tc::fence_after_sync();
@@ -1008,8 +1018,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         tc::mbar_wait(bG, it & 1u, 10000000ull);
         tc::mbar_wait(bW, it & 1u, 10000000ull);
     }
+    if (tid == kStager) tc::bulk_wait_all();
+    __syncthreads();  // with thread 0's wait below: every block write of this CTA is done
     if (tid == 0) {
-        tc::bulk_wait_all();  // every block write of this CTA is done
+        tc::bulk_wait_all();
         if (!failed && pending >= 0) {  // the last item of this CTA
             asm volatile("fence.proxy.async.global;\n" ::: "memory");
             release(pending);
