@@ -347,27 +347,54 @@ def main():
     tflops = flops / (ms * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers ---------------
+    # Every step copies its inputs from pinned host memory, runs the prefill and
+    # reads its output back. Consecutive steps are pipelined the way a serving
+    # loop would run them: host-to-device copies on one stream, the prefill on
+    # the main one, device-to-host reads on a third, with two sets of device
+    # buffers, so that step i + 1's inputs and step i - 1's output cross the
+    # host link while step i computes.
     pin = lambda t: t.cpu().pin_memory()
     hq, hk, hv, hg, hb = pin(x.q), pin(x.k), pin(x.v), pin(x.g), pin(x.beta)
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv, dg, db = (torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta))
+    dbufs = [[torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta)] for _ in range(2)]
+    douts = [out, torch.empty_like(out)]
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
     d2h = hout.numel() * hout.element_size()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]      # inputs of buffer set b on the device
+    ev_run = [torch.cuda.Event() for _ in range(2)]     # prefill of set b done
+    ev_out = [torch.cuda.Event() for _ in range(2)]     # output of set b read back
+    for b in range(2):  # all sets free at the start
+        ev_run[b].record(stream)
+        ev_out[b].record(stream)
 
-    def e2e_step():
-        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb)):
-            d_.copy_(h_, non_blocking=True)
-        kda.kda_prefill(dq, dk, dv, dg, db, x.scale, chunk=C, out=out, final_state=fin,
+    def e2e_step(i):
+        b = i % 2
+        dq, dk, dv, dg, db = dbufs[b]
+        s_in.wait_event(ev_run[b])  # the prefill that read this set is done
+        with torch.cuda.stream(s_in):
+            for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (dg, hg), (db, hb)):
+                d_.copy_(h_, non_blocking=True)
+            ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # this set's previous output was read back
+        kda.kda_prefill(dq, dk, dv, dg, db, x.scale, chunk=C, out=douts[b], final_state=fin,
                         workspace=ws, stream=stream)
-        hout.copy_(out, non_blocking=True)
+        ev_run[b].record(stream)
+        s_out.wait_event(ev_run[b])
+        with torch.cuda.stream(s_out):
+            hout.copy_(douts[b], non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(3):
-        e2e_step()
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     e2e_steps = max(3, min(args.steps, 20))
     ev0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    s_in.wait_event(ev0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_stream(s_out)
     ev1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
@@ -376,7 +403,7 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         e2e_ms = float(t.item())
     e2e_val = units / (e2e_ms * 1e-3) / 1e6
-    del dq, dk, dv, dg, db, hq, hk, hv, hg, hb, hout
+    del dbufs, douts, hq, hk, hv, hg, hb, hout
 
     # ---- layer prologue / epilogue on the same rows (HBM streams) ----------
     layer = None
