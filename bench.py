@@ -155,6 +155,24 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+def rank_seed(base, rank):
+    """Each rank draws its own independent batch: the units shard across ranks
+    with no exchange between them (weak scaling)."""
+    return base + 7919 * rank
+
+
+def max_over_ranks(x, world, device):
+    """The largest value of x over all ranks (x itself on one rank): a step
+    counts as done when the slowest rank is done."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -291,7 +309,7 @@ def main():
 
     # ---- prefill workload (each rank: its own independent batch) -----------
     x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16",
-                              seed=PREFILL["seed"] + 7919 * rank, device=dev)
+                              seed=rank_seed(PREFILL["seed"], rank), device=dev)
     H, T = PREFILL["H"], PREFILL["T"]
     out = torch.empty_like(x.q)
     fin = torch.empty((1, H, D, D), dtype=torch.float32, device=dev)
@@ -323,10 +341,7 @@ def main():
     if world > 1:
         dist.barrier()
     ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     assert kda.kda_workspace_status(ws) == kda.KDA_OK
     units = H * T * world
     value = units / (ms * 1e-3) / 1e6
@@ -398,10 +413,7 @@ def main():
     ev1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e_val = units / (e2e_ms * 1e-3) / 1e6
     del dbufs, douts, hq, hk, hv, hg, hb, hout
 
@@ -425,13 +437,13 @@ def main():
             kda.kda_layer_prologue(*raw[:4], braw, *convs, stream=stream)
         ev1.record(stream)
         torch.cuda.synchronize()
-        pro_ms = ev0.elapsed_time(ev1) / reps_l
+        pro_ms = max_over_ranks(ev0.elapsed_time(ev1) / reps_l, world, dev)
         ev0.record(stream)
         for _ in range(reps_l):
             kda.kda_layer_epilogue(raw[0], raw[4], nw, y=ly, stream=stream)
         ev1.record(stream)
         torch.cuda.synchronize()
-        epi_ms = ev0.elapsed_time(ev1) / reps_l
+        epi_ms = max_over_ranks(ev0.elapsed_time(ev1) / reps_l, world, dev)
         rows = T * H
         pro_bytes = rows * (4 * 2 * D + 2 + 3 * 2 * D + 4 * D + 2)  # bf16 rows in, q k v g beta out
         epi_bytes = rows * 3 * 2 * D
@@ -452,7 +464,7 @@ def main():
     if not args.no_decode:
         B, Hd, S = DECODE["B"], DECODE["H"], DECODE["steps"]
         dqq, dkk, dvv, dgg, dbb, state, dscale = inputs.decode_inputs(
-            B=B, H=Hd, steps=S, seed=DECODE["seed"] + 7919 * rank, device=dev)
+            B=B, H=Hd, steps=S, seed=rank_seed(DECODE["seed"], rank), device=dev)
         dout = torch.empty((S, B, Hd, D), dtype=torch.bfloat16, device=dev)
         g_stream = torch.cuda.Stream()
         g_stream.wait_stream(stream)
@@ -477,7 +489,7 @@ def main():
                 graph.replay()
         e1.record(g_stream)
         torch.cuda.synchronize()
-        dms = e0.elapsed_time(e1) / (reps * S)
+        dms = max_over_ranks(e0.elapsed_time(e1) / (reps * S), world, dev)
         state_bytes = decode_bytes_per_head_token() * B * Hd
         gbs = state_bytes / (dms * 1e-3) / 1e9
         decode = {
@@ -498,7 +510,7 @@ def main():
         # multi-token decode through a state pool: T = 4 tokens per sequence,
         # pool entries addressed by a permutation (16 calls in a CUDA graph)
         Tm, calls = 4, 16
-        xm = inputs.prefill_inputs([Tm] * B, H=Hd, io="bf16", seed=DECODE["seed"] + 5 + 7919 * rank,
+        xm = inputs.prefill_inputs([Tm] * B, H=Hd, io="bf16", seed=rank_seed(DECODE["seed"] + 5, rank),
                                    device=dev)
         shp = (B, Tm, Hd, D)
         mq, mk, mv, mg = (t.view(shp) for t in (xm.q, xm.k, xm.v, xm.g))
@@ -527,7 +539,7 @@ def main():
                 graph.replay()
         e1.record(g_stream)
         torch.cuda.synchronize()
-        mms = e0.elapsed_time(e1) / (reps * calls)
+        mms = max_over_ranks(e0.elapsed_time(e1) / (reps * calls), world, dev)
         mgbs = state_bytes / (mms * 1e-3) / 1e9
         decode["multi_token_pool"] = {
             "workload": "B=256, H=96, T=4 tokens per sequence per call, pool entries by a "
