@@ -214,7 +214,8 @@ int kda_decode(const void *q, const void *k, const void *v, const float *g, cons
  * DEVICE int32 [N + 1] offsets of packed sequences (NULL: one sequence);
  * convolutions never cross a sequence start. Outputs may not alias inputs.
  * Pointer alignment: 8 bytes (bf16) or 16 bytes (fp32) for the [.., D] rows,
- * 16 bytes for g.
+ * 16 bytes for g and for the conv weights; a misaligned pointer returns
+ * KDA_ERR_INVALID_ARG before any launch.
  *
  * kda_layer_epilogue: y = o / sqrt(mean(o^2) + 1e-6) * w * sigmoid(gate_raw)
  * per (token, head) over its D channels: o, gate_raw, y io dtype

@@ -230,6 +230,8 @@ int kda_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
                           static_cast<const void *>(k), static_cast<const void *>(v)})
         if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
     if (!aligned16(g)) return KDA_ERR_INVALID_ARG;
+    // a lane reads its 4 channels x W taps of [H, D, W] weights as float4
+    if (!aligned16(conv_q) || !aligned16(conv_k) || !aligned16(conv_v)) return KDA_ERR_INVALID_ARG;
     NvtxRange range("kda_layer_prologue");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const cudaError_t e =

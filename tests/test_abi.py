@@ -159,3 +159,29 @@ def test_product_path_has_no_cpu_fallback():
     assert "oracle" not in src.replace("no CPU fallback", "")
     for f in os.listdir(os.path.join(ROOT, "kimi_delta_attention_rule_gb300", "csrc")):
         assert "oracle" not in open(os.path.join(ROOT, "kimi_delta_attention_rule_gb300", "csrc", f)).read()
+
+
+def test_layer_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)
+    odd = ctypes.c_void_p(0x100008)  # 8-byte aligned, not 16
+    pro = lib.kda_layer_prologue
+    def call_pro(W=4, D=128, io=0, T=16, H=2, conv=fake, q=fake, g=fake):
+        return pro(q, fake, fake, fake, fake, conv, fake, fake, W, None, 1, T, H, D, io, fake,
+                   fake, fake, g, fake, None)
+    assert call_pro(W=0) == kda.KDA_ERR_UNSUPPORTED and call_pro(W=5) == kda.KDA_ERR_UNSUPPORTED
+    assert call_pro(D=64) == kda.KDA_ERR_UNSUPPORTED and call_pro(io=7) == kda.KDA_ERR_UNSUPPORTED
+    assert call_pro(T=-1) == kda.KDA_ERR_INVALID_ARG and call_pro(H=0) == kda.KDA_ERR_INVALID_ARG
+    assert call_pro(q=None) == kda.KDA_ERR_INVALID_ARG
+    assert call_pro(q=ctypes.c_void_p(0x100004)) == kda.KDA_ERR_INVALID_ARG  # bf16 rows: 8 B
+    assert call_pro(io=1, q=odd) == kda.KDA_ERR_INVALID_ARG                  # fp32 rows: 16 B
+    assert call_pro(g=odd) == kda.KDA_ERR_INVALID_ARG
+    assert call_pro(conv=odd) == kda.KDA_ERR_INVALID_ARG                     # weights: 16 B
+    assert call_pro(T=0) == kda.KDA_OK
+    epi = lib.kda_layer_epilogue
+    def call_epi(D=128, io=0, T=16, o=fake, w=fake):
+        return epi(o, fake, w, T, 2, D, io, fake, None)
+    assert call_epi(D=64) == kda.KDA_ERR_UNSUPPORTED and call_epi(io=7) == kda.KDA_ERR_UNSUPPORTED
+    assert call_epi(T=-1) == kda.KDA_ERR_INVALID_ARG and call_epi(o=None) == kda.KDA_ERR_INVALID_ARG
+    assert call_epi(w=odd) == kda.KDA_ERR_INVALID_ARG
+    assert call_epi(io=1, o=odd) == kda.KDA_ERR_INVALID_ARG
+    assert call_epi(T=0) == kda.KDA_OK
