@@ -163,17 +163,24 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
  *                       per-block ready flag; chosen when the chains take at
  *                       most a third of the SMs;
  *   KDA_SCHEDULE_DIRECT fp32 I/O: one kernel on CUDA cores.
- * With cu_seqlens a schedule kernel runs first. The environment variable
- * KDA_PREFILL_SCHEDULE=split|fused overrides the bf16 choice ("fused" needs
- * fewer chains than SMs). Test hook (failure detection, never for production):
- * with KDA_TEST_FLAG_TIMEOUT_MS=<ms> a fused launch runs its chains without any
- * producer and with that bound on each wait, so every chain gives up after
- * <ms> and kda_workspace_status() reports KDA_ERR_TIMEOUT; outputs are garbage. Returns the schedule, or the negated kda_status on
- * invalid sizes or a failed device query. The result does not depend on the
- * schedule: both bf16 schedules run the same arithmetic.
+ * With cu_seqlens a schedule kernel runs first. kda_prefill_set_schedule
+ * overrides the bf16 choice. Returns the schedule, or the negated kda_status
+ * on invalid sizes or a failed device query. The result does not depend on
+ * the schedule: both bf16 schedules run the same arithmetic.
  */
 int kda_prefill_schedule(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
                          int32_t varlen);
+
+/*
+ * Process-wide override of the bf16 prefill schedule, for tuning and for tests
+ * that run both schedules on the same inputs: -1 = the automatic choice (the
+ * default), KDA_SCHEDULE_SPLIT or KDA_SCHEDULE_FUSED ("fused" still needs
+ * fewer chains than SMs). When the library is loaded the environment variable
+ * KDA_PREFILL_SCHEDULE=split|fused sets the initial value; it is not read
+ * again. Calls already enqueued are not affected. Returns the previous value,
+ * or -KDA_ERR_INVALID_ARG for any other argument.
+ */
+int kda_prefill_set_schedule(int schedule);
 
 /*
  * Decode of T new tokens for each of B sequences (T = 1: one step; T up to 64,
@@ -262,6 +269,8 @@ int kda_check_cu_seqlens(const int32_t *cu_seqlens_host, int32_t N, int32_t T_to
  *  - All calls share the one array and each call clears its status word
  *    first: calls that overlap on the GPU race on it, so the caller must
  *    serialise them (one stream, or events between streams).
+ *  - Errors found on the device (malformed cu_seqlens, a timed-out wait) are
+ *    recorded in the array's status word; read them with kda_noalloc_status().
  *  - It allocates nothing (no cudaMalloc / cudaFree, no allocating library
  *    routine).
  */
@@ -269,6 +278,19 @@ int kda_prefill_noalloc(const void *q, const void *k, const void *v, const float
                         const void *beta, float scale, const float *init_state,
                         const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
                         int32_t chunk, int32_t io, void *out, float *final_state, void *stream);
+
+/*
+ * The device status word of kda_prefill_noalloc's static array on the current
+ * device (the counterpart of kda_workspace_status for that entry point; the
+ * pages have no counterpart either): synchronises `stream`, then reads and
+ * clears the word. It reports the device-side errors of the noalloc calls
+ * since the last read (each call clears the word before its kernels run, so
+ * normally those of the last call): KDA_OK, KDA_ERR_DEVICE (malformed
+ * cu_seqlens), KDA_ERR_TIMEOUT, or KDA_ERR_CUDA if a CUDA call failed. Like
+ * the entry point itself it allocates nothing; make the first call on a
+ * device before any stream capture.
+ */
+int kda_noalloc_status(void *stream);
 
 #ifdef __cplusplus
 }

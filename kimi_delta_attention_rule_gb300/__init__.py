@@ -33,7 +33,8 @@ KDA_SCHEDULE_DIRECT = 2
 EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size", "kda_prefill",
             "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
             "kda_prefill_schedule", "kda_decode", "kda_prefill_ex", "kda_layer_prologue",
-            "kda_layer_epilogue")
+            "kda_layer_epilogue", "kda_prefill_set_schedule", "kda_prefill_noalloc",
+            "kda_noalloc_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,17 @@ def load() -> ctypes.CDLL:
         lib.kda_layer_prologue.restype = ctypes.c_int
         lib.kda_layer_epilogue.argtypes = [P, P, P, I32, I32, I32, I32, P, P]
         lib.kda_layer_epilogue.restype = ctypes.c_int
+        lib.kda_prefill_set_schedule.argtypes = [ctypes.c_int]
+        lib.kda_prefill_set_schedule.restype = ctypes.c_int
+        lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32,
+                                            P, P, P]
+        lib.kda_prefill_noalloc.restype = ctypes.c_int
+        lib.kda_noalloc_status.argtypes = [P]
+        lib.kda_noalloc_status.restype = ctypes.c_int
+        # test-only entry point (include/kda_testing.h)
+        lib.kda_testing_prefill_chain_timeout.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32,
+                                                          I32, I32, I32, P, P, P, SZ, I32, P]
+        lib.kda_testing_prefill_chain_timeout.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -134,6 +146,16 @@ def kda_prefill_schedule(N: int, T: int, H: int, D: int, chunk: int, io: int,
     if s < 0:
         raise KDAError(-s, "kda_prefill_schedule")
     return s
+
+
+def kda_prefill_set_schedule(schedule: int) -> int:
+    """Process-wide override of the bf16 prefill schedule (C entry point
+    ``kda_prefill_set_schedule``): -1 = automatic, KDA_SCHEDULE_SPLIT or
+    KDA_SCHEDULE_FUSED. Returns the previous value."""
+    prev = int(load().kda_prefill_set_schedule(int(schedule)))
+    if prev < -1:
+        raise KDAError(-prev, "kda_prefill_set_schedule")
+    return prev
 
 
 def prefill_workspace(q, cu_seqlens=None, N=None, T=None, chunk=64):
@@ -278,6 +300,38 @@ def kda_layer_epilogue(o, gate_raw, norm_weight, y=None, stream=None):
 
 def kda_workspace_status(workspace, stream=None) -> int:
     return int(load().kda_workspace_status(_ptr(workspace), _stream_ptr(stream)))
+
+
+def kda_prefill_noalloc(q, k, v, g, beta, scale, init_state=None, cu_seqlens=None, chunk=64,
+                        out=None, final_state=None, stream=None, N=None, T=None):
+    """kda_prefill without a workspace (C entry point ``kda_prefill_noalloc``):
+    its scratch is the library's static device array. Returns (out,
+    final_state); device-side errors are read with kda_noalloc_status()."""
+    lib = load()
+    io = _io_code(q.dtype)
+    T_total, H, D = q.shape
+    if cu_seqlens is not None:
+        N, T = cu_seqlens.numel() - 1, T_total
+    else:
+        N = 1 if N is None else N
+        T = T_total // N if T is None else T
+    _check_cuda(q, k, v, g, beta, init_state, cu_seqlens, out, final_state)
+    if out is None:
+        out = torch.empty_like(q)
+    if final_state is None:
+        final_state = torch.empty((N, H, D, D), dtype=torch.float32, device=q.device)
+    rc = lib.kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+                                 _ptr(init_state), _ptr(cu_seqlens), N, T, H, D, chunk, io,
+                                 _ptr(out), _ptr(final_state), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_prefill_noalloc")
+    return out, final_state
+
+
+def kda_noalloc_status(stream=None) -> int:
+    """Reads and clears the device status word of kda_prefill_noalloc's static
+    array on the current device (C entry point ``kda_noalloc_status``)."""
+    return int(load().kda_noalloc_status(_stream_ptr(stream)))
 
 
 def kda_check_cu_seqlens(cu_host, T_total: int) -> int:

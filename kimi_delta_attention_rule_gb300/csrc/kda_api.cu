@@ -8,6 +8,7 @@
 #include <nvtx3/nvToolsExt.h>  // header-only: ranges are free unless a profiler is attached
 
 #include "kda.h"
+#include "kda_testing.h"
 #include "kda_common.cuh"
 
 namespace kda {
@@ -26,8 +27,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const void *beta, float scale, const float *init,
                               const int32_t *cu, int N, int T, int T_total, int H,
                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
-                              void *out, float *fin, unsigned char *ws, cudaStream_t stream);
+                              void *out, float *fin, unsigned char *ws, unsigned test_wait_ms,
+                              cudaStream_t stream);
 int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen);
+int prefill_tc_set_schedule(int s);
 template <typename IO>
 cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
                                   const void *alpha_raw, const void *beta_raw, const float *wq,
@@ -120,12 +123,19 @@ int kda_check_cu_seqlens(const int32_t *cu, int32_t N, int32_t T_total) {
     return KDA_OK;
 }
 
-int kda_prefill_ex(const void *q, const void *k, const void *v, const float *g,
-                   const void *beta, float scale, const float *init_state,
-                   const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
-                   int32_t chunk, int32_t io, int32_t g_per_channel, int32_t snapshot_interval,
-                   int32_t max_snapshots, float *snapshots, void *out, float *final_state,
-                   void *workspace, size_t workspace_bytes, void *stream) {
+}  // extern "C"
+
+namespace {
+
+// kda_prefill_ex, plus the failure-detection test mode (test_wait_ms > 0:
+// bf16 chains launched without producers, each wait bounded by test_wait_ms).
+int prefill_impl(const void *q, const void *k, const void *v, const float *g, const void *beta,
+                 float scale, const float *init_state, const int32_t *cu_seqlens, int32_t N,
+                 int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io, int32_t g_per_channel,
+                 int32_t snapshot_interval, int32_t max_snapshots, float *snapshots, void *out,
+                 float *final_state, void *workspace, size_t workspace_bytes, unsigned test_wait_ms,
+                 void *stream) {
+
     long long T_total = 0;
     const int rc = check_prefill_dims(N, T, H, D, chunk, io, cu_seqlens != nullptr, &T_total);
     if (rc != KDA_OK) return rc;
@@ -166,9 +176,45 @@ int kda_prefill_ex(const void *q, const void *k, const void *v, const float *g,
     } else {
         e = kda::launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T,
                                    (int)T_total, H, g_per_channel, si, sm, snapshots, out,
-                                   final_state, static_cast<unsigned char *>(workspace), st);
+                                   final_state, static_cast<unsigned char *>(workspace),
+                                   test_wait_ms, st);
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int kda_prefill_ex(const void *q, const void *k, const void *v, const float *g,
+                   const void *beta, float scale, const float *init_state,
+                   const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
+                   int32_t chunk, int32_t io, int32_t g_per_channel, int32_t snapshot_interval,
+                   int32_t max_snapshots, float *snapshots, void *out, float *final_state,
+                   void *workspace, size_t workspace_bytes, void *stream) {
+    return prefill_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk, io,
+                        g_per_channel, snapshot_interval, max_snapshots, snapshots, out,
+                        final_state, workspace, workspace_bytes, 0u, stream);
+}
+
+int kda_prefill_set_schedule(int schedule) {
+    if (schedule != -1 && schedule != KDA_SCHEDULE_SPLIT && schedule != KDA_SCHEDULE_FUSED)
+        return -KDA_ERR_INVALID_ARG;
+    return kda::prefill_tc_set_schedule(schedule);
+}
+
+int kda_testing_prefill_chain_timeout(const void *q, const void *k, const void *v,
+                                      const float *g, const void *beta, float scale,
+                                      const float *init_state, const int32_t *cu_seqlens,
+                                      int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
+                                      int32_t io, void *out, float *final_state, void *workspace,
+                                      size_t workspace_bytes, int32_t wait_ms, void *stream) {
+    if (io != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (wait_ms <= 0 || wait_ms > 10000) return KDA_ERR_INVALID_ARG;
+    return prefill_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk, io, 1,
+                        0, 0, nullptr, out, final_state, workspace, workspace_bytes,
+                        (unsigned)wait_ms, stream);
 }
 
 int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,

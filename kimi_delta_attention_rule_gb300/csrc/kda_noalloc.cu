@@ -17,7 +17,10 @@
 // Every call shares the one array: calls that overlap on the GPU (other
 // streams, or other threads) race on it and must be serialised by the
 // caller. The status word it holds is cleared by each call before its
-// kernels run.
+// kernels run, and kda_noalloc_status() reads it: the caller has no address
+// of the array, so device-side errors of these calls (malformed offsets, a
+// timed-out wait) are reported through that query instead of
+// kda_workspace_status().
 #include <cuda_runtime.h>
 #include <mutex>
 #include <stdint.h>
@@ -70,6 +73,14 @@ int kda_prefill_noalloc(const void *q, const void *k, const void *v, const float
     if (rc != KDA_OK) return rc;
     return kda_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk, io,
                        out, final_state, scratch, kNoallocScratchBytes, stream);
+}
+
+int kda_noalloc_status(void *stream) {
+    void *scratch = nullptr;
+    const int rc = scratch_for_current_device(&scratch);
+    if (rc != KDA_OK) return rc;
+    // the status word is the first word of the array, as of any workspace
+    return kda_workspace_status(scratch, stream);
 }
 
 }  // extern "C"

@@ -52,6 +52,7 @@
 
 #include <cuda.h>  // CUtensorMap (the encoder is resolved at run time)
 
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 
@@ -1441,10 +1442,25 @@ bool make_token_map(CUtensorMap *m, const void *base, bool f32, int H, int T_tot
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Schedule override: -1 = automatic, 0 = split, 1 = fused. Its initial value
+// comes from the environment variable KDA_PREFILL_SCHEDULE ("split" or
+// "fused"), read once when the library is loaded; kda_prefill_set_schedule
+// changes it afterwards.
+namespace {
+int initial_schedule_override() {
+    const char *env = getenv("KDA_PREFILL_SCHEDULE");
+    if (env && strcmp(env, "split") == 0) return 0;
+    if (env && strcmp(env, "fused") == 0) return 1;
+    return -1;
+}
+std::atomic<int> g_schedule_override{initial_schedule_override()};
+}  // namespace
+
+int prefill_tc_set_schedule(int s) { return g_schedule_override.exchange(s); }
+
 // Which schedule runs: the fused cooperative kernel when the chains leave most
-// SMs to the producers (N H <= SMs / 3), else K1 then K2. The environment
-// variable KDA_PREFILL_SCHEDULE = "split" or "fused" overrides the choice
-// ("fused" still needs N H < SMs and a cooperative launch).
+// SMs to the producers (N H <= SMs / 3), else K1 then K2. The override forces
+// either ("fused" still needs N H < SMs and a cooperative launch).
 // Returns 1 (fused), 0 (K1 then K2) or -1 (the device could not be queried).
 int prefill_tc_schedule(long long nchains, long long nitems) {
     int dev = 0, nsm = 0, coop = 0;
@@ -1452,10 +1468,10 @@ int prefill_tc_schedule(long long nchains, long long nitems) {
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
         return -1;
-    const char *env = getenv("KDA_PREFILL_SCHEDULE");
+    const int force = g_schedule_override.load();
     bool fused = 3 * nchains <= nsm;
-    if (env && strcmp(env, "split") == 0) fused = false;
-    if (env && strcmp(env, "fused") == 0) fused = nchains < nsm;
+    if (force == 0) fused = false;
+    if (force == 1) fused = nchains < nsm;
     fused = fused && nitems > 0 && coop;
     if (!fused) return 0;
     if (cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1476,7 +1492,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               const void *beta, float scale, const float *init,
                               const int32_t *cu, int N, int T, int T_total, int H,
                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
-                              void *out, float *fin, unsigned char *ws, cudaStream_t stream) {
+                              void *out, float *fin, unsigned char *ws, unsigned test_wait_ms,
+                              cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(pf::prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pf::kPrepSmem);
@@ -1499,11 +1516,18 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     off += pad256((size_t)nitems * 4);
     unsigned char *blocks = ws + off;
     const long long nchains = (long long)N * H;
-    const int sched = prefill_tc_schedule(nchains, nitems);
+    // failure-detection test: the fused schedule with its chains alone
+    const int sched = test_wait_ms ? 1 : prefill_tc_schedule(nchains, nitems);
     int dev = 0, nsm = 0;
     if (sched < 0 || cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return cudaErrorUnknown;
+    if (test_wait_ms) {  // every chain resident at once, in one cooperative launch
+        if (nchains >= nsm || nitems == 0) return cudaErrorInvalidValue;
+        e = cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pf::kFusedSmem);
+        if (e != cudaSuccess) return e;
+    }
     if (varlen) pf::schedule_kernel<<<1, 1024, 0, stream>>>(cu, N, T_total, first_chunk, status);
     const bool fused = sched == 1;
 
@@ -1537,11 +1561,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         if (e != cudaSuccess) return e;
         int nch = (int)nchains;
         unsigned grid = (unsigned)nsm;
-        // Failure-detection test hook: the chains run with no producer at all and
-        // a short wait bound, so that every wait for a ready flag runs out.
-        if (const char *tt = getenv("KDA_TEST_FLAG_TIMEOUT_MS")) {
-            grid = (unsigned)nch;
-            ra.wait_ns = (unsigned long long)strtoul(tt, nullptr, 10) * 1000000ull;
+        if (test_wait_ms) {  // chains with no producer at all and a short wait bound:
+            grid = (unsigned)nch;  // every wait for a ready flag runs out
+            ra.wait_ns = (unsigned long long)test_wait_ms * 1000000ull;
         }
         void *args[] = {&pa, &ra, &nch, &ready};
         return cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(grid),

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def header_functions():
-    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    import glob
+    src = "".join(open(p).read() for p in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))))
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src)))
 
@@ -185,3 +186,19 @@ def test_layer_argument_validation(lib):
     assert call_epi(w=odd) == kda.KDA_ERR_INVALID_ARG
     assert call_epi(io=1, o=odd) == kda.KDA_ERR_INVALID_ARG
     assert call_epi(T=0) == kda.KDA_OK
+
+
+def test_schedule_override_validates_and_returns_the_previous_value(lib):
+    # a process-wide setting: no device is touched
+    assert lib.kda_prefill_set_schedule(7) == -kda.KDA_ERR_INVALID_ARG
+    prev = kda.kda_prefill_set_schedule(kda.KDA_SCHEDULE_SPLIT)
+    assert kda.kda_prefill_set_schedule(kda.KDA_SCHEDULE_FUSED) == kda.KDA_SCHEDULE_SPLIT
+    assert kda.kda_prefill_set_schedule(prev) == kda.KDA_SCHEDULE_FUSED
+
+
+def test_testing_entry_point_rejects_bad_arguments(lib):
+    f = lib.kda_testing_prefill_chain_timeout
+    args = [None] * 5 + [1.0, None, None, 1, 64, 2, 128, 64]
+    assert f(*args, kda.KDA_F32, None, None, None, 0, 50, None) == kda.KDA_ERR_UNSUPPORTED
+    assert f(*args, kda.KDA_BF16, None, None, None, 0, 0, None) == kda.KDA_ERR_INVALID_ARG
+    assert f(*args, kda.KDA_BF16, None, None, None, 0, 50, None) == kda.KDA_ERR_INVALID_ARG

@@ -20,43 +20,10 @@ import oracle
 from oracle import layer as oracle_layer
 import kimi_delta_attention_rule_gb300 as kda
 from kimi_delta_attention_rule_gb300 import inputs
+from tests.parity import (DEV, TOL_BF16, TOL_F32, check_prefill, np32, oracle_prefill,
+                          out_err, prefill_schedule, rel_err, run_gpu_prefill)
 
 pytestmark = pytest.mark.gpu
-
-TOL_BF16 = 2e-2
-TOL_F32 = 1e-4
-DEV = "cuda:0"
-
-
-def bf16_half_spacing(ref):
-    """Half the distance between adjacent bf16 numbers at |ref| (8-bit
-    significand: spacing 2^(e - 7) in the binade [2^e, 2^(e+1)))."""
-    _, e = np.frexp(np.abs(ref))
-    e = np.maximum(e, -125)  # bf16 subnormal spacing floor
-    return np.ldexp(1.0, e - 9)
-
-
-def rel_err(got, ref, stored_bf16=False, ulps=0.5):
-    ref = np.asarray(ref, dtype=np.float64)
-    got = np.asarray(got, dtype=np.float64)
-    assert got.shape == ref.shape
-    assert np.all(np.isfinite(got)), "non-finite GPU output"
-    diff = np.abs(got - ref)
-    if stored_bf16:
-        diff = np.maximum(diff - 2 * ulps * bf16_half_spacing(ref), 0.0)
-    rms = float(np.sqrt(np.mean(ref ** 2)))
-    if rms == 0.0:
-        return float(np.max(diff))
-    return float(np.max(diff)) / rms
-
-
-def out_err(out, ref):
-    """Error of an output tensor against the oracle (storage-aware)."""
-    return rel_err(np32(out), ref, stored_bf16=(out.dtype == torch.bfloat16))
-
-
-def np32(t):
-    return t.detach().float().cpu().numpy()
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -64,33 +31,6 @@ def _lib():
     from kimi_delta_attention_rule_gb300 import build as kbuild
     kbuild.build()
     kda.load()
-
-
-def run_gpu_prefill(x, chunk, with_init=True):
-    cu = x.cu_seqlens.to(DEV) if x.cu_seqlens is not None else None
-    init = x.init_state.to(DEV) if (with_init and x.init_state is not None) else None
-    q = x.q.to(DEV)
-    ws = kda.prefill_workspace(q, cu, chunk=chunk)
-    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
-                               x.beta.to(DEV), x.scale, init_state=init, cu_seqlens=cu,
-                               chunk=chunk, workspace=ws)
-    assert kda.kda_workspace_status(ws) == kda.KDA_OK
-    torch.cuda.synchronize()
-    return out, fin
-
-
-def oracle_prefill(x, with_init=True):
-    init = x.init_state.double().numpy() if (with_init and x.init_state is not None) else None
-    return oracle.prefill(np32(x.q), np32(x.k), np32(x.v), np32(x.g), np32(x.beta), x.scale,
-                          init_state=init, cu_seqlens=x.cu_seqlens.numpy())
-
-
-def check_prefill(x, chunk, tol, with_init=True):
-    out, fin = run_gpu_prefill(x, chunk, with_init)
-    ro, rf = oracle_prefill(x, with_init)
-    eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
-    assert eo <= tol and ef <= tol, (eo, ef)
-    return eo, ef
 
 
 # ---------------------------------------------------------------- fp32 I/O
@@ -229,15 +169,15 @@ def scalar_decay_inputs(lens, H, io, seed):
 
 
 @pytest.mark.parametrize("mode", ["split", "fused"])
-def test_bf16_prefill_scalar_decay(monkeypatch, mode):
+def test_bf16_prefill_scalar_decay(mode):
     """g of shape [T_total, H] (one decay per token and head) equals the
     channel-wise path with that decay on every channel."""
-    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", mode)
     x, gs, x_full = scalar_decay_inputs([300, 1, 129], 2, "bf16", 71)
     cu = x.cu_seqlens.to(DEV)
-    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), gs.to(DEV),
-                               x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
-                               cu_seqlens=cu, chunk=64)
+    with prefill_schedule(mode):
+        out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), gs.to(DEV),
+                                   x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
+                                   cu_seqlens=cu, chunk=64)
     torch.cuda.synchronize()
     ro, rf = oracle_prefill(x_full)
     assert out_err(out, ro) <= TOL_BF16 and rel_err(fin.cpu().numpy(), rf) <= TOL_BF16
@@ -256,18 +196,17 @@ def test_f32_prefill_scalar_decay():
 @pytest.mark.parametrize("io,chunk,tol,mode", [("bf16", 64, TOL_BF16, "split"),
                                                 ("bf16", 64, TOL_BF16, "fused"),
                                                 ("f32", 16, TOL_F32, None)])
-def test_prefill_snapshots(monkeypatch, io, chunk, tol, mode):
+def test_prefill_snapshots(io, chunk, tol, mode):
     """The state after every 64 tokens of each sequence equals the oracle's
     final state of that prefix; slots past a sequence's end stay untouched."""
-    if mode:
-        monkeypatch.setenv("KDA_PREFILL_SCHEDULE", mode)
     lens, H, S, every = [300, 200], 2, 4, 64
     x = inputs.prefill_inputs(lens, H=H, io=io, seed=73, init="normal")
     snaps = torch.full((len(lens), S, H, 128, 128), 7.0, dtype=torch.float32, device=DEV)
-    out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
-                               x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
-                               cu_seqlens=x.cu_seqlens.to(DEV), chunk=chunk,
-                               snapshot_interval=every, snapshots=snaps)
+    with prefill_schedule(mode):
+        out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
+                                   x.beta.to(DEV), x.scale, init_state=x.init_state.to(DEV),
+                                   cu_seqlens=x.cu_seqlens.to(DEV), chunk=chunk,
+                                   snapshot_interval=every, snapshots=snaps)
     torch.cuda.synchronize()
     ro, rf = oracle_prefill(x)
     assert out_err(out, ro) <= tol and rel_err(fin.cpu().numpy(), rf) <= tol
@@ -530,7 +469,7 @@ def test_varlen_full_size():
 
 # ---------------------------------------------------------------- schedules
 @pytest.mark.parametrize("lens,H", [([1000], 3), ([5, 0, 129, 1], 2), ([64] * 40, 2)])
-def test_bf16_split_and_fused_schedules_agree(monkeypatch, lens, H):
+def test_bf16_split_and_fused_schedules_agree(lens, H):
     """The two-kernel schedule and the fused cooperative one run the same
     arithmetic: both match the oracle and agree bit for bit. ([64] * 40 with
     H = 2 is 80 chains, over a third of the SMs: the automatic choice there is
@@ -538,9 +477,8 @@ def test_bf16_split_and_fused_schedules_agree(monkeypatch, lens, H):
     x = inputs.prefill_inputs(lens, H=H, io="bf16", seed=21, init="normal")
     res = {}
     for mode in ("split", "fused"):
-        monkeypatch.setenv("KDA_PREFILL_SCHEDULE", mode)
-        res[mode] = run_gpu_prefill(x, 64)
-    monkeypatch.delenv("KDA_PREFILL_SCHEDULE")
+        with prefill_schedule(mode):
+            res[mode] = run_gpu_prefill(x, 64)
     ro, rf = oracle_prefill(x)
     for mode, (out, fin) in res.items():
         eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
@@ -566,32 +504,36 @@ def test_bf16_non_monotone_offsets_skip_the_call():
     assert torch.all(out == 7.0) and torch.all(fin == 7.0)
 
 
-def test_fused_chain_waits_are_bounded(monkeypatch):
+def test_fused_chain_waits_are_bounded():
     """A chain whose producer never comes gives up after its wait bound and
     reports KDA_ERR_TIMEOUT through the status word; the context stays usable
-    and the next call is correct. (Test hook: chains launched without
-    producers, 50 ms bound; nothing faults or hangs.)"""
+    and the next call is correct. (Test-only entry point: the chains are
+    launched without producers and with a 50 ms bound; nothing faults or
+    hangs.)"""
     x = inputs.prefill_inputs([200, 64], H=2, io="bf16", seed=101, init="normal")
     q = x.q.to(DEV)
     cu = x.cu_seqlens.to(DEV)
     ws = kda.prefill_workspace(q, cu, chunk=64)
-    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", "fused")
-    monkeypatch.setenv("KDA_TEST_FLAG_TIMEOUT_MS", "50")
-    kda.kda_prefill(q, x.k.to(DEV), x.v.to(DEV), x.g.to(DEV), x.beta.to(DEV), x.scale,
-                    init_state=x.init_state.to(DEV), cu_seqlens=cu, chunk=64, workspace=ws)
+    out = torch.empty_like(q)
+    fin = torch.empty((2, 2, 128, 128), dtype=torch.float32, device=DEV)
+    rc = kda.load().kda_testing_prefill_chain_timeout(
+        kda._ptr(q), kda._ptr(x.k.to(DEV)), kda._ptr(x.v.to(DEV)), kda._ptr(x.g.to(DEV)),
+        kda._ptr(x.beta.to(DEV)), x.scale, kda._ptr(x.init_state.to(DEV)), kda._ptr(cu), 2,
+        q.shape[0], 2, 128, 64, kda.KDA_BF16, kda._ptr(out), kda._ptr(fin), kda._ptr(ws),
+        ws.numel(), 50, kda._stream_ptr(None))
+    assert rc == kda.KDA_OK, kda.status_string(rc)
     assert kda.kda_workspace_status(ws) == kda.KDA_ERR_TIMEOUT
-    monkeypatch.delenv("KDA_TEST_FLAG_TIMEOUT_MS")
     check_prefill(x, 64, TOL_BF16)
 
 
-def test_prefill_schedule_choice(monkeypatch):
-    """Few chains (N H <= SMs / 3): fused; many chains: split; the
-    environment variable overrides."""
+def test_prefill_schedule_choice():
+    """Few chains (N H <= SMs / 3): fused; many chains: split; the override
+    (kda_prefill_set_schedule) wins while it is set."""
     f = kda.kda_prefill_schedule
-    monkeypatch.delenv("KDA_PREFILL_SCHEDULE", raising=False)
-    assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
-    assert f(64, 1 << 16, 32, 128, 64, kda.KDA_BF16, True) == kda.KDA_SCHEDULE_SPLIT
-    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", "split")
-    assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_SPLIT
-    monkeypatch.setenv("KDA_PREFILL_SCHEDULE", "fused")
-    assert f(40, 64, 2, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
+    with prefill_schedule(None):
+        assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
+        assert f(64, 1 << 16, 32, 128, 64, kda.KDA_BF16, True) == kda.KDA_SCHEDULE_SPLIT
+    with prefill_schedule("split"):
+        assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_SPLIT
+    with prefill_schedule("fused"):
+        assert f(40, 64, 2, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED

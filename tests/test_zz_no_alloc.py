@@ -3,35 +3,27 @@ allocate device memory (it takes its scratch from a static device array in
 the library instead of a caller-provided workspace). Checked through the C
 ABI against kda_prefill, the entry point that takes a workspace, on two
 calls in a row (the second call reuses the array the first one left
-behind). This file is collected last on purpose."""
+behind): both run the same kernels on the same inputs, so their results must
+agree bit for bit; one comparison against the fp64 oracle as well. Device
+errors are read back with kda_noalloc_status. This file is collected last on
+purpose."""
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
+import oracle
 import kimi_delta_attention_rule_gb300 as kda
 from kimi_delta_attention_rule_gb300 import build as kbuild, inputs
+from tests.parity import TOL_BF16, np32, out_err, rel_err
 
 pytestmark = pytest.mark.gpu
-TOL_BF16 = 2e-2
 
 
 def _noalloc_fn():
     kbuild.build()
     lib = kda.load()
-    f = lib.kda_prefill_noalloc
-    P, I32 = ctypes.c_void_p, ctypes.c_int32
-    f.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, I32, I32, I32, I32, I32, I32, P, P, P]
-    f.restype = ctypes.c_int
-    return f
-
-
-def _max_rel(a, b):
-    a = a.double().cpu().numpy()
-    b = b.double().cpu().numpy()
-    rms = float(np.sqrt(np.mean(b ** 2))) or 1.0
-    return float(np.max(np.abs(a - b))) / rms
+    return lib.kda_prefill_noalloc
 
 
 def test_noalloc_matches_workspace_entry_point_twice():
@@ -50,12 +42,37 @@ def test_noalloc_matches_workspace_entry_point_twice():
         fin = torch.full((N, H, 128, 128), float("nan"), dtype=torch.float32, device=dev)
         rc = f(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), b.data_ptr(), x.scale,
                init.data_ptr(), cu.data_ptr(), N, T, H, 128, 64, kda.KDA_BF16, out.data_ptr(),
-               fin.data_ptr(), stream)
+               fin.data_ptr(), ctypes.c_void_p(stream))
         assert rc == kda.KDA_OK, kda.status_string(rc)
-        torch.cuda.synchronize()
-        assert torch.isfinite(out.float()).all() and torch.isfinite(fin).all()
-        assert _max_rel(out, ref_out) <= TOL_BF16
-        assert _max_rel(fin, ref_fin) <= TOL_BF16
+        assert kda.kda_noalloc_status() == kda.KDA_OK
+        assert torch.equal(out, ref_out)
+        assert torch.equal(fin, ref_fin)
+    ro, rf = oracle.prefill(np32(x.q), np32(x.k), np32(x.v), np32(x.g), np32(x.beta), x.scale,
+                            init_state=x.init_state.double().numpy(),
+                            cu_seqlens=x.cu_seqlens.numpy())
+    assert out_err(out, ro) <= TOL_BF16
+    assert rel_err(fin.cpu().numpy(), rf) <= TOL_BF16
+
+
+def test_noalloc_reports_bad_offsets_through_its_status_query():
+    """Offsets that go back and forth are flagged on the device; the caller of
+    the noalloc entry point reads the flag with kda_noalloc_status (which also
+    clears it), and a correct call afterwards reports KDA_OK."""
+    _noalloc_fn()
+    dev = torch.device("cuda:0")
+    T_total, N = 129, 5
+    x = inputs.prefill_inputs([T_total], H=1, io="bf16", seed=32)
+    q, k, v, g, b = (t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta))
+    cu = torch.tensor([0 if i % 2 == 0 else T_total for i in range(N + 1)], dtype=torch.int32,
+                      device=dev)
+    out = torch.full_like(q, 7.0)
+    kda.kda_prefill_noalloc(q, k, v, g, b, x.scale, cu_seqlens=cu, out=out)
+    assert kda.kda_noalloc_status() == kda.KDA_ERR_DEVICE
+    assert kda.kda_noalloc_status() == kda.KDA_OK  # the read cleared it
+    assert torch.all(out == 7.0)  # the call was skipped as a whole
+    good = torch.tensor([0, T_total], dtype=torch.int32, device=dev)
+    kda.kda_prefill_noalloc(q, k, v, g, b, x.scale, cu_seqlens=good, out=out)
+    assert kda.kda_noalloc_status() == kda.KDA_OK
 
 
 def test_noalloc_rejects_bad_arguments_like_kda_prefill():
