@@ -51,8 +51,10 @@ typedef enum {
     KDA_ERR_CUDA = 3,        /* a CUDA launch or runtime call failed */
     KDA_ERR_TIMEOUT = 4,     /* a bounded device-side wait ran out */
     KDA_ERR_DEVICE = 5,      /* the device flagged bad input (e.g. cu_seqlens) */
-    KDA_ERR_TOO_LARGE = 6    /* kda_prefill_noalloc: the sizes need more scratch than its
+    KDA_ERR_TOO_LARGE = 6,   /* kda_prefill_noalloc: the sizes need more scratch than its
                                 static array holds */
+    KDA_ERR_RANGE = 7        /* a bf16 prefill state came out non-finite (inputs outside the
+                                range that kda_prefill states) */
 } kda_status;
 
 typedef enum { KDA_BF16 = 0, KDA_F32 = 1 } kda_dtype;
@@ -74,7 +76,7 @@ int kda_abi_version(void);
  * meaning as in kda_prefill; varlen != 0 when cu_seqlens will be passed, and
  * then T is the packed total). Returns 0 when the sizes are invalid. The
  * workspace holds the device status word, the chunk schedule and, for bf16
- * I/O, one 74,240-byte prepared block per (chunk, head). It must be 256-byte
+ * I/O, one 74,368-byte prepared block per (chunk, head). It must be 256-byte
  * aligned and must not be shared by calls in flight at the same time.
  */
 size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
@@ -106,6 +108,17 @@ size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, in
  * 256-byte aligned. Each call clears its status word on the stream before
  * the kernels run.
  * Pointer alignment: q, k, v, out 16 bytes; g, states 16 bytes.
+ * Range (bf16 I/O): the chunk products that involve keys and queries (their
+ * Gram matrices) run in bf16; the state path (beta v, the pseudo-values, U and
+ * a copy of the state) runs in fp16 for its longer significand, with a
+ * power-of-two scale per chunk for beta v and per value column for the state,
+ * so any magnitude of v and of the initial state up to about 1e20 is handled,
+ * including changes by many orders of magnitude along a sequence. Keys and
+ * queries enter fp16 after the decay weights (k e^{-a}, q e^{a} <= 1 per
+ * factor): their entries and the products |q||k| must stay well below 6e4, as
+ * they do for the L2-normalised keys and queries of a KDA layer. If an fp16
+ * value overflows anyway, the final state comes out non-finite and
+ * kda_workspace_status() reports KDA_ERR_RANGE (never silently).
  * Returns KDA_OK after enqueueing the work on `stream`.
  */
 int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,
@@ -241,8 +254,9 @@ int kda_layer_epilogue(const void *o, const void *gate_raw, const float *norm_we
 
 /*
  * Synchronises `stream`, then reads and clears the device status word of a
- * kda_prefill workspace. Returns KDA_OK, KDA_ERR_DEVICE (malformed
- * cu_seqlens were seen), KDA_ERR_TIMEOUT or KDA_ERR_CUDA.
+ * kda_prefill workspace. Returns KDA_OK, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE
+ * (malformed cu_seqlens were seen), KDA_ERR_RANGE (a final state of the bf16
+ * path was not finite) or KDA_ERR_CUDA, the first that applies in this order.
  */
 int kda_workspace_status(void *workspace, void *stream);
 

@@ -24,6 +24,7 @@ KDA_ERR_CUDA = 3
 KDA_ERR_TIMEOUT = 4
 KDA_ERR_DEVICE = 5
 KDA_ERR_TOO_LARGE = 6
+KDA_ERR_RANGE = 7
 KDA_BF16 = 0
 KDA_F32 = 1
 KDA_SCHEDULE_SPLIT = 0

@@ -91,6 +91,7 @@ const char *kda_status_string(int status) {
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
         case KDA_ERR_DEVICE: return "KDA_ERR_DEVICE";
         case KDA_ERR_TOO_LARGE: return "KDA_ERR_TOO_LARGE";
+        case KDA_ERR_RANGE: return "KDA_ERR_RANGE";
         default: return "KDA_ERR_UNKNOWN";
     }
 }
@@ -322,6 +323,7 @@ int kda_workspace_status(void *workspace, void *stream) {
     if (cudaStreamSynchronize(st) != cudaSuccess) return KDA_ERR_CUDA;
     if (word & kda::kStatusTimeout) return KDA_ERR_TIMEOUT;
     if (word & kda::kStatusBadSeqlens) return KDA_ERR_DEVICE;
+    if (word & kda::kStatusRange) return KDA_ERR_RANGE;
     return KDA_OK;
 }
 

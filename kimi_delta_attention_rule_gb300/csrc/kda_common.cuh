@@ -16,6 +16,7 @@ constexpr float kGMax = 0.0f;
 // Device-side status bits written into the first word of a workspace.
 constexpr uint32_t kStatusBadSeqlens = 1u;
 constexpr uint32_t kStatusTimeout = 2u;
+constexpr uint32_t kStatusRange = 4u;  // a result of the bf16 prefill is not finite
 
 __device__ __forceinline__ float clamp_g(float g) { return fminf(fmaxf(g, kGMin), kGMax); }
 

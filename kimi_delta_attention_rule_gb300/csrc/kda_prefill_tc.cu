@@ -67,8 +67,47 @@ constexpr uint32_t kB3 = kB12 + 128 * 128 * 2;    // fp16 MN-major [k = t'][n]: 
                                                   //   n = 64 + key: k_t' e^{a_C - a_t'}
 constexpr uint32_t kUt = kB3 + 64 * 192 * 2;      // fp16 [j][t], 128-B rows, chunks swizzled: U~^T
 constexpr uint32_t kGam = kUt + 128 * 128;        // fp32 [128] e^{a_C}
-constexpr uint32_t kBlock = kGam + 128 * 4;       // 74240 B
+constexpr uint32_t kNu = kGam + 128 * 4;          // int32 nu: beta v (and so U~) is stored
+                                                  //   scaled by 2^-nu (rest of 128 B unused)
+constexpr uint32_t kBlock = kNu + 128;            // 74368 B
 static_assert(kBlock % 128 == 0, "block size");
+
+// Range of the fp16 operands. Only the Gram operands need bf16's exponent
+// range; the state path (beta v, U~, U, the fp16 copy of the state) runs in
+// fp16 for its longer significand, with power-of-two scales so that any value
+// and state magnitude fits (a power of two moves only the exponent: exact):
+//   K1: beta v is stored as beta v 2^-nu, 2^nu the least power of two above a
+//       bound of max |beta v| over the chunk, so U~ is stored as U~ 2^-nu;
+//   K2: value column j (one TMEM lane) keeps its fp32 state, the fp16 state
+//       copy, U and O in units of 2^sig_j (see recur_chain).
+// e_ceil(x): the least e with |x| < 2^e (-127 for x = 0).
+__device__ __forceinline__ int e_ceil(float x) {
+    const uint32_t u = __float_as_uint(x) & 0x7fffffffu;
+    const int be = (int)(u >> 23);
+    return be == 0 ? (u == 0 ? -127 : -126) : be - 126;
+}
+// 2^e as a float, for |e| <= 126
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((127 + e) << 23); }
+// largest magnitude among eight packed bf16 values, as a float
+__device__ __forceinline__ float max_abs_bf16x8(uint4 p) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&p);
+    const __nv_bfloat162 m = __hmax2(__hmax2(__habs2(h[0]), __habs2(h[1])),
+                                     __hmax2(__habs2(h[2]), __habs2(h[3])));
+    return fmaxf(__low2float(m), __high2float(m));
+}
+// largest |x| of n floats (n a power of two), as a tree
+template <int n>
+__device__ __forceinline__ float max_abs(const float *x) {
+    float m[n / 2];
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) m[i] = fmaxf(fabsf(x[2 * i]), fabsf(x[2 * i + 1]));
+#pragma unroll
+    for (int w = n / 4; w >= 1; w /= 2) {
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    }
+    return m[0];
+}
 
 // U~^T row j holds tokens 0..63; its 16-byte chunk c (tokens 8 c .. 8 c + 7) sits at
 // chunk c ^ (j % 8): K1 writes whole 32-byte sectors, and K2's reads of 8 consecutive
@@ -205,7 +244,7 @@ constexpr uint32_t kOffVs = kOffVb + 64 * 128 * 2;             // bf16 staged v:
 constexpr uint32_t kOffSqe = kOffVs + 2 * kRegion;
 constexpr uint32_t kOffSb3 = kOffSqe + 64 * 128 * 2;
 constexpr uint32_t kPrepSmem = kOffSb3 + 64 * 192 * 2;
-static_assert(128 * 128 + 128 * 4 <= 64 * 192 * 2, "U~^T and e^{a_C} fit the Sb3 staging");
+static_assert(kBlock - kUt <= 64 * 192 * 2, "U~^T, e^{a_C} and nu fit the Sb3 staging");
 // after the Gram products, inside X:
 constexpr uint32_t kOffT = kOffX;                              // fp16 K-major [64][64]: T
 constexpr uint32_t kOffAh = kOffT + 64 * 64 * 2;               // fp16 [64][72]: A below the diagonal blocks
@@ -416,6 +455,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t pbars[4];  // Gram products, W / U~ products, staged g, staged q k v
     __shared__ uint32_t ptmem_slot;
+    __shared__ int sVexp;  // per item: e_ceil of a bound of max |beta v| (atomicMax)
     const uint32_t sbase = smem_u32(smem);
     float *sRef = reinterpret_cast<float *>(smem + kOffRef);
     float *sQsum = reinterpret_cast<float *>(smem + kOffQsum);
@@ -435,6 +475,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         tc::tmem_relinquish();
     }
     if (tid == 0) {
+        sVexp = -127;
         tc::mbar_init(bG, 1);
         tc::mbar_init(bW, 1);
         tc::mbar_init(bInG, 1);
@@ -617,6 +658,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // half of the operands, which runs while the tensor core forms the Gram products
     float xs[2][8], ys[2][8];
     {
+        float bvmax = 0.f;  // >= |beta v| over this thread's values
         const int c0 = op_c0, tl = op_lt;
         const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
 #pragma unroll
@@ -680,7 +722,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             md += __shfl_xor_sync(0xffffffffu, md, 8);
             md += __shfl_xor_sync(0xffffffffu, md, 16);
             if (lane < 8) sMdp[(warp >> 2) * C + t] = md;
+            bvmax = fmaxf(bvmax, fabsf(sBeta[t]) * max_abs_bf16x8(uv[m]));
         }
+        const int ev = __reduce_max_sync(0xffffffffu, e_ceil(bvmax));
+        if (lane == 0) atomicMax(&sVexp, ev);
     }
     tc::fence_async_smem();  // operands -> tensor core
     tc::fence_before_sync();
@@ -711,6 +756,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     }
 
     // ---- the other operands, meanwhile (same thread mapping) --------------------------
+    // beta v is stored as beta v 2^-nu (below 1); nu = 0 for an all-zero chunk
+    const int nu = sVexp == -127 ? 0 : max(-100, min(sVexp, 126));
     {
         const int c0 = op_c0;
         const float *tab = reinterpret_cast<const float *>(smem + kOffTab);
@@ -724,7 +771,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             unpack8_bf16(uq[m], qq);
             unpack8_bf16(uk[m], kk);
             unpack8_bf16(uv[m], vv);
-            const float bt = sBeta[t];
+            const float bt = sBeta[t], btv = bt * exp2i(-nu);  // beta 2^-nu (exact)
             float ea[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) ea[e] = er[e] * xs[m][e];                 // e^{a_t}
@@ -735,7 +782,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             for (int e = 0; e < 8; ++e) o[e] = bt * kk[e] * ea[e];                // beta k e^{a}
             *reinterpret_cast<uint4 *>(smem + kOffKtb + off_mn128(t, c0)) = pack8_f16(o);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) o[e] = bt * vv[e];                        // beta v
+            for (int e = 0; e < 8; ++e) o[e] = btv * vv[e];                       // beta v 2^-nu
             *reinterpret_cast<uint4 *>(smem + kOffVb + off_mn128(t, c0)) = pack8_f16(o);
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * (ec[e] * ys[m][e]);        // k e^{a_C - a}
@@ -987,6 +1034,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         *reinterpret_cast<uint4 *>(su + ut_off(jj, (t0 >> 3) + 1)) = pack8_f16_u(&ru[0][8]);
         if (tid < 128)
             reinterpret_cast<float *>(su + kGam)[tid] = reinterpret_cast<const float *>(smem + kOffGamS)[tid];
+        if (tid == 0) {  // the block's scale; a fresh maximum for the next item
+            *reinterpret_cast<int *>(su + kNu) = nu;
+            sVexp = -127;
+        }
     }
     tc::fence_async_smem();  // W, U~^T, e^{a_C} staging -> bulk stores
     if (ready && it == 0 && tid == kStager) tc::bulk_wait_all();  // published at once, below
@@ -996,7 +1047,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (failed) break;
     if (tid == 0) {
         tc::bulk_s2g(blk + kB12, sbase + kOffSqe, 64 * 256);             // W
-        tc::bulk_s2g(blk + kUt, sbase + kOffSb3, kBlock - kUt);          // U~^T, e^{a_C}
+        tc::bulk_s2g(blk + kUt, sbase + kOffSb3, kBlock - kUt);          // U~^T, e^{a_C}, nu
         tc::bulk_commit();
     }
     if (ready) {
@@ -1048,7 +1099,17 @@ constexpr int kRecThreads = 512;  // thread = (value column j, quarter); all war
 constexpr uint32_t kOffBuf0 = 0;
 constexpr uint32_t kOffBuf1 = kBlock;
 constexpr uint32_t kOffO = 2 * kBlock;               // bf16 [t][j] output staging, 2 chunks
-constexpr uint32_t kRecSmem = kOffO + 2 * 64 * 128 * 2;
+constexpr uint32_t kOffXch = kOffO + 2 * 64 * 128 * 2;  // int [3][4][128]: exponents exchanged
+                                                        //   between the four threads of a lane
+constexpr uint32_t kRecSmem = kOffXch + 3 * 4 * 128 * 4;
+// Scale of the chain (value column j = TMEM lane j keeps its fp32 state, the
+// fp16 state copy, U and O in units of 2^sig_j):
+constexpr int kSigTarget = 10;      // a rescaled lane's largest magnitude lies in [2^9, 2^10)
+constexpr int kSigBandLo = -2;      // the periodic check rescales lanes whose largest
+constexpr int kSigBandHi = 12;      //   magnitude leaves [2^-3, 2^12)
+constexpr int kSigEvery = 4;        // chunks between periodic checks
+constexpr int kSigUpad = 4;         // |U~| of a chunk is taken as below 2^(nu + kSigUpad)
+constexpr int kSigMin = -60, kSigMax = 60;
 static_assert(kRecSmem <= 227 * 1024, "shared memory budget");
 static_assert(kRecThreads == kPrepThreads, "the fused kernel runs both roles");
 // TMEM columns: [0, 64) P^T, [64, 128) O^T, [128, 256) the fp32 state S^T,
@@ -1240,16 +1301,42 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             if (ready && known_set < 1) refresh();
             check_issue(1);
         }
+        // Scale: lane j (value column j) works in units of 2^sig, the same for its
+        // four threads, so that the fp16 values of the chain (U and the state
+        // copy) stay near 2^kSigTarget, far inside fp16, whatever the magnitudes
+        // of v and of the state. sig starts from exact maxima (the initial state,
+        // exchanged between the lane's threads, and the first block's nu). It moves
+        // up at a chunk's start when that chunk's values need it (nu is in the
+        // block; the decision needs no exchange), and every kSigEvery chunks the
+        // exact largest state magnitude of each lane, exchanged along with the next
+        // barrier, brings a lane that left [2^kSigBandLo, 2^kSigBandHi) back to
+        // 2^kSigTarget one chunk later (so that growing and shrinking states keep
+        // their range and precision). None of this adds a barrier or lengthens the
+        // chain beyond a few integer operations; scaling by powers of two is exact.
+        // A non-finite final state is reported (kStatusRange).
+        int *xS = reinterpret_cast<int *>(smem + kOffXch), *xR = xS + 1024;
+        auto lane_max = [&](const int *x) {
+            return max(max(x[j], x[128 + j]), max(x[256 + j], x[384 + j]));
+        };
+        auto clamp_sig = [](int x) { return min(kSigMax, max(kSigMin, x)); };
         // initial state, keys [32 qd, 32 qd + 32) of column j: fp16 copy -> S^T,
         // and Diag(e^{a_C}) S0 (the first chunk's decay) -> TMEM
         float s0[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e)
             s0[e] = init ? init[head_state + (size_t)(32 * qd + e) * 128 + j] : 0.f;
+        xS[qd * 128 + j] = e_ceil(max_abs<32>(s0));
         sync_check();  // the first load was issued (or failed)
         wait(bL0, 0);
+        // both the state and U~ start near 2^kSigTarget (the state from its exact maximum)
+        int sig = clamp_sig(max(lane_max(xS) - kSigTarget,
+                                *reinterpret_cast<const int *>(smem + kOffBuf0 + kNu) + kSigUpad - kSigTarget));
+        float so = scale * exp2i(sig);  // output factor of this lane
         {
             const float *gam0 = reinterpret_cast<const float *>(smem + kOffBuf0 + kGam) + 32 * qd;
+            const float f0 = exp2i(-sig);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) s0[e] *= f0;
             uint32_t w16[16];  // keys 32 qd + 2 c, + 1 -> TMEM column kColSh + 16 qd + c
 #pragma unroll
             for (int c2 = 0; c2 < 16; ++c2) w16[c2] = pack_f16(s0[2 * c2], s0[2 * c2 + 1]);
@@ -1260,25 +1347,54 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             tc::tmem_st16(tlane + kColS + 32 * qd + 16, s0 + 16);
             tc::tmem_wait_st();
         }
-        sync_check();
+        sync_check();  // (xS is written again only after further barriers)
         if (tid == 0 && !failed) issue_mma1(0);
 
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
             const unsigned char *buf = smem + buf_off(c);
 
-            // U^T = U~^T - P^T for t in [16 qd, 16 qd + 16) -> shared (fp16)
+            // U^T = U~^T 2^nu - P^T for t in [16 qd, 16 qd + 16) -> TMEM (fp16), in units of 2^sig
             if (tid == kLoader) {  // while the first product runs
                 if (ready && known_set < c + 1) refresh();
                 check_issue(c + 1);
             }
             wait(bL(c), (uint32_t)((c >> 1) & 1));
+            // this chunk's values may need a larger scale (rare: v grew)
+            const int nu_c = *reinterpret_cast<const int *>(buf + kNu);
+            const int sig_up = clamp_sig(nu_c + kSigUpad - kSigTarget);
+            const bool up = sig_up > sig && !failed;
+            float fu = exp2i(max(-126, min(126, nu_c - sig)));  // U~ 2^nu in units of 2^sig
             wait(bM1, (uint32_t)(c & 1));
             tc::fence_after_sync();
+            uint32_t w8[8];  // tokens 16 qd + 2 c, + 1 -> TMEM column kColU + 8 qd + c
             {
                 uint32_t pr[1][16];
                 tc::tmem_ld_cols<1>(tlane + kColP + 16 * qd, pr);
-                uint32_t w8[8];  // tokens 16 qd + 2 c, + 1 -> TMEM column kColU + 8 qd + c
+                if (__any_sync(0xffffffffu, up)) {  // TMEM accesses are warp-wide
+                    // P^T (registers), O~^T and the state (TMEM) into units of 2^sig_up
+                    const float sc = up ? exp2i(sig - sig_up) : 1.f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pr[0][e] = __float_as_uint(__uint_as_float(pr[0][e]) * sc);
+                    uint32_t ro[1][16], rs[2][16];
+                    tc::tmem_ld_cols<1>(tlane + kColO + 16 * qd, ro);
+                    tc::tmem_ld_cols<2>(tlane + kColS + 32 * qd, rs);
+                    float vo[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) vo[e] = __uint_as_float(ro[0][e]) * sc;
+                    tc::tmem_st16(tlane + kColO + 16 * qd, vo);
+#pragma unroll
+                    for (int gi = 0; gi < 2; ++gi) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) vo[e] = __uint_as_float(rs[gi][e]) * sc;
+                        tc::tmem_st16(tlane + kColS + 32 * qd + 16 * gi, vo);
+                    }
+                    if (up) {
+                        sig = sig_up;
+                        so = scale * exp2i(sig);
+                        fu = exp2i(max(-126, min(126, nu_c - sig)));
+                    }
+                }
 #pragma unroll
                 for (int gi = 0; gi < 2; ++gi) {
                     const uint4 u = *reinterpret_cast<const uint4 *>(buf + ut_off(j, 2 * qd + gi));
@@ -1287,8 +1403,8 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                     for (int e = 0; e < 4; ++e) {
                         const float2 a = __half22float2(hu[e]);
                         const int t = 8 * gi + 2 * e;
-                        w8[4 * gi + e] = pack_f16(a.x - __uint_as_float(pr[0][t]),
-                                                  a.y - __uint_as_float(pr[0][t + 1]));
+                        w8[4 * gi + e] = pack_f16(fmaf(a.x, fu, -__uint_as_float(pr[0][t])),
+                                                  fmaf(a.y, fu, -__uint_as_float(pr[0][t + 1])));
                     }
                 }
                 tc::tmem_st8u(tlane + kColU + 8 * qd, w8);
@@ -1301,6 +1417,14 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 check_issue(c + 1);
             }
             if (c > 0) write_out(c - 1);  // meanwhile, the previous chunk's output rows
+            // the next chunk's scale: the periodic check, from the exact maxima
+            // shared before the previous barrier (absolute exponents)
+            int sig_next = sig;
+            if (c % kSigEvery == 0 && c > 0) {
+                const int r = lane_max(xR) - sig;  // largest |S_c| in units of 2^sig
+                if (r < kSigBandLo || r > kSigBandHi)  // (not below what this chunk's values need)
+                    sig_next = max(sig_up, clamp_sig(r + sig - kSigTarget));
+            }
 
             // new state (keys [32 qd, +32)) and this chunk's O (t in [16 qd, +16))
             wait(bM2, (uint32_t)(c & 1));
@@ -1312,30 +1436,24 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO + (c & 1) * 16384);
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(scale * __uint_as_float(orr[0][e]));
+                    sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(so * __uint_as_float(orr[0][e]));
+            }
+            float sf[32];  // the new state, in units of 2^sig_next
+            {
+                const float f = exp2i(sig - sig_next);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) sf[e] = __uint_as_float(sr[e >> 4][e & 15]);
+                if (sig_next != sig) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) sf[e] *= f;
+                }
             }
             if (c + 1 < nchunks) {  // the fp16 copy of the new state: the next first product's A
                 uint32_t w16[16];
 #pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2)
-                    w16[c2] = pack_f16(__uint_as_float(sr[c2 >> 3][(2 * c2) & 15]),
-                                       __uint_as_float(sr[c2 >> 3][(2 * c2 + 1) & 15]));
+                for (int c2 = 0; c2 < 16; ++c2) w16[c2] = pack_f16(sf[2 * c2], sf[2 * c2 + 1]);
                 tc::tmem_st16u(tlane + kColSh + 16 * qd, w16);
                 tc::tmem_wait_st();
-            } else if (fin) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    fin[head_state + (size_t)(32 * qd + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
-            }
-            if (ra.snaps) {  // the state after every snap_interval tokens of the sequence
-                const int done = min((c + 1) * C, t1 - t0);
-                const int si = done / ra.snap_interval - 1;
-                if (done % ra.snap_interval == 0 && si < ra.snap_max) {
-                    float *dst = ra.snaps + (((size_t)n * ra.snap_max + si) * H + h) * 128 * 128;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        dst[(size_t)(32 * qd + e) * 128 + j] = __uint_as_float(sr[e >> 4][e & 15]);
-                }
             }
             // this chunk's buffer is no longer read: chunk c + 2 may use it; chunk
             // c + 1 must be on its way before anyone waits for it
@@ -1348,18 +1466,45 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
             // this chunk's buffer is free: without flags, fetch chunk c + 2 into it now
             if (tid == kLoader) check_issue(c + 2);  // known to exist (or no flags)
 
-
-            // while the next product runs: pre-scale the state by the next chunk's decay
+            // while the next product runs: the state out (last chunk, snapshots), and
+            // pre-scaled by the next chunk's decay
+            if (c + 1 == nchunks) {
+                const float fs = exp2i(sig_next);
+                bool finite = true;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float x = sf[e] * fs;
+                    finite = finite && isfinite(x);
+                    if (fin) fin[head_state + (size_t)(32 * qd + e) * 128 + j] = x;
+                }
+                if (!finite) atomicOr(ra.status, kStatusRange);  // an fp16 value overflowed
+            }
+            if (ra.snaps) {  // the state after every snap_interval tokens of the sequence
+                const int done = min((c + 1) * C, t1 - t0);
+                const int si = done / ra.snap_interval - 1;
+                if (done % ra.snap_interval == 0 && si < ra.snap_max) {
+                    float *dst = ra.snaps + (((size_t)n * ra.snap_max + si) * H + h) * 128 * 128;
+                    const float fs = exp2i(sig_next);
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) dst[(size_t)(32 * qd + e) * 128 + j] = sf[e] * fs;
+                }
+            }
             if (c + 1 < nchunks) {
                 const float *gam = reinterpret_cast<const float *>(smem + buf_off(c + 1) + kGam) + 32 * qd;
 #pragma unroll
                 for (int gi = 0; gi < 2; ++gi) {
                     float vv[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) vv[e] = __uint_as_float(sr[gi][e]) * gam[16 * gi + e];
+                    for (int e = 0; e < 16; ++e) vv[e] = sf[16 * gi + e] * gam[16 * gi + e];
                     tc::tmem_st16(tlane + kColS + 32 * qd + 16 * gi, vv);
                 }
+                if ((c + 1) % kSigEvery == 0)  // the periodic check's exact maxima
+                    xR[qd * 128 + j] = e_ceil(max_abs<32>(sf)) + sig_next;
                 tc::tmem_wait_st();
+            }
+            if (sig_next != sig) {
+                sig = sig_next;
+                so = scale * exp2i(sig);
             }
         }
         write_out(nchunks - 1);  // staged before the last barrier of the loop

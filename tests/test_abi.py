@@ -36,20 +36,22 @@ def test_exports_every_declared_symbol(lib):
 
 def test_status_strings(lib):
     for code, name in [(0, "KDA_OK"), (1, "KDA_ERR_INVALID_ARG"), (2, "KDA_ERR_UNSUPPORTED"),
-                       (3, "KDA_ERR_CUDA"), (4, "KDA_ERR_TIMEOUT"), (5, "KDA_ERR_DEVICE")]:
+                       (3, "KDA_ERR_CUDA"), (4, "KDA_ERR_TIMEOUT"), (5, "KDA_ERR_DEVICE"),
+                       (6, "KDA_ERR_TOO_LARGE"), (7, "KDA_ERR_RANGE")]:
         assert kda.status_string(code) == name
     assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
     assert lib.kda_abi_version() == 100
 
 
 def test_workspace_size(lib):
-    # bf16: status word + one 74240-byte prepared block and one 4-byte ready
+    # bf16: status word + one prepared block (BLOCK bytes) and one 4-byte ready
     # flag per (chunk, head)
-    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 128 * 32 * 74240
-    assert kda.kda_prefill_workspace_size(4, 100, 2, 128, 64, kda.KDA_BF16) >= 4 * 2 * 2 * 74240
+    BLOCK = 74368
+    assert kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16) >= 128 * 32 * BLOCK
+    assert kda.kda_prefill_workspace_size(4, 100, 2, 128, 64, kda.KDA_BF16) >= 4 * 2 * 2 * BLOCK
     # packed: T is the total; one spare chunk slot per sequence at most
     vl = kda.kda_prefill_workspace_size(64, 1 << 20, 32, 128, 64, kda.KDA_BF16, varlen=True)
-    assert ((1 << 20) // 64) * 32 * 74240 <= vl <= ((1 << 20) // 64 + 64) * 32 * 74244 + 4096
+    assert ((1 << 20) // 64) * 32 * BLOCK <= vl <= ((1 << 20) // 64 + 64) * 32 * (BLOCK + 4) + 4096
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_F32) >= 256
     assert kda.kda_prefill_workspace_size(1, 64, 2, 64, 64, kda.KDA_BF16) == 0      # D != 128
     assert kda.kda_prefill_workspace_size(1, 64, 2, 128, 16, kda.KDA_BF16) == 0     # chunk
