@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -237,6 +238,146 @@ def cpu_baseline(budget_s=10.0, max_reps=20):
                       % (reps, total)}
 
 
+def time_prefill_calls(call, stream, min_s=0.5, warm=2):
+    """ms per call of `call()` on `stream` (CUDA events), over a number of calls
+    fixed from one timed warm-up call so that the timed region lasts about min_s."""
+    import torch
+    for _ in range(warm):
+        call()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = max(3, math.ceil(min_s * 1e3 / e0.elapsed_time(e1)))
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / n, n
+
+
+def oracle_sample_rate(x, seqs, heads, max_tokens, init=None):
+    """fp64 oracle head-tokens/s on a slice of a workload (host cores)."""
+    import numpy as np
+    import oracle
+    oracle.build()
+    cu = [0] + list(np.cumsum(x.lens))
+    parts = [(cu[n], min(cu[n + 1], cu[n] + max_tokens)) for n in seqs]
+    f = lambda t: np.concatenate([t[a:b][:, heads].float().cpu().numpy() for a, b in parts])
+    lens = [b - a for a, b in parts]
+    cus = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    ini = None if init is None else init[seqs][:, heads].double().cpu().numpy()
+    args = (f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta), x.scale)
+    t0 = time.perf_counter()
+    oracle.prefill(*args, init_state=ini, cu_seqlens=cus)
+    sec = time.perf_counter() - t0
+    units = sum(lens) * len(heads)
+    return {"value": units / sec / 1e6, "unit": "Mtok/s", "cores": oracle.default_threads(),
+            "kind": "oracle", "sample": "%d tokens x %d heads of %d sequence(s), %.2f s"
+            % (max(lens), len(heads), len(seqs), sec)}
+
+
+def lpt_tail(chunks, nsm, longest_first=True):
+    """Modelled share of the recurrence kernel's time in which some SMs are idle:
+    chains of the given chunk counts started in order (longest first, or as
+    given) on nsm SMs, one chain per SM at a time: 1 - total / (nsm * makespan)."""
+    import heapq
+    load = [0] * nsm
+    heapq.heapify(load)
+    for c in (sorted(chunks, reverse=True) if longest_first else chunks):
+        heapq.heappush(load, heapq.heappop(load) + c)
+    span = max(load)
+    return 1.0 - sum(chunks) / (nsm * span) if span else 0.0
+
+
+def bench_workloads(args, world, rank, dev, stream, peaks, peak_src):
+    """The append-prefill (H=96) and packed varlen (64 sequences) workloads:
+    Mtok/s, HBM roofline on minimal bytes, the pages' FLOP count against the
+    bf16 peak, the schedule, and a sampled oracle rate."""
+    import torch
+    import kimi_delta_attention_rule_gb300 as kda
+    from kimi_delta_attention_rule_gb300 import inputs
+    nsm = torch.cuda.get_device_properties(dev).multi_processor_count
+    res = {}
+
+    def line(name, desc, T_total, H, N, ms, calls, sched, extra):
+        units = T_total * H * world
+        state_bytes = 2 * N * H * D * D * 4  # initial state read, final state written
+        byts = prefill_bytes_per_head_token() * T_total * H + state_bytes
+        chunks = extra.pop("chunk_heads")
+        gbs = byts / (ms * 1e-3) / 1e9
+        tf = prefill_flops_per_chunk() * chunks / (ms * 1e-3) / 1e12
+        res[name] = dict(workload=desc, value=units / (ms * 1e-3) / 1e6, unit="Mtok/s",
+                         ms_per_call=ms, calls_timed=calls,
+                         schedule={0: "split", 1: "fused"}[sched],
+                         roofline={"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                                   "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                                   "peak_source": peak_src, "algorithmic_bytes_per_launch": byts},
+                         tensor={"tflops_pages_count": tf, "peak": peaks["bf16_tflops"],
+                                 "frac": tf / peaks["bf16_tflops"]},
+                         gpu_launches=calls * (1 if sched == 1 else 2) + (calls if N > 1 else 0),
+                         **extra)
+
+    # append: a 32768-token prefill (untimed) gives the state; the 65536 new
+    # tokens are the timed call
+    w = inputs.WORKLOADS["append_h96"]
+    P, Ta, Ha = w["prior"], w["T"], w["H"]
+    x = inputs.prefill_inputs([P + Ta], H=Ha, io="bf16", seed=rank_seed(w["seed"], rank), device=dev)
+    _, s_prior = kda.kda_prefill(x.q[:P], x.k[:P], x.v[:P], x.g[:P], x.beta[:P], x.scale, chunk=C)
+    qa, ka, va, ga, ba = (t[P:] for t in (x.q, x.k, x.v, x.g, x.beta))
+    out = torch.empty_like(qa)
+    fin = torch.empty_like(s_prior)
+    ws = kda.prefill_workspace(qa, None, N=1, T=Ta)
+    sched = kda.kda_prefill_schedule(1, Ta, Ha, D, C, kda.KDA_BF16)
+    ms, n = time_prefill_calls(lambda: kda.kda_prefill(qa, ka, va, ga, ba, x.scale, init_state=s_prior,
+                                                       chunk=C, out=out, final_state=fin,
+                                                       workspace=ws, stream=stream), stream)
+    ms = max_over_ranks(ms, world, dev)
+    assert kda.kda_workspace_status(ws) == kda.KDA_OK
+    extra = {"chunk_heads": Ha * (Ta // C), "workspace_bytes": ws.numel()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        xs = inputs.PrefillInputs(qa, ka, va, ga, ba, None, None, x.scale, [Ta])
+        extra["cpu_oracle"] = oracle_sample_rate(xs, [0], list(range(16)), 4096)
+    line("append", "append_h96: H=96, D=128, fp32 state of a 32768-token prefill, then 65536 "
+         "new bf16 tokens, chunk 64", Ta, Ha, 1, ms, n, sched, extra)
+    del x, s_prior, qa, ka, va, ga, ba, out, fin, ws
+    torch.cuda.empty_cache()
+
+    # varlen: 64 packed sequences, lengths U[1024, 32768], H=32, g near the floor
+    w = inputs.WORKLOADS["varlen64_h32_floor"]
+    lens = inputs.varlen_lengths(w["n_seqs"], w["lo"], w["hi"], seed=w["seed"])
+    x = inputs.prefill_inputs(lens, H=w["H"], io="bf16", seed=rank_seed(w["seed"], rank),
+                              g_mode="floor", init="normal", device=dev)
+    Nv, Hv, Tv = len(lens), w["H"], sum(lens)
+    out = torch.empty_like(x.q)
+    fin = torch.empty_like(x.init_state)
+    ws = kda.prefill_workspace(x.q, x.cu_seqlens)
+    sched = kda.kda_prefill_schedule(Nv, Tv, Hv, D, C, kda.KDA_BF16, True)
+    ms, n = time_prefill_calls(lambda: kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale,
+                                                       init_state=x.init_state,
+                                                       cu_seqlens=x.cu_seqlens, chunk=C, out=out,
+                                                       final_state=fin, workspace=ws,
+                                                       stream=stream), stream)
+    ms = max_over_ranks(ms, world, dev)
+    assert kda.kda_workspace_status(ws) == kda.KDA_OK
+    chunks = [math.ceil(L / C) for L in lens]
+    extra = {"chunk_heads": sum(chunks) * Hv, "workspace_bytes": ws.numel(),
+             "chains": Nv * Hv, "recurrence_tail_share_model": lpt_tail(chunks * Hv, nsm),
+             "recurrence_tail_share_model_in_index_order":
+                 lpt_tail([c for c in chunks for _ in range(Hv)], nsm, longest_first=False),
+             "recurrence_order": "longest first (chunk-count classes)"}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        extra["cpu_oracle"] = oracle_sample_rate(x, [0], list(range(16)), 4096, init=x.init_state)
+    line("varlen", "varlen64_h32_floor: 64 packed sequences, lengths U[1024, 32768] (%d tokens), "
+         "H=32, D=128, bf16, g near the -5 floor, random initial states" % Tv, Tv, Hv, Nv, ms, n,
+         sched, extra)
+    del x, out, fin, ws
+    torch.cuda.empty_cache()
+    return res
+
+
 def ncu_case(args):
     """A single kernel launched warmup + 1 times: the target of ncu captures."""
     import torch
@@ -281,6 +422,10 @@ def main():
     ap.add_argument("--ncu-case", choices=["prefill", "decode", "layer"], default=None,
                     help="run only `warmup` + 1 launches of one kernel (for ncu captures)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"])
+    ap.add_argument("--min-timed-s", type=float, default=1.0,
+                    help="the headline's timed region repeats blocks of K steps for at least this long")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the append (H=96) and varlen (64 sequences) prefill lines")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.ncu_case:
@@ -325,22 +470,34 @@ def main():
         kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, cu_seqlens=None, chunk=C, out=out,
                         final_state=fin, workspace=ws, stream=stream)
 
-    for _ in range(max(3, args.warmup)):
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
         step()
     torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(max(0, args.warmup - 3) + 2):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    est_ms = ev0.elapsed_time(ev1) / (max(0, args.warmup - 3) + 2)
+    # The timed region is `blocks` blocks of exactly K steps each, enough blocks
+    # for at least --min-timed-s seconds (the same count on every rank), so that
+    # the clocks are sampled under load and one short window does not decide.
+    blocks = max(1, math.ceil(args.min_timed_s * 1e3 / (args.steps * est_ms)))
+    blocks = int(max_over_ranks(blocks, world, dev))
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         ev0.record(stream)
-        for _ in range(args.steps):
-            step()
+        for _ in range(blocks):
+            for _ in range(args.steps):
+                step()
         ev1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = ev0.elapsed_time(ev1) / (blocks * args.steps)
     ms = max_over_ranks(ms, world, dev)
     assert kda.kda_workspace_status(ws) == kda.KDA_OK
     units = H * T * world
@@ -555,6 +712,10 @@ def main():
         decode["gpu_launches"] += reps * calls
         del graph, xm, mq, mk, mv, mg, mb, pool, perm, mout
 
+    workloads = None
+    if not args.no_workloads:
+        workloads = bench_workloads(args, world, rank, dev, stream, peaks, peak_src)
+
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
@@ -569,7 +730,8 @@ def main():
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta sigmoid(N), "
                 "g -5*sigmoid(N))",
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": T, "heads": H,
-                   "parallelism": "dp%d" % world,
+                   "parallelism": "dp%d" % world, "timed_blocks_of_K_steps": blocks,
+                   "timed_steps": blocks * args.steps,
                    "l2": "inputs (%.0f MB) larger than L2; no flush" % (
                        (bpt - 2 * D) * H * T / 1e6)},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"],
@@ -583,10 +745,12 @@ def main():
                    "flops_per_launch": flops},
         "e2e": {"value": e2e_val, "unit": "Mtok/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches": blocks * args.steps * launches_per_step,
         "clocks": clocks,
         "decode": decode,
         "layer": layer,
+        "append": (workloads or {}).get("append"),
+        "varlen": (workloads or {}).get("varlen"),
         "cpu_baseline": cpu,
     }
     print(json.dumps(line))

@@ -138,7 +138,11 @@ __device__ __forceinline__ void store_h(unsigned char *base, uint32_t off, float
 }
 
 // Chunk slots: first_chunk[n] = sum_{m < n} ceil(L_m / C), first_chunk[N] = total,
-// first_chunk[N + 1] = the most chunks of one sequence. The offsets are checked
+// first_chunk[N + 1] = the most chunks of one sequence; first_chunk[N + 2 + r]
+// = the sequence that the recurrence kernel runs r-th: longest first, by
+// floor(log2(chunks)) classes (a counting sort; the order within a class does
+// not matter), so that the long chains start in the first wave and the short
+// ones fill the tail. The offsets are checked
 // as a whole (cu[0] = 0, non-decreasing, cu[N] <= T_total): the slot count
 // sized on the host only bounds the blocks of offsets that pass. If they do
 // not, the status word is flagged, first_chunk[N] = 0 and first_chunk[N + 1] =
@@ -150,22 +154,30 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
     __shared__ int32_t part[1024];
     __shared__ int32_t maxc_s;
     __shared__ int bad_s;
+    constexpr int kClasses = 33;  // chunk-count classes: 0 (empty), 1 + floor(log2(chunks))
+    __shared__ int32_t cls_n[kClasses], cls_base[kClasses];
     const int tid = threadIdx.x;
     if (tid == 0) {
         maxc_s = 0;
         bad_s = (cu[0] != 0) || (cu[N] > T_total);
     }
+    if (tid < kClasses) cls_n[tid] = 0;
     __syncthreads();
     const int per = (N + 1023) / 1024;
     const int lo = min(N, tid * per), hi = min(N, lo + per);
+    auto chunks_of = [&](int n) {
+        const int32_t L = cu[n + 1] - cu[n];
+        return L > 0 ? (L + C - 1) / C : 0;
+    };
+    auto class_of = [](int32_t nc) { return nc > 0 ? 32 - __clz(nc) : 0; };
     int32_t s = 0, mc = 0;
     bool bad = false;
     for (int n = lo; n < hi; ++n) {
-        const int32_t L = cu[n + 1] - cu[n];
-        bad |= L < 0;
-        const int32_t nc = L > 0 ? (L + C - 1) / C : 0;
+        bad |= cu[n + 1] < cu[n];
+        const int32_t nc = chunks_of(n);
         s += nc;
         mc = max(mc, nc);
+        atomicAdd(&cls_n[class_of(nc)], 1);
     }
     if (bad) atomicOr(&bad_s, 1);
     if (mc > 0) atomicMax(&maxc_s, mc);
@@ -177,18 +189,27 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
         part[tid] += v;
         __syncthreads();
     }
+    if (tid == 0) {  // classes in descending order: the longest chains first
+        int32_t b = 0;
+        for (int k = kClasses - 1; k >= 0; --k) {
+            cls_base[k] = b;
+            b += cls_n[k];
+        }
+    }
     const bool any_bad = bad_s != 0;
     int32_t run = tid > 0 ? part[tid - 1] : 0;
     for (int n = lo; n < hi; ++n) {
         first_chunk[n] = any_bad ? 0 : run;
-        const int32_t L = cu[n + 1] - cu[n];
-        run += L > 0 ? (L + C - 1) / C : 0;
+        run += chunks_of(n);
     }
     if (tid == 1023) {
         first_chunk[N] = any_bad ? 0 : part[1023];
         first_chunk[N + 1] = any_bad ? -1 : maxc_s;
         if (any_bad) atomicOr(status, kStatusBadSeqlens);
     }
+    __syncthreads();
+    for (int n = lo; n < hi; ++n)
+        first_chunk[N + 2 + atomicAdd(&cls_base[class_of(chunks_of(n))], 1)] = n;
 }
 
 // ============================================================================
@@ -1521,8 +1542,15 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     if (warp == 0) tc::tmem_dealloc(tm, kTmemCols);
 }
 
+// With packed sequences, CTA b runs head b % H of the (b / H)-th sequence in
+// the longest-first order of the schedule.
 __global__ void __launch_bounds__(kRecThreads, 1) recur_kernel(RecArgs ra) {
-    recur_chain(ra, blockIdx.x, nullptr);
+    int chain = blockIdx.x;
+    if (ra.cu) {
+        if (ra.first_chunk[ra.N + 1] < 0) return;  // malformed offsets, already flagged
+        chain = ra.first_chunk[ra.N + 2 + chain / ra.H] * ra.H + chain % ra.H;
+    }
+    recur_chain(ra, chain, nullptr);
 }
 
 // K1 and K2 in one cooperative launch (every CTA resident): CTAs [0, nchains)
@@ -1549,7 +1577,7 @@ long long prefill_slots(int N, long long T, long long T_total, bool varlen) {
 
 size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen) {
     const long long slots = prefill_slots(N, T, T_total, varlen);
-    const size_t sched = varlen ? pad256((size_t)(N + 2) * 4) : 0;
+    const size_t sched = varlen ? pad256((size_t)(2 * N + 2) * 4) : 0;
     return 256 + sched + pad256((size_t)slots * H * 4) + (size_t)slots * H * pf::kBlock;
 }
 
@@ -1655,7 +1683,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     int32_t *first_chunk = nullptr;
     if (varlen) {
         first_chunk = reinterpret_cast<int32_t *>(ws + off);
-        off += pad256((size_t)(N + 2) * 4);
+        off += pad256((size_t)(2 * N + 2) * 4);
     }
     int *ready = reinterpret_cast<int *>(ws + off);
     off += pad256((size_t)nitems * 4);

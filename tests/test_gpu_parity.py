@@ -537,3 +537,14 @@ def test_prefill_schedule_choice():
         assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_SPLIT
     with prefill_schedule("fused"):
         assert f(40, 64, 2, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
+
+
+def test_bf16_split_longest_first_order_many_chains():
+    """More chains than SMs with ragged lengths (the recurrence kernel runs the
+    sequences longest first, by chunk-count classes, including empty ones):
+    every chain's output and final state match the oracle."""
+    gen = np.random.default_rng(5)
+    lens = [int(x) for x in gen.integers(0, 400, size=45)] + [0, 1, 64, 65]
+    x = inputs.prefill_inputs(lens, H=4, io="bf16", seed=23, init="normal")
+    with prefill_schedule("split"):
+        check_prefill(x, 64, TOL_BF16)
