@@ -403,6 +403,17 @@ def ncu_case(args):
                                   device=dev)
         for _ in range(args.warmup + 1):
             kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, chunk=C)
+    elif args.ncu_case == "decode_multi":  # T = 4 tokens per sequence through a permuted pool
+        B, Hd, Tm = args.decode_batch, DECODE["H"], 4
+        xm = inputs.prefill_inputs([Tm] * B, H=Hd, io="bf16", seed=DECODE["seed"] + 5, device=dev)
+        shp = (B, Tm, Hd, D)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(DECODE["seed"] + 6)
+        pool = 0.02 * torch.randn((B, Hd, D, D), generator=gen, device=dev)
+        perm = torch.randperm(B, generator=gen, device=dev).to(torch.int32)
+        for _ in range(args.warmup + 1):
+            kda.kda_decode(xm.q.view(shp), xm.k.view(shp), xm.v.view(shp), xm.g.view(shp),
+                           xm.beta.view(B, Tm, Hd), xm.scale, pool, state_indices=perm)
     else:
         q, k, v, g, beta, state, scale = inputs.decode_inputs(
             B=args.decode_batch, H=DECODE["H"], steps=1, seed=DECODE["seed"], device=dev)
@@ -419,7 +430,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "layer"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_multi", "layer"], default=None,
                     help="run only `warmup` + 1 launches of one kernel (for ncu captures)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"])
     ap.add_argument("--min-timed-s", type=float, default=1.0,

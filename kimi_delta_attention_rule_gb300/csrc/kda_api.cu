@@ -240,7 +240,10 @@ int kda_decode(const void *q, const void *k, const void *v, const float *g, cons
     if (state_indices == nullptr && pool_size < B) return KDA_ERR_INVALID_ARG;
     if (B == 0 || T == 0) return KDA_OK;
     if (!q || !k || !v || !g || !beta || !state_pool || !out) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(state_pool)) return KDA_ERR_INVALID_ARG;
+    // rows of q, k, v (and g per channel) are copied in 16-byte pieces
+    if (!aligned16(state_pool) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+        !aligned16(out) || (g_per_channel && !aligned16(g)))
+        return KDA_ERR_INVALID_ARG;
     NvtxRange range("kda_decode");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e =

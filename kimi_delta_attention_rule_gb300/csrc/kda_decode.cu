@@ -110,6 +110,205 @@ __global__ void __launch_bounds__(kDecThreads, 2)
     for (int r = 0; r < kDecRowsPerWarp; ++r) S4[(w * kDecRowsPerWarp + r) * (kD / 4) + lane] = s[r];
 }
 
+// ---------------------------------------------------------------------------
+// Several tokens per sequence (2 <= T <= kPipeMaxT): the T-token update takes
+// longer than streaming the state, so a CTA that loads, updates and stores one
+// head at a time leaves HBM idle while it computes. decode_pipe_kernel is
+// persistent (two CTAs per SM) and overlaps the two: while a head's T tokens
+// are applied to its state in registers, each thread copies its own 256-byte
+// share of the NEXT head's state (and a share of its input rows) into shared
+// memory with cp.async, and the finished state goes out with plain stores. A
+// thread reads back only the state it copied itself, so that hand-off needs no
+// barrier. Thread mapping as in decode_kernel (warp w: rows [16 w, + 16); lane
+// l: columns [4 l, + 4)); per token, the warps' partial sums S'^T k and S'^T q
+// go to shared memory and all 256 threads finish them (threads 0..127 the
+// sums S'^T k and u, threads 128..255 those of S'^T q and the output), two
+// barriers per token. Arithmetic as in decode_kernel.
+constexpr int kPipeMaxT = 8;
+constexpr int kPipeThreads = 256;
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(smem_dst)),
+                 "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
+
+template <typename IO>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+    decode_pipe_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
+                       const float *__restrict__ g, const IO *__restrict__ beta, float scale,
+                       int B, int T, int H, int g_per_channel, float *__restrict__ pool,
+                       int pool_size, const int32_t *__restrict__ idx, IO *__restrict__ out) {
+    // one token's input row in shared memory: q, k, v (IO), then g (fp32, per channel)
+    const int io_row = kD * (int)sizeof(IO);
+    const int row_bytes = 3 * io_row + (g_per_channel ? kD * 4 : 0);
+    const int buf_bytes = kPipeMaxT * row_bytes;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    float4 *sS = reinterpret_cast<float4 *>(dsm);  // [128 rows][32 float4]: the next state
+    unsigned char *sIn = dsm + kD * kD * 4;        // two input buffers
+    __shared__ float s_kq[kPipeMaxT], s_beta[kPipeMaxT], s_gs[kPipeMaxT];
+    __shared__ __align__(16) float s_a[kPipeMaxT][kD], s_kf[kPipeMaxT][kD], s_qf[kPipeMaxT][kD];
+    __shared__ __align__(16) float s_red[2][kPipeThreads / 32][kD];  // [k, q][warp]
+    __shared__ __align__(16) float s_u[kD];
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nitems = B * H;
+    auto slot_of = [&](int it) { return idx ? idx[it / H] : it / H; };
+    auto valid = [&](int it) {
+        const int sl = slot_of(it);
+        return sl >= 0 && sl < pool_size;
+    };
+    auto next_valid = [&](int it) {  // the first valid item at or after `it` (stride gridDim.x)
+        while (it < nitems && !valid(it)) it += gridDim.x;
+        return it;
+    };
+    // copies of item `it` (pool entry `slot`) issued by this thread: its state
+    // share, and a share of the input rows into buffer `bi`; beta and a scalar
+    // decay go to registers
+    float beta_r = 0.f, gs_r = 0.f;
+    auto prefetch = [&](int it, int slot, int bi) {
+        const int b = it / H, h = it - b * H;
+        const float4 *src = reinterpret_cast<const float4 *>(pool + ((size_t)slot * H + h) * kD * kD);
+#pragma unroll
+        for (int r = 0; r < kDecRowsPerWarp; ++r) {
+            const int o = (w * kDecRowsPerWarp + r) * (kD / 4) + lane;
+            cp_async16(&sS[o], &src[o]);
+        }
+        unsigned char *dst = sIn + bi * buf_bytes;
+        const int per_row = row_bytes / 16, total = T * per_row;
+        for (int c = tid; c < total; c += kPipeThreads) {
+            const int t = c / per_row, o = (c - t * per_row) * 16;
+            const size_t row = ((size_t)b * T + t) * H + h;
+            const void *gsrc;
+            if (o < 3 * io_row) {
+                const IO *base = o < io_row ? q : (o < 2 * io_row ? k : v);
+                gsrc = reinterpret_cast<const unsigned char *>(base + row * kD) + (o % io_row);
+            } else {
+                gsrc = reinterpret_cast<const unsigned char *>(g + row * kD) + (o - 3 * io_row);
+            }
+            cp_async16(dst + t * row_bytes + o, gsrc);
+        }
+        if (tid < T) {
+            const size_t row = ((size_t)b * T + tid) * H + h;
+            beta_r = to_f32(beta[row]);
+            if (!g_per_channel) gs_r = g[row];
+        }
+    };
+
+    // items of this CTA: the current one, and the next one (with its pool entry),
+    // found one item ahead so that the index lookups never delay a prefetch
+    int it = next_valid(blockIdx.x);
+    if (it >= nitems) return;
+    int slot = slot_of(it);
+    prefetch(it, slot, 0);
+    cp_async_commit();
+    int nit = next_valid(it + gridDim.x);
+    int nslot = nit < nitems ? slot_of(nit) : 0;
+    float4 s[kDecRowsPerWarp];
+#pragma unroll 1
+    for (int n = 0; it < nitems; ++n) {
+        const int b = it / H, h = it - b * H;
+        float4 *S4 = reinterpret_cast<float4 *>(pool + ((size_t)slot * H + h) * kD * kD);
+        cp_async_wait_all();
+#pragma unroll
+        for (int r = 0; r < kDecRowsPerWarp; ++r) s[r] = sS[(w * kDecRowsPerWarp + r) * (kD / 4) + lane];
+        if (tid < T) {
+            s_beta[tid] = beta_r;
+            s_gs[tid] = gs_r;
+        }
+        __syncthreads();  // this item's inputs (copied by all threads) are in place
+        const unsigned char *in = sIn + (n & 1) * buf_bytes;
+        if (nit < nitems) prefetch(nit, nslot, (n + 1) & 1);
+        cp_async_commit();
+        // the item after next: its lookups overlap this item's tokens
+        const int nnit = nit < nitems ? next_valid(nit + gridDim.x) : nitems;
+        const int nnslot = nnit < nitems ? slot_of(nnit) : 0;
+        // per token: decays and k, q in fp32; k . q (one warp per token)
+        if (tid < kD) {
+            for (int t = 0; t < T; ++t) {
+                const unsigned char *rw = in + t * row_bytes;
+                const float gv = g_per_channel ? reinterpret_cast<const float *>(rw + 3 * io_row)[tid]
+                                               : s_gs[t];
+                s_a[t][tid] = __expf(clamp_g(gv));
+                s_qf[t][tid] = to_f32(reinterpret_cast<const IO *>(rw)[tid]);
+                s_kf[t][tid] = to_f32(reinterpret_cast<const IO *>(rw + io_row)[tid]);
+            }
+        }
+        if (w < T) {
+            const IO *qt = reinterpret_cast<const IO *>(in + w * row_bytes);
+            const IO *kt = reinterpret_cast<const IO *>(in + w * row_bytes + io_row);
+            float p = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) p += to_f32(kt[lane * 4 + e]) * to_f32(qt[lane * 4 + e]);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if (lane == 0) s_kq[w] = p;
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            float4 rk = make_float4(0.f, 0.f, 0.f, 0.f), rq = rk;
+            const float4 *a4 = reinterpret_cast<const float4 *>(&s_a[t][w * kDecRowsPerWarp]);
+            const float4 *k4 = reinterpret_cast<const float4 *>(&s_kf[t][w * kDecRowsPerWarp]);
+            const float4 *q4 = reinterpret_cast<const float4 *>(&s_qf[t][w * kDecRowsPerWarp]);
+#pragma unroll
+            for (int r4 = 0; r4 < kDecRowsPerWarp / 4; ++r4) {
+                const float4 a = a4[r4], kk = k4[r4], qq = q4[r4];  // broadcasts: 4 rows each
+                const float av[4] = {a.x, a.y, a.z, a.w}, kv[4] = {kk.x, kk.y, kk.z, kk.w};
+                const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float4 &x = s[4 * r4 + e];
+                    x.x *= av[e]; x.y *= av[e]; x.z *= av[e]; x.w *= av[e];
+                    rk.x += x.x * kv[e]; rk.y += x.y * kv[e]; rk.z += x.z * kv[e]; rk.w += x.w * kv[e];
+                    rq.x += x.x * qv[e]; rq.y += x.y * qv[e]; rq.z += x.z * qv[e]; rq.w += x.w * qv[e];
+                }
+            }
+            *reinterpret_cast<float4 *>(&s_red[0][w][lane * 4]) = rk;
+            *reinterpret_cast<float4 *>(&s_red[1][w][lane * 4]) = rq;
+            __syncthreads();
+            // column c = tid % 128: threads below 128 sum S'^T k and form u, the
+            // others sum S'^T q (they write the output once u is known)
+            const int c = tid & (kD - 1), part = tid >> 7;
+            float R = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < kPipeThreads / 32; ++ww) R += s_red[part][ww][c];
+            if (part == 0) {
+                const float vc = to_f32(reinterpret_cast<const IO *>(in + t * row_bytes + 2 * io_row)[c]);
+                s_u[c] = s_beta[t] * (vc - R);
+            }
+            __syncthreads();  // s_u ready; s_red free for the next token
+            if (part == 1)
+                out[(((size_t)b * T + t) * H + h) * kD + c] = from_f32<IO>(scale * (R + s_kq[t] * s_u[c]));
+            const float4 u4 = *reinterpret_cast<const float4 *>(&s_u[lane * 4]);
+#pragma unroll
+            for (int r4 = 0; r4 < kDecRowsPerWarp / 4; ++r4) {
+                const float4 kk = k4[r4];
+                const float kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    float4 &x = s[4 * r4 + e];
+                    x.x += kv[e] * u4.x; x.y += kv[e] * u4.y; x.z += kv[e] * u4.z; x.w += kv[e] * u4.w;
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < kDecRowsPerWarp; ++r) S4[(w * kDecRowsPerWarp + r) * (kD / 4) + lane] = s[r];
+        it = nit;
+        slot = nslot;
+        nit = nnit;
+        nslot = nnslot;
+    }
+    cp_async_wait_all();  // nothing may be in flight when the CTA exits
+}
+
+template <typename IO>
+size_t decode_pipe_smem() {
+    return (size_t)kD * kD * 4 + 2 * (size_t)kPipeMaxT * (3 * kD * sizeof(IO) + kD * 4);
+}
+
 template <typename IO>
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *g,
                           const void *beta, float scale, int B, int T, int H, int g_per_channel,
@@ -117,6 +316,22 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
                           cudaStream_t stream) {
     const long long grid = (long long)B * H;
     if (grid == 0 || T == 0) return cudaSuccess;
+    if (T >= 2 && T <= kPipeMaxT) {
+        const size_t smem = decode_pipe_smem<IO>();
+        int dev = 0, nsm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_pipe_kernel<IO>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const long long pgrid = grid < 2LL * nsm ? grid : 2LL * nsm;
+        decode_pipe_kernel<IO><<<(unsigned)pgrid, kPipeThreads, smem, stream>>>(
+            static_cast<const IO *>(q), static_cast<const IO *>(k), static_cast<const IO *>(v), g,
+            static_cast<const IO *>(beta), scale, B, T, H, g_per_channel, pool, pool_size, idx,
+            static_cast<IO *>(out));
+        return cudaGetLastError();
+    }
     decode_kernel<IO><<<(unsigned)grid, kDecThreads, 0, stream>>>(
         static_cast<const IO *>(q), static_cast<const IO *>(k), static_cast<const IO *>(v), g,
         static_cast<const IO *>(beta), scale, T, H, g_per_channel, pool, pool_size, idx,

@@ -57,11 +57,20 @@ __global__ void __launch_bounds__(128, 1)
         mbar_init(smem_u32(&bar), 1);
         fence_mbar_init();
     }
-    fence_async_smem();
     fence_before_sync();
     __syncthreads();
     fence_after_sync();
     const uint32_t tm = tmem_base;
+    {  // zero every lane of the N result columns: lanes the MMA does not write
+       // (M = 64) then read as 0, not as what an earlier kernel left in TMEM
+        const float zero[16] = {};
+        for (int c = 0; c < N; c += 16) tmem_st16(tm + ((uint32_t)(32 * warp) << 16) + (uint32_t)c, zero);
+        tmem_wait_st();
+    }
+    fence_async_smem();
+    fence_before_sync();
+    __syncthreads();
+    fence_after_sync();
     if (tid == 0) {
         const uint32_t idesc = idesc_f16(M, N, f16, a_mn, b_mn);
         // descriptor fields for B; mn_swap = 1 passes them in the opposite

@@ -144,6 +144,11 @@ def test_decode_multi_argument_validation(lib):
     assert call(args(P=3)) == kda.KDA_ERR_INVALID_ARG         # pool smaller than B, no indices
     assert call(args(T=-1)) == kda.KDA_ERR_INVALID_ARG
     assert call(args(pool=ctypes.c_void_p(0x100004))) == kda.KDA_ERR_INVALID_ARG  # misaligned
+    mis = ctypes.c_void_p(0x100008)  # input rows are copied in 16-byte pieces
+    for name in ("q", "k", "v", "g", "out"):
+        assert call(args(**{name: mis})) == kda.KDA_ERR_INVALID_ARG, name
+    # a scalar decay per (token, head) is read element by element: any alignment
+    assert call(args(g=mis, gpc=0, B=0)) == kda.KDA_OK
     assert call(args(q=None)) == kda.KDA_ERR_INVALID_ARG
     assert call(args(B=0)) == kda.KDA_OK and call(args(T=0)) == kda.KDA_OK  # nothing to do
 

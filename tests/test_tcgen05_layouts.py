@@ -67,7 +67,8 @@ def test_mnmajor_b(lib, N, K):
     """LBO = stride along K, SBO = stride along N, as for K-major tiles."""
     errs = {swap: run(lib, N, K, 1, f16, swap) for swap in (0, 1) for f16 in (0, 1)}
     assert run(lib, N, K, 1, 0, 0) < 1e-5 and run(lib, N, K, 1, 1, 0) < 1e-5
-    assert run(lib, N, K, 1, 1, 1) > 1e-2  # the other field order reads other data
+    # the other field order reads other data (which may decode to inf or NaN)
+    assert not run(lib, N, K, 1, 1, 1) <= 1e-2
 
 
 @pytest.mark.parametrize("N,K", [(16, 128), (32, 128), (128, 64)])
