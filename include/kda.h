@@ -253,6 +253,32 @@ int kda_layer_epilogue(const void *o, const void *gate_raw, const float *norm_we
                        int32_t T_total, int32_t H, int32_t D, int32_t io, void *y, void *stream);
 
 /*
+ * kda_layer_prologue at decode time: T new tokens for each of B sequences,
+ * with the short convolutions' windows carried between calls ("Kimi Linear":
+ * the convolution applies to every token, so a decoding sequence keeps the
+ * last W - 1 projected inputs of q, k and v).
+ *   q_raw, k_raw, v_raw, alpha_raw : io dtype [B, T, H, D]   beta_raw : io dtype [B, T, H]
+ *   conv_state : io dtype [pool_size, 3 (q, k, v), W - 1, H, D], updated in place:
+ *                row r of an entry is the raw input W - 1 - r tokens back (the
+ *                most recent last). A new sequence starts from zeros (the left
+ *                padding of kda_layer_prologue); after a prompt of length L, rows
+ *                hold the prompt's raw inputs L - W + 1 .. L - 1 (zeros before 0).
+ *                May be NULL when W = 1.
+ *   state_indices : DEVICE int32 [B], the pool entry of each sequence, or NULL
+ *                (sequence b uses entry b); an index < 0 or >= pool_size skips
+ *                its sequence (nothing written). Indices must be distinct.
+ *   outputs q, k, v : io dtype [B, T, H, D]; g : fp32 [B, T, H, D]; beta : io dtype [B, T, H]
+ * Weights, arithmetic, alignment and return codes as kda_layer_prologue (the
+ * conv_state rows like the [.., D] rows). B = 0 or T = 0 is a no-op.
+ */
+int kda_layer_prologue_decode(const void *q_raw, const void *k_raw, const void *v_raw,
+                              const void *alpha_raw, const void *beta_raw, const float *conv_q,
+                              const float *conv_k, const float *conv_v, int32_t W, int32_t B,
+                              int32_t T, int32_t H, int32_t D, int32_t io, void *conv_state,
+                              int32_t pool_size, const int32_t *state_indices, void *q, void *k,
+                              void *v, float *g, void *beta, void *stream);
+
+/*
  * Synchronises `stream`, then reads and clears the device status word of a
  * kda_prefill workspace. Returns KDA_OK, KDA_ERR_TIMEOUT, KDA_ERR_DEVICE
  * (malformed cu_seqlens were seen), KDA_ERR_RANGE (a final state of the bf16

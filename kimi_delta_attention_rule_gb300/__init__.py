@@ -35,7 +35,7 @@ EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size"
             "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
             "kda_prefill_schedule", "kda_decode", "kda_prefill_ex", "kda_layer_prologue",
             "kda_layer_epilogue", "kda_prefill_set_schedule", "kda_prefill_noalloc",
-            "kda_noalloc_status")
+            "kda_noalloc_status", "kda_layer_prologue_decode")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,6 +84,8 @@ def load() -> ctypes.CDLL:
         lib.kda_layer_prologue.restype = ctypes.c_int
         lib.kda_layer_epilogue.argtypes = [P, P, P, I32, I32, I32, I32, P, P]
         lib.kda_layer_epilogue.restype = ctypes.c_int
+        lib.kda_layer_prologue_decode.argtypes = [P] * 8 + [I32] * 6 + [P, I32, P] + [P] * 6
+        lib.kda_layer_prologue_decode.restype = ctypes.c_int
         lib.kda_prefill_set_schedule.argtypes = [ctypes.c_int]
         lib.kda_prefill_set_schedule.restype = ctypes.c_int
         lib.kda_prefill_noalloc.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32,
@@ -280,6 +282,37 @@ def kda_layer_prologue(q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q, conv_k,
                                 _ptr(g), _ptr(beta), _stream_ptr(stream))
     if rc != KDA_OK:
         raise KDAError(rc, "kda_layer_prologue")
+    return q, k, v, g, beta
+
+
+def kda_layer_prologue_decode(q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q, conv_k, conv_v,
+                              conv_state, state_indices=None, stream=None):
+    """The layer steps before the operator for T new tokens per sequence (C entry
+    point ``kda_layer_prologue_decode``): rows [B, T, H, D] of projected q, k, v,
+    alpha and beta [B, T, H]; conv_* fp32 [H, D, W]; conv_state [P, 3, W - 1,
+    H, D] in the rows' dtype (updated in place; None when W = 1); state_indices
+    device int32 [B] or None. Returns (q, k, v, g, beta) for ``kda_decode``."""
+    lib = load()
+    io = _io_code(q_raw.dtype)
+    B, T, H, D = q_raw.shape
+    W = conv_q.shape[2]
+    _check_cuda(q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q, conv_k, conv_v, conv_state,
+                state_indices)
+    if conv_state is not None and conv_state.dtype != q_raw.dtype:
+        raise ValueError("conv_state must have the rows' dtype")
+    if state_indices is not None and state_indices.dtype != torch.int32:
+        raise ValueError("state_indices must be int32")
+    P = conv_state.shape[0] if conv_state is not None else B
+    q, k, v = (torch.empty_like(q_raw) for _ in range(3))
+    g = torch.empty((B, T, H, D), dtype=torch.float32, device=q_raw.device)
+    beta = torch.empty_like(beta_raw)
+    rc = lib.kda_layer_prologue_decode(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(alpha_raw),
+                                       _ptr(beta_raw), _ptr(conv_q), _ptr(conv_k), _ptr(conv_v),
+                                       W, B, T, H, D, io, _ptr(conv_state), P,
+                                       _ptr(state_indices), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                       _ptr(beta), _stream_ptr(stream))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_layer_prologue_decode")
     return q, k, v, g, beta
 
 

@@ -40,6 +40,13 @@ cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const vo
 template <typename IO>
 cudaError_t launch_layer_epilogue(const void *o, const void *gate_raw, const float *w,
                                   long long T_total, int H, void *y, cudaStream_t stream);
+template <typename IO>
+cudaError_t launch_layer_prologue_decode(const void *q_raw, const void *k_raw, const void *v_raw,
+                                         const void *alpha_raw, const void *beta_raw,
+                                         const float *wq, const float *wk, const float *wv, int W,
+                                         int B, int T, int H, void *conv_state, int pool_size,
+                                         const int32_t *idx, void *q, void *k, void *v, float *g,
+                                         void *beta, cudaStream_t stream);
 }  // namespace kda
 
 namespace {
@@ -292,6 +299,42 @@ int kda_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
             : kda::launch_layer_prologue<__nv_bfloat16>(q_raw, k_raw, v_raw, alpha_raw, beta_raw,
                                                         conv_q, conv_k, conv_v, W, cu_seqlens, N,
                                                         T_total, H, q, k, v, g, beta, st);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+int kda_layer_prologue_decode(const void *q_raw, const void *k_raw, const void *v_raw,
+                              const void *alpha_raw, const void *beta_raw, const float *conv_q,
+                              const float *conv_k, const float *conv_v, int32_t W, int32_t B,
+                              int32_t T, int32_t H, int32_t D, int32_t io, void *conv_state,
+                              int32_t pool_size, const int32_t *state_indices, void *q, void *k,
+                              void *v, float *g, void *beta, void *stream) {
+    if (B < 0 || T < 0 || H <= 0 || D <= 0 || pool_size < 0) return KDA_ERR_INVALID_ARG;
+    if (io != KDA_BF16 && io != KDA_F32) return KDA_ERR_UNSUPPORTED;
+    if (D != kda::kD || W < 1 || W > 4) return KDA_ERR_UNSUPPORTED;
+    if ((long long)B * T * H > (1LL << 33)) return KDA_ERR_INVALID_ARG;
+    if (state_indices == nullptr && pool_size < B) return KDA_ERR_INVALID_ARG;
+    if (B == 0 || T == 0) return KDA_OK;
+    if (!q_raw || !k_raw || !v_raw || !alpha_raw || !beta_raw || !conv_q || !conv_k || !conv_v ||
+        !q || !k || !v || !g || !beta || (W > 1 && !conv_state))
+        return KDA_ERR_INVALID_ARG;
+    const unsigned a = io == KDA_F32 ? 15u : 7u;  // row pieces of 4 channels
+    for (const void *p : {q_raw, k_raw, v_raw, alpha_raw, static_cast<const void *>(q),
+                          static_cast<const void *>(k), static_cast<const void *>(v),
+                          static_cast<const void *>(conv_state)})
+        if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(g) || !aligned16(conv_q) || !aligned16(conv_k) || !aligned16(conv_v))
+        return KDA_ERR_INVALID_ARG;
+    NvtxRange range("kda_layer_prologue_decode");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const cudaError_t e =
+        io == KDA_F32
+            ? kda::launch_layer_prologue_decode<float>(q_raw, k_raw, v_raw, alpha_raw, beta_raw,
+                                                       conv_q, conv_k, conv_v, W, B, T, H,
+                                                       conv_state, pool_size, state_indices, q, k,
+                                                       v, g, beta, st)
+            : kda::launch_layer_prologue_decode<__nv_bfloat16>(
+                  q_raw, k_raw, v_raw, alpha_raw, beta_raw, conv_q, conv_k, conv_v, W, B, T, H,
+                  conv_state, pool_size, state_indices, q, k, v, g, beta, st);
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -240,6 +240,94 @@ __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
     cp_async_wait<0>();
 }
 
+// Prologue at decode time: T new tokens per sequence, the convolution windows
+// carried between calls in a state pool. One warp per (sequence, head), lane =
+// 4 channels: the W - 1 previous raw inputs of q, k, v come from the sequence's
+// pool entry (conv_state [P][3][W - 1][H][D], io dtype, rows in token order,
+// the most recent last), slide along in registers over the T tokens, and the
+// last W - 1 raw inputs go back to the entry. The arithmetic per token is that
+// of layer_prologue_kernel. A pool index < 0 or >= P skips the sequence.
+template <typename IO, int W>
+__global__ void __launch_bounds__(32 * kLayerRowsPerCta)
+    layer_prologue_decode_kernel(const IO *__restrict__ q_raw, const IO *__restrict__ k_raw,
+                                 const IO *__restrict__ v_raw, const IO *__restrict__ alpha_raw,
+                                 const IO *__restrict__ beta_raw, const float *__restrict__ wq,
+                                 const float *__restrict__ wk, const float *__restrict__ wv,
+                                 int B, int T, int H, IO *__restrict__ conv_state, int pool_size,
+                                 const int32_t *__restrict__ idx, IO *__restrict__ q,
+                                 IO *__restrict__ k, IO *__restrict__ v, float *__restrict__ g,
+                                 IO *__restrict__ beta) {
+    constexpr int WP = W > 1 ? W - 1 : 1;
+    const int lane = threadIdx.x & 31, c0 = 4 * lane;
+    const long long wid = (long long)blockIdx.x * kLayerRowsPerCta + (threadIdx.x >> 5);
+    if (wid >= (long long)B * H) return;
+    const int b = (int)(wid / H), h = (int)(wid % H);
+    const int slot = idx ? idx[b] : b;
+    if (slot < 0 || slot >= pool_size) return;  // padding entry
+    const IO *raw3[3] = {q_raw, k_raw, v_raw};
+    const float *w3[3] = {wq, wk, wv};
+    float wl[3][4 * W];  // [tensor][channel * W + tap]
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int i = 0; i < W; ++i)
+            *reinterpret_cast<float4 *>(&wl[m][4 * i]) =
+                *reinterpret_cast<const float4 *>(w3[m] + ((size_t)h * kD + c0) * W + 4 * i);
+    // the state row of tensor m holding the input i tokens back (1 <= i < W)
+    auto state_row = [&](int m, int i) {
+        return conv_state + ((((size_t)slot * 3 + m) * (W - 1) + (W - 1 - i)) * H + h) * kD + c0;
+    };
+    Raw4<IO> win[3][WP];  // win[m][i - 1]: the input i tokens back, as stored
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int i = 1; i < W; ++i) win[m][i - 1] = ld_raw4<IO>(state_row(m, i));
+    IO *out3[3] = {q, k, v};
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+        const size_t row = ((size_t)b * T + t) * H + h, o = row * kD + c0;
+#pragma unroll
+        for (int m = 0; m < 3; ++m) {
+            const Raw4<IO> cx = ld_raw4<IO>(raw3[m] + o);
+            float x[4], acc[4];
+            cvt4(cx, x);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[e] = wl[m][e * W + W - 1] * x[e];
+#pragma unroll
+            for (int i = 1; i < W; ++i) {
+                float xp[4];
+                cvt4(win[m][i - 1], xp);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] += wl[m][e * W + W - 1 - i] * xp[e];
+            }
+            if (m < 2) {  // q, k: L2 norm over the row
+                const float sc = rsqrtf(
+                    warp_sum(acc[0] * acc[0] + acc[1] * acc[1] + acc[2] * acc[2] + acc[3] * acc[3]) +
+                    kL2Eps);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[e] *= sc;
+            }
+            store4<IO>(out3[m] + o, acc);
+            if (W > 1) {  // slide the window
+#pragma unroll
+                for (int i = WP - 1; i > 0; --i) win[m][i] = win[m][i - 1];
+                win[m][0] = cx;
+            }
+        }
+        float al[4];
+        load4<IO>(alpha_raw + o, al);
+        *reinterpret_cast<float4 *>(g + o) =
+            make_float4(-5.f * sigmoidf_(al[0]), -5.f * sigmoidf_(al[1]), -5.f * sigmoidf_(al[2]),
+                        -5.f * sigmoidf_(al[3]));
+        if (lane == 0) beta[row] = from_f32<IO>(sigmoidf_(to_f32(beta_raw[row])));
+    }
+#pragma unroll
+    for (int m = 0; m < 3; ++m)
+#pragma unroll
+        for (int i = 1; i < W; ++i)
+            *reinterpret_cast<decltype(win[m][i - 1].v) *>(state_row(m, i)) = win[m][i - 1].v;
+}
+
 template <typename IO>
 __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
     layer_epilogue_kernel(const IO *__restrict__ o, const IO *__restrict__ gate_raw,
@@ -287,6 +375,34 @@ cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const vo
 }
 
 template <typename IO>
+cudaError_t launch_layer_prologue_decode(const void *q_raw, const void *k_raw, const void *v_raw,
+                                         const void *alpha_raw, const void *beta_raw,
+                                         const float *wq, const float *wk, const float *wv, int W,
+                                         int B, int T, int H, void *conv_state, int pool_size,
+                                         const int32_t *idx, void *q, void *k, void *v, float *g,
+                                         void *beta, cudaStream_t stream) {
+    const long long warps = (long long)B * H;
+    if (warps == 0 || T == 0) return cudaSuccess;
+    const unsigned grid = (unsigned)((warps + kLayerRowsPerCta - 1) / kLayerRowsPerCta);
+#define KDA_PROLOGUE_DEC(WW)                                                                      \
+    layer_prologue_decode_kernel<IO, WW><<<grid, 32 * kLayerRowsPerCta, 0, stream>>>(            \
+        static_cast<const IO *>(q_raw), static_cast<const IO *>(k_raw),                           \
+        static_cast<const IO *>(v_raw), static_cast<const IO *>(alpha_raw),                       \
+        static_cast<const IO *>(beta_raw), wq, wk, wv, B, T, H, static_cast<IO *>(conv_state),    \
+        pool_size, idx, static_cast<IO *>(q), static_cast<IO *>(k), static_cast<IO *>(v), g,      \
+        static_cast<IO *>(beta))
+    switch (W) {
+        case 1: KDA_PROLOGUE_DEC(1); break;
+        case 2: KDA_PROLOGUE_DEC(2); break;
+        case 3: KDA_PROLOGUE_DEC(3); break;
+        case 4: KDA_PROLOGUE_DEC(4); break;
+        default: return cudaErrorInvalidValue;
+    }
+#undef KDA_PROLOGUE_DEC
+    return cudaGetLastError();
+}
+
+template <typename IO>
 cudaError_t launch_layer_epilogue(const void *o, const void *gate_raw, const float *w,
                                   long long T_total, int H, void *y, cudaStream_t stream) {
     const long long rows = T_total * H;
@@ -306,6 +422,14 @@ template cudaError_t launch_layer_prologue<float>(const void *, const void *, co
 template cudaError_t launch_layer_prologue<__nv_bfloat16>(
     const void *, const void *, const void *, const void *, const void *, const float *,
     const float *, const float *, int, const int32_t *, int, long long, int, void *, void *,
+    void *, float *, void *, cudaStream_t);
+template cudaError_t launch_layer_prologue_decode<float>(
+    const void *, const void *, const void *, const void *, const void *, const float *,
+    const float *, const float *, int, int, int, int, void *, int, const int32_t *, void *, void *,
+    void *, float *, void *, cudaStream_t);
+template cudaError_t launch_layer_prologue_decode<__nv_bfloat16>(
+    const void *, const void *, const void *, const void *, const void *, const float *,
+    const float *, const float *, int, int, int, int, void *, int, const int32_t *, void *, void *,
     void *, float *, void *, cudaStream_t);
 template cudaError_t launch_layer_epilogue<float>(const void *, const void *, const float *,
                                                   long long, int, void *, cudaStream_t);

@@ -209,3 +209,21 @@ def test_testing_entry_point_rejects_bad_arguments(lib):
     assert f(*args, kda.KDA_F32, None, None, None, 0, 50, None) == kda.KDA_ERR_UNSUPPORTED
     assert f(*args, kda.KDA_BF16, None, None, None, 0, 0, None) == kda.KDA_ERR_INVALID_ARG
     assert f(*args, kda.KDA_BF16, None, None, None, 0, 50, None) == kda.KDA_ERR_INVALID_ARG
+
+
+def test_layer_prologue_decode_argument_validation(lib):
+    fake = ctypes.c_void_p(0x100000)
+    f = lib.kda_layer_prologue_decode
+    args = lambda **kw: dict(dict(W=4, B=2, T=1, H=2, D=128, io=0, st=fake, P=2, idx=None,
+                                  p=fake), **kw)
+    call = lambda a: f(a["p"], fake, fake, fake, fake, fake, fake, fake, a["W"], a["B"], a["T"],
+                       a["H"], a["D"], a["io"], a["st"], a["P"], a["idx"], fake, fake, fake, fake,
+                       fake, None)
+    assert call(args(W=5)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(args(D=64)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(args(io=3)) == kda.KDA_ERR_UNSUPPORTED
+    assert call(args(P=1)) == kda.KDA_ERR_INVALID_ARG           # pool smaller than B, no indices
+    assert call(args(st=None)) == kda.KDA_ERR_INVALID_ARG       # W > 1 needs the state
+    assert call(args(st=ctypes.c_void_p(0x100002))) == kda.KDA_ERR_INVALID_ARG  # misaligned
+    assert call(args(p=ctypes.c_void_p(0x100004))) == kda.KDA_ERR_INVALID_ARG
+    assert call(args(B=0)) == kda.KDA_OK and call(args(T=0)) == kda.KDA_OK

@@ -273,6 +273,64 @@ def test_layer_prologue_runs(io, tol, lens, W):
 
 
 @pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+@pytest.mark.parametrize("W", [1, 2, 4])
+def test_layer_prologue_decode(io, tol, W):
+    """The prologue at decode time, with the convolution windows carried in a
+    state pool between calls (one call of 2 tokens, then two of 1), sequences
+    after prompts of 0, 1, 5 and 9 tokens, one padding index: each new token
+    equals the oracle prologue over the whole sequence; the pool entries end
+    holding the last W - 1 raw inputs exactly; unused entries are untouched."""
+    H, P, NEW = 3, 6, 4
+    prompt = [0, 1, 5, 9]
+    idx = [4, 0, -1, 2]
+    B = len(prompt)
+    dt = torch.bfloat16 if io == "bf16" else torch.float32
+    gen = torch.Generator().manual_seed(301 + W)
+    seqs = [[torch.randn(L + NEW, H, 128, generator=gen).to(dt) for _ in range(4)] +
+            [torch.randn(L + NEW, H, generator=gen).to(dt)] for L in prompt]
+    ws = [0.5 * torch.randn(H, 128, W, generator=gen) for _ in range(3)]
+    pool = torch.randn(P, 3, W - 1, H, 128, generator=gen).to(dt)  # garbage in unused entries
+    for b, L in enumerate(prompt):
+        if idx[b] < 0:
+            continue
+        pool[idx[b]].zero_()
+        for m in range(3):
+            for r in range(W - 1):  # row r: the input W - 1 - r tokens back
+                t = L - (W - 1 - r)
+                if t >= 0:
+                    pool[idx[b], m, r] = seqs[b][m][t]
+    pool0 = pool.clone()
+    dpool = pool.to(DEV)
+    didx = torch.tensor(idx, dtype=torch.int32, device=DEV)
+    dws = [w.to(DEV) for w in ws]
+    got = [[] for _ in range(5)]
+    for t0, T in ((0, 2), (2, 1), (3, 1)):
+        pick = lambda m: torch.stack([seqs[b][m][prompt[b] + t0:prompt[b] + t0 + T]
+                                      for b in range(B)]).to(DEV).contiguous()
+        outs = kda.kda_layer_prologue_decode(*(pick(m) for m in range(5)), *dws,
+                                             dpool, state_indices=didx)
+        for m in range(5):
+            got[m].append(outs[m])
+    torch.cuda.synchronize()
+    got = [torch.cat(x, dim=1) for x in got]  # [B, NEW, ...]
+    for b, L in enumerate(prompt):
+        if idx[b] < 0:
+            continue
+        cu = np.array([0, L + NEW], dtype=np.int32)
+        ref = oracle_layer.prologue(*(np32(seqs[b][m]) for m in range(5)), *map(np32, ws), cu)
+        for m in (0, 1, 2, 4):
+            assert out_err(got[m][b], ref[m][L:]) <= tol, (b, m)
+        assert rel_err(got[3][b].cpu().numpy(), ref[3][L:]) <= 1e-5, b
+        for m in range(3):
+            for r in range(W - 1):
+                t = L + NEW - (W - 1 - r)
+                want = seqs[b][m][t] if t >= 0 else torch.zeros(H, 128, dtype=dt)
+                assert torch.equal(dpool[idx[b], m, r].cpu(), want), (b, m, r)
+    unused = [p for p in range(P) if p not in idx]
+    assert torch.equal(dpool[unused].cpu(), pool0[unused])
+
+
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
 def test_layer_epilogue(io, tol):
     gen = torch.Generator().manual_seed(91)
     dt = torch.bfloat16 if io == "bf16" else torch.float32
