@@ -302,6 +302,25 @@ def bench_workloads(args, world, rank, dev, stream, peaks, peak_src):
     nsm = torch.cuda.get_device_properties(dev).multi_processor_count
     res = {}
 
+    def bounded(run, ws_full, N, T, H, varlen, units, ms_full):
+        """The same call with the ring-sized workspace (the fused schedule with
+        per-chain rings of prepared blocks): its plan, time and throughput."""
+        nb = kda.kda_prefill_workspace_size_ring(N, T, H, D, C, kda.KDA_BF16, varlen)
+        if nb == 0 or nb >= ws_full.numel():
+            return {"workspace_bytes": nb, "plan": "full workspace (no smaller plan)"}
+        ws_r = torch.empty(nb, dtype=torch.uint8, device=dev)
+        pl = kda.kda_prefill_plan(N, T, H, D, C, kda.KDA_BF16, varlen, nb)
+        ms_r, n_r = time_prefill_calls(lambda: run(ws_r), stream)
+        ms_r = max_over_ranks(ms_r, world, dev)
+        assert kda.kda_workspace_status(ws_r) == kda.KDA_OK
+        del ws_r
+        return {"workspace_bytes": nb, "ms_per_call": ms_r, "calls_timed": n_r,
+                "value": units / (ms_r * 1e-3) / 1e6, "unit": "Mtok/s",
+                "vs_full_workspace": ms_full / ms_r,
+                "plan": {"schedule": "fused", "groups": pl.groups,
+                         "group_chains": pl.group_chains, "ring": pl.ring},
+                "gpu_launches": n_r * (pl.groups + (1 if varlen else 0))}
+
     def line(name, desc, T_total, H, N, ms, calls, sched, extra):
         units = T_total * H * world
         state_bytes = 2 * N * H * D * D * 4  # initial state read, final state written
@@ -331,12 +350,13 @@ def bench_workloads(args, world, rank, dev, stream, peaks, peak_src):
     fin = torch.empty_like(s_prior)
     ws = kda.prefill_workspace(qa, None, N=1, T=Ta)
     sched = kda.kda_prefill_schedule(1, Ta, Ha, D, C, kda.KDA_BF16)
-    ms, n = time_prefill_calls(lambda: kda.kda_prefill(qa, ka, va, ga, ba, x.scale, init_state=s_prior,
-                                                       chunk=C, out=out, final_state=fin,
-                                                       workspace=ws, stream=stream), stream)
+    run = lambda w_: kda.kda_prefill(qa, ka, va, ga, ba, x.scale, init_state=s_prior, chunk=C,
+                                      out=out, final_state=fin, workspace=w_, stream=stream)
+    ms, n = time_prefill_calls(lambda: run(ws), stream)
     ms = max_over_ranks(ms, world, dev)
     assert kda.kda_workspace_status(ws) == kda.KDA_OK
-    extra = {"chunk_heads": Ha * (Ta // C), "workspace_bytes": ws.numel()}
+    extra = {"chunk_heads": Ha * (Ta // C), "workspace_bytes": ws.numel(),
+             "bounded_workspace": bounded(run, ws, 1, Ta, Ha, False, Ta * Ha * world, ms)}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         xs = inputs.PrefillInputs(qa, ka, va, ga, ba, None, None, x.scale, [Ta])
         extra["cpu_oracle"] = oracle_sample_rate(xs, [0], list(range(16)), 4096)
@@ -355,15 +375,15 @@ def bench_workloads(args, world, rank, dev, stream, peaks, peak_src):
     fin = torch.empty_like(x.init_state)
     ws = kda.prefill_workspace(x.q, x.cu_seqlens)
     sched = kda.kda_prefill_schedule(Nv, Tv, Hv, D, C, kda.KDA_BF16, True)
-    ms, n = time_prefill_calls(lambda: kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale,
-                                                       init_state=x.init_state,
-                                                       cu_seqlens=x.cu_seqlens, chunk=C, out=out,
-                                                       final_state=fin, workspace=ws,
-                                                       stream=stream), stream)
+    run = lambda w_: kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, init_state=x.init_state,
+                                      cu_seqlens=x.cu_seqlens, chunk=C, out=out, final_state=fin,
+                                      workspace=w_, stream=stream)
+    ms, n = time_prefill_calls(lambda: run(ws), stream)
     ms = max_over_ranks(ms, world, dev)
     assert kda.kda_workspace_status(ws) == kda.KDA_OK
     chunks = [math.ceil(L / C) for L in lens]
     extra = {"chunk_heads": sum(chunks) * Hv, "workspace_bytes": ws.numel(),
+             "bounded_workspace": bounded(run, ws, Nv, Tv, Hv, True, Tv * Hv * world, ms),
              "chains": Nv * Hv, "recurrence_tail_share_model": lpt_tail(chunks * Hv, nsm),
              "recurrence_tail_share_model_in_index_order":
                  lpt_tail([c for c in chunks for _ in range(Hv)], nsm, longest_first=False),
@@ -514,6 +534,27 @@ def main():
     units = H * T * world
     value = units / (ms * 1e-3) / 1e6
     clocks = clk.summary()
+
+    # the same step with the ring-sized workspace (bounded: blocks in per-chain
+    # rings instead of one per chunk)
+    ring_bytes = kda.kda_prefill_workspace_size_ring(1, T, H, D, C, kda.KDA_BF16)
+    bounded_ws = None
+    if 0 < ring_bytes < ws.numel():
+        ws_r = torch.empty(ring_bytes, dtype=torch.uint8, device=dev)
+        pl = kda.kda_prefill_plan(1, T, H, D, C, kda.KDA_BF16, False, ring_bytes)
+        ms_r, n_r = time_prefill_calls(
+            lambda: kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, chunk=C, out=out,
+                                    final_state=fin, workspace=ws_r, stream=stream), stream)
+        ms_r = max_over_ranks(ms_r, world, dev)
+        assert kda.kda_workspace_status(ws_r) == kda.KDA_OK
+        bounded_ws = {"workspace_bytes": ring_bytes, "full_workspace_bytes": ws.numel(),
+                      "ms_per_call": ms_r, "calls_timed": n_r,
+                      "value": H * T * world / (ms_r * 1e-3) / 1e6, "unit": "Mtok/s",
+                      "vs_full_workspace": ms / ms_r,
+                      "plan": {"schedule": "fused", "groups": pl.groups,
+                               "group_chains": pl.group_chains, "ring": pl.ring},
+                      "gpu_launches": n_r * pl.groups}
+        del ws_r
 
     peaks, peak_src = load_peaks()
     tr_pf = measured_traffic("prefill_h32_t8192")
@@ -758,6 +799,7 @@ def main():
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": blocks * args.steps * launches_per_step,
         "clocks": clocks,
+        "bounded_workspace": bounded_ws,
         "decode": decode,
         "layer": layer,
         "append": (workloads or {}).get("append"),

@@ -72,15 +72,52 @@ const char *kda_status_string(int status);
 int kda_abi_version(void);
 
 /*
- * Bytes of device workspace that kda_prefill needs for these sizes (same
- * meaning as in kda_prefill; varlen != 0 when cu_seqlens will be passed, and
- * then T is the packed total). Returns 0 when the sizes are invalid. The
+ * Bytes of device workspace for kda_prefill's fastest plan at these sizes
+ * (same meaning as in kda_prefill; varlen != 0 when cu_seqlens will be passed,
+ * and then T is the packed total). Returns 0 when the sizes are invalid. The
  * workspace holds the device status word, the chunk schedule and, for bf16
- * I/O, one 74,368-byte prepared block per (chunk, head). It must be 256-byte
- * aligned and must not be shared by calls in flight at the same time.
+ * I/O, one 74,368-byte prepared block per (chunk, head) plus (fused schedule)
+ * one ready flag per block: it grows with the number of tokens. It must be
+ * 256-byte aligned and must not be shared by calls in flight at the same time.
+ *
+ * kda_prefill accepts any workspace of at least kda_prefill_workspace_size_min
+ * bytes and runs the fastest plan that it holds (kda_prefill_plan reports
+ * which):
+ *  - at least kda_prefill_workspace_size: the fastest plan;
+ *  - else, at least kda_prefill_workspace_size_ring: the fused schedule with
+ *    its blocks in a ring of up to 16 per chain, chains in groups of the
+ *    modelled best size, one cooperative launch per group. Its size depends on
+ *    the number of chains in a group, not on the sequence lengths (about
+ *    35 MB for a group of 29 chains);
+ *  - else the same with fewer chains per group (the most that fit), down to
+ *    one chain (kda_prefill_workspace_size_min, about 1.2 MB) -- slower.
+ * All plans give bit-identical results. fp32 I/O needs 256 bytes.
  */
 size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
                                   int32_t io, int32_t varlen);
+size_t kda_prefill_workspace_size_ring(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
+                                       int32_t io, int32_t varlen);
+size_t kda_prefill_workspace_size_min(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
+                                      int32_t io, int32_t varlen);
+
+/* The plan that kda_prefill runs for these sizes and workspace size. */
+typedef struct {
+    int32_t schedule;     /* kda_schedule */
+    int32_t groups;       /* fused: cooperative launches, one per group of chains */
+    int32_t group_chains; /* fused: (sequence, head) chains per group */
+    int32_t ring;         /* fused: prepared blocks per chain in its ring; 0 = one per chunk */
+    size_t bytes;         /* workspace bytes that the plan uses */
+} kda_prefill_plan_info;
+
+/*
+ * Writes to *plan the plan that kda_prefill runs for these sizes (as in
+ * kda_prefill_workspace_size) with a workspace of workspace_bytes bytes on the
+ * current device. Returns KDA_OK; KDA_ERR_INVALID_ARG when the sizes are
+ * invalid, plan is NULL or the workspace is below the minimum; KDA_ERR_CUDA
+ * when the device cannot be queried.
+ */
+int kda_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
+                     int32_t varlen, size_t workspace_bytes, kda_prefill_plan_info *plan);
 
 /*
  * Chunked-parallel KDA prefill over N sequences.
@@ -104,9 +141,10 @@ size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, in
  * chunk: tokens per chunk, 64 (bf16 or fp32 I/O) or 16 (fp32 I/O). The
  * result does not depend on the chunk size beyond rounding.
  * scale: multiplies the readout (e.g. 1/sqrt(D)).
- * workspace: device buffer of at least kda_prefill_workspace_size() bytes,
- * 256-byte aligned. Each call clears its status word on the stream before
- * the kernels run.
+ * workspace: device buffer of at least kda_prefill_workspace_size_min()
+ * bytes, 256-byte aligned; the plan depends on its size (see
+ * kda_prefill_workspace_size). Each call clears its status word on the stream
+ * before the kernels run.
  * Pointer alignment: q, k, v, out 16 bytes; g, states 16 bytes.
  * Range (bf16 I/O): the chunk products that involve keys and queries (their
  * Gram matrices) run in bf16; the state path (beta v, the pseudo-values, U and
@@ -166,7 +204,8 @@ int kda_decode_step(const void *q, const void *k, const void *v, const float *g,
 
 /*
  * Kernel schedule that kda_prefill uses for these sizes on the current device
- * (arguments as in kda_prefill_workspace_size):
+ * with a workspace of kda_prefill_workspace_size bytes (arguments as in
+ * kda_prefill_workspace_size):
  *   KDA_SCHEDULE_SPLIT  bf16: the chunk-preparation kernel over all
  *                       (chunk, head) blocks, then the recurrence kernel,
  *                       one CTA per (sequence, head) chain;
@@ -302,8 +341,11 @@ int kda_check_cu_seqlens(const int32_t *cu_seqlens_host, int32_t N, int32_t T_to
  * for such callers only.
  *  - Arguments, layouts, stream semantics and results are those of
  *    kda_prefill without the workspace arguments.
- *  - Sizes whose kda_prefill_workspace_size() exceeds 16 MiB are rejected
- *    with KDA_ERR_TOO_LARGE; nothing is launched.
+ *  - It runs the plan that a 16 MiB workspace gets (kda_prefill_plan with
+ *    workspace_bytes = 16 MiB): the fastest one while it fits, else the
+ *    fused schedule with rings. Sizes whose kda_prefill_workspace_size_min()
+ *    exceeds 16 MiB (only packed batches of about two million sequences) are
+ *    rejected with KDA_ERR_TOO_LARGE; nothing is launched.
  *  - The first call on a device (with that device current) looks up the
  *    array's device address; make that first call before any stream capture.
  *  - All calls share the one array and each call clears its status word

@@ -35,7 +35,15 @@ EXPORTED = ("kda_status_string", "kda_abi_version", "kda_prefill_workspace_size"
             "kda_decode_step", "kda_workspace_status", "kda_check_cu_seqlens",
             "kda_prefill_schedule", "kda_decode", "kda_prefill_ex", "kda_layer_prologue",
             "kda_layer_epilogue", "kda_prefill_set_schedule", "kda_prefill_noalloc",
-            "kda_noalloc_status", "kda_layer_prologue_decode")
+            "kda_noalloc_status", "kda_layer_prologue_decode", "kda_prefill_workspace_size_ring",
+            "kda_prefill_workspace_size_min", "kda_prefill_plan")
+
+
+class PrefillPlanInfo(ctypes.Structure):
+    """kda_prefill_plan_info: the plan that kda_prefill runs."""
+    _fields_ = [("schedule", ctypes.c_int32), ("groups", ctypes.c_int32),
+                ("group_chains", ctypes.c_int32), ("ring", ctypes.c_int32),
+                ("bytes", ctypes.c_size_t)]
 
 _lock = threading.Lock()
 _lib = None
@@ -63,6 +71,12 @@ def load() -> ctypes.CDLL:
         lib.kda_abi_version.restype = ctypes.c_int
         lib.kda_prefill_workspace_size.argtypes = [I32] * 7
         lib.kda_prefill_workspace_size.restype = SZ
+        lib.kda_prefill_workspace_size_ring.argtypes = [I32] * 7
+        lib.kda_prefill_workspace_size_ring.restype = SZ
+        lib.kda_prefill_workspace_size_min.argtypes = [I32] * 7
+        lib.kda_prefill_workspace_size_min.restype = SZ
+        lib.kda_prefill_plan.argtypes = [I32] * 7 + [SZ, ctypes.POINTER(PrefillPlanInfo)]
+        lib.kda_prefill_plan.restype = ctypes.c_int
         lib.kda_prefill.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32, I32, I32, I32, P, P,
                                     P, SZ, P]
         lib.kda_prefill.restype = ctypes.c_int
@@ -141,6 +155,29 @@ def kda_prefill_workspace_size(N: int, T: int, H: int, D: int, chunk: int, io: i
     return int(load().kda_prefill_workspace_size(N, T, H, D, chunk, io, int(bool(varlen))))
 
 
+def kda_prefill_workspace_size_ring(N: int, T: int, H: int, D: int, chunk: int, io: int,
+                                    varlen: bool = False) -> int:
+    return int(load().kda_prefill_workspace_size_ring(N, T, H, D, chunk, io, int(bool(varlen))))
+
+
+def kda_prefill_workspace_size_min(N: int, T: int, H: int, D: int, chunk: int, io: int,
+                                   varlen: bool = False) -> int:
+    return int(load().kda_prefill_workspace_size_min(N, T, H, D, chunk, io, int(bool(varlen))))
+
+
+def kda_prefill_plan(N: int, T: int, H: int, D: int, chunk: int, io: int, varlen: bool,
+                     workspace_bytes: int) -> PrefillPlanInfo:
+    """The plan kda_prefill runs for these sizes and workspace size (C entry
+    point ``kda_prefill_plan``); raises on invalid sizes or a workspace below
+    the minimum."""
+    info = PrefillPlanInfo()
+    rc = int(load().kda_prefill_plan(N, T, H, D, chunk, io, int(bool(varlen)),
+                                     int(workspace_bytes), ctypes.byref(info)))
+    if rc != KDA_OK:
+        raise KDAError(rc, "kda_prefill_plan")
+    return info
+
+
 def kda_prefill_schedule(N: int, T: int, H: int, D: int, chunk: int, io: int,
                          varlen: bool = False) -> int:
     """KDA_SCHEDULE_* that kda_prefill uses for these sizes on the current
@@ -161,17 +198,22 @@ def kda_prefill_set_schedule(schedule: int) -> int:
     return prev
 
 
-def prefill_workspace(q, cu_seqlens=None, N=None, T=None, chunk=64):
-    """A device workspace of kda_prefill_workspace_size() bytes for these
-    inputs (torch allocates it; the library never does)."""
+_WS_SIZE = {"fast": kda_prefill_workspace_size, "ring": kda_prefill_workspace_size_ring,
+            "min": kda_prefill_workspace_size_min}
+
+
+def prefill_workspace(q, cu_seqlens=None, N=None, T=None, chunk=64, kind="fast"):
+    """A device workspace for these inputs (torch allocates it; the library
+    never does): kind "fast" = kda_prefill_workspace_size() bytes (the fastest
+    plan), "ring" = kda_prefill_workspace_size_ring() (bounded: blocks in
+    per-chain rings), "min" = kda_prefill_workspace_size_min()."""
     T_total, H, D = q.shape
     if cu_seqlens is not None:
         N, T = cu_seqlens.numel() - 1, T_total
     else:
         N = 1 if N is None else N
         T = T_total // N if T is None else T
-    nbytes = kda_prefill_workspace_size(N, T, H, D, chunk, _io_code(q.dtype),
-                                        cu_seqlens is not None)
+    nbytes = _WS_SIZE[kind](N, T, H, D, chunk, _io_code(q.dtype), cu_seqlens is not None)
     return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
 
 

@@ -22,14 +22,15 @@ cudaError_t launch_prefill_f32(const float *q, const float *k, const float *v, c
                                const int32_t *cu, int N, int T, int T_total, int H, int chunk,
                                int g_per_channel, int snap_interval, int snap_max, float *snaps,
                                float *out, float *fin, uint32_t *status, cudaStream_t stream);
-size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen);
+size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen, int kind);
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const void *beta, float scale, const float *init,
                               const int32_t *cu, int N, int T, int T_total, int H,
                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
-                              void *out, float *fin, unsigned char *ws, unsigned test_wait_ms,
-                              cudaStream_t stream);
-int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen);
+                              void *out, float *fin, unsigned char *ws, size_t ws_bytes,
+                              unsigned test_wait_ms, cudaStream_t stream);
+void prefill_tc_query(int N, long long T, long long T_total, int H, bool varlen, size_t budget,
+                      PrefillPlan &p);
 int prefill_tc_set_schedule(int s);
 template <typename IO>
 cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
@@ -54,11 +55,14 @@ namespace {
 constexpr size_t kWorkspaceBytes = 256;  // device status word, padded to 256 B
 constexpr int32_t kMaxDecodeTokens = 64;  // beyond a chunk, the prefill path is the better one
 
-// Workspace of one call: status word, plus (bf16 path) the chunk schedule and
-// one 74,240-byte prepared block per (chunk, head).
-size_t workspace_bytes_for(int32_t N, int32_t T, int32_t H, int32_t io, bool varlen) {
+// Workspace of one call: status word, plus (bf16 path) the chunk schedule,
+// the fused schedule's flags and the 74,368-byte prepared blocks. kind 1: the
+// fastest plan's size (one block per chunk and head); 2: the ring plan's
+// (blocks in flight per chain, bounded by the group, not the length); 3: the
+// smallest size kda_prefill accepts.
+size_t workspace_bytes_for(int32_t N, int32_t T, int32_t H, int32_t io, bool varlen, int kind) {
     if (io == KDA_F32) return kWorkspaceBytes;
-    return kda::prefill_tc_workspace(N, T, T, H, varlen);
+    return kda::prefill_tc_workspace(N, T, T, H, varlen, kind);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -109,18 +113,48 @@ size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, in
                                   int32_t io, int32_t varlen) {
     long long tt = 0;
     if (check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt) != KDA_OK) return 0;
-    return workspace_bytes_for(N, T, H, io, varlen != 0);
+    return workspace_bytes_for(N, T, H, io, varlen != 0, 1);
+}
+
+size_t kda_prefill_workspace_size_ring(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
+                                       int32_t io, int32_t varlen) {
+    long long tt = 0;
+    if (check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt) != KDA_OK) return 0;
+    return workspace_bytes_for(N, T, H, io, varlen != 0, 2);
+}
+
+size_t kda_prefill_workspace_size_min(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
+                                      int32_t io, int32_t varlen) {
+    long long tt = 0;
+    if (check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt) != KDA_OK) return 0;
+    return workspace_bytes_for(N, T, H, io, varlen != 0, 3);
+}
+
+int kda_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
+                     int32_t varlen, size_t workspace_bytes, kda_prefill_plan_info *plan) {
+    if (plan == nullptr) return KDA_ERR_INVALID_ARG;
+    long long tt = 0;
+    const int rc = check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt);
+    if (rc != KDA_OK) return rc;
+    if (io == KDA_F32) {
+        if (workspace_bytes < kWorkspaceBytes) return KDA_ERR_INVALID_ARG;
+        *plan = kda_prefill_plan_info{KDA_SCHEDULE_DIRECT, 0, 0, 0, kWorkspaceBytes};
+        return KDA_OK;
+    }
+    kda::PrefillPlan p;
+    kda::prefill_tc_query(N, T, tt, H, varlen != 0, workspace_bytes, p);
+    if (p.schedule == -2) return KDA_ERR_INVALID_ARG;
+    if (p.schedule < 0) return KDA_ERR_CUDA;
+    *plan = kda_prefill_plan_info{p.schedule == 1 ? KDA_SCHEDULE_FUSED : KDA_SCHEDULE_SPLIT,
+                                  p.groups, p.group_chains, p.ring, p.bytes};
+    return KDA_OK;
 }
 
 int kda_prefill_schedule(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, int32_t io,
                          int32_t varlen) {
-    long long tt = 0;
-    const int rc = check_prefill_dims(N, T, H, D, chunk, io, varlen != 0, &tt);
-    if (rc != KDA_OK) return -rc;
-    if (io == KDA_F32) return KDA_SCHEDULE_DIRECT;
-    const int s = kda::prefill_tc_schedule(N, T, tt, H, varlen != 0);
-    if (s < 0) return -KDA_ERR_CUDA;
-    return s == 1 ? KDA_SCHEDULE_FUSED : KDA_SCHEDULE_SPLIT;
+    kda_prefill_plan_info p;
+    const int rc = kda_prefill_plan(N, T, H, D, chunk, io, varlen, SIZE_MAX, &p);
+    return rc == KDA_OK ? p.schedule : -rc;
 }
 
 int kda_check_cu_seqlens(const int32_t *cu, int32_t N, int32_t T_total) {
@@ -156,7 +190,7 @@ int prefill_impl(const void *q, const void *k, const void *v, const float *g, co
         if ((long long)N * max_snapshots * H > (1LL << 40)) return KDA_ERR_INVALID_ARG;
     }
     if (workspace == nullptr ||
-        workspace_bytes < workspace_bytes_for(N, T, H, io, cu_seqlens != nullptr) ||
+        workspace_bytes < workspace_bytes_for(N, T, H, io, cu_seqlens != nullptr, 3) ||
         (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return KDA_ERR_INVALID_ARG;
     if (N == 0) return KDA_OK;
@@ -185,7 +219,7 @@ int prefill_impl(const void *q, const void *k, const void *v, const float *g, co
         e = kda::launch_prefill_tc(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T,
                                    (int)T_total, H, g_per_channel, si, sm, snapshots, out,
                                    final_state, static_cast<unsigned char *>(workspace),
-                                   test_wait_ms, st);
+                                   workspace_bytes, test_wait_ms, st);
     }
     return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -20,6 +20,14 @@ constexpr uint32_t kStatusRange = 4u;  // a result of the bf16 prefill is not fi
 
 __device__ __forceinline__ float clamp_g(float g) { return fminf(fmaxf(g, kGMin), kGMax); }
 
+// How the bf16 prefill runs for given sizes (host side): schedule 1 = fused
+// (groups of group_chains chains, `groups` cooperative launches; ring > 0:
+// blocks in per-chain rings of that length), 0 = split; bytes of workspace.
+struct PrefillPlan {
+    int schedule, groups, group_chains, ring;
+    size_t bytes;
+};
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

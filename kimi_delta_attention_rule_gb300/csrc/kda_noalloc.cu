@@ -60,8 +60,11 @@ int kda_prefill_noalloc(const void *q, const void *k, const void *v, const float
                         const void *beta, float scale, const float *init_state,
                         const int32_t *cu_seqlens, int32_t N, int32_t T, int32_t H, int32_t D,
                         int32_t chunk, int32_t io, void *out, float *final_state, void *stream) {
+    // the smallest workspace the call accepts; kda_prefill then runs the
+    // fastest plan that the array holds (the ring plan when the one with a
+    // block per chunk does not fit)
     const size_t need =
-        kda_prefill_workspace_size(N, T, H, D, chunk, io, cu_seqlens != nullptr ? 1 : 0);
+        kda_prefill_workspace_size_min(N, T, H, D, chunk, io, cu_seqlens != nullptr ? 1 : 0);
     if (need == 0) {
         // same validation (and error code) as kda_prefill
         return kda_prefill(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk,

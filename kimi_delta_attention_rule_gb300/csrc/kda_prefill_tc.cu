@@ -52,6 +52,7 @@
 
 #include <cuda.h>  // CUtensorMap (the encoder is resolved at run time)
 
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -390,14 +391,42 @@ struct PrepArgs {
     int g_per_channel;  // 0: g is [T_total][H], one decay per token and head
     unsigned char *blocks;
     uint32_t *status;
+    // fused schedule: chain ranks [gbase, gbase + gcount) of the recurrence
+    // order. ring > 0: each chain has a ring of `ring` blocks and progress[i] =
+    // the chunks chain i has loaded; ring = 0: one block per (chunk slot, head)
+    // and flags [head][slot] (nslots slots).
+    int ring, gbase, gcount, nslots;
+    int *progress;
 };
 
 constexpr uint64_t kPrepWaitLimit = 2000000000ull;  // 2 s bound on an MMA completion
 
-// K1 over items first, first + stride, ... (slot-major order, or chunk-major
-// when `ready` is given). The next item's g, q, k, v are staged with cp.async
-// into shared regions that are dead at that point. With `ready`, each finished
-// block is published with a release store of ready[slot H + h] = 1.
+// The chain (n H + h) of rank r in the recurrence order: with packed sequences
+// the schedule's longest-first order of sequences, heads consecutive.
+__device__ __forceinline__ int chain_of_rank(int r, const int32_t *cu, const int32_t *first_chunk,
+                                             int N, int H) {
+    return cu ? first_chunk[N + 2 + r / H] * H + r % H : r;
+}
+// A chain's load progress, read by a producer. A relaxed load: the producer
+// only issues its bulk stores into the ring entry after the loaded value (a
+// control dependency) and a proxy fence, and the chain stored the value after
+// its bulk load from that entry had completed.
+__device__ __forceinline__ int ld_progress(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// K1 over items first, first + stride, ... The next item's g, q, k, v are
+// staged by TMA into shared regions that are dead at that point.
+//   split schedule (`ready` null): slot-major over all (chunk slot, head)
+//     blocks, block (slot H + h);
+//   fused schedule: chunk-major over the group's chains; each finished block is
+//     published with a release store of its ready flag = c + 1. Blocks either
+//     one per (chunk slot, head), flags [head][slot], or (ring mode, bounded
+//     workspace) in a ring per chain: block and flag (i ring + c % ring) of
+//     chain i, and before a block overwrites its ring entry the producer waits
+//     (bounded) until the chain has loaded chunk c - ring.
 __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int stride,
                                           int *ready) {
     const __nv_bfloat16 *__restrict__ q = pa.q, *__restrict__ k = pa.k, *__restrict__ v = pa.v;
@@ -406,25 +435,36 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const int32_t *__restrict__ cu = pa.cu, *__restrict__ first_chunk = pa.first_chunk;
     const int N = pa.N, T = pa.T, H = pa.H;
     unsigned char *__restrict__ blocks = pa.blocks;
-    const bool chunk_major = ready != nullptr;
-    const int nslots = pa.nitems / H;  // ready flags are [head][slot]
+    const bool fused = ready != nullptr;  // chunk-major over a group of chains
+    const int RG = pa.ring;
+    const bool ring = fused && RG > 0;      // blocks in per-chain rings
     int nitems = pa.nitems;
-    if (chunk_major) {
-        const int maxc = cu ? first_chunk[N + 1] : (T + C - 1) / C;
-        nitems = maxc > 0 ? maxc * N * H : 0;
+    if (fused) {  // the most chunks of one chain in the group
+        int maxc = 0;
+        if (!cu) {
+            maxc = (T + C - 1) / C;
+        } else if (first_chunk[N + 1] >= 0) {
+            for (int i = 0; i < pa.gcount; ++i) {
+                const int n = chain_of_rank(pa.gbase + i, cu, first_chunk, N, H) / H;
+                const int L = cu[n + 1] - cu[n];
+                maxc = max(maxc, L > 0 ? (L + C - 1) / C : 0);
+            }
+        }
+        nitems = maxc * pa.gcount;
     }
     // Item cursor: items are visited first, first + stride, ..., so the digits of
     // an item index advance by carries and the loop needs no division:
-    //   chunk-major: idx = (c N + n) H + h   -> (h, mid = n, top = c), radices H, N;
+    //   ring: idx = c gcount + i   -> (h = i, mid = 0, top = c), radices gcount, 1;
     //   slot-major, equal lengths: idx = (n cpn + c) H + h -> (h, mid = c, top = n);
     //   slot-major, packed: idx = slot H + h -> (h, mid = slot), mid without carry.
     struct Cur { int h, mid, top; };
     const int cpn = (T + C - 1) / C;
-    const int R2 = chunk_major ? N : (cu ? 0x7fffffff : cpn);
+    const int HD = fused ? pa.gcount : H;
+    const int R2 = fused ? 1 : (cu ? 0x7fffffff : cpn);
     auto split = [&](int x) {
         Cur r;
-        r.h = x % H;
-        const int q = x / H;
+        r.h = x % HD;
+        const int q = x / HD;
         r.mid = R2 == 0x7fffffff ? q : q % R2;
         r.top = R2 == 0x7fffffff ? 0 : q / R2;
         return r;
@@ -433,8 +473,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     auto advance = [&](Cur r) {
         r.h += sd.h;
         int carry = 0;
-        if (r.h >= H) {
-            r.h -= H;
+        if (r.h >= HD) {
+            r.h -= HD;
             carry = 1;
         }
         r.mid += sd.mid + carry;
@@ -445,26 +485,41 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         r.top += sd.top;
         return r;
     };
-    // the tokens of an item; false if it has none (past a sequence's end)
-    auto tokens = [&](Cur r, int &slot_, int &h_, int &tc_, int &L_) -> bool {
-        h_ = r.h;
+    // An item: its block index and ready-flag index, head, first token and
+    // length, and (fused) the chain in the group and the chunk; false if it has
+    // no tokens (past a sequence's end).
+    struct Item { size_t blk, flag; int h, tc, L, gi, c; };
+    auto tokens = [&](Cur r, Item &it_) -> bool {
         int n, c;
-        if (chunk_major) {
-            n = r.mid;
+        if (fused) {
+            const int chain = chain_of_rank(pa.gbase + r.h, cu, first_chunk, N, H);
+            n = chain / H;
+            it_.h = chain - n * H;
             c = r.top;
-        } else if (!cu) {
-            c = r.mid;
-            n = r.top;
-            if (n >= N) return false;
-        } else if (!slot_to_chunk(r.mid, cu, first_chunk, N, T, n, c)) {
-            return false;
+            it_.gi = r.h;
+        } else {
+            it_.h = r.h;
+            if (!cu) {
+                c = r.mid;
+                n = r.top;
+                if (n >= N) return false;
+            } else if (!slot_to_chunk(r.mid, cu, first_chunk, N, T, n, c)) {
+                return false;
+            }
         }
         const int t0 = cu ? cu[n] : n * T;
         const int t1 = cu ? cu[n + 1] : t0 + T;
-        tc_ = t0 + c * C;
-        if (t1 < t0 || tc_ >= t1) return false;
-        slot_ = (cu ? (chunk_major ? first_chunk[n] + c : r.mid) : n * cpn + c);
-        L_ = min(C, t1 - tc_);
+        it_.tc = t0 + c * C;
+        if (t1 < t0 || it_.tc >= t1) return false;
+        it_.c = c;
+        if (ring) {
+            it_.blk = it_.flag = (size_t)it_.gi * RG + c % RG;
+        } else {
+            const int slot = cu ? (fused ? first_chunk[n] + c : r.mid) : n * cpn + c;
+            it_.blk = (size_t)slot * H + it_.h;
+            it_.flag = (size_t)it_.h * pa.nslots + slot;
+        }
+        it_.L = min(C, t1 - it_.tc);
         return true;
     };
     if (first >= nitems) return;  // no item: no TMEM either
@@ -477,6 +532,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     __shared__ __align__(8) uint64_t pbars[4];  // Gram products, W / U~ products, staged g, staged q k v
     __shared__ uint32_t ptmem_slot;
     __shared__ int sVexp;  // per item: e_ceil of a bound of max |beta v| (atomicMax)
+    __shared__ __align__(16) int sProg[4];  // ring mode: four chains' progress, read ahead
     const uint32_t sbase = smem_u32(smem);
     float *sRef = reinterpret_cast<float *>(smem + kOffRef);
     float *sQsum = reinterpret_cast<float *>(smem + kOffQsum);
@@ -558,11 +614,11 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     int staged = -1;
     unsigned short beta_next = 0;
     {
-        int slot_, h_, tc_, L_;
-        if (tokens(split(first), slot_, h_, tc_, L_)) {
-            stage_g(tc_, h_, L_);
-            stage_qkv(tc_, h_);
-            if (beta_thr) beta_next = load_beta(tc_, h_, L_);
+        Item f;
+        if (tokens(split(first), f)) {
+            stage_g(f.tc, f.h, f.L);
+            stage_qkv(f.tc, f.h);
+            if (beta_thr) beta_next = load_beta(f.tc, f.h, f.L);
             staged = first;
         }
     }
@@ -576,8 +632,20 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // this item's T phase, where that warp is otherwise idle.
     constexpr int kReleaser = kPrepThreads - 32;
     long long pending = -1;
-    auto release = [&](long long idx) {
-        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + idx), "r"(1u) : "memory");
+    uint32_t pending_val = 0;
+    auto release = [&](long long idx, uint32_t val) {
+        asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(ready + idx), "r"(val) : "memory");
+    };
+    // ring mode: wait (bounded) until chain i has loaded chunk `need` - 1; gives
+    // up at once if another party of the launch has given up
+    auto wait_progress = [&](int i, int need) -> bool {
+        if (ld_progress(pa.progress + i) >= need) return true;
+        const uint64_t t0 = tc::globaltimer_ns();
+        while (true) {
+            if (ld_progress(pa.progress + i) >= need) return true;
+            if (*reinterpret_cast<volatile uint32_t *>(pa.status) & kStatusTimeout) return false;
+            if (tc::globaltimer_ns() - t0 > kPrepWaitLimit) return false;
+        }
     };
 
     // operand-phase mapping: channels op_c0 .. + 8 of token op_lt of two 16-token
@@ -596,21 +664,32 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const uint64_t dVb = tc::smem_desc(sbase + kOffVb, 2048, 128);
 
     bool failed = false;
+    int next_slot = -2;  // ring mode: sProg[next_slot] holds the next item's chain progress
+                         // (-1: not needed, -2: not read)
     uint32_t it = 0;  // items done by this CTA (mbarrier phase)
     Cur cur = split(first);
 #pragma unroll 1
     for (int item = first; item < nitems; item += stride, cur = advance(cur)) {
-    int slot, h, tc, L;
-    if (!tokens(cur, slot, h, tc, L)) continue;
+    Item cit;
+    if (!tokens(cur, cit)) continue;
+    const int h = cit.h, tc = cit.tc, L = cit.L;
     if (staged != item) {  // the previous item could not prefetch this one
         stage_g(tc, h, L);
         stage_qkv(tc, h);
         if (beta_thr) beta_next = load_beta(tc, h, L);
     }
-    unsigned char *blk = blocks + ((size_t)slot * H + h) * kBlock;
-    int nslot, nh, ntc, nL;  // the next item of this CTA
+    unsigned char *blk = blocks + cit.blk * kBlock;
+    Item nx;  // the next item of this CTA
     const int nitem = item + stride;
-    const bool has_next = nitem < nitems && tokens(advance(cur), nslot, nh, ntc, nL);
+    const bool has_next = nitem < nitems && tokens(advance(cur), nx);
+    const int nh = nx.h, ntc = nx.tc, nL = nx.L;
+    // ring mode: is this block's ring entry free (chunk c - ring loaded by its
+    // chain)? The staging thread copied the chain's progress into shared memory
+    // at the end of the previous item, with cp.async (which no barrier waits
+    // for), and looks at it where it stores; it waits only if the entry is not
+    // free by then (the value may be a little old, never too new)
+    const int prog_slot = next_slot;
+    next_slot = -1;
 
     if (beta_thr) sBeta[tid - 64] = __bfloat162float(__ushort_as_bfloat16(beta_next));
     if (!gpc && tid < C) reinterpret_cast<float *>(smem + kOffGs)[tid] = gs_next;
@@ -895,9 +974,29 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     failed = __syncthreads_or(failed) != 0;
     tc::fence_after_sync();
     if (failed) break;
+    // The previous item's block is complete (both halves were awaited before the
+    // barrier): an idle lane publishes it now, before the staging thread may wait
+    // for this item's ring entry, so that no producer waits while holding a
+    // finished block back (that is what keeps the ring waits from deadlocking).
+    if (pending >= 0 && tid == kReleaser) {
+        asm volatile("fence.proxy.async.global;\n" ::: "memory");
+        release(pending, pending_val);
+    }
     if (tid == kStager) {  // (thread 0 and the diagonal-block warps go on to the T phase)
-        tc::bulk_s2g(blk + kB12 + 64 * 256, sbase + kOffSqe, 64 * 256);  // q e^{a}
-        tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);          // [M ; k e^{a_C - a}]
+        // ring mode: this block's ring entry must have been loaded by its chain
+        if (ring && cit.c >= RG) {
+            int seen = -1;
+            if (prog_slot >= 0) {
+                asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+                seen = *reinterpret_cast<volatile int *>(&sProg[prog_slot]);
+            }
+            if (seen < cit.c - RG + 1 && !wait_progress(cit.gi, cit.c - RG + 1)) failed = true;
+        }
+        if (!failed) {
+            if (ring) asm volatile("fence.proxy.async.global;\n" ::: "memory");
+            tc::bulk_s2g(blk + kB12 + 64 * 256, sbase + kOffSqe, 64 * 256);  // q e^{a}
+            tc::bulk_s2g(blk + kB3, sbase + kOffSb3, 64 * 192 * 2);          // [M ; k e^{a_C - a}]
+        }
         tc::bulk_commit();
     }
     if (has_next) {  // the next item's q, k, v are on their way
@@ -963,10 +1062,6 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(rr + 8, cc2)) = pack_f16(-acc[nt][2], -acc[nt][3]);
             }
         };
-        if (pending >= 0 && tid == kReleaser) {  // idle here: publish the previous item's block
-            asm volatile("fence.proxy.async.global;\n" ::: "memory");
-            release(pending);
-        }
         if (warp < 2) {
             const int i = 1 + 2 * warp, j = i - 1;
             float xacc[2][4] = {};
@@ -1067,19 +1162,28 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     tc::fence_after_sync();
     if (failed) break;
     if (tid == 0) {
+        if (ring) asm volatile("fence.proxy.async.global;\n" ::: "memory");  // after the ring wait
         tc::bulk_s2g(blk + kB12, sbase + kOffSqe, 64 * 256);             // W
         tc::bulk_s2g(blk + kUt, sbase + kOffSb3, kBlock - kUt);          // U~^T, e^{a_C}, nu
         tc::bulk_commit();
+    }
+    if (ring && has_next && nx.c >= RG && tid == kStager) {  // 16 bytes through L2
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n"
+                     "cp.async.commit_group;\n" ::"r"(smem_u32(sProg)),
+                     "l"(pa.progress + (nx.gi & ~3))
+                     : "memory");
+        next_slot = nx.gi & 3;
     }
     if (ready) {
         if (it == 0) {  // the chains wait for the first blocks: publish this one at once
             if (tid == 0) {
                 tc::bulk_wait_all();
                 asm volatile("fence.proxy.async.global;\n" ::: "memory");
-                release((long long)h * nslots + slot);
+                release((long long)cit.flag, (uint32_t)cit.c + 1u);
             }
         } else {
-            pending = (long long)h * nslots + slot;
+            pending = (long long)cit.flag;
+            pending_val = (uint32_t)cit.c + 1u;
         }
     }
     ++it;
@@ -1097,9 +1201,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         tc::bulk_wait_all();
         if (!failed && pending >= 0) {  // the last item of this CTA
             asm volatile("fence.proxy.async.global;\n" ::: "memory");
-            release(pending);
+            release(pending, pending_val);
         }
     }
+    if (tid == kStager) asm volatile("cp.async.wait_group 0;\n" ::: "memory");  // progress reads
     if (failed && n_staged > 0) {  // staged copies still in flight: the last phase issued
         tc::mbar_wait(bInG, (n_staged - 1) & 1u, 10000000ull);
         tc::mbar_wait(bInQKV, (n_staged - 1) & 1u, 10000000ull);
@@ -1152,7 +1257,10 @@ struct RecArgs {
     float *fin;
     float *snaps;  // [N][snap_max][H][128][128], or null
     int snap_interval, snap_max;
-    int nslots;  // chunk slots: the ready flags are [head][slot]
+    int ring;        // ring > 0: blocks (gi ring + c % ring), flags ready[gi ring + c % ring] = c + 1;
+                     // ring = 0: blocks (slot H + h), flags ready[h nslots + slot] = c + 1
+    int nslots;
+    int *progress;   // ring > 0: progress[gi] = chunks of this chain loaded
     uint32_t *status;
     unsigned long long wait_ns;  // bound on every wait of a chain (ns)
 };
@@ -1168,9 +1276,12 @@ __device__ __forceinline__ uint4 flags4_acquire(const int *f) {
 }
 
 
-// K2 for one chain (sequence n, head h). With `ready`, the block of chunk slot
-// s is loaded only after ready[s H + h] is set by its producer.
-__device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const int *ready) {
+// K2 for one chain (sequence n, head h). Split schedule (`ready` null): the
+// blocks of all chunks are in place. Fused: chunk c's block is loaded once its
+// ready flag = c + 1; in ring mode this chain is number gi of its group, chunk
+// c's block and flag are ring entry (gi ring + c % ring), and progress[gi]
+// tells the producers which entries may be overwritten.
+__device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi, const int *ready) {
     const int32_t *__restrict__ cu = ra.cu;
     const int N = ra.N, T = ra.T, H = ra.H;
     const float scale = ra.scale;
@@ -1211,8 +1322,12 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     const uint32_t tlane = tm + ((uint32_t)(32 * (warp & 3)) << 16);
 
     const size_t head_state = ((size_t)n * H + h) * 128 * 128;
-    const unsigned char *blk0 = ra.blocks + ((size_t)fc * H + h) * kBlock;
-    const size_t blk_stride = (size_t)H * kBlock;
+    const int RG = ra.ring;
+    // the block of chunk x
+    auto blk_of = [&](int x) -> const unsigned char * {
+        return ready && RG > 0 ? ra.blocks + ((size_t)gi * RG + x % RG) * kBlock
+                               : ra.blocks + ((size_t)(fc + x) * H + h) * kBlock;
+    };
 
     // Bounded wait; a timeout is recorded and turns every later wait into a
     // no-op, so all threads still pass the same barriers and the kernel ends.
@@ -1237,19 +1352,31 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
     auto issue_one = [&]() {
         const int c = next_load++;
         tc::mbar_arrive_expect_tx(bL(c), kBlock);
-        tc::bulk_g2s(sbase + buf_off(c), blk0 + (size_t)c * blk_stride, kBlock, bL(c));
+        tc::bulk_g2s(sbase + buf_off(c), blk_of(c), kBlock, bL(c));
     };
     auto refresh = [&]() {  // one read of the aligned group holding the next unknown flag
         const int x = known_set + 1;
         if (x >= nchunks) return;
-        const size_t a = (size_t)h * ra.nslots + fc + x, base = a & ~(size_t)3;
+        // flag of chunk x: ring entry x % R of this chain (R a multiple of 4), or
+        // [h][fc + x]; the group of four around it holds chunks y0 .. y0 + 3
+        size_t base;
+        int y0;
+        if (RG > 0) {
+            const int sx = x % RG;
+            base = (size_t)gi * RG + (sx & ~3);
+            y0 = x - (sx & 3);
+        } else {
+            const size_t a = (size_t)h * ra.nslots + fc + x;
+            base = a & ~(size_t)3;
+            y0 = x - (int)(a - base);
+        }
         const uint4 v = flags4_acquire(ready + base);
         const uint32_t fl[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int y = x + i - (int)(a - base);  // chunk of flag i (this chain's if y >= x)
+            const int y = y0 + i;  // (a chunk of this chain if y >= x)
             if (y < x) continue;
-            if (y >= nchunks || fl[i] == 0) break;
+            if (y >= nchunks || fl[i] != (uint32_t)y + 1u) break;
             known_set = y;
         }
     };
@@ -1381,6 +1508,12 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, const 
                 check_issue(c + 1);
             }
             wait(bL(c), (uint32_t)((c >> 1) & 1));
+            // the ring entry of chunk c may be reused: its load has completed (the
+            // wait above saw it), so a plain store that follows it is enough
+            if (ready && RG > 0 && tid == kLoader && !failed)
+                asm volatile("st.relaxed.gpu.global.u32 [%0], %1;\n" ::"l"(ra.progress + gi),
+                             "r"(c + 1)
+                             : "memory");
             // this chunk's values may need a larger scale (rare: v grew)
             const int nu_c = *reinterpret_cast<const int *>(buf + kNu);
             const int sig_up = clamp_sig(nu_c + kSigUpad - kSigTarget);
@@ -1550,35 +1683,185 @@ __global__ void __launch_bounds__(kRecThreads, 1) recur_kernel(RecArgs ra) {
         if (ra.first_chunk[ra.N + 1] < 0) return;  // malformed offsets, already flagged
         chain = ra.first_chunk[ra.N + 2 + chain / ra.H] * ra.H + chain % ra.H;
     }
-    recur_chain(ra, chain, nullptr);
+    recur_chain(ra, chain, 0, nullptr);
 }
 
-// K1 and K2 in one cooperative launch (every CTA resident): CTAs [0, nchains)
-// run the chains, the rest prepare blocks in chunk-major order and publish
-// each one through `ready`. Producers never wait, so the chains always make
-// progress; every wait of a chain is bounded.
+// K1 and K2 in one cooperative launch (every CTA resident) for one group of
+// chains: CTAs [0, gcount) run the group's chains, the rest prepare their
+// blocks in chunk-major order into per-chain rings and publish each one through
+// `ready`. A producer waits (bounded) only for a ring entry that its chain has
+// not loaded yet, and that wait ends: the earliest block not yet produced waits
+// only for earlier chunks of its own chain, which are all produced. Every wait
+// of a chain is bounded too; whoever gives up first flags the status word, and
+// the others stop at once.
 constexpr uint32_t kFusedSmem = kRecSmem > (uint32_t)kPrepSmem ? kRecSmem : (uint32_t)kPrepSmem;
 __global__ void __launch_bounds__(kRecThreads, 1)
-    fused_kernel(const __grid_constant__ PrepArgs pa, RecArgs ra, int nchains, int *ready) {
-    if ((int)blockIdx.x < nchains) recur_chain(ra, blockIdx.x, ready);
-    else prep_loop(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
+    fused_kernel(const __grid_constant__ PrepArgs pa, RecArgs ra, int *ready) {
+    const int nchains = pa.gcount;
+    if ((int)blockIdx.x < nchains) {
+        if (pa.cu && pa.first_chunk[pa.N + 1] < 0) return;  // malformed offsets, already flagged
+        recur_chain(ra, chain_of_rank(pa.gbase + blockIdx.x, pa.cu, pa.first_chunk, pa.N, pa.H),
+                    blockIdx.x, ready);
+    } else {
+        prep_loop(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
+    }
 }
 
 }  // namespace pf
 
-// Workspace: [0, 256) status word | schedule (N + 2 int32, varlen only) |
-// ready flags (one int32 per chunk block) | chunk blocks; each region 256-byte padded.
+// Workspace: [0, 256) status word | schedule (2 N + 2 int32, varlen only) |
+// then by schedule (each region 256-byte padded):
+//   split:        one block per (chunk slot, head);
+//   fused:        ready flags [H][slots] | one block per (chunk slot, head);
+//   fused, ring:  ready flags [G][R] and progress [G] | rings, G R blocks
+//                 (G = the most chains of one group, R = the ring length):
+//                 bounded by the group, not by the sequence length.
+// kda_prefill runs the fastest plan that its workspace holds.
 namespace {
 size_t pad256(size_t x) { return (x + 255) / 256 * 256; }
+// Chunk slots of the prepared blocks (none without tokens: then only the
+// recurrence kernel runs, copying initial to final states).
 long long prefill_slots(int N, long long T, long long T_total, bool varlen) {
+    if (T_total <= 0) return 0;
     return varlen ? (T_total + pf::C - 1) / pf::C + N : (long long)N * ((T + pf::C - 1) / pf::C);
+}
+constexpr int kRing = 16;  // blocks per chain in flight in ring mode (a multiple of 4)
+// Chains per fused launch when they are many (groups run one after the other):
+// the G that minimises the modelled time of all groups, a group of x chains of L
+// chunks taking max(L t_chain, x L t_block / (SMs - x)) with the measured paces
+// t_chain ~ 1.6 us per chunk of a chain and t_block ~ 6.8 us per block of a
+// producer SM; L is the chunks per sequence (the mean for packed sequences).
+int group_chains(long long nchains, long long chunks_per_chain, int nsm) {
+    if (nchains <= 0) return 1;
+    if (3 * nchains <= nsm) return (int)nchains;  // one group
+    const double tc = 1.6, tp = 6.8, L = (double)(chunks_per_chain > 0 ? chunks_per_chain : 1);
+    auto f = [&](long long x) { return std::max(L * tc, x * L * tp / (double)(nsm - x)); };
+    long long best = 1;
+    double best_t = 1e300;
+    for (long long G = 1; G <= nsm / 2 && G <= nchains; ++G) {
+        const long long groups = (nchains + G - 1) / G, last = nchains - (groups - 1) * G;
+        const double t = (groups - 1) * f(G) + f(last);
+        if (t < best_t * 0.999) {
+            best_t = t;
+            best = G;
+        }
+    }
+    return (int)best;
 }
 }  // namespace
 
-size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen) {
-    const long long slots = prefill_slots(N, T, T_total, varlen);
-    const size_t sched = varlen ? pad256((size_t)(2 * N + 2) * 4) : 0;
-    return 256 + sched + pad256((size_t)slots * H * 4) + (size_t)slots * H * pf::kBlock;
+int prefill_tc_schedule_override();
+
+namespace {
+// What every plan for these sizes shares.
+struct PlanSizes {
+    int nsm, coop, force;
+    long long nchains, slots, L, maxc;
+    size_t base;  // status word and (packed sequences) the chunk schedule
+};
+bool plan_sizes(int N, long long T, long long T_total, int H, bool varlen, PlanSizes &z) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&z.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&z.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+        return false;
+    z.force = prefill_tc_schedule_override();  // -1 auto, 0 split, 1 fused
+    z.nchains = (long long)N * H;
+    z.slots = prefill_slots(N, T, T_total, varlen);
+    z.base = 256 + (varlen ? pad256((size_t)(2 * N + 2) * 4) : 0);
+    z.L = varlen ? (N > 0 ? (T_total / N + pf::C - 1) / pf::C : 0) : (T + pf::C - 1) / pf::C;
+    z.maxc = ((varlen ? T_total : T) + pf::C - 1) / pf::C;
+    return true;
+}
+bool can_fuse(const PlanSizes &z) { return z.coop && z.nchains > 0 && z.slots > 0; }
+// The fastest plan: the fused schedule (one block per chunk and head) when the
+// chains take at most a third of the SMs, else K1 then K2; the override forces
+// either.
+PrefillPlan fast_plan(const PlanSizes &z, int H) {
+    PrefillPlan p{0, 0, 0, 0, 0};
+    const bool fused = can_fuse(z) && (z.force == 1 || (z.force == -1 && 3 * z.nchains <= z.nsm));
+    p.schedule = fused ? 1 : 0;
+    p.bytes = z.base + (size_t)z.slots * H * pf::kBlock;
+    if (fused) {
+        p.group_chains = group_chains(z.nchains, z.L, z.nsm);
+        p.groups = (int)((z.nchains + p.group_chains - 1) / p.group_chains);
+        p.bytes += pad256((size_t)z.slots * H * 4);
+    }
+    return p;
+}
+// The fused schedule with rings, G chains per group (G <= 0: the modelled
+// best); false when the fused kernel cannot run or the split one is forced.
+bool ring_plan(const PlanSizes &z, long long G, PrefillPlan &p) {
+    if (!can_fuse(z) || z.force == 0) return false;
+    if (G <= 0) G = group_chains(z.nchains, z.L, z.nsm);
+    G = std::max(1LL, std::min(G, z.nchains));
+    p.schedule = 1;
+    p.group_chains = (int)G;
+    p.ring = (int)std::min<long long>(kRing, std::max<long long>(4, (z.maxc + 3) / 4 * 4));
+    p.groups = (int)((z.nchains + G - 1) / G);
+    p.bytes = z.base + pad256((size_t)G * (p.ring + 1) * 4) + (size_t)G * p.ring * pf::kBlock;
+    return true;
+}
+}  // namespace
+
+// The plan for these sizes that a workspace of `budget` bytes gets: the
+// fastest plan if it fits; else the fused schedule with rings, with the
+// modelled best number of chains per group or, if that does not fit, the most
+// that do. kind 1 / 2 / 3 ask for the fastest plan, the ring plan with the best
+// group, and the smallest accepted plan, whatever the budget. False when
+// nothing fits (or the device cannot be queried).
+bool prefill_tc_plan(int N, long long T, long long T_total, int H, bool varlen, size_t budget,
+                     int kind, PrefillPlan &p) {
+    PlanSizes z;
+    if (!plan_sizes(N, T, T_total, H, varlen, z)) return false;
+    const PrefillPlan fast = fast_plan(z, H);
+    if (kind == 1) {
+        p = fast;
+        return true;
+    }
+    PrefillPlan r;
+    const bool have_ring = ring_plan(z, 0, r);
+    if (kind == 2) {
+        if (!have_ring) return false;
+        p = r;
+        return true;
+    }
+    if (kind == 3) {
+        PrefillPlan r1;
+        p = (ring_plan(z, 1, r1) && r1.bytes < fast.bytes) ? r1 : fast;
+        return true;
+    }
+    if (budget >= fast.bytes) {
+        p = fast;
+        return true;
+    }
+    if (!have_ring) return false;
+    if (budget >= r.bytes) {
+        p = r;
+        return true;
+    }
+    if (budget <= z.base) return false;
+    // an upper bound on the chains that fit (blocks only), then down to the
+    // first that fits with its flags (below the modelled best: r.group_chains)
+    long long G = std::min<long long>((long long)((budget - z.base) / ((size_t)r.ring * pf::kBlock)),
+                                      r.group_chains - 1);
+    while (G >= 1) {
+        if (ring_plan(z, G, r) && budget >= r.bytes) {
+            p = r;
+            return true;
+        }
+        --G;
+    }
+    return false;
+}
+
+size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen, int kind) {
+    PrefillPlan p;
+    if (prefill_tc_plan(N, T, T_total, H, varlen, 0, kind, p)) return p.bytes;
+    if (kind == 2) return 0;
+    // no device to ask: the split schedule's size
+    return 256 + (varlen ? pad256((size_t)(2 * N + 2) * 4) : 0) +
+           (size_t)prefill_slots(N, T, T_total, varlen) * H * pf::kBlock;
 }
 
 // cuTensorMapEncodeTiled, looked up once through the runtime (no link-time
@@ -1631,42 +1914,39 @@ std::atomic<int> g_schedule_override{initial_schedule_override()};
 
 int prefill_tc_set_schedule(int s) { return g_schedule_override.exchange(s); }
 
-// Which schedule runs: the fused cooperative kernel when the chains leave most
-// SMs to the producers (N H <= SMs / 3), else K1 then K2. The override forces
-// either ("fused" still needs N H < SMs and a cooperative launch).
-// Returns 1 (fused), 0 (K1 then K2) or -1 (the device could not be queried).
-int prefill_tc_schedule(long long nchains, long long nitems) {
-    int dev = 0, nsm = 0, coop = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
-        return -1;
-    const int force = g_schedule_override.load();
-    bool fused = 3 * nchains <= nsm;
-    if (force == 0) fused = false;
-    if (force == 1) fused = nchains < nsm;
-    fused = fused && nitems > 0 && coop;
-    if (!fused) return 0;
-    if (cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)pf::kFusedSmem) != cudaSuccess)
-        return -1;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::fused_kernel, pf::kRecThreads,
-                                                      pf::kFusedSmem) != cudaSuccess)
-        return -1;
-    return per_sm >= 1 ? 1 : 0;
-}
+int prefill_tc_schedule_override() { return g_schedule_override.load(); }
 
-int prefill_tc_schedule(int N, long long T, long long T_total, int H, bool varlen) {
-    return prefill_tc_schedule((long long)N * H, prefill_slots(N, T, T_total, varlen) * H);
+// The plan that a workspace of `budget` bytes gets, with p.schedule 1 (fused),
+// 0 (K1 then K2), -1 (the device could not be queried or cannot run the fused
+// kernel's launch) or -2 (the workspace is too small).
+void prefill_tc_query(int N, long long T, long long T_total, int H, bool varlen, size_t budget,
+                      PrefillPlan &p) {
+    if (!prefill_tc_plan(N, T, T_total, H, varlen, budget, 0, p)) {
+        PrefillPlan any;
+        p = PrefillPlan{prefill_tc_plan(N, T, T_total, H, varlen, 0, 3, any) ? -2 : -1, 0, 0, 0, 0};
+        return;
+    }
+    if (p.schedule == 1) {
+        if (cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)pf::kFusedSmem) != cudaSuccess) {
+            p.schedule = -1;
+            return;
+        }
+        int per_sm = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::fused_kernel,
+                                                          pf::kRecThreads, pf::kFusedSmem) !=
+                cudaSuccess ||
+            per_sm < 1)
+            p.schedule = -1;
+    }
 }
 
 cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const float *g,
                               const void *beta, float scale, const float *init,
                               const int32_t *cu, int N, int T, int T_total, int H,
                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
-                              void *out, float *fin, unsigned char *ws, unsigned test_wait_ms,
-                              cudaStream_t stream) {
+                              void *out, float *fin, unsigned char *ws, size_t ws_bytes,
+                              unsigned test_wait_ms, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(pf::prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pf::kPrepSmem);
@@ -1679,30 +1959,40 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     const long long slots = prefill_slots(N, T, T_total, varlen);
     const long long nitems = slots * H;
     if (nitems > 0x7fffffffLL) return cudaErrorInvalidValue;
+    const long long nchains = (long long)N * H;
+    // the fastest plan that the workspace holds
+    PrefillPlan plan;
+    if (!prefill_tc_plan(N, T, T_total, H, varlen, ws_bytes, 0, plan))
+        return cudaErrorInvalidValue;
+    if (test_wait_ms && (plan.schedule != 1 || plan.groups != 1)) return cudaErrorInvalidValue;
+    int dev = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorUnknown;
     size_t off = 256;
     int32_t *first_chunk = nullptr;
     if (varlen) {
         first_chunk = reinterpret_cast<int32_t *>(ws + off);
         off += pad256((size_t)(2 * N + 2) * 4);
     }
-    int *ready = reinterpret_cast<int *>(ws + off);
-    off += pad256((size_t)nitems * 4);
-    unsigned char *blocks = ws + off;
-    const long long nchains = (long long)N * H;
-    // failure-detection test: the fused schedule with its chains alone
-    const int sched = test_wait_ms ? 1 : prefill_tc_schedule(nchains, nitems);
-    int dev = 0, nsm = 0;
-    if (sched < 0 || cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return cudaErrorUnknown;
-    if (test_wait_ms) {  // every chain resident at once, in one cooperative launch
-        if (nchains >= nsm || nitems == 0) return cudaErrorInvalidValue;
+    const bool fused = plan.schedule == 1;
+    int *ready = nullptr, *progress = nullptr;
+    size_t flag_bytes = 0;
+    if (fused) {
+        ready = reinterpret_cast<int *>(ws + off);
+        if (plan.ring > 0) {
+            progress = ready + (size_t)plan.group_chains * plan.ring;
+            flag_bytes = pad256((size_t)plan.group_chains * (plan.ring + 1) * 4);
+        } else {
+            flag_bytes = pad256((size_t)nitems * 4);
+        }
+        off += flag_bytes;
         e = cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pf::kFusedSmem);
         if (e != cudaSuccess) return e;
     }
+    unsigned char *blocks = ws + off;
     if (varlen) pf::schedule_kernel<<<1, 1024, 0, stream>>>(cu, N, T_total, first_chunk, status);
-    const bool fused = sched == 1;
 
     pf::PrepArgs pa;
     memset(&pa, 0, sizeof(pa));
@@ -1725,22 +2015,34 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     pa.g_per_channel = g_per_channel;
     pa.blocks = blocks;
     pa.status = status;
+    pa.ring = plan.ring;
+    pa.nslots = (int)slots;
+    pa.progress = progress;
     pf::RecArgs ra{cu, first_chunk, N, T, T_total, H, scale, init, blocks,
                    static_cast<__nv_bfloat16 *>(out), fin,
                    snap_interval > 0 ? snaps : nullptr, snap_interval > 0 ? snap_interval : 1,
-                   snap_max, (int)slots, status, pf::kWaitLimit};
+                   snap_max, plan.ring, (int)slots, progress, status, pf::kWaitLimit};
     if (fused) {
-        e = cudaMemsetAsync(ready, 0, (size_t)nitems * 4, stream);
-        if (e != cudaSuccess) return e;
-        int nch = (int)nchains;
-        unsigned grid = (unsigned)nsm;
-        if (test_wait_ms) {  // chains with no producer at all and a short wait bound:
-            grid = (unsigned)nch;  // every wait for a ready flag runs out
-            ra.wait_ns = (unsigned long long)test_wait_ms * 1000000ull;
+        // groups of chains (in the recurrence order) one after the other, each in
+        // one cooperative launch with its flags cleared before it
+        for (int gi = 0; gi < plan.groups; ++gi) {
+            pa.gbase = gi * plan.group_chains;
+            pa.gcount = (int)std::min<long long>(plan.group_chains, nchains - pa.gbase);
+            if (gi == 0 || plan.ring > 0) {  // (without rings, every group has its own flags)
+                e = cudaMemsetAsync(ready, 0, flag_bytes, stream);
+                if (e != cudaSuccess) return e;
+            }
+            unsigned grid = (unsigned)nsm;
+            if (test_wait_ms) {  // chains with no producer at all and a short wait bound:
+                grid = (unsigned)pa.gcount;  // every wait for a ready flag runs out
+                ra.wait_ns = (unsigned long long)test_wait_ms * 1000000ull;
+            }
+            void *args[] = {&pa, &ra, &ready};
+            e = cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(grid),
+                                            dim3(pf::kRecThreads), args, pf::kFusedSmem, stream);
+            if (e != cudaSuccess) return e;
         }
-        void *args[] = {&pa, &ra, &nch, &ready};
-        return cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(grid),
-                                           dim3(pf::kRecThreads), args, pf::kFusedSmem, stream);
+        return cudaSuccess;
     }
     if (nitems > 0) {
         const int grid = (int)(nitems < nsm ? nitems : nsm);  // one persistent CTA per SM

@@ -54,11 +54,13 @@ def np32(t):
     return t.detach().float().cpu().numpy()
 
 
-def run_gpu_prefill(x, chunk, with_init=True):
+def run_gpu_prefill(x, chunk, with_init=True, ws_kind="fast"):
+    """One kda_prefill call on x with a workspace of the given kind ("fast",
+    "ring", "min": the plan follows from its size)."""
     cu = x.cu_seqlens.to(DEV) if x.cu_seqlens is not None else None
     init = x.init_state.to(DEV) if (with_init and x.init_state is not None) else None
     q = x.q.to(DEV)
-    ws = kda.prefill_workspace(q, cu, chunk=chunk)
+    ws = kda.prefill_workspace(q, cu, chunk=chunk, kind=ws_kind)
     out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), x.g.to(DEV),
                                x.beta.to(DEV), x.scale, init_state=init, cu_seqlens=cu,
                                chunk=chunk, workspace=ws)
@@ -84,8 +86,10 @@ def check_prefill(x, chunk, tol, with_init=True):
 @contextlib.contextmanager
 def prefill_schedule(mode):
     """Force the bf16 prefill schedule ("split", "fused" or None for the
-    automatic choice) for the calls inside the block."""
-    code = {None: -1, "split": kda.KDA_SCHEDULE_SPLIT, "fused": kda.KDA_SCHEDULE_FUSED}[mode]
+    automatic choice) for the calls inside the block. ("ring": the automatic
+    choice; the caller passes a ring-sized workspace.)"""
+    code = {None: -1, "ring": -1, "split": kda.KDA_SCHEDULE_SPLIT,
+            "fused": kda.KDA_SCHEDULE_FUSED}[mode]
     prev = kda.kda_prefill_set_schedule(code)
     try:
         yield

@@ -562,16 +562,17 @@ def test_bf16_non_monotone_offsets_skip_the_call():
     assert torch.all(out == 7.0) and torch.all(fin == 7.0)
 
 
-def test_fused_chain_waits_are_bounded():
+@pytest.mark.parametrize("ws_kind", ["fast", "ring"])
+def test_fused_chain_waits_are_bounded(ws_kind):
     """A chain whose producer never comes gives up after its wait bound and
     reports KDA_ERR_TIMEOUT through the status word; the context stays usable
     and the next call is correct. (Test-only entry point: the chains are
     launched without producers and with a 50 ms bound; nothing faults or
-    hangs.)"""
+    hangs.) With the ring workspace, the blocks live in per-chain rings."""
     x = inputs.prefill_inputs([200, 64], H=2, io="bf16", seed=101, init="normal")
     q = x.q.to(DEV)
     cu = x.cu_seqlens.to(DEV)
-    ws = kda.prefill_workspace(q, cu, chunk=64)
+    ws = kda.prefill_workspace(q, cu, chunk=64, kind=ws_kind)
     out = torch.empty_like(q)
     fin = torch.empty((2, 2, 128, 128), dtype=torch.float32, device=DEV)
     rc = kda.load().kda_testing_prefill_chain_timeout(
@@ -585,16 +586,23 @@ def test_fused_chain_waits_are_bounded():
 
 
 def test_prefill_schedule_choice():
-    """Few chains (N H <= SMs / 3): fused; many chains: split; the override
-    (kda_prefill_set_schedule) wins while it is set."""
+    """With the full workspace: fused for few chains (N H <= SMs / 3), split
+    for many; the override (kda_prefill_set_schedule) wins while it is set.
+    The ring workspace does not grow with the sequence length."""
     f = kda.kda_prefill_schedule
+    bf = kda.KDA_BF16
     with prefill_schedule(None):
-        assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
-        assert f(64, 1 << 16, 32, 128, 64, kda.KDA_BF16, True) == kda.KDA_SCHEDULE_SPLIT
+        assert f(1, 8192, 32, 128, 64, bf) == kda.KDA_SCHEDULE_FUSED
+        assert f(64, 1 << 16, 32, 128, 64, bf, True) == kda.KDA_SCHEDULE_SPLIT
+        r1 = kda.kda_prefill_workspace_size_ring(1, 8192, 32, 128, 64, bf)
+        r2 = kda.kda_prefill_workspace_size_ring(1, 1 << 17, 32, 128, 64, bf)
+        assert r1 == r2 < 64 << 20
+        assert kda.kda_prefill_workspace_size(1, 1 << 17, 32, 128, 64, bf) > 2048 * 32 * 74368
     with prefill_schedule("split"):
-        assert f(1, 8192, 32, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_SPLIT
+        assert f(1, 8192, 32, 128, 64, bf) == kda.KDA_SCHEDULE_SPLIT
+        assert kda.kda_prefill_workspace_size_ring(1, 8192, 32, 128, 64, bf) == 0
     with prefill_schedule("fused"):
-        assert f(40, 64, 2, 128, 64, kda.KDA_BF16) == kda.KDA_SCHEDULE_FUSED
+        assert f(40, 64, 2, 128, 64, bf) == kda.KDA_SCHEDULE_FUSED
 
 
 def test_bf16_split_longest_first_order_many_chains():

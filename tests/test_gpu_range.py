@@ -6,7 +6,8 @@ The operator is linear in v and in the initial state, so these inputs are
 as valid as the unit-scale ones; the bf16 prefill carries the value side of
 its state path (beta v, the pseudo-values, the state operand of the chunk
 products) in fp16 and must rescale it rather than overflow. Both bf16
-schedules, the fp32 path and decode are covered. Metric and bars as in the
+schedules (and the fused one with per-chain rings), the fp32 path and decode
+are covered. Metric and bars as in the
 other parity tests (relative to the RMS of the oracle's result, so they do
 not depend on the scale).
 """
@@ -60,12 +61,12 @@ def _id(c):
     return ",".join("%s=%s" % kv for kv in c.items())
 
 
-@pytest.mark.parametrize("mode", ["split", "fused"])
+@pytest.mark.parametrize("mode", ["split", "fused", "ring"])
 @pytest.mark.parametrize("case", CASES, ids=_id)
 def test_bf16_prefill_scaled(case, mode):
     x = scaled_inputs("bf16", 201, **case)
     with prefill_schedule(mode):
-        out, fin = run_gpu_prefill(x, 64)
+        out, fin = run_gpu_prefill(x, 64, ws_kind="ring" if mode == "ring" else "fast")
     ro, rf = oracle_prefill(x)
     eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
     assert eo <= TOL_BF16 and ef <= TOL_BF16, (eo, ef)
@@ -82,7 +83,7 @@ def test_bf16_prefill_scaled_long(case):
     assert eo <= TOL_BF16 and ef <= TOL_BF16, (eo, ef)
 
 
-@pytest.mark.parametrize("mode", ["split", "fused"])
+@pytest.mark.parametrize("mode", ["split", "fused", "ring"])
 @pytest.mark.parametrize("first,then", [(1e-3, 1e4), (1e4, 1e-3), (1.0, 3e4)])
 def test_bf16_prefill_value_jump(first, then, mode):
     """The magnitude of v changes by up to 1e7 within a sequence (after 192
@@ -96,7 +97,7 @@ def test_bf16_prefill_value_jump(first, then, mode):
     v[700:] *= then
     x.v = v.to(torch.bfloat16)
     with prefill_schedule(mode):
-        out, fin = run_gpu_prefill(x, 64)
+        out, fin = run_gpu_prefill(x, 64, ws_kind="ring" if mode == "ring" else "fast")
     ro, rf = oracle_prefill(x)
     eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
     assert eo <= TOL_BF16 and ef <= TOL_BF16, (eo, ef)

@@ -83,11 +83,45 @@ def test_noalloc_rejects_bad_arguments_like_kda_prefill():
     assert rc == kda.KDA_ERR_UNSUPPORTED
 
 
-def test_noalloc_rejects_sizes_beyond_its_static_scratch():
+def test_noalloc_runs_the_ring_plan_when_the_full_one_does_not_fit():
+    """H=16, T=2048: the full plan needs ~38 MB of prepared blocks, beyond the
+    16 MiB array; the call runs the fused schedule with rings (fewer chains
+    per group than the modelled best, so more than one group) and agrees bit
+    for bit with kda_prefill on a full workspace."""
     f = _noalloc_fn()
-    # H=32, T=8192 needs ~312 MB of prepared chunk blocks: far beyond 16 MiB
-    need = kda.kda_prefill_workspace_size(1, 8192, 32, 128, 64, kda.KDA_BF16, False)
+    dev = torch.device("cuda:0")
+    N, T, H = 1, 2048, 16
+    bf = kda.KDA_BF16
+    assert kda.kda_prefill_workspace_size(N, T, H, 128, 64, bf, True) > 16 << 20
+    plan = kda.kda_prefill_plan(N, T, H, 128, 64, bf, True, 16 << 20)
+    assert plan.schedule == kda.KDA_SCHEDULE_FUSED and plan.ring > 0 and plan.groups > 1
+    x = inputs.prefill_inputs([T], H=H, io="bf16", seed=33, init="normal")
+    q, k, v, g, b = (t.to(dev) for t in (x.q, x.k, x.v, x.g, x.beta))
+    init, cu = x.init_state.to(dev), x.cu_seqlens.to(dev)
+    ref_out, ref_fin = kda.kda_prefill(q, k, v, g, b, x.scale, init_state=init, cu_seqlens=cu,
+                                       chunk=64)
+    torch.cuda.synchronize()
+    out = torch.full_like(q, float("nan"))
+    fin = torch.full((N, H, 128, 128), float("nan"), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream().cuda_stream
+    rc = f(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), b.data_ptr(), x.scale,
+           init.data_ptr(), cu.data_ptr(), N, T, H, 128, 64, bf, out.data_ptr(), fin.data_ptr(),
+           ctypes.c_void_p(stream))
+    assert rc == kda.KDA_OK, kda.status_string(rc)
+    assert kda.kda_noalloc_status() == kda.KDA_OK
+    assert torch.equal(out, ref_out)
+    assert torch.equal(fin, ref_fin)
+
+
+def test_noalloc_rejects_sizes_beyond_its_static_scratch():
+    """Only the per-sequence schedule data can outgrow the array: about two
+    million packed sequences. Rejected before anything is launched (the
+    pointers are never read)."""
+    f = _noalloc_fn()
+    N = 2_200_000
+    need = kda.kda_prefill_workspace_size_min(N, N, 1, 128, 64, kda.KDA_BF16, True)
     assert need > 16 << 20
-    rc = f(None, None, None, None, None, 1.0, None, None, 1, 8192, 32, 128, 64, kda.KDA_BF16,
-           None, None, None)
+    cu = torch.zeros(4, dtype=torch.int32, device="cuda:0")  # not read
+    rc = f(None, None, None, None, None, 1.0, None, cu.data_ptr(), N, N, 1, 128, 64,
+           kda.KDA_BF16, None, None, None)
     assert rc == kda.KDA_ERR_TOO_LARGE
