@@ -14,6 +14,9 @@
 // references r_i (the cumulative decay just before tile i):
 //   row operand x_t e^{a_t - r_i} (<= 1),  column operand k_s e^{r_i - a_s}
 //   (<= 1 before the tile, <= e^80 inside it); products are e^{a_t - a_s}.
+// With one decay per token and head (the Gated DeltaNet form) the factor is the
+// same on every channel, so the Gram matrices are those of q and k themselves
+// (exact bf16 operands) times e^{a_t - a_s}, applied in fp32 after the product.
 //
 // Per chunk, with S0 the state at the chunk start:
 //   A = beta * strict_lower(Gram(k, k)),  M = lower(Gram(q, k))   [bf16 tcgen05]
@@ -723,6 +726,11 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
 #pragma unroll
         for (int r = 0; r < 16; ++r)
             *reinterpret_cast<float *>(smem + kOffAcum + a_off(16 * ti4 + r, ch)) = a[r] + off;
+        if (!gpc && ch == 0) {  // one decay per token: a_t kept for the Gram read-back
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                reinterpret_cast<float *>(smem + kOffGs)[16 * ti4 + r] = a[r] + off;
+        }
         float *tab = reinterpret_cast<float *>(smem + kOffTab);
         const float rnext = ti4 == 3 ? rr[4] : (ti4 == 2 ? rr[3] : (ti4 == 1 ? rr[2] : rr[1]));
         tab[(kTabEr + ti4) * 128 + ch] = __expf(off);
@@ -783,6 +791,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 ys[m][e] = ed[e] * ix[e];     // e^{r_{i+1} - a_t}  in [e^-80, 1]
                 md += qq[e] * kk[e];
             }
+            if (!gpc) {
+                // one decay per token: the Gram operands are q and k themselves (exact
+                // in bf16), and the read-back applies e^{a_t - a_s} in fp32
+                *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + tl, c0)) = uk[m];
+                *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + 16 + tl, c0)) = uq[m];
+                for (int i2 = i; i2 < 4; ++i2)
+                    *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(i2, i) + tl, c0)) =
+                        uk[m];
+            } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e) o[e] = kk[e] * xs[m][e];
             *reinterpret_cast<uint4 *>(smem + kOffX + off_k128(32 * i + tl, c0)) = pack8_bf16(o);
@@ -816,6 +833,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 for (int e = 0; e < 8; ++e) o[e] = kk[e] * (f[e] * ys[m][e]);
                 *reinterpret_cast<uint4 *>(smem + kOffKh + off_k128(16 * kh_slot(3, 0) + tl, c0)) =
                     pack8_bf16(o);
+            }
             }
             // q_t . k_t (the diagonal of M: no decay): 32 channels per warp here,
             // the four warps of the tile are added in the Gram read-back
@@ -934,6 +952,13 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         if (diag && part == 1) md_s = sMdp[s] + sMdp[C + s] + sMdp[2 * C + s] + sMdp[3 * C + s];
         uint32_t rv[1][16];
         tc::tmem_ld_cols<1>(tquart + (uint32_t)tcol, rv);
+        if (valid && !gpc) {  // one decay per token: Gram of q, k times e^{a_t - a_s}
+            const float *as = reinterpret_cast<const float *>(smem + kOffGs);
+            const float a_s = as[s];
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+                rv[0][n] = __float_as_uint(__uint_as_float(rv[0][n]) * __expf(as[16 * i + n] - a_s));
+        }
         if (valid) {
             if (part == 0) {
                 if (diag) {

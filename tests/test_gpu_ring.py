@@ -102,6 +102,12 @@ def test_ring_plan_with_snapshots_and_per_head_decay():
         res.append((out, fin, snaps))
     for a, b in zip(res[0], res[1]):
         assert torch.equal(a, b)
+    # and the full-workspace result against the oracle (every channel of the
+    # decay = channel 0, the per-head decay the kernels read)
+    x.g = x.g[..., :1].expand_as(x.g).contiguous()
+    ro, rf = oracle_prefill(x)
+    assert out_err(res[0][0], ro) <= TOL_BF16
+    assert rel_err(res[0][1].cpu().numpy(), rf) <= TOL_BF16
 
 
 def test_workspace_below_the_minimum_is_rejected():
