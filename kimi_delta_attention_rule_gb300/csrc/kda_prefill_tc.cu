@@ -430,6 +430,7 @@ __device__ __forceinline__ int ld_progress(const int *p) {
 //     workspace) in a ring per chain: block and flag (i ring + c % ring) of
 //     chain i, and before a block overwrites its ring entry the producer waits
 //     (bounded) until the chain has loaded chunk c - ring.
+template <bool kRingMode, bool kChannelDecay>
 __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int stride,
                                           int *ready) {
     const __nv_bfloat16 *__restrict__ q = pa.q, *__restrict__ k = pa.k, *__restrict__ v = pa.v;
@@ -439,8 +440,10 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const int N = pa.N, T = pa.T, H = pa.H;
     unsigned char *__restrict__ blocks = pa.blocks;
     const bool fused = ready != nullptr;  // chunk-major over a group of chains
-    const int RG = pa.ring;
-    const bool ring = fused && RG > 0;      // blocks in per-chain rings
+    // blocks in per-chain rings (a separate instantiation: the ring logic costs
+    // the other modes registers and time when it is merely present)
+    const int RG = kRingMode ? pa.ring : 0;
+    const bool ring = kRingMode && fused && RG > 0;
     int nitems = pa.nitems;
     if (fused) {  // the most chunks of one chain in the group
         int maxc = 0;
@@ -579,7 +582,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // T phase (where the q, k, v copies are issued)
     constexpr int kStager = kPrepThreads - 64;
     uint32_t n_staged = 0;  // stagings issued (each completes one phase of both barriers)
-    const bool gpc = pa.g_per_channel != 0;
+    const bool gpc = kChannelDecay;  // pa.g_per_channel != 0 (an instantiation each)
     float gs_next = 0.f;  // scalar mode: the decay of token tid of the staged item
     auto stage_g = [&](int tc_, int h_, int L_) {
         ++n_staged;
@@ -1239,8 +1242,9 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (warp == 0) tc::tmem_dealloc(tm, kPrepTmemCols);
 }
 
+template <bool kChannelDecay>
 __global__ void __launch_bounds__(kPrepThreads, 1) prep_kernel(const __grid_constant__ PrepArgs pa) {
-    prep_loop(pa, blockIdx.x, gridDim.x, nullptr);
+    prep_loop<false, kChannelDecay>(pa, blockIdx.x, gridDim.x, nullptr);
 }
 
 // ============================================================================
@@ -1306,6 +1310,7 @@ __device__ __forceinline__ uint4 flags4_acquire(const int *f) {
 // ready flag = c + 1; in ring mode this chain is number gi of its group, chunk
 // c's block and flag are ring entry (gi ring + c % ring), and progress[gi]
 // tells the producers which entries may be overwritten.
+template <bool kRingMode>
 __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi, const int *ready) {
     const int32_t *__restrict__ cu = ra.cu;
     const int N = ra.N, T = ra.T, H = ra.H;
@@ -1347,7 +1352,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
     const uint32_t tlane = tm + ((uint32_t)(32 * (warp & 3)) << 16);
 
     const size_t head_state = ((size_t)n * H + h) * 128 * 128;
-    const int RG = ra.ring;
+    const int RG = kRingMode ? ra.ring : 0;
     // the block of chunk x
     auto blk_of = [&](int x) -> const unsigned char * {
         return ready && RG > 0 ? ra.blocks + ((size_t)gi * RG + x % RG) * kBlock
@@ -1708,7 +1713,7 @@ __global__ void __launch_bounds__(kRecThreads, 1) recur_kernel(RecArgs ra) {
         if (ra.first_chunk[ra.N + 1] < 0) return;  // malformed offsets, already flagged
         chain = ra.first_chunk[ra.N + 2 + chain / ra.H] * ra.H + chain % ra.H;
     }
-    recur_chain(ra, chain, 0, nullptr);
+    recur_chain<false>(ra, chain, 0, nullptr);
 }
 
 // K1 and K2 in one cooperative launch (every CTA resident) for one group of
@@ -1720,16 +1725,24 @@ __global__ void __launch_bounds__(kRecThreads, 1) recur_kernel(RecArgs ra) {
 // of a chain is bounded too; whoever gives up first flags the status word, and
 // the others stop at once.
 constexpr uint32_t kFusedSmem = kRecSmem > (uint32_t)kPrepSmem ? kRecSmem : (uint32_t)kPrepSmem;
+template <bool kRingMode, bool kChannelDecay>
 __global__ void __launch_bounds__(kRecThreads, 1)
     fused_kernel(const __grid_constant__ PrepArgs pa, RecArgs ra, int *ready) {
+    // kRingMode: blocks in per-chain rings (pa.ring = ra.ring > 0)
     const int nchains = pa.gcount;
     if ((int)blockIdx.x < nchains) {
         if (pa.cu && pa.first_chunk[pa.N + 1] < 0) return;  // malformed offsets, already flagged
-        recur_chain(ra, chain_of_rank(pa.gbase + blockIdx.x, pa.cu, pa.first_chunk, pa.N, pa.H),
+        recur_chain<kRingMode>(ra, chain_of_rank(pa.gbase + blockIdx.x, pa.cu, pa.first_chunk, pa.N, pa.H),
                     blockIdx.x, ready);
     } else {
-        prep_loop(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
+        prep_loop<kRingMode, kChannelDecay>(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
     }
+}
+inline const void *fused_fn(bool ring, bool channel_decay) {
+    return ring ? (channel_decay ? (const void *)fused_kernel<true, true>
+                                 : (const void *)fused_kernel<true, false>)
+                : (channel_decay ? (const void *)fused_kernel<false, true>
+                                 : (const void *)fused_kernel<false, false>);
 }
 
 }  // namespace pf
@@ -1952,13 +1965,14 @@ void prefill_tc_query(int N, long long T, long long T_total, int H, bool varlen,
         return;
     }
     if (p.schedule == 1) {
-        if (cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        const void *fk = pf::fused_fn(p.ring > 0, true);
+        if (cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pf::kFusedSmem) != cudaSuccess) {
             p.schedule = -1;
             return;
         }
         int per_sm = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pf::fused_kernel,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fk,
                                                           pf::kRecThreads, pf::kFusedSmem) !=
                 cudaSuccess ||
             per_sm < 1)
@@ -1972,8 +1986,9 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                               int g_per_channel, int snap_interval, int snap_max, float *snaps,
                               void *out, float *fin, unsigned char *ws, size_t ws_bytes,
                               unsigned test_wait_ms, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(pf::prep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const void *prep_fn = g_per_channel ? (const void *)pf::prep_kernel<true>
+                                        : (const void *)pf::prep_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(prep_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)pf::kPrepSmem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(pf::recur_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -2001,6 +2016,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
         off += pad256((size_t)(2 * N + 2) * 4);
     }
     const bool fused = plan.schedule == 1;
+    const void *fused_fn = pf::fused_fn(plan.ring > 0, g_per_channel != 0);
     int *ready = nullptr, *progress = nullptr;
     size_t flag_bytes = 0;
     if (fused) {
@@ -2012,7 +2028,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
             flag_bytes = pad256((size_t)nitems * 4);
         }
         off += flag_bytes;
-        e = cudaFuncSetAttribute(pf::fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fused_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)pf::kFusedSmem);
         if (e != cudaSuccess) return e;
     }
@@ -2063,7 +2079,7 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                 ra.wait_ns = (unsigned long long)test_wait_ms * 1000000ull;
             }
             void *args[] = {&pa, &ra, &ready};
-            e = cudaLaunchCooperativeKernel((const void *)pf::fused_kernel, dim3(grid),
+            e = cudaLaunchCooperativeKernel(fused_fn, dim3(grid),
                                             dim3(pf::kRecThreads), args, pf::kFusedSmem, stream);
             if (e != cudaSuccess) return e;
         }
@@ -2071,7 +2087,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     }
     if (nitems > 0) {
         const int grid = (int)(nitems < nsm ? nitems : nsm);  // one persistent CTA per SM
-        pf::prep_kernel<<<grid, pf::kPrepThreads, pf::kPrepSmem, stream>>>(pa);
+        void *args[] = {&pa};
+        e = cudaLaunchKernel(prep_fn, dim3(grid), dim3(pf::kPrepThreads), args, pf::kPrepSmem,
+                             stream);
+        if (e != cudaSuccess) return e;
     }
     pf::recur_kernel<<<(unsigned)nchains, pf::kRecThreads, pf::kRecSmem, stream>>>(ra);
     return cudaGetLastError();
