@@ -278,6 +278,9 @@ static_assert(kOffXh + 4 * 16 * 24 * 2 <= kOffKh, "T scratch inside X");
 // staged q, k of the next item: inside Kh (free after the Gram products)
 constexpr uint32_t kOffQs = kOffKh, kOffKs = kOffKh + 2 * kRegion;
 static_assert(kOffKs + 2 * kRegion <= kOffKtb, "q, k staging inside Kh");
+// staged beta of the next item (TMA: 64 tokens x 8 heads of bf16), after q and k
+constexpr uint32_t kOffBs = kOffKs + 2 * kRegion;
+static_assert(kOffBs + 64 * 16 <= kOffKtb, "beta staging inside Kh");
 static_assert(kOffX % 1024 == 0 && kOffKh % 1024 == 0 && kOffVs % 1024 == 0, "swizzled regions");
 
 // byte offset of 16-byte chunk `chunk` of row t in a 128-byte-swizzled region
@@ -293,6 +296,14 @@ __device__ __forceinline__ uint32_t qkv_off(int t, int c8) {
     return (uint32_t)(c8 >> 6) * kRegion + swz128(t, (c8 & 63) >> 3);
 }
 // 3-D tensor-map load (box of the map) into shared memory, counted on `bar`
+// 2-D tensor-map load ([T_total][H] per-token values; box = 64 tokens x 16 bytes of heads)
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
                                             int c2, uint32_t bar) {
     asm volatile(
@@ -385,6 +396,10 @@ __device__ __forceinline__ void lds8(const float *s, float *x) {
 
 struct PrepArgs {
     CUtensorMap tmq, tmk, tmv, tmg;  // [T_total][H][128]: boxes of 64 tokens x 64 (bf16) / 32 (fp32) channels
+    // [T_total][H] beta (bf16) and one decay per token and head (fp32): boxes of 64
+    // tokens x 16 bytes of heads, used when H allows 16-byte rows (else plain loads)
+    CUtensorMap tmb, tmgs;
+    int beta_tma, gs_tma;
     const __nv_bfloat16 *q, *k, *v;
     const float *g;
     const __nv_bfloat16 *beta;
@@ -592,6 +607,11 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
 #pragma unroll
                 for (int r = 0; r < 4; ++r) tma_load_3d(uG + r * kRegion, &pa.tmg, 32 * r, h_, tc_, bInG);
             }
+        } else if (pa.gs_tma) {  // 64 tokens x 4 heads -> the a buffer
+            if (tid == kStager) {
+                tc::mbar_arrive_expect_tx(bInG, 64 * 16);
+                tma_load_2d(uG, &pa.tmgs, h_ & ~3, tc_, bInG);
+            }
         } else {
             if (tid == kStager) tc::mbar_arrive_expect_tx(bInG, 0);  // nothing in flight: the phase completes
             if (tid < C) gs_next = tid < L_ ? g[((size_t)tc_ + tid) * H + h_] : 0.f;
@@ -599,19 +619,22 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     };
     auto stage_qkv = [&](int tc_, int h_) {
         if (tid == kStager) {
-            tc::mbar_arrive_expect_tx(bInQKV, 6 * kRegion);
+            tc::mbar_arrive_expect_tx(bInQKV, 6 * kRegion + (pa.beta_tma ? 64 * 16 : 0));
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 tma_load_3d(uQ + r * kRegion, &pa.tmq, 64 * r, h_, tc_, bInQKV);
                 tma_load_3d(uK + r * kRegion, &pa.tmk, 64 * r, h_, tc_, bInQKV);
                 tma_load_3d(uV + r * kRegion, &pa.tmv, 64 * r, h_, tc_, bInQKV);
             }
+            if (pa.beta_tma) tma_load_2d(sbase + kOffBs, &pa.tmb, h_ & ~7, tc_, bInQKV);
         }
     };
     // beta of token tid - 64 of an item, held by warps 2 and 3 (not by the warps of
-    // the T phase's diagonal blocks); raw bits, converted only where used, so that
-    // the load does not stall the issuing warp
+    // the T phase's diagonal blocks): staged by TMA with q, k, v when H is a
+    // multiple of 8, else loaded into a register (raw bits, converted only where
+    // used; a CTA barrier then waits for that load, which is why TMA is preferred)
     const bool beta_thr = tid >= 64 && tid < 64 + C;
+    const bool beta_reg = beta_thr && !pa.beta_tma;
     auto load_beta = [&](int tc_, int h_, int L_) -> unsigned short {
         const int t = tid - 64;
         return t < L_ ? __bfloat16_as_ushort(beta[((size_t)tc_ + t) * H + h_]) : (unsigned short)0;
@@ -624,7 +647,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         if (tokens(split(first), f)) {
             stage_g(f.tc, f.h, f.L);
             stage_qkv(f.tc, f.h);
-            if (beta_thr) beta_next = load_beta(f.tc, f.h, f.L);
+            if (beta_reg) beta_next = load_beta(f.tc, f.h, f.L);
             staged = first;
         }
     }
@@ -682,7 +705,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (staged != item) {  // the previous item could not prefetch this one
         stage_g(tc, h, L);
         stage_qkv(tc, h);
-        if (beta_thr) beta_next = load_beta(tc, h, L);
+        if (beta_reg) beta_next = load_beta(tc, h, L);
     }
     unsigned char *blk = blocks + cit.blk * kBlock;
     Item nx;  // the next item of this CTA
@@ -697,12 +720,17 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const int prog_slot = next_slot;
     next_slot = -1;
 
-    if (beta_thr) sBeta[tid - 64] = __bfloat162float(__ushort_as_bfloat16(beta_next));
-    if (!gpc && tid < C) reinterpret_cast<float *>(smem + kOffGs)[tid] = gs_next;
+    if (beta_reg) sBeta[tid - 64] = __bfloat162float(__ushort_as_bfloat16(beta_next));
+    if (!gpc && !pa.gs_tma && tid < C) reinterpret_cast<float *>(smem + kOffGs)[tid] = gs_next;
     if (!failed && !tc::mbar_wait(bInG, it & 1u, kPrepWaitLimit)) failed = true;
     if (!failed && !tc::mbar_wait(bInQKV, it & 1u, kPrepWaitLimit)) failed = true;
     failed = __syncthreads_or(failed) != 0;
     if (failed) break;
+    if (beta_thr && pa.beta_tma) {  // from the staged box (read before the next barrier)
+        const int t = tid - 64;
+        sBeta[t] = t < L ? __bfloat162float(reinterpret_cast<const __nv_bfloat16 *>(smem + kOffBs)[8 * t + (h & 7)])
+                         : 0.f;
+    }
 
     // ---- cumulative decay: thread = (channel, 16-token tile), in place over g --------
     {
@@ -711,7 +739,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         for (int r = 0; r < 16; ++r) {  // rows past the chunk: g = 0
             const int t = 16 * ti4 + r;
             const float gv = gpc ? *reinterpret_cast<const float *>(smem + kOffAcum + a_off(t, ch))
-                                 : reinterpret_cast<const float *>(smem + kOffGs)[t];
+                             : pa.gs_tma ? reinterpret_cast<const float *>(smem + kOffAcum)[4 * t + (h & 3)]
+                                         : reinterpret_cast<const float *>(smem + kOffGs)[t];
             a[r] = t < L ? clamp_g(gv) : 0.f;
         }
 #pragma unroll
@@ -1028,11 +1057,25 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         tc::bulk_commit();
     }
     if (has_next) {  // the next item's q, k, v are on their way
-        if (beta_thr) beta_next = load_beta(ntc, nh, nL);
+        if (beta_reg) beta_next = load_beta(ntc, nh, nL);
         staged = nitem;
     }
 
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
+    // Without rings: warps 0..14 only (named barrier 1), so that the last warp
+    // publishes the previous block meanwhile (its release store waits ~1,500
+    // cycles for the ordering of prior writes) and rejoins at the full barrier
+    // before the W / U~ products. (barrier.sync, the form that lets a warp's lanes
+    // arrive apart.) In ring mode all warps take part: measured faster there.
+    constexpr bool kTOff15 = !kRingMode;
+    auto tsync = [&]() {
+        if (kTOff15) {
+            if (warp < kPrepWarps - 1)
+                asm volatile("barrier.sync 1, %0;\n" ::"n"(kPrepThreads - 32) : "memory");
+        } else {
+            __syncthreads();
+        }
+    };
     const uint32_t aT = sbase + kOffT, aAh = sbase + kOffAh;
     if (tid < 64) {
         // column cc of the inverse of block b by forward substitution: entry r is
@@ -1057,9 +1100,9 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) store_h(smem + kOffT, off_k64(16 * b + r, 16 * b + cc), x[r]);
-    } else {
+    } else if (!kTOff15 || warp < kPrepWarps - 1) {
         // blocks above the diagonal of T: zero
-        for (int idx = tid - 64; idx < 6 * 128; idx += kPrepThreads - 64) {
+        for (int idx = tid - 64; idx < 6 * 128; idx += kPrepThreads - (kTOff15 ? 96 : 64)) {
             const int b_ = idx >> 7, e = idx & 127;
             const int bi = b_ < 3 ? 0 : (b_ < 5 ? 1 : 2);
             const int bj = b_ < 3 ? b_ + 1 : (b_ < 5 ? b_ - 1 : 3);
@@ -1067,7 +1110,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(t, s2)) = 0u;
         }
     }
-    __syncthreads();
+    tsync();
     {
         // Below the diagonal blocks, in two rounds (16x16 tiles, fp16 tensor cores):
         //  1. T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22;
@@ -1108,7 +1151,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             mma_f16_16816(tacc[1], af, bf[2], bf[3]);
             store_tile_T(16 * i, 16 * j, tacc);
         }
-        __syncthreads();
+        tsync();
         if (warp < 4) {  // X = A_BA T_AA, block (r, c), r in {2, 3}, c in {0, 1}
             const int r = 2 + (warp >> 1), c = warp & 1;
             float xacc[2][4] = {};
@@ -1123,7 +1166,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
             }
             store_tile(sXh + warp * 16 * 24, 24, xacc, 1.f);
         }
-        __syncthreads();
+        tsync();
         if (warp < 4) {  // T_rc = -sum_{k = 2}^{r} T_rk X_kc
             const int r = 2 + (warp >> 1), c = warp & 1;
             float tacc[2][4] = {};
@@ -1936,6 +1979,24 @@ bool make_token_map(CUtensorMap *m, const void *base, bool f32, int H, int T_tot
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [T_total][H] per-token values (bf16 beta or fp32 decay); box = 64 tokens x 16
+// bytes of heads. Only when a row of H values is a multiple of 16 bytes (the
+// tensor map's stride rule) and the base is 16-byte aligned; false otherwise.
+bool make_head_map(CUtensorMap *m, const void *base, bool f32, int H, int T_total) {
+    const EncodeTiledFn fn = encode_tiled();
+    const cuuint64_t es = f32 ? 4 : 2;
+    if (fn == nullptr || base == nullptr || ((uintptr_t)base & 15u) != 0 || (H * es) % 16 != 0)
+        return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T_total};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * es};
+    const cuuint32_t box[2] = {(cuuint32_t)(16 / es), 64u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+              const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Schedule override: -1 = automatic, 0 = split, 1 = fused. Its initial value
 // comes from the environment variable KDA_PREFILL_SCHEDULE ("split" or
 // "fused"), read once when the library is loaded; kda_prefill_set_schedule
@@ -2042,6 +2103,10 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                         make_token_map(&pa.tmv, v, false, H, T_total) &&
                         (!g_per_channel || make_token_map(&pa.tmg, g, true, H, T_total))))
         return cudaErrorUnknown;
+    if (nitems > 0) {
+        pa.beta_tma = make_head_map(&pa.tmb, beta, false, H, T_total) ? 1 : 0;
+        pa.gs_tma = !g_per_channel && make_head_map(&pa.tmgs, g, true, H, T_total) ? 1 : 0;
+    }
     pa.q = static_cast<const __nv_bfloat16 *>(q);
     pa.k = static_cast<const __nv_bfloat16 *>(k);
     pa.v = static_cast<const __nv_bfloat16 *>(v);

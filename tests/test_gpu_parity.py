@@ -168,11 +168,13 @@ def scalar_decay_inputs(lens, H, io, seed):
     return x, gs, x_full
 
 
+@pytest.mark.parametrize("H", [2, 8])
 @pytest.mark.parametrize("mode", ["split", "fused"])
-def test_bf16_prefill_scalar_decay(mode):
+def test_bf16_prefill_scalar_decay(mode, H):
     """g of shape [T_total, H] (one decay per token and head) equals the
-    channel-wise path with that decay on every channel."""
-    x, gs, x_full = scalar_decay_inputs([300, 1, 129], 2, "bf16", 71)
+    channel-wise path with that decay on every channel. (H = 8: beta and the
+    decays are staged by TMA; H = 2: loaded per token.)"""
+    x, gs, x_full = scalar_decay_inputs([300, 1, 129], H, "bf16", 71)
     cu = x.cu_seqlens.to(DEV)
     with prefill_schedule(mode):
         out, fin = kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), gs.to(DEV),
@@ -198,6 +200,27 @@ def test_bf16_prefill_scalar_decay_cancellation(lens, H, seed):
     torch.cuda.synchronize()
     ro, rf = oracle_prefill(x_full)
     assert out_err(out, ro) <= TOL_BF16 and rel_err(fin.cpu().numpy(), rf) <= TOL_BF16
+
+
+@pytest.mark.parametrize("per_head_g", [False, True])
+def test_bf16_beta_staging_paths_agree(per_head_g):
+    """beta at a 2-byte offset (no 16-byte rows for the tensor map: loaded per
+    token) and beta 16-byte aligned (staged by TMA with q, k, v) give the same
+    bits."""
+    x = inputs.prefill_inputs([300, 1, 129], H=8, io="bf16", seed=74, init="normal")
+    g = x.g[..., 0].contiguous() if per_head_g else x.g
+    b_al = x.beta.to(DEV)
+    raw = torch.empty(b_al.numel() + 1, dtype=torch.bfloat16, device=DEV)
+    b_off = raw[1:].view_as(b_al)
+    b_off.copy_(b_al)
+    assert b_off.data_ptr() % 16 != 0
+    res = []
+    for b in (b_al, b_off):
+        res.append(kda.kda_prefill(x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g.to(DEV), b, x.scale,
+                                   init_state=x.init_state.to(DEV),
+                                   cu_seqlens=x.cu_seqlens.to(DEV), chunk=64))
+    torch.cuda.synchronize()
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
 
 
 def test_f32_prefill_scalar_decay():
