@@ -247,9 +247,12 @@ int kda_prefill_set_schedule(int schedule);
  *   state_indices : DEVICE int32 [B], the pool entry of each sequence, or NULL
  *             (sequence b uses entry b; then pool_size >= B). An index < 0 or
  *             >= pool_size skips its sequence (no output, no state change).
- *             Indices must be distinct among the sequences of one call.
- *   out : io dtype [B, T, H, D]
- * Pointer alignment: 16 bytes. Needs no workspace. T = 0 or B = 0 is a no-op.
+ *             Indices must be distinct among the sequences of one call: two
+ *             sequences on one entry update it concurrently, and the entry
+ *             and both outputs are then undefined (not detected).
+ *   out : io dtype [B, T, H, D]; must not alias the inputs or the pool.
+ * Pointer alignment: 16 bytes (q, k, v, out, the pool; g when per channel).
+ * Needs no workspace. T = 0 or B = 0 is a no-op.
  * Returns KDA_ERR_UNSUPPORTED for T > 64, D != 128 or an unknown io.
  */
 int kda_decode(const void *q, const void *k, const void *v, const float *g, const void *beta,
