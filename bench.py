@@ -47,9 +47,11 @@ def prefill_flops_per_chunk(c=C, d=D):
     return 12 * c ** 3 + 8 * c * c * d + 6 * c * d * d
 
 
-def decode_bytes_per_head_token(d=D):
-    """~8 D^2 bytes per head and token: fp32 state read + write (same section)."""
-    return 8 * d * d
+def decode_bytes_per_head_call(tokens=1, d=D):
+    """Minimal HBM bytes per head and decode call of `tokens` tokens: the fp32
+    state read and written once (~8 D^2, same section), plus each token's row
+    (q, k, v, out in bf16, g in fp32, beta in bf16)."""
+    return 8 * d * d + tokens * prefill_bytes_per_head_token()
 
 
 def decode_flops_per_head_token(d=D):
@@ -699,7 +701,7 @@ def main():
         e1.record(g_stream)
         torch.cuda.synchronize()
         dms = max_over_ranks(e0.elapsed_time(e1) / (reps * S), world, dev)
-        state_bytes = decode_bytes_per_head_token() * B * Hd
+        state_bytes = decode_bytes_per_head_call(1) * B * Hd
         gbs = state_bytes / (dms * 1e-3) / 1e9
         decode = {
             "workload": "decode_b256_h96: B=256, H=96, D=128, 64 steps per graph, fp32 state "
@@ -749,7 +751,8 @@ def main():
         e1.record(g_stream)
         torch.cuda.synchronize()
         mms = max_over_ranks(e0.elapsed_time(e1) / (reps * calls), world, dev)
-        mgbs = state_bytes / (mms * 1e-3) / 1e9
+        multi_bytes = decode_bytes_per_head_call(Tm) * B * Hd
+        mgbs = multi_bytes / (mms * 1e-3) / 1e9
         decode["multi_token_pool"] = {
             "workload": "B=256, H=96, T=4 tokens per sequence per call, pool entries by a "
                         "permutation, 16 calls per graph",
@@ -757,8 +760,10 @@ def main():
             "tokens_per_s": Tm * B * Hd / (mms * 1e-3),
             "roofline": {"bound": "hbm", "achieved": mgbs, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": mgbs / peaks["hbm_gbs"],
-                         "kernel": "decode_kernel",
-                         "algorithmic_bytes_per_launch": state_bytes},
+                         "traffic": (measured_traffic("decode_multi_b256_h96_t4") or {}).get(
+                             "bytes_per_launch"),
+                         "peak_source": peak_src, "kernel": "decode_chunk_kernel",
+                         "algorithmic_bytes_per_launch": multi_bytes},
             "gpu_launches": reps * calls,
         }
         decode["gpu_launches"] += reps * calls

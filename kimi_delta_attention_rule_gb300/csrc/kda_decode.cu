@@ -304,6 +304,263 @@ __global__ void __launch_bounds__(kPipeThreads, 2)
     cp_async_wait_all();  // nothing may be in flight when the CTA exits
 }
 
+// ---------------------------------------------------------------------------
+// 2 <= T <= 4 tokens per sequence: decode_chunk_kernel. Same pipeline as
+// decode_pipe_kernel (persistent, two CTAs per SM, the next head's state and
+// token rows copied ahead with cp.async), but the T tokens are applied in
+// chunked form against the head's starting state S0, which needs five CTA
+// barriers per head instead of two per token. With A_t = sum_{r <= t} of the
+// clamped decays (per key channel), the same algebra as the prefill's chunks
+// ("Kimi K3: The Manos, The Mythos, The Legendos", section "FlashKDA 算法"),
+// solved token by token per value column instead of through an inverse:
+//   r_k(t) = S0^T (e^{A_t} k_t) + sum_{s < t} c_kk[t][s] u_s,
+//            c_kk[t][s] = sum_c k_s k_t e^{A_t - A_s}
+//   u_t    = beta_t (v_t - r_k(t))
+//   o_t    = scale (S0^T (e^{A_t} q_t) + sum_{s <= t} c_qk[t][s] u_s),
+//            c_qk[t][s] = sum_c k_s q_t e^{A_t - A_s}
+//   S_T    = Diag(e^{A_{T-1}}) S0 + sum_s (e^{A_{T-1} - A_s} k_s) u_s^T
+// (T <= 4 and g >= -5 keep every factor within e^{+-20} in fp32).
+constexpr int kChunkMaxT = 4;
+
+template <typename IO>
+__global__ void __launch_bounds__(kPipeThreads, 2)
+    decode_chunk_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
+                        const float *__restrict__ g, const IO *__restrict__ beta, float scale,
+                        int B, int T, int H, int g_per_channel, float *__restrict__ pool,
+                        int pool_size, const int32_t *__restrict__ idx, IO *__restrict__ out) {
+    const int io_row = kD * (int)sizeof(IO);
+    const int row_bytes = 3 * io_row + (g_per_channel ? kD * 4 : 0);
+    const int buf_bytes = kChunkMaxT * row_bytes;
+    extern __shared__ __align__(16) unsigned char dsm[];
+    float4 *sS = reinterpret_cast<float4 *>(dsm);  // [128 rows][32 float4]: the next state
+    unsigned char *sIn = dsm + kD * kD * 4;        // two input buffers
+    __shared__ float s_beta[kChunkMaxT], s_gs[kChunkMaxT];
+    __shared__ float s_ckk[kChunkMaxT][kChunkMaxT], s_cqk[kChunkMaxT][kChunkMaxT];
+    __shared__ __align__(16) float s_kt[kChunkMaxT][kD], s_qt[kChunkMaxT][kD], s_kb[kChunkMaxT][kD];
+    __shared__ __align__(16) float s_v[kChunkMaxT][kD], s_u[kChunkMaxT][kD];
+    __shared__ __align__(16) float s_eA[kD], s_ieA[kD];  // e^{A_{T-1}}, e^{-A_{T-1}}
+    __shared__ __align__(16) float s_red[kChunkMaxT][kPipeThreads / 32][kD];
+
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int nitems = B * H;
+    auto slot_of = [&](int it) { return idx ? idx[it / H] : it / H; };
+    auto valid = [&](int it) {
+        const int sl = slot_of(it);
+        return sl >= 0 && sl < pool_size;
+    };
+    auto next_valid = [&](int it) {
+        while (it < nitems && !valid(it)) it += gridDim.x;
+        return it;
+    };
+    float beta_r = 0.f, gs_r = 0.f;
+    auto prefetch = [&](int it, int slot, int bi) {  // as in decode_pipe_kernel
+        const int b = it / H, h = it - b * H;
+        const float4 *src = reinterpret_cast<const float4 *>(pool + ((size_t)slot * H + h) * kD * kD);
+#pragma unroll
+        for (int r = 0; r < kDecRowsPerWarp; ++r) {
+            const int o = (w * kDecRowsPerWarp + r) * (kD / 4) + lane;
+            cp_async16(&sS[o], &src[o]);
+        }
+        unsigned char *dst = sIn + bi * buf_bytes;
+        const int per_row = row_bytes / 16, total = T * per_row;
+        for (int c = tid; c < total; c += kPipeThreads) {
+            const int t = c / per_row, o = (c - t * per_row) * 16;
+            const size_t row = ((size_t)b * T + t) * H + h;
+            const void *gsrc;
+            if (o < 3 * io_row) {
+                const IO *base = o < io_row ? q : (o < 2 * io_row ? k : v);
+                gsrc = reinterpret_cast<const unsigned char *>(base + row * kD) + (o % io_row);
+            } else {
+                gsrc = reinterpret_cast<const unsigned char *>(g + row * kD) + (o - 3 * io_row);
+            }
+            cp_async16(dst + t * row_bytes + o, gsrc);
+        }
+        if (tid < T) {
+            const size_t row = ((size_t)b * T + tid) * H + h;
+            beta_r = to_f32(beta[row]);
+            if (!g_per_channel) gs_r = g[row];
+        }
+    };
+
+    int it = next_valid(blockIdx.x);
+    if (it >= nitems) return;
+    int slot = slot_of(it);
+    prefetch(it, slot, 0);
+    cp_async_commit();
+    int nit = next_valid(it + gridDim.x);
+    int nslot = nit < nitems ? slot_of(nit) : 0;
+    float4 s[kDecRowsPerWarp];
+#pragma unroll 1
+    for (int n = 0; it < nitems; ++n) {
+        const int b = it / H, h = it - b * H;
+        float4 *S4 = reinterpret_cast<float4 *>(pool + ((size_t)slot * H + h) * kD * kD);
+        cp_async_wait_all();
+#pragma unroll
+        for (int r = 0; r < kDecRowsPerWarp; ++r) s[r] = sS[(w * kDecRowsPerWarp + r) * (kD / 4) + lane];
+        if (tid < T) {
+            s_beta[tid] = beta_r;
+            s_gs[tid] = gs_r;
+        }
+        __syncthreads();  // (1) this item's inputs are in place
+        const unsigned char *in = sIn + (n & 1) * buf_bytes;
+        if (nit < nitems) prefetch(nit, nslot, (n + 1) & 1);
+        cp_async_commit();
+        const int nnit = nit < nitems ? next_valid(nit + gridDim.x) : nitems;
+        const int nnslot = nnit < nitems ? slot_of(nnit) : 0;
+
+        // per key channel c: A_t, the decayed keys and queries, v, and the final decay
+        if (tid < kD) {
+            const int c = tid;
+            float A[kChunkMaxT], kk[kChunkMaxT];
+            float acc = 0.f;
+#pragma unroll
+            for (int t = 0; t < kChunkMaxT; ++t) {
+                if (t < T) {
+                    const unsigned char *rw = in + t * row_bytes;
+                    const float gv = g_per_channel ? reinterpret_cast<const float *>(rw + 3 * io_row)[c]
+                                                   : s_gs[t];
+                    acc += clamp_g(gv);
+                    A[t] = acc;
+                    const float ea = __expf(acc);
+                    kk[t] = to_f32(reinterpret_cast<const IO *>(rw + io_row)[c]);
+                    s_kt[t][c] = ea * kk[t];
+                    s_qt[t][c] = ea * to_f32(reinterpret_cast<const IO *>(rw)[c]);
+                    s_v[t][c] = to_f32(reinterpret_cast<const IO *>(rw + 2 * io_row)[c]);
+                }
+            }
+            s_eA[c] = __expf(acc);
+            s_ieA[c] = __expf(-acc);
+#pragma unroll
+            for (int t = 0; t < kChunkMaxT; ++t)
+                if (t < T) s_kb[t][c] = __expf(acc - A[t]) * kk[t];
+        }
+        __syncthreads();  // (2)
+        // the coefficients (warp w: pairs w and w + 8 of the T x T grid) and the
+        // partial sums S0^T (e^{A_t} k_t) of this warp's 16 rows
+        for (int pr = w; pr < T * T; pr += kPipeThreads / 32) {
+            const int t = pr / T, s2 = pr - t * T;  // c_kk for s2 < t, c_qk for s2 <= t
+            if (s2 <= t) {
+                float pk = 0.f, pq = 0.f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = lane * 4 + e;
+                    const float f = s_kb[s2][c] * s_ieA[c];  // k_s e^{-A_s}
+                    pk += f * s_kt[t][c];
+                    pq += f * s_qt[t][c];
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    pk += __shfl_xor_sync(0xffffffffu, pk, off);
+                    pq += __shfl_xor_sync(0xffffffffu, pq, off);
+                }
+                if (lane == 0) {
+                    s_ckk[t][s2] = pk;
+                    s_cqk[t][s2] = pq;
+                }
+            }
+        }
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            float4 rk = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 *k4 = reinterpret_cast<const float4 *>(&s_kt[t][w * kDecRowsPerWarp]);
+#pragma unroll
+            for (int r4 = 0; r4 < kDecRowsPerWarp / 4; ++r4) {
+                const float4 kk = k4[r4];
+                const float kv[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 &x = s[4 * r4 + e];
+                    rk.x += x.x * kv[e]; rk.y += x.y * kv[e]; rk.z += x.z * kv[e]; rk.w += x.w * kv[e];
+                }
+            }
+            *reinterpret_cast<float4 *>(&s_red[t][w][lane * 4]) = rk;
+        }
+        __syncthreads();  // (3)
+        // column c: r_k(t) and the recurrence for u_t, token by token
+        if (tid < kD) {
+            const int c = tid;
+            float u[kChunkMaxT];
+#pragma unroll
+            for (int t = 0; t < kChunkMaxT; ++t) {
+                if (t < T) {
+                    float R = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kPipeThreads / 32; ++ww) R += s_red[t][ww][c];
+#pragma unroll
+                    for (int s2 = 0; s2 < kChunkMaxT; ++s2)
+                        if (s2 < t) R += s_ckk[t][s2] * u[s2];
+                    u[t] = s_beta[t] * (s_v[t][c] - R);
+                    s_u[t][c] = u[t];
+                }
+            }
+        }
+        __syncthreads();  // (4) u in place; the partial sums are free
+#pragma unroll 1
+        for (int t = 0; t < T; ++t) {
+            float4 rq = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 *q4 = reinterpret_cast<const float4 *>(&s_qt[t][w * kDecRowsPerWarp]);
+#pragma unroll
+            for (int r4 = 0; r4 < kDecRowsPerWarp / 4; ++r4) {
+                const float4 qq = q4[r4];
+                const float qv[4] = {qq.x, qq.y, qq.z, qq.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 &x = s[4 * r4 + e];
+                    rq.x += x.x * qv[e]; rq.y += x.y * qv[e]; rq.z += x.z * qv[e]; rq.w += x.w * qv[e];
+                }
+            }
+            *reinterpret_cast<float4 *>(&s_red[t][w][lane * 4]) = rq;
+        }
+        // the new state: e^{A_{T-1}} S0 + sum_s (e^{A_{T-1} - A_s} k_s) u_s^T, stored
+        {
+            float4 u4[kChunkMaxT];
+#pragma unroll
+            for (int t = 0; t < kChunkMaxT; ++t)
+                u4[t] = t < T ? *reinterpret_cast<const float4 *>(&s_u[t][lane * 4])
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int r = 0; r < kDecRowsPerWarp; ++r) {
+                const int row = w * kDecRowsPerWarp + r;
+                const float ea = s_eA[row];
+                float4 x = s[r];
+                x.x *= ea; x.y *= ea; x.z *= ea; x.w *= ea;
+#pragma unroll
+                for (int t = 0; t < kChunkMaxT; ++t) {
+                    const float kb = t < T ? s_kb[t][row] : 0.f;
+                    x.x += kb * u4[t].x; x.y += kb * u4[t].y; x.z += kb * u4[t].z; x.w += kb * u4[t].w;
+                }
+                S4[row * (kD / 4) + lane] = x;
+            }
+        }
+        __syncthreads();  // (5) the partial sums S0^T (e^{A_t} q_t)
+        if (tid >= kD) {  // column c: the outputs of the T tokens
+            const int c = tid - kD;
+#pragma unroll
+            for (int t = 0; t < kChunkMaxT; ++t) {
+                if (t < T) {
+                    float R = 0.f;
+#pragma unroll
+                    for (int ww = 0; ww < kPipeThreads / 32; ++ww) R += s_red[t][ww][c];
+#pragma unroll
+                    for (int s2 = 0; s2 < kChunkMaxT; ++s2)
+                        if (s2 <= t) R += s_cqk[t][s2] * s_u[s2][c];
+                    out[(((size_t)b * T + t) * H + h) * kD + c] = from_f32<IO>(scale * R);
+                }
+            }
+        }
+        it = nit;
+        slot = nslot;
+        nit = nnit;
+        nslot = nnslot;
+    }
+    cp_async_wait_all();  // nothing may be in flight when the CTA exits
+}
+
+template <typename IO>
+size_t decode_chunk_smem() {
+    return (size_t)kD * kD * 4 + 2 * (size_t)kChunkMaxT * (3 * kD * sizeof(IO) + kD * 4);
+}
+
 template <typename IO>
 size_t decode_pipe_smem() {
     return (size_t)kD * kD * 4 + 2 * (size_t)kPipeMaxT * (3 * kD * sizeof(IO) + kD * 4);
@@ -316,7 +573,23 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const flo
                           cudaStream_t stream) {
     const long long grid = (long long)B * H;
     if (grid == 0 || T == 0) return cudaSuccess;
-    if (T >= 2 && T <= kPipeMaxT) {
+    if (T >= 2 && T <= kChunkMaxT) {
+        const size_t smem = decode_chunk_smem<IO>();
+        int dev = 0, nsm = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(decode_chunk_kernel<IO>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        const long long pgrid = grid < 2LL * nsm ? grid : 2LL * nsm;
+        decode_chunk_kernel<IO><<<(unsigned)pgrid, kPipeThreads, smem, stream>>>(
+            static_cast<const IO *>(q), static_cast<const IO *>(k), static_cast<const IO *>(v), g,
+            static_cast<const IO *>(beta), scale, B, T, H, g_per_channel, pool, pool_size, idx,
+            static_cast<IO *>(out));
+        return cudaGetLastError();
+    }
+    if (T > kChunkMaxT && T <= kPipeMaxT) {
         const size_t smem = decode_pipe_smem<IO>();
         int dev = 0, nsm = 0;
         cudaError_t e = cudaGetDevice(&dev);

@@ -420,6 +420,35 @@ def test_multi_token_decode(io, tol, T):
     assert rel_err(st.cpu().numpy(), rf) <= tol
 
 
+@pytest.mark.parametrize("io,tol,T", [("bf16", TOL_BF16, 2), ("bf16", TOL_BF16, 4),
+                                      ("bf16", TOL_BF16, 8), ("f32", TOL_F32, 3),
+                                      ("f32", TOL_F32, 4)])
+@pytest.mark.parametrize("scalar_g", [False, True])
+def test_multi_token_decode_many_heads(io, tol, T, scalar_g):
+    """512 (sequence, head) items, more than one CTA per SM takes: the
+    persistent multi-token kernel runs several items per CTA through its
+    rotating buffers. Pool entries by a permutation with padding entries
+    (skipped) and entries no sequence uses (bit-identical afterwards)."""
+    B, H, P = 64, 8, 80
+    gen = np.random.default_rng(T + 17)
+    perm = gen.permutation(P)[:B].astype(np.int64)
+    perm[[3, 17, 40]] = -1
+    idx = [int(x) for x in perm]
+    q, k, v, g, beta, scale, pool, run, slot, ro, rf = multi_decode_case(
+        B, T, H, io, 77 + T, scalar_g=scalar_g, P=P, idx=idx)
+    st = pool.to(DEV)
+    dt = q.dtype
+    out = torch.full((B, T, H, 128), 7.0, dtype=dt, device=DEV)
+    kda.kda_decode(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), scale, st,
+                   state_indices=torch.tensor(idx, dtype=torch.int32, device=DEV), out=out)
+    torch.cuda.synchronize()
+    assert out_err(out[run], ro) <= tol
+    assert rel_err(st[slot].cpu().numpy(), rf) <= tol
+    assert torch.all(out[[3, 17, 40]] == 7.0)
+    unused = [p for p in range(P) if p not in slot]
+    assert torch.equal(st[unused].cpu(), pool[unused])
+
+
 @pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
 def test_decode_scalar_decay(io, tol):
     """One decay per (token, head) (g of shape [B, T, H]) equals the
