@@ -74,6 +74,9 @@ constexpr uint32_t kGam = kUt + 128 * 128;        // fp32 [128] e^{a_C}
 constexpr uint32_t kNu = kGam + 128 * 4;          // int32 nu: beta v (and so U~) is stored
                                                   //   scaled by 2^-nu (rest of 128 B unused)
 constexpr uint32_t kBlock = kNu + 128;            // 74368 B
+// Blocks in flight per chain in ring mode (bounded workspace): a compile-time
+// constant, so that the ring indexing is masks and takes no registers.
+constexpr int kRingLen = 16;
 static_assert(kBlock % 128 == 0, "block size");
 
 // Range of the fp16 operands. Only the Gram operands need bf16's exponent
@@ -457,7 +460,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const bool fused = ready != nullptr;  // chunk-major over a group of chains
     // blocks in per-chain rings (a separate instantiation: the ring logic costs
     // the other modes registers and time when it is merely present)
-    const int RG = kRingMode ? pa.ring : 0;
+    const int RG = kRingMode ? kRingLen : 0;
     const bool ring = kRingMode && fused && RG > 0;
     int nitems = pa.nitems;
     if (fused) {  // the most chunks of one chain in the group
@@ -667,10 +670,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     };
     // ring mode: wait (bounded) until chain i has loaded chunk `need` - 1; gives
     // up at once if another party of the launch has given up
+    // The poll backs off (up to ~0.5 us): the chains that it waits for read their
+    // blocks through the same L2, and a producer that waits is ahead anyway.
     auto wait_progress = [&](int i, int need) -> bool {
         if (ld_progress(pa.progress + i) >= need) return true;
         const uint64_t t0 = tc::globaltimer_ns();
+        unsigned pause = 32;
         while (true) {
+            __nanosleep(pause);
+            pause = pause < 512 ? 2 * pause : 512;
             if (ld_progress(pa.progress + i) >= need) return true;
             if (*reinterpret_cast<volatile uint32_t *>(pa.status) & kStatusTimeout) return false;
             if (tc::globaltimer_ns() - t0 > kPrepWaitLimit) return false;
@@ -1395,7 +1403,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
     const uint32_t tlane = tm + ((uint32_t)(32 * (warp & 3)) << 16);
 
     const size_t head_state = ((size_t)n * H + h) * 128 * 128;
-    const int RG = kRingMode ? ra.ring : 0;
+    const int RG = kRingMode ? kRingLen : 0;
     // the block of chunk x
     auto blk_of = [&](int x) -> const unsigned char * {
         return ready && RG > 0 ? ra.blocks + ((size_t)gi * RG + x % RG) * kBlock
@@ -1658,13 +1666,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
             tc::fence_after_sync();
             uint32_t sr[2][16], orr[1][16];
             tc::tmem_ld_cols<2>(tlane + kColS + 32 * qd, sr);
-            tc::tmem_ld_cols<1>(tlane + kColO + 16 * qd, orr);
-            {  // this chunk's output rows -> staging, written out during the next chunk
-                __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO + (c & 1) * 16384);
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(so * __uint_as_float(orr[0][e]));
-            }
+            tc::tmem_ld_cols<1>(tlane + kColO + 16 * qd, orr);  // staged after the next issue
             float sf[32];  // the new state, in units of 2^sig_next
             {
                 const float f = exp2i(sig - sig_next);
@@ -1690,6 +1692,13 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
             // fp16 state, are in TMEM: no proxy fence before these barriers)
             sync_check();
             if (tid == 0 && c + 1 < nchunks && !failed) issue_mma1(c + 1);
+            {  // this chunk's output rows -> staging (off the chain's critical path: the
+               // next product is under way), written out during the next chunk
+                __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(smem + kOffO + (c & 1) * 16384);
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    sO[(16 * qd + e) * 128 + j] = __float2bfloat16_rn(so * __uint_as_float(orr[0][e]));
+            }
             // this chunk's buffer is free: without flags, fetch chunk c + 2 into it now
             if (tid == kLoader) check_issue(c + 2);  // known to exist (or no flags)
 
@@ -1734,7 +1743,8 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
                 so = scale * exp2i(sig);
             }
         }
-        write_out(nchunks - 1);  // staged before the last barrier of the loop
+        __syncthreads();  // the last chunk's output rows were staged after the loop's last barrier
+        write_out(nchunks - 1);
     }
 
     if (failed) {
@@ -1806,7 +1816,7 @@ long long prefill_slots(int N, long long T, long long T_total, bool varlen) {
     if (T_total <= 0) return 0;
     return varlen ? (T_total + pf::C - 1) / pf::C + N : (long long)N * ((T + pf::C - 1) / pf::C);
 }
-constexpr int kRing = 16;  // blocks per chain in flight in ring mode (a multiple of 4)
+constexpr int kRing = pf::kRingLen;  // blocks per chain in flight in ring mode (a multiple of 4)
 // Chains per fused launch when they are many (groups run one after the other):
 // the G that minimises the modelled time of all groups, a group of x chains of L
 // chunks taking max(L t_chain, x L t_block / (SMs - x)) with the measured paces
@@ -1878,7 +1888,7 @@ bool ring_plan(const PlanSizes &z, long long G, PrefillPlan &p) {
     G = std::max(1LL, std::min(G, z.nchains));
     p.schedule = 1;
     p.group_chains = (int)G;
-    p.ring = (int)std::min<long long>(kRing, std::max<long long>(4, (z.maxc + 3) / 4 * 4));
+    p.ring = kRing;
     p.groups = (int)((z.nchains + G - 1) / G);
     p.bytes = z.base + pad256((size_t)G * (p.ring + 1) * 4) + (size_t)G * p.ring * pf::kBlock;
     return true;

@@ -34,7 +34,7 @@ def _lens(name):
     if name == "packed":     # 160 ragged chains incl. empty ones, longest first
         gen = np.random.default_rng(17)
         return [int(x) for x in gen.integers(0, 900, size=38)] + [0, 1], 4
-    return [5, 0, 129, 1], 2  # "tiny": ring shorter than the default 16
+    return [5, 0, 129, 1], 2  # "tiny": a ring longer than the sequences
 
 
 def _sizes(x, H):
