@@ -420,11 +420,13 @@ def ncu_case(args):
         for _ in range(args.warmup + 1):
             kda.kda_layer_prologue(*raw[:4], braw, *convs)
             kda.kda_layer_epilogue(raw[0], raw[4], nw)
-    elif args.ncu_case == "prefill":
+    elif args.ncu_case in ("prefill", "prefill_ring"):
         x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"],
                                   device=dev)
+        kind = "ring" if args.ncu_case == "prefill_ring" else "fast"
+        ws = kda.prefill_workspace(x.q, None, N=1, T=PREFILL["T"], chunk=C, kind=kind)
         for _ in range(args.warmup + 1):
-            kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, chunk=C)
+            kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, chunk=C, workspace=ws)
     elif args.ncu_case == "decode_multi":  # T = 4 tokens per sequence through a permuted pool
         B, Hd, Tm = args.decode_batch, DECODE["H"], 4
         xm = inputs.prefill_inputs([Tm] * B, H=Hd, io="bf16", seed=DECODE["seed"] + 5, device=dev)
@@ -452,7 +454,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "decode", "decode_multi", "layer"], default=None,
+    ap.add_argument("--ncu-case", choices=["prefill", "prefill_ring", "decode", "decode_multi", "layer"],
+                    default=None,
                     help="run only `warmup` + 1 launches of one kernel (for ncu captures)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"])
     ap.add_argument("--min-timed-s", type=float, default=1.0,
@@ -549,7 +552,9 @@ def main():
                                     final_state=fin, workspace=ws_r, stream=stream), stream)
         ms_r = max_over_ranks(ms_r, world, dev)
         assert kda.kda_workspace_status(ws_r) == kda.KDA_OK
+        tr_ring = measured_traffic("prefill_ring_h32_t8192")
         bounded_ws = {"workspace_bytes": ring_bytes, "full_workspace_bytes": ws.numel(),
+                      "traffic": tr_ring["bytes_per_launch"] if tr_ring else None,
                       "ms_per_call": ms_r, "calls_timed": n_r,
                       "value": H * T * world / (ms_r * 1e-3) / 1e6, "unit": "Mtok/s",
                       "vs_full_workspace": ms / ms_r,
