@@ -9,6 +9,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "kda.h"  /* kda_prefill_plan_info */
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -32,6 +34,22 @@ int kda_testing_prefill_chain_timeout(const void *q, const void *k, const void *
                                       int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
                                       int32_t io, void *out, float *final_state, void *workspace,
                                       size_t workspace_bytes, int32_t wait_ms, void *stream);
+
+/*
+ * The workspace-plan selection of the bf16 prefill (the host logic behind
+ * kda_prefill_plan) for given device properties instead of the current
+ * device's, so that it can be checked without a GPU: sm_count SMs,
+ * cooperative != 0 if cooperative launches are supported, schedule_override
+ * -1 (automatic), KDA_SCHEDULE_SPLIT or KDA_SCHEDULE_FUSED. kind 0: the plan
+ * that a workspace of workspace_bytes gets; 1: the fastest plan; 2: the ring
+ * plan with the modelled best group; 3: the smallest accepted plan (kinds 1-3
+ * ignore workspace_bytes). Sizes as in kda_prefill_workspace_size (D = 128,
+ * chunk 64). Writes *plan and returns KDA_OK; KDA_ERR_INVALID_ARG when the
+ * arguments are invalid or no plan fits. Launches nothing, needs no device.
+ */
+int kda_testing_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t varlen, int32_t sm_count,
+                             int32_t cooperative, int32_t schedule_override, int32_t kind,
+                             size_t workspace_bytes, kda_prefill_plan_info *plan);
 
 #ifdef __cplusplus
 }

@@ -111,6 +111,8 @@ def load() -> ctypes.CDLL:
         lib.kda_testing_prefill_chain_timeout.argtypes = [P, P, P, P, P, F32, P, P, I32, I32, I32,
                                                           I32, I32, I32, P, P, P, SZ, I32, P]
         lib.kda_testing_prefill_chain_timeout.restype = ctypes.c_int
+        lib.kda_testing_prefill_plan.argtypes = [I32] * 8 + [SZ, ctypes.POINTER(PrefillPlanInfo)]
+        lib.kda_testing_prefill_plan.restype = ctypes.c_int
         _lib = lib
         return lib
 

@@ -32,6 +32,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
 void prefill_tc_query(int N, long long T, long long T_total, int H, bool varlen, size_t budget,
                       PrefillPlan &p);
 int prefill_tc_set_schedule(int s);
+bool prefill_tc_plan_for(int N, long long T, long long T_total, int H, bool varlen, int nsm,
+                         int coop, int force, size_t budget, int kind, PrefillPlan &p);
 template <typename IO>
 cudaError_t launch_layer_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
                                   const void *alpha_raw, const void *beta_raw, const float *wq,
@@ -257,6 +259,23 @@ int kda_testing_prefill_chain_timeout(const void *q, const void *k, const void *
     return prefill_impl(q, k, v, g, beta, scale, init_state, cu_seqlens, N, T, H, D, chunk, io, 1,
                         0, 0, nullptr, out, final_state, workspace, workspace_bytes,
                         (unsigned)wait_ms, stream);
+}
+
+int kda_testing_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t varlen, int32_t sm_count,
+                             int32_t cooperative, int32_t schedule_override, int32_t kind,
+                             size_t workspace_bytes, kda_prefill_plan_info *plan) {
+    if (plan == nullptr || kind < 0 || kind > 3 || schedule_override < -1 || schedule_override > 1)
+        return KDA_ERR_INVALID_ARG;
+    long long tt = 0;
+    const int rc = check_prefill_dims(N, T, H, kda::kD, 64, KDA_BF16, varlen != 0, &tt);
+    if (rc != KDA_OK) return rc;
+    kda::PrefillPlan p;
+    if (!kda::prefill_tc_plan_for(N, T, tt, H, varlen != 0, sm_count, cooperative != 0,
+                                  schedule_override, workspace_bytes, kind, p))
+        return KDA_ERR_INVALID_ARG;
+    *plan = kda_prefill_plan_info{p.schedule == 1 ? KDA_SCHEDULE_FUSED : KDA_SCHEDULE_SPLIT,
+                                  p.groups, p.group_chains, p.ring, p.bytes};
+    return KDA_OK;
 }
 
 int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,

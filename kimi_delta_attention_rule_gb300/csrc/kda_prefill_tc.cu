@@ -1850,19 +1850,18 @@ struct PlanSizes {
     long long nchains, slots, L, maxc;
     size_t base;  // status word and (packed sequences) the chunk schedule
 };
-bool plan_sizes(int N, long long T, long long T_total, int H, bool varlen, PlanSizes &z) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&z.nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&z.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
-        return false;
-    z.force = prefill_tc_schedule_override();  // -1 auto, 0 split, 1 fused
+PlanSizes plan_sizes(int N, long long T, long long T_total, int H, bool varlen, int nsm, int coop,
+                     int force) {
+    PlanSizes z;
+    z.nsm = nsm;
+    z.coop = coop;
+    z.force = force;  // -1 auto, 0 split, 1 fused
     z.nchains = (long long)N * H;
     z.slots = prefill_slots(N, T, T_total, varlen);
     z.base = 256 + (varlen ? pad256((size_t)(2 * N + 2) * 4) : 0);
     z.L = varlen ? (N > 0 ? (T_total / N + pf::C - 1) / pf::C : 0) : (T + pf::C - 1) / pf::C;
     z.maxc = ((varlen ? T_total : T) + pf::C - 1) / pf::C;
-    return true;
+    return z;
 }
 bool can_fuse(const PlanSizes &z) { return z.coop && z.nchains > 0 && z.slots > 0; }
 // The fastest plan: the fused schedule (one block per chunk and head) when the
@@ -1895,16 +1894,18 @@ bool ring_plan(const PlanSizes &z, long long G, PrefillPlan &p) {
 }
 }  // namespace
 
-// The plan for these sizes that a workspace of `budget` bytes gets: the
-// fastest plan if it fits; else the fused schedule with rings, with the
-// modelled best number of chains per group or, if that does not fit, the most
-// that do. kind 1 / 2 / 3 ask for the fastest plan, the ring plan with the best
-// group, and the smallest accepted plan, whatever the budget. False when
-// nothing fits (or the device cannot be queried).
-bool prefill_tc_plan(int N, long long T, long long T_total, int H, bool varlen, size_t budget,
-                     int kind, PrefillPlan &p) {
-    PlanSizes z;
-    if (!plan_sizes(N, T, T_total, H, varlen, z)) return false;
+// The plan for these sizes that a workspace of `budget` bytes gets on a device
+// with `nsm` SMs (cooperative launches if `coop`), under the schedule override
+// `force`: the fastest plan if it fits; else the fused schedule with rings, with
+// the modelled best number of chains per group or, if that does not fit, the
+// most that do. kind 1 / 2 / 3 ask for the fastest plan, the ring plan with the
+// best group, and the smallest accepted plan, whatever the budget. False when
+// nothing fits. (Host logic only: the test entry point runs it for given
+// device properties.)
+bool prefill_tc_plan_for(int N, long long T, long long T_total, int H, bool varlen, int nsm,
+                         int coop, int force, size_t budget, int kind, PrefillPlan &p) {
+    if (nsm <= 0) return false;
+    const PlanSizes z = plan_sizes(N, T, T_total, H, varlen, nsm, coop, force);
     const PrefillPlan fast = fast_plan(z, H);
     if (kind == 1) {
         p = fast;
@@ -1944,6 +1945,18 @@ bool prefill_tc_plan(int N, long long T, long long T_total, int H, bool varlen, 
         --G;
     }
     return false;
+}
+
+// The same on the current device, under the process-wide override.
+bool prefill_tc_plan(int N, long long T, long long T_total, int H, bool varlen, size_t budget,
+                     int kind, PrefillPlan &p) {
+    int dev = 0, nsm = 0, coop = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+        return false;
+    return prefill_tc_plan_for(N, T, T_total, H, varlen, nsm, coop, prefill_tc_schedule_override(),
+                               budget, kind, p);
 }
 
 size_t prefill_tc_workspace(int N, long long T, long long T_total, int H, bool varlen, int kind) {
