@@ -151,3 +151,37 @@ def test_no_tokens_copies_initial_to_final_state(lens):
                                workspace=ws)
     assert kda.kda_workspace_status(ws) == kda.KDA_OK
     assert torch.equal(fin, init) and out.numel() == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("workload", ["append_h96", "varlen64_h32_floor"])
+def test_ring_plan_full_size_bitwise(workload):
+    """The full-size append (H=96, 65,536 tokens after a 32,768-token prefill)
+    and packed varlen (64 sequences) workloads: the ring workspace (tens of MB,
+    fused schedule in groups) and the full workspace (GBs, split schedule)
+    give the same bits, outputs and final states. (Their parity with the oracle
+    is sampled in tests/test_gpu_parity.py.)"""
+    w = inputs.WORKLOADS[workload]
+    if workload == "append_h96":
+        P, Ta, H = w["prior"], w["T"], w["H"]
+        x = inputs.prefill_inputs([P + Ta], H=H, io="bf16", seed=w["seed"], device=DEV)
+        _, init = kda.kda_prefill(x.q[:P], x.k[:P], x.v[:P], x.g[:P], x.beta[:P], x.scale, chunk=64)
+        q, k, v, g, b = (t[P:] for t in (x.q, x.k, x.v, x.g, x.beta))
+        cu, N, T = None, 1, Ta
+    else:
+        lens = inputs.varlen_lengths(w["n_seqs"], w["lo"], w["hi"], seed=w["seed"])
+        H = w["H"]
+        x = inputs.prefill_inputs(lens, H=H, io="bf16", seed=w["seed"], g_mode="floor",
+                                  init="normal", device=DEV)
+        q, k, v, g, b, init, cu = x.q, x.k, x.v, x.g, x.beta, x.init_state, x.cu_seqlens
+        N, T = len(lens), q.shape[0]
+    res = []
+    for kind in ("fast", "ring"):
+        ws = kda.prefill_workspace(q, cu, N=N, T=T, chunk=64, kind=kind)
+        res.append(kda.kda_prefill(q, k, v, g, b, x.scale, init_state=init, cu_seqlens=cu,
+                                   chunk=64, workspace=ws, N=N, T=T))
+        assert kda.kda_workspace_status(ws) == kda.KDA_OK
+        del ws
+    torch.cuda.synchronize()
+    assert torch.equal(res[0][0], res[1][0])
+    assert torch.equal(res[0][1], res[1][1])
