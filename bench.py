@@ -420,10 +420,12 @@ def ncu_case(args):
         for _ in range(args.warmup + 1):
             kda.kda_layer_prologue(*raw[:4], braw, *convs)
             kda.kda_layer_epilogue(raw[0], raw[4], nw)
-    elif args.ncu_case in ("prefill", "prefill_ring"):
-        x = inputs.prefill_inputs([PREFILL["T"]], H=PREFILL["H"], io="bf16", seed=PREFILL["seed"],
+    elif args.ncu_case in ("prefill", "prefill_ring", "prefill_ring_h96"):
+        # prefill_ring_h96: T=8192 with K3's 96 heads, ring workspace (96 chains in groups)
+        Hc = 96 if args.ncu_case == "prefill_ring_h96" else PREFILL["H"]
+        x = inputs.prefill_inputs([PREFILL["T"]], H=Hc, io="bf16", seed=PREFILL["seed"],
                                   device=dev)
-        kind = "ring" if args.ncu_case == "prefill_ring" else "fast"
+        kind = "fast" if args.ncu_case == "prefill" else "ring"
         ws = kda.prefill_workspace(x.q, None, N=1, T=PREFILL["T"], chunk=C, kind=kind)
         for _ in range(args.warmup + 1):
             kda.kda_prefill(x.q, x.k, x.v, x.g, x.beta, x.scale, chunk=C, workspace=ws)
@@ -454,7 +456,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
-    ap.add_argument("--ncu-case", choices=["prefill", "prefill_ring", "decode", "decode_multi", "layer"],
+    ap.add_argument("--ncu-case", choices=["prefill", "prefill_ring", "prefill_ring_h96", "decode",
+                                           "decode_multi", "layer"],
                     default=None,
                     help="run only `warmup` + 1 launches of one kernel (for ncu captures)")
     ap.add_argument("--decode-batch", type=int, default=DECODE["B"])
