@@ -43,7 +43,7 @@ class PrefillPlanInfo(ctypes.Structure):
     """kda_prefill_plan_info: the plan that kda_prefill runs."""
     _fields_ = [("schedule", ctypes.c_int32), ("groups", ctypes.c_int32),
                 ("group_chains", ctypes.c_int32), ("ring", ctypes.c_int32),
-                ("bytes", ctypes.c_size_t)]
+                ("bytes", ctypes.c_size_t), ("lead_items", ctypes.c_int64)]
 
 _lock = threading.Lock()
 _lib = None

@@ -109,7 +109,7 @@ const char *kda_status_string(int status) {
     }
 }
 
-int kda_abi_version(void) { return 100; }
+int kda_abi_version(void) { return 101; }
 
 size_t kda_prefill_workspace_size(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk,
                                   int32_t io, int32_t varlen) {
@@ -140,7 +140,7 @@ int kda_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, 
     if (rc != KDA_OK) return rc;
     if (io == KDA_F32) {
         if (workspace_bytes < kWorkspaceBytes) return KDA_ERR_INVALID_ARG;
-        *plan = kda_prefill_plan_info{KDA_SCHEDULE_DIRECT, 0, 0, 0, kWorkspaceBytes};
+        *plan = kda_prefill_plan_info{KDA_SCHEDULE_DIRECT, 0, 0, 0, kWorkspaceBytes, 0};
         return KDA_OK;
     }
     kda::PrefillPlan p;
@@ -148,7 +148,7 @@ int kda_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, 
     if (p.schedule == -2) return KDA_ERR_INVALID_ARG;
     if (p.schedule < 0) return KDA_ERR_CUDA;
     *plan = kda_prefill_plan_info{p.schedule == 1 ? KDA_SCHEDULE_FUSED : KDA_SCHEDULE_SPLIT,
-                                  p.groups, p.group_chains, p.ring, p.bytes};
+                                  p.groups, p.group_chains, p.ring, p.bytes, p.lead_items};
     return KDA_OK;
 }
 
@@ -274,7 +274,7 @@ int kda_testing_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t varlen, in
                                   schedule_override, workspace_bytes, kind, p))
         return KDA_ERR_INVALID_ARG;
     *plan = kda_prefill_plan_info{p.schedule == 1 ? KDA_SCHEDULE_FUSED : KDA_SCHEDULE_SPLIT,
-                                  p.groups, p.group_chains, p.ring, p.bytes};
+                                  p.groups, p.group_chains, p.ring, p.bytes, p.lead_items};
     return KDA_OK;
 }
 

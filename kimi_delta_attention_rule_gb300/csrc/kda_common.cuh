@@ -22,10 +22,13 @@ __device__ __forceinline__ float clamp_g(float g) { return fminf(fmaxf(g, kGMin)
 
 // How the bf16 prefill runs for given sizes (host side): schedule 1 = fused
 // (groups of group_chains chains, `groups` cooperative launches; ring > 0:
-// blocks in per-chain rings of that length), 0 = split; bytes of workspace.
+// blocks in per-chain rings of that length; lead_items > 0: that many blocks
+// are prepared by a launch of producers only before the chains start), 0 =
+// split; bytes of workspace.
 struct PrefillPlan {
-    int schedule, groups, group_chains, ring;
-    size_t bytes;
+    int schedule = 0, groups = 0, group_chains = 0, ring = 0;
+    size_t bytes = 0;
+    long long lead_items = 0;
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

@@ -56,6 +56,7 @@
 #include <cuda.h>  // CUtensorMap (the encoder is resolved at run time)
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -417,6 +418,10 @@ struct PrepArgs {
     // the chunks chain i has loaded; ring = 0: one block per (chunk slot, head)
     // and flags [head][slot] (nslots slots).
     int ring, gbase, gcount, nslots;
+    // fused schedule: CTAs [0, chain_ctas) run chains (0: a launch of producers
+    // only); the producers prepare items [item_begin, item_end) of the group's
+    // chunk-major order
+    int chain_ctas, item_begin, item_end;
     int *progress;
 };
 
@@ -474,7 +479,7 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                 maxc = max(maxc, L > 0 ? (L + C - 1) / C : 0);
             }
         }
-        nitems = maxc * pa.gcount;
+        nitems = min(maxc * pa.gcount, pa.item_end);
     }
     // Item cursor: items are visited first, first + stride, ..., so the digits of
     // an item index advance by carries and the loop needs no division:
@@ -1782,13 +1787,14 @@ template <bool kRingMode, bool kChannelDecay>
 __global__ void __launch_bounds__(kRecThreads, 1)
     fused_kernel(const __grid_constant__ PrepArgs pa, RecArgs ra, int *ready) {
     // kRingMode: blocks in per-chain rings (pa.ring = ra.ring > 0)
-    const int nchains = pa.gcount;
+    const int nchains = pa.chain_ctas;
     if ((int)blockIdx.x < nchains) {
         if (pa.cu && pa.first_chunk[pa.N + 1] < 0) return;  // malformed offsets, already flagged
         recur_chain<kRingMode>(ra, chain_of_rank(pa.gbase + blockIdx.x, pa.cu, pa.first_chunk, pa.N, pa.H),
                     blockIdx.x, ready);
     } else {
-        prep_loop<kRingMode, kChannelDecay>(pa, blockIdx.x - nchains, gridDim.x - nchains, ready);
+        prep_loop<kRingMode, kChannelDecay>(pa, pa.item_begin + (int)blockIdx.x - nchains,
+                                            gridDim.x - nchains, ready);
     }
 }
 inline const void *fused_fn(bool ring, bool channel_decay) {
@@ -1847,7 +1853,8 @@ namespace {
 // What every plan for these sizes shares.
 struct PlanSizes {
     int nsm, coop, force;
-    long long nchains, slots, L, maxc;
+    bool equal_lengths;  // every chain has maxc_chain chunks
+    long long nchains, slots, L, maxc, maxc_chain;
     size_t base;  // status word and (packed sequences) the chunk schedule
 };
 PlanSizes plan_sizes(int N, long long T, long long T_total, int H, bool varlen, int nsm, int coop,
@@ -1861,22 +1868,55 @@ PlanSizes plan_sizes(int N, long long T, long long T_total, int H, bool varlen, 
     z.base = 256 + (varlen ? pad256((size_t)(2 * N + 2) * 4) : 0);
     z.L = varlen ? (N > 0 ? (T_total / N + pf::C - 1) / pf::C : 0) : (T + pf::C - 1) / pf::C;
     z.maxc = ((varlen ? T_total : T) + pf::C - 1) / pf::C;
+    // the longest chain's chunks (packed sequences: at most the whole batch)
+    z.maxc_chain = varlen ? z.maxc : (T + pf::C - 1) / pf::C;
+    z.equal_lengths = !varlen || N == 1;
     return z;
 }
 bool can_fuse(const PlanSizes &z) { return z.coop && z.nchains > 0 && z.slots > 0; }
-// The fastest plan: the fused schedule (one block per chunk and head) when the
-// chains take at most a third of the SMs, else K1 then K2; the override forces
-// either.
+// Paces measured on GB300 at D = 128, for the choice between schedules: K1 per
+// block and K2 per chunk of a chain, each kernel alone, and both roles inside
+// the fused kernel while the other role runs on the remaining SMs (shared
+// memory system and power budget; the chains also read the ready flags).
+constexpr double kPaceBlockUs = 6.1, kPaceChainUs = 1.58;
+constexpr double kPaceBlockFusedUs = 6.3, kPaceChainFusedUs = 2.15;
+constexpr int kMinProducers = 16;
+// The fastest plan, one block per chunk and head:
+//  - chains on at most a third of the SMs: the fused schedule;
+//  - up to all SMs but kMinProducers: the fused schedule with a lead, if the
+//    model below says it is faster than K1 then K2 — a launch of producers only
+//    prepares the first `lead` blocks (chunk-major) on every SM, then the chains
+//    start at once while the remaining SMs prepare the rest, lead chosen so that
+//    the rest is done by the time the chains need it: lead = blocks - (SMs -
+//    chains) / t_block_fused x L t_chain_fused. (This uses the SMs that K2
+//    alone would leave idle.) Model: split = blocks t_block / SMs + L t_chain;
+//    lead = lead t_block_fused / SMs + L t_chain_fused; the lead plan when it
+//    is at least 3 % faster. (Only for chains of one known length: with
+//    packed sequences the host knows neither the lengths nor the longest.)
+//  - otherwise K1 then K2. The override forces the split or the fused schedule
+//    (in groups of chains when they are many).
 PrefillPlan fast_plan(const PlanSizes &z, int H) {
-    PrefillPlan p{0, 0, 0, 0, 0};
-    const bool fused = can_fuse(z) && (z.force == 1 || (z.force == -1 && 3 * z.nchains <= z.nsm));
-    p.schedule = fused ? 1 : 0;
+    PrefillPlan p{0, 0, 0, 0, 0, 0};
     p.bytes = z.base + (size_t)z.slots * H * pf::kBlock;
-    if (fused) {
-        p.group_chains = group_chains(z.nchains, z.L, z.nsm);
-        p.groups = (int)((z.nchains + p.group_chains - 1) / p.group_chains);
-        p.bytes += pad256((size_t)z.slots * H * 4);
+    if (!can_fuse(z) || z.force == 0) return p;
+    const bool fused = z.force == 1 || 3 * z.nchains <= z.nsm;
+    long long lead = 0;
+    if (!fused) {
+        if (z.nchains > z.nsm - kMinProducers || !z.equal_lengths) return p;
+        const double blocks = (double)z.slots * H, Lc = (double)z.maxc_chain;
+        const double rest = (double)(z.nsm - z.nchains) / kPaceBlockFusedUs * Lc * kPaceChainFusedUs;
+        const double lead_d = blocks - rest;
+        const double t_split = blocks * kPaceBlockUs / z.nsm + Lc * kPaceChainUs;
+        const double t_lead =
+            (lead_d > 0 ? lead_d : 0.0) * kPaceBlockFusedUs / z.nsm + Lc * kPaceChainFusedUs;
+        if (!(t_lead < 0.97 * t_split)) return p;
+        lead = lead_d > 0 ? (long long)lead_d : 0;
     }
+    p.schedule = 1;
+    p.group_chains = lead > 0 || !fused ? (int)z.nchains : group_chains(z.nchains, z.L, z.nsm);
+    p.groups = (int)((z.nchains + p.group_chains - 1) / p.group_chains);
+    p.lead_items = lead;
+    p.bytes += pad256((size_t)z.slots * H * 4);
     return p;
 }
 // The fused schedule with rings, G chains per group (G <= 0: the modelled
@@ -1888,6 +1928,7 @@ bool ring_plan(const PlanSizes &z, long long G, PrefillPlan &p) {
     p.schedule = 1;
     p.group_chains = (int)G;
     p.ring = kRing;
+    p.lead_items = 0;
     p.groups = (int)((z.nchains + G - 1) / G);
     p.bytes = z.base + pad256((size_t)G * (p.ring + 1) * 4) + (size_t)G * p.ring * pf::kBlock;
     return true;
@@ -1911,7 +1952,7 @@ bool prefill_tc_plan_for(int N, long long T, long long T_total, int H, bool varl
         p = fast;
         return true;
     }
-    PrefillPlan r;
+    PrefillPlan r{0, 0, 0, 0, 0, 0};
     const bool have_ring = ring_plan(z, 0, r);
     if (kind == 2) {
         if (!have_ring) return false;
@@ -1919,7 +1960,7 @@ bool prefill_tc_plan_for(int N, long long T, long long T_total, int H, bool varl
         return true;
     }
     if (kind == 3) {
-        PrefillPlan r1;
+        PrefillPlan r1{0, 0, 0, 0, 0, 0};
         p = (ring_plan(z, 1, r1) && r1.bytes < fast.bytes) ? r1 : fast;
         return true;
     }
@@ -2045,7 +2086,7 @@ void prefill_tc_query(int N, long long T, long long T_total, int H, bool varlen,
                       PrefillPlan &p) {
     if (!prefill_tc_plan(N, T, T_total, H, varlen, budget, 0, p)) {
         PrefillPlan any;
-        p = PrefillPlan{prefill_tc_plan(N, T, T_total, H, varlen, 0, 3, any) ? -2 : -1, 0, 0, 0, 0};
+        p = PrefillPlan{prefill_tc_plan(N, T, T_total, H, varlen, 0, 3, any) ? -2 : -1, 0, 0, 0, 0, 0};
         return;
     }
     if (p.schedule == 1) {
@@ -2162,11 +2203,27 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
                 if (e != cudaSuccess) return e;
             }
             unsigned grid = (unsigned)nsm;
+            void *args[] = {&pa, &ra, &ready};
+            pa.chain_ctas = pa.gcount;
+            pa.item_begin = 0;
+            pa.item_end = INT_MAX;
+            if (plan.lead_items > 0 && plan.ring == 0 && !test_wait_ms) {
+                // the lead: the first blocks of the chunk-major order on every SM,
+                // by producers only (published through the same flags), then the
+                // chains start with them in place
+                pa.chain_ctas = 0;
+                pa.item_end = (int)std::min<long long>(plan.lead_items, nitems);
+                e = cudaLaunchCooperativeKernel(fused_fn, dim3(grid), dim3(pf::kRecThreads), args,
+                                                pf::kFusedSmem, stream);
+                if (e != cudaSuccess) return e;
+                pa.chain_ctas = pa.gcount;
+                pa.item_begin = pa.item_end;
+                pa.item_end = INT_MAX;
+            }
             if (test_wait_ms) {  // chains with no producer at all and a short wait bound:
                 grid = (unsigned)pa.gcount;  // every wait for a ready flag runs out
                 ra.wait_ns = (unsigned long long)test_wait_ms * 1000000ull;
             }
-            void *args[] = {&pa, &ra, &ready};
             e = cudaLaunchCooperativeKernel(fused_fn, dim3(grid),
                                             dim3(pf::kRecThreads), args, pf::kFusedSmem, stream);
             if (e != cudaSuccess) return e;

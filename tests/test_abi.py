@@ -40,7 +40,7 @@ def test_status_strings(lib):
                        (6, "KDA_ERR_TOO_LARGE"), (7, "KDA_ERR_RANGE")]:
         assert kda.status_string(code) == name
     assert kda.status_string(99) == "KDA_ERR_UNKNOWN"
-    assert lib.kda_abi_version() == 100
+    assert lib.kda_abi_version() == 101
 
 
 def test_workspace_size(lib):

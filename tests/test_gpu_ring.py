@@ -110,6 +110,49 @@ def test_ring_plan_with_snapshots_and_per_head_decay():
     assert rel_err(res[0][1].cpu().numpy(), rf) <= TOL_BF16
 
 
+@pytest.mark.parametrize("case", ["h64_t2048", "h80_t600_one_packed", "h40_n2_per_head"])
+def test_lead_plan_agrees_with_split_and_oracle(case):
+    """Chains on more than a third of the SMs but fewer than the SMs less 16,
+    all of one length: the full workspace gets the fused schedule with a lead
+    (a launch of producers only, then the chains with the remaining SMs
+    preparing the rest). Same arithmetic as K1 then K2: bit for bit the split
+    results, and within the bf16 tolerance of the oracle."""
+    per_head = case.endswith("per_head")
+    if case == "h64_t2048":
+        N, L, H, packed = 1, 2048, 64, False
+    elif case == "h80_t600_one_packed":
+        N, L, H, packed = 1, 600, 80, True   # one packed sequence, ragged tail
+    else:
+        N, L, H, packed = 2, 777, 40, False  # 80 chains, one decay per head
+    x = inputs.prefill_inputs([L] * N, H=H, io="bf16", seed=305, init="normal")
+    bf = kda.KDA_BF16
+    T_arg = N * L if packed else L
+    full = kda.kda_prefill_workspace_size(N, T_arg, H, 128, 64, bf, packed)
+    plan = kda.kda_prefill_plan(N, T_arg, H, 128, 64, bf, packed, full)
+    assert plan.schedule == kda.KDA_SCHEDULE_FUSED and plan.ring == 0
+    assert plan.groups == 1 and plan.group_chains == N * H
+    assert 0 < plan.lead_items < N * H * ((L + 63) // 64)
+    g = x.g[..., 0].contiguous() if per_head else x.g
+    args = (x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g.to(DEV), x.beta.to(DEV), x.scale)
+    cu = x.cu_seqlens.to(DEV) if packed else None
+    res = {}
+    for mode in (None, "split"):
+        with prefill_schedule(mode):
+            ws = kda.prefill_workspace(args[0], cu, N=N, T=L, chunk=64)
+            out, fin = kda.kda_prefill(*args, init_state=x.init_state.to(DEV), cu_seqlens=cu,
+                                       chunk=64, workspace=ws, N=N, T=L)
+            assert kda.kda_workspace_status(ws) == kda.KDA_OK
+            torch.cuda.synchronize()
+            res[mode] = (out, fin)
+    assert torch.equal(res[None][0], res["split"][0])
+    assert torch.equal(res[None][1], res["split"][1])
+    if per_head:
+        x.g = x.g[..., :1].expand_as(x.g).contiguous()
+    ro, rf = oracle_prefill(x)
+    assert out_err(res[None][0], ro) <= TOL_BF16
+    assert rel_err(res[None][1].cpu().numpy(), rf) <= TOL_BF16
+
+
 def test_workspace_below_the_minimum_is_rejected():
     x = inputs.prefill_inputs([300, 40], H=2, io="bf16", seed=303, init="normal")
     N, T, H = _sizes(x, 2)

@@ -41,9 +41,81 @@ def test_fastest_plan_few_chains_is_fused_one_block_per_chunk(plan):
 
 
 def test_fastest_plan_many_chains_is_split(plan):
-    rc, p = plan(1, 65536, 96, kind=1)
+    """More chains than the SMs less 16 (2 x 96 = 192): K1 then K2."""
+    rc, p = plan(2, 65536, 96, kind=1)
+    assert rc == kda.KDA_OK and p.schedule == kda.KDA_SCHEDULE_SPLIT and p.lead_items == 0
+    assert p.bytes == 256 + 2 * 1024 * 96 * BLOCK
+
+
+def _lead_model(nchains, L, nsm=NSM):
+    """The schedule model with the paces measured on GB300 (K1 6.1 us per block
+    and K2 1.58 us per chunk alone; 6.3 and 2.15 inside the fused kernel)."""
+    blocks = nchains * L
+    lead = blocks - (nsm - nchains) / 6.3 * L * 2.15
+    t_split = blocks * 6.1 / nsm + L * 1.58
+    t_lead = max(lead, 0) * 6.3 / nsm + L * 2.15
+    return max(lead, 0), t_lead < 0.97 * t_split
+
+
+def test_fastest_plan_mid_chain_count_has_a_lead(plan):
+    """64 chains of 1,024 chunks: the fused schedule with a lead. The rest
+    after the lead is what the 88 other SMs prepare while the chains run
+    (88 / 6.3 us x 1,024 chunks x 2.15 us ~ 30,750 blocks), so the chains never
+    wait for a block that is not in the lead or made in time."""
+    rc, p = plan(1, 65536, 64, kind=1)
+    blocks = 1024 * 64
+    lead, chosen = _lead_model(64, 1024)
+    assert chosen
+    assert rc == kda.KDA_OK and p.schedule == kda.KDA_SCHEDULE_FUSED and p.ring == 0
+    assert p.groups == 1 and p.group_chains == 64
+    assert abs(p.lead_items - lead) <= 1 and 0 < p.lead_items < blocks
+    assert p.bytes == 256 + pad256(blocks * 4) + blocks * BLOCK
+    # the same count of chains as 2 sequences x 32 heads
+    rc, p2 = plan(2, 65536, 32, kind=1)
+    assert p2.schedule == kda.KDA_SCHEDULE_FUSED and p2.lead_items == p.lead_items
+
+
+@pytest.mark.parametrize("N,T,H", [(1, 65536, 96), (1, 65536, 112), (1, 8192, 96), (2, 8192, 40),
+                                   (1, 16384, 64), (1, 2048, 64), (2, 777, 40), (1, 600, 80),
+                                   (1, 640, 51), (3, 64, 40)])
+def test_lead_plan_follows_the_model(plan, N, T, H):
+    rc, p = plan(N, T, H, kind=1)
+    L = (T + 63) // 64
+    lead, chosen = _lead_model(N * H, L)
+    assert rc == kda.KDA_OK
+    if 3 * N * H <= NSM:
+        assert p.schedule == kda.KDA_SCHEDULE_FUSED and p.lead_items == 0
+    elif chosen:
+        assert p.schedule == kda.KDA_SCHEDULE_FUSED and abs(p.lead_items - lead) <= 1
+        assert p.groups == 1 and p.group_chains == N * H
+    else:
+        assert p.schedule == kda.KDA_SCHEDULE_SPLIT and p.lead_items == 0
+
+
+def test_lead_only_when_modelled_faster(plan):
+    # 128 chains leave 24 producers: the lead plan models no faster than split
+    rc, p = plan(1, 65536, 128, kind=1)
     assert rc == kda.KDA_OK and p.schedule == kda.KDA_SCHEDULE_SPLIT
-    assert p.bytes == 256 + 1024 * 96 * BLOCK
+    # 137 chains: more than the SMs less 16
+    rc, p = plan(1, 65536, 137, kind=1)
+    assert p.schedule == kda.KDA_SCHEDULE_SPLIT and p.lead_items == 0
+    # 64 chains of 32 chunks: lead
+    rc, p = plan(1, 2048, 64, kind=1)
+    assert p.schedule == kda.KDA_SCHEDULE_FUSED and 0 < p.lead_items < 32 * 64
+    # packed sequences of unknown lengths: no lead
+    rc, p = plan(2, 65536, 32, varlen=True, kind=1)
+    assert p.schedule == kda.KDA_SCHEDULE_SPLIT and p.lead_items == 0
+    # one packed sequence: its length is known
+    rc, p = plan(1, 65536, 64, varlen=True, kind=1)
+    assert p.schedule == kda.KDA_SCHEDULE_FUSED and p.lead_items > 0
+    # the override: split, or fused without a lead
+    rc, p = plan(1, 65536, 64, kind=1, force=0)
+    assert p.schedule == kda.KDA_SCHEDULE_SPLIT and p.lead_items == 0
+    rc, p = plan(1, 65536, 64, kind=1, force=1)
+    assert p.schedule == kda.KDA_SCHEDULE_FUSED and p.lead_items == 0
+    # ring plans have no lead
+    rc, p = plan(1, 65536, 64, kind=2)
+    assert p.ring == 16 and p.lead_items == 0
 
 
 def test_ring_plan_does_not_grow_with_the_length(plan):
