@@ -288,7 +288,8 @@ int kda_decode(const void *q, const void *k, const void *v, const float *g, cons
  *
  * kda_layer_epilogue: y = o / sqrt(mean(o^2) + 1e-6) * w * sigmoid(gate_raw)
  * per (token, head) over its D channels: o, gate_raw, y io dtype
- * [T_total, H, D]; norm_weight fp32 [D] (16-byte aligned).
+ * [T_total, H, D], 16-byte aligned (both dtypes); norm_weight fp32 [D]
+ * (16-byte aligned).
  *
  * Both return KDA_ERR_UNSUPPORTED for D != 128, W outside 1..4 or an unknown
  * io; T_total = 0 is a no-op.

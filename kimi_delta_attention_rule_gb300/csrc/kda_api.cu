@@ -399,9 +399,9 @@ int kda_layer_epilogue(const void *o, const void *gate_raw, const float *norm_we
     if ((long long)T_total * H > (1LL << 33)) return KDA_ERR_INVALID_ARG;
     if (T_total == 0) return KDA_OK;
     if (!o || !gate_raw || !norm_weight || !y) return KDA_ERR_INVALID_ARG;
-    const unsigned a = io == KDA_F32 ? 15u : 7u;
+    // rows are read and written 8 channels (16 or 32 bytes) per lane
     for (const void *p : {o, gate_raw, static_cast<const void *>(y)})
-        if (reinterpret_cast<uintptr_t>(p) & a) return KDA_ERR_INVALID_ARG;
+        if (!aligned16(p)) return KDA_ERR_INVALID_ARG;
     if (!aligned16(norm_weight)) return KDA_ERR_INVALID_ARG;
     NvtxRange range("kda_layer_epilogue");
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -12,7 +12,8 @@
 // RMS-normalised over the head's 128 channels (eps 1e-6) with a weight per
 // channel and multiplied by sigmoid(gate).
 //
-// Both kernels are HBM streams over [T_total, H, 128] rows, 4 channels per lane.
+// Both kernels are HBM streams over [T_total, H, 128] rows (the prologue 4
+// channels per lane, the epilogue 8).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -328,24 +329,86 @@ __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
             *reinterpret_cast<decltype(win[m][i - 1].v) *>(state_row(m, i)) = win[m][i - 1].v;
 }
 
+// Epilogue: 16 lanes per row (8 channels each, 16-byte loads of bf16), two rows
+// per warp step, kEpiSteps steps per warp with every load issued before the
+// first row is reduced.
+constexpr int kEpiSteps = 4;
+template <typename IO>
+struct Raw8;
+template <>
+struct Raw8<float> {
+    float4 a, b;
+};
+template <>
+struct Raw8<__nv_bfloat16> {
+    uint4 a;
+};
+__device__ __forceinline__ Raw8<float> ld_raw8(const float *p) {
+    Raw8<float> r;
+    r.a = *reinterpret_cast<const float4 *>(p);
+    r.b = *reinterpret_cast<const float4 *>(p + 4);
+    return r;
+}
+__device__ __forceinline__ Raw8<__nv_bfloat16> ld_raw8(const __nv_bfloat16 *p) {
+    Raw8<__nv_bfloat16> r;
+    r.a = *reinterpret_cast<const uint4 *>(p);
+    return r;
+}
+__device__ __forceinline__ void cvt8(const Raw8<float> &r, float *x) {
+    x[0] = r.a.x; x[1] = r.a.y; x[2] = r.a.z; x[3] = r.a.w;
+    x[4] = r.b.x; x[5] = r.b.y; x[6] = r.b.z; x[7] = r.b.w;
+}
+__device__ __forceinline__ void cvt8(const Raw8<__nv_bfloat16> &r, float *x) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&r.a);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[2 * e] = __low2float(h[e]);
+        x[2 * e + 1] = __high2float(h[e]);
+    }
+}
+__device__ __forceinline__ void st8(float *p, const float *x) {
+    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+    *reinterpret_cast<float4 *>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+}
+__device__ __forceinline__ void st8(__nv_bfloat16 *p, const float *x) {
+    *reinterpret_cast<uint4 *>(p) =
+        make_uint4(pack_bf16(x[0], x[1]), pack_bf16(x[2], x[3]), pack_bf16(x[4], x[5]), pack_bf16(x[6], x[7]));
+}
 template <typename IO>
 __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
     layer_epilogue_kernel(const IO *__restrict__ o, const IO *__restrict__ gate_raw,
                           const float *__restrict__ w, long long rows, IO *__restrict__ y) {
-    const int lane = threadIdx.x & 31;
-    const long long r = (long long)blockIdx.x * kLayerRowsPerCta + (threadIdx.x >> 5);
-    if (r >= rows) return;
-    const size_t off = (size_t)r * kD + 4 * lane;
-    float a[4], gr[4];
-    load4<IO>(o + off, a);
-    load4<IO>(gate_raw + off, gr);
-    const float s =
-        rsqrtf(warp_sum(a[0] * a[0] + a[1] * a[1] + a[2] * a[2] + a[3] * a[3]) * (1.f / kD) + kRmsEps);
-    const float4 wv = *reinterpret_cast<const float4 *>(w + 4 * lane);
-    const float wl[4] = {wv.x, wv.y, wv.z, wv.w};
+    const int lane = threadIdx.x & 31, c0 = 8 * (lane & 15);
+    const long long r0 = ((long long)blockIdx.x * kLayerRowsPerCta + (threadIdx.x >> 5)) * (2 * kEpiSteps) +
+                         (lane >> 4);
+    Raw8<IO> ro[kEpiSteps], rg[kEpiSteps];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) a[e] = a[e] * s * wl[e] * sigmoidf_(gr[e]);
-    store4<IO>(y + off, a);
+    for (int st = 0; st < kEpiSteps; ++st) {
+        const long long r = r0 + 2 * st;
+        if (r < rows) {
+            ro[st] = ld_raw8(o + (size_t)r * kD + c0);
+            rg[st] = ld_raw8(gate_raw + (size_t)r * kD + c0);
+        }
+    }
+    float wl[8];
+    *reinterpret_cast<float4 *>(wl) = *reinterpret_cast<const float4 *>(w + c0);
+    *reinterpret_cast<float4 *>(wl + 4) = *reinterpret_cast<const float4 *>(w + c0 + 4);
+#pragma unroll
+    for (int st = 0; st < kEpiSteps; ++st) {
+        const long long r = r0 + 2 * st;
+        float a[8], gr[8];
+        cvt8(ro[st], a);
+        cvt8(rg[st], gr);
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss += a[e] * a[e];
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);  // the row's 16 lanes
+        const float sc = rsqrtf(ss * (1.f / kD) + kRmsEps);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a[e] = a[e] * sc * wl[e] * sigmoidf_(gr[e]);
+        if (r < rows) st8(y + (size_t)r * kD + c0, a);
+    }
 }
 
 template <typename IO>
@@ -407,7 +470,8 @@ cudaError_t launch_layer_epilogue(const void *o, const void *gate_raw, const flo
                                   long long T_total, int H, void *y, cudaStream_t stream) {
     const long long rows = T_total * H;
     if (rows == 0) return cudaSuccess;
-    const long long grid = (rows + kLayerRowsPerCta - 1) / kLayerRowsPerCta;
+    const long long per_cta = (long long)kLayerRowsPerCta * 2 * kEpiSteps;
+    const long long grid = (rows + per_cta - 1) / per_cta;
     layer_epilogue_kernel<IO><<<(unsigned)grid, 32 * kLayerRowsPerCta, 0, stream>>>(
         static_cast<const IO *>(o), static_cast<const IO *>(gate_raw), w, rows,
         static_cast<IO *>(y));

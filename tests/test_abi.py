@@ -192,6 +192,7 @@ def test_layer_argument_validation(lib):
     assert call_epi(T=-1) == kda.KDA_ERR_INVALID_ARG and call_epi(o=None) == kda.KDA_ERR_INVALID_ARG
     assert call_epi(w=odd) == kda.KDA_ERR_INVALID_ARG
     assert call_epi(io=1, o=odd) == kda.KDA_ERR_INVALID_ARG
+    assert call_epi(io=0, o=odd) == kda.KDA_ERR_INVALID_ARG  # bf16 rows too: 16 B per lane
     assert call_epi(T=0) == kda.KDA_OK
 
 

@@ -371,11 +371,14 @@ def test_layer_prologue_decode(io, tol, W):
 
 
 @pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
-def test_layer_epilogue(io, tol):
+@pytest.mark.parametrize("T", [37, 1000])
+def test_layer_epilogue(io, tol, T):
+    """37 x 4 = 148 rows: three CTAs of 64 rows, the last one ragged; 1000 x 4
+    = 4,000 rows: 63 CTAs, 32 rows in the last."""
     gen = torch.Generator().manual_seed(91)
     dt = torch.bfloat16 if io == "bf16" else torch.float32
-    o = (3 * torch.randn(37, 4, 128, generator=gen)).to(dt)
-    gr = torch.randn(37, 4, 128, generator=gen).to(dt)
+    o = (3 * torch.randn(T, 4, 128, generator=gen)).to(dt)
+    gr = torch.randn(T, 4, 128, generator=gen).to(dt)
     w = 1 + 0.1 * torch.randn(128, generator=gen)
     y = kda.kda_layer_epilogue(o.to(DEV), gr.to(DEV), w.to(DEV))
     torch.cuda.synchronize()
