@@ -56,6 +56,7 @@
 #include <cuda.h>  // CUtensorMap (the encoder is resolved at run time)
 
 #include <algorithm>
+#include <type_traits>
 #include <climits>
 #include <atomic>
 #include <cstdlib>
@@ -78,6 +79,13 @@ constexpr uint32_t kBlock = kNu + 128;            // 74368 B
 // Blocks in flight per chain in ring mode (bounded workspace): a compile-time
 // constant, so that the ring indexing is masks and takes no registers.
 constexpr int kRingLen = 16;
+// Ring mode: each chain's ready flags and its progress counter sit on cache
+// lines of their own (32 ints), so that no line is written by more than one
+// chain or polled for more than one chain: with the flags of all chains packed
+// together the call's time depended ~2x on where the workspace started (the
+// hot lines sharing L2 slices).
+constexpr int kLineInts = 32;
+static_assert(kRingLen <= kLineInts, "a chain's ring flags fit one line");
 static_assert(kBlock % 128 == 0, "block size");
 
 // Range of the fp16 operands. Only the Gram operands need bf16's exponent
@@ -224,7 +232,9 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
 // K1: chunk preparation
 // ============================================================================
 // One CTA (16 warps) per SM, persistent over (chunk, head) items. Per item:
-//   cumulative decay a (thread = channel x 16-token tile);
+//   cumulative decay a (thread = channel x 16-token tile; for all but a CTA's
+//   first item it was formed during the previous item's T phase, by the warps
+//   that phase leaves idle);
 //   one pass over the tokens builds every operand (thread = 8 channels x two
 //   tokens of one 16-token tile; 8 consecutive lanes take 8 consecutive
 //   tokens, so that their 16-byte stores into the core-matrix layouts fall in
@@ -239,7 +249,6 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int32_t *__restric
 // Every output goes to the chunk block in global memory, already in the
 // layout K2 reads.
 constexpr int kPrepThreads = 512;
-constexpr int kPrepWarps = kPrepThreads / 32;
 constexpr int kLDC = 72;   // fp16 pitch of the C x C scratch tiles
 __host__ __device__ constexpr uint32_t align1k(uint32_t x) { return (x + 1023u) & ~1023u; }
 // Staged inputs arrive by TMA with the 128-byte swizzle: a region holds 64 token
@@ -250,8 +259,7 @@ constexpr uint32_t kRegion = 64 * 128;                         // 8 KiB, 1 KiB a
 constexpr uint32_t kOffAcum = 0;                               // fp32 a (g staged here): 4 regions
 constexpr uint32_t kOffRef = align1k(kOffAcum + 4 * kRegion);  // fp32 [4][128] r_i
 constexpr uint32_t kOffQsum = kOffRef + 4 * 128 * 4;           // fp32 [4][128] per-tile sums of g
-constexpr uint32_t kOffAc = kOffQsum + 4 * 128 * 4;            // fp32 [128] a_C
-constexpr uint32_t kOffBeta = kOffAc + 128 * 4;                // fp32 [64]
+constexpr uint32_t kOffBeta = kOffQsum + 4 * 128 * 4;          // fp32 [64]
 constexpr uint32_t kOffMdp = kOffBeta + C * 4;                 // fp32 [4][64] partial q_t . k_t
 constexpr uint32_t kOffAd = kOffMdp + 4 * C * 4;               // fp32 [4][16][16] diagonal blocks of A
 // per-channel exponential tables (fp32 [k][128] each), so that every operand
@@ -260,8 +268,8 @@ constexpr uint32_t kOffAd = kOffMdp + 4 * C * 4;               // fp32 [4][16][1
 //   kE21 = e^{r_2 - r_1}, kE31 = e^{r_3 - r_1}, kE32 = e^{r_3 - r_2}  (r_4 = a_C)
 constexpr uint32_t kOffTab = kOffAd + 4 * 256 * 4;
 constexpr int kTabEr = 0, kTabEd = 4, kTabEc = 8, kTabE21 = 12, kTabE31 = 13, kTabE32 = 14;
-constexpr uint32_t kOffGamS = kOffTab + 16 * 128 * 4;          // fp32 [128] e^{a_C}, until the block is written
-constexpr uint32_t kOffGs = kOffGamS + 128 * 4;                // fp32 [64] one decay per token (scalar mode)
+constexpr uint32_t kOffGamS = kOffTab + 16 * 128 * 4;          // fp32 [2][128] e^{a_C} by item parity, until the block is written
+constexpr uint32_t kOffGs = kOffGamS + 2 * 128 * 4;            // fp32 [64] one decay per token (scalar mode)
 constexpr uint32_t kOffX = align1k(kOffGs + C * 4);            // bf16 K-major [128][128]: row 32 i + 16 w + t % 16
 constexpr uint32_t kOffKh = kOffX + 128 * 128 * 2;             // bf16 K-major [160][128]: 10 column tiles
 constexpr uint32_t kOffKtb = kOffKh + 160 * 128 * 2;           // fp16 MN-major [s][c]: beta k e^{a}
@@ -414,8 +422,8 @@ struct PrepArgs {
     unsigned char *blocks;
     uint32_t *status;
     // fused schedule: chain ranks [gbase, gbase + gcount) of the recurrence
-    // order. ring > 0: each chain has a ring of `ring` blocks and progress[i] =
-    // the chunks chain i has loaded; ring = 0: one block per (chunk slot, head)
+    // order. ring > 0: each chain has a ring of `ring` blocks and progress[32 i]
+    // = the chunks chain i has loaded; ring = 0: one block per (chunk slot, head)
     // and flags [head][slot] (nslots slots).
     int ring, gbase, gcount, nslots;
     // fused schedule: CTAs [0, chain_ctas) run chains (0: a launch of producers
@@ -450,9 +458,10 @@ __device__ __forceinline__ int ld_progress(const int *p) {
 //   fused schedule: chunk-major over the group's chains; each finished block is
 //     published with a release store of its ready flag = c + 1. Blocks either
 //     one per (chunk slot, head), flags [head][slot], or (ring mode, bounded
-//     workspace) in a ring per chain: block and flag (i ring + c % ring) of
-//     chain i, and before a block overwrites its ring entry the producer waits
-//     (bounded) until the chain has loaded chunk c - ring.
+//     workspace) in a ring per chain: block (i ring + c % ring) and flag
+//     (32 i + c % ring) of chain i, and before a block overwrites its ring
+//     entry the producer waits (bounded) until the chain has loaded chunk
+//     c - ring.
 template <bool kRingMode, bool kChannelDecay>
 __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int stride,
                                           int *ready) {
@@ -542,7 +551,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         if (t1 < t0 || it_.tc >= t1) return false;
         it_.c = c;
         if (ring) {
-            it_.blk = it_.flag = (size_t)it_.gi * RG + c % RG;
+            it_.blk = (size_t)it_.gi * RG + c % RG;
+            it_.flag = (size_t)it_.gi * kLineInts + c % RG;
         } else {
             const int slot = cu ? (fused ? first_chunk[n] + c : r.mid) : n * cpn + c;
             it_.blk = (size_t)slot * H + it_.h;
@@ -555,17 +565,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cq = 2 * (lane & 3);
-    const int ch = tid & 127, ti4 = tid >> 7;  // cumulative-sum role: (channel, tile)
 
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t pbars[4];  // Gram products, W / U~ products, staged g, staged q k v
     __shared__ uint32_t ptmem_slot;
     __shared__ int sVexp;  // per item: e_ceil of a bound of max |beta v| (atomicMax)
-    __shared__ __align__(16) int sProg[4];  // ring mode: four chains' progress, read ahead
+    __shared__ __align__(16) int sProg[4];  // ring mode: the next item's chain progress, read ahead
     const uint32_t sbase = smem_u32(smem);
     float *sRef = reinterpret_cast<float *>(smem + kOffRef);
     float *sQsum = reinterpret_cast<float *>(smem + kOffQsum);
-    float *sAcT = reinterpret_cast<float *>(smem + kOffAc);
     float *sBeta = reinterpret_cast<float *>(smem + kOffBeta);
     float *sMdp = reinterpret_cast<float *>(smem + kOffMdp);
     float *sAd = reinterpret_cast<float *>(smem + kOffAd);
@@ -678,15 +686,18 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     // The poll backs off (up to ~0.5 us): the chains that it waits for read their
     // blocks through the same L2, and a producer that waits is ahead anyway.
     auto wait_progress = [&](int i, int need) -> bool {
-        if (ld_progress(pa.progress + i) >= need) return true;
+        const int *pr = pa.progress + (size_t)i * kLineInts;
+        if (ld_progress(pr) >= need) return true;
         const uint64_t t0 = tc::globaltimer_ns();
         unsigned pause = 32;
-        while (true) {
+        for (unsigned n = 1;; ++n) {
             __nanosleep(pause);
             pause = pause < 512 ? 2 * pause : 512;
-            if (ld_progress(pa.progress + i) >= need) return true;
-            if (*reinterpret_cast<volatile uint32_t *>(pa.status) & kStatusTimeout) return false;
-            if (tc::globaltimer_ns() - t0 > kPrepWaitLimit) return false;
+            if (ld_progress(pr) >= need) return true;
+            if (n % 8 == 0) {  // (the status word is shared by every CTA: read it seldom)
+                if (*reinterpret_cast<volatile uint32_t *>(pa.status) & kStatusTimeout) return false;
+                if (tc::globaltimer_ns() - t0 > kPrepWaitLimit) return false;
+            }
         }
     };
 
@@ -705,8 +716,69 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     const uint64_t dKtb = tc::smem_desc(sbase + kOffKtb, 2048, 128);
     const uint64_t dVb = tc::smem_desc(sbase + kOffVb, 2048, 128);
 
+    // Cumulative decay of an item whose g is staged in the a buffer, in place:
+    // thread u handles channel u % 128 and TPT consecutive 16-token tiles from
+    // tile (u / 128) TPT; TPT = 1: all 512 threads (CTA barrier), TPT = 2: the
+    // 256 threads of warps 4..11 during the previous item's T phase (named
+    // barrier 2). Writes a, r_i, the exponential tables and e^{a_C} (buffer gsel).
+    auto cum_decay = [&](auto tpt_c, int u, int L_, int h_, int gsel) {
+        constexpr int TPT = decltype(tpt_c)::value;
+        const int chu = u & 127, tb = (u >> 7) * TPT;
+        float a[TPT][16];
+#pragma unroll
+        for (int q = 0; q < TPT; ++q) {
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {  // rows past the chunk: g = 0
+                const int t = 16 * (tb + q) + r;
+                const float gv = gpc ? *reinterpret_cast<const float *>(smem + kOffAcum + a_off(t, chu))
+                                 : pa.gs_tma ? reinterpret_cast<const float *>(smem + kOffAcum)[4 * t + (h_ & 3)]
+                                             : reinterpret_cast<const float *>(smem + kOffGs)[t];
+                a[q][r] = t < L_ ? clamp_g(gv) : 0.f;
+            }
+#pragma unroll
+            for (int r = 1; r < 16; ++r) a[q][r] += a[q][r - 1];
+            sQsum[(tb + q) * 128 + chu] = a[q][15];
+        }
+        if (TPT == 1)
+            __syncthreads();
+        else
+            asm volatile("barrier.sync 2, 256;\n" ::: "memory");
+        float rr[5];  // r_0 .. r_3, and r_4 = a_C
+        rr[0] = 0.f;
+#pragma unroll
+        for (int i2 = 0; i2 < 4; ++i2) rr[i2 + 1] = rr[i2] + sQsum[i2 * 128 + chu];
+        float *tab = reinterpret_cast<float *>(smem + kOffTab);
+#pragma unroll
+        for (int q = 0; q < TPT; ++q) {
+            const int ti = tb + q;
+            float off = rr[0];
+#pragma unroll
+            for (int i2 = 1; i2 < 4; ++i2) off = ti == i2 ? rr[i2] : off;
+            sRef[ti * 128 + chu] = off;  // cumulative decay just before tile ti
+#pragma unroll
+            for (int r = 0; r < 16; ++r)
+                *reinterpret_cast<float *>(smem + kOffAcum + a_off(16 * ti + r, chu)) = a[q][r] + off;
+            if (!gpc && chu == 0) {  // one decay per token: a_t kept for the Gram read-back
+#pragma unroll
+                for (int r = 0; r < 16; ++r)
+                    reinterpret_cast<float *>(smem + kOffGs)[16 * ti + r] = a[q][r] + off;
+            }
+            const float rnext = ti == 3 ? rr[4] : (ti == 2 ? rr[3] : (ti == 1 ? rr[2] : rr[1]));
+            tab[(kTabEr + ti) * 128 + chu] = __expf(off);
+            tab[(kTabEd + ti) * 128 + chu] = __expf(rnext - off);   // >= e^-80
+            tab[(kTabEc + ti) * 128 + chu] = __expf(rr[4] - rnext); // <= 1
+            if (ti == 0) {
+                tab[kTabE21 * 128 + chu] = __expf(rr[2] - rr[1]);
+                tab[kTabE31 * 128 + chu] = __expf(rr[3] - rr[1]);
+                tab[kTabE32 * 128 + chu] = __expf(rr[3] - rr[2]);
+            }
+            if (ti == 3) reinterpret_cast<float *>(smem + kOffGamS)[gsel * 128 + chu] = __expf(rr[4]);
+        }
+    };
+    int decayed = -1;  // the item whose cumulative decay is already in place
+
     bool failed = false;
-    int next_slot = -2;  // ring mode: sProg[next_slot] holds the next item's chain progress
+    int next_slot = -2;  // ring mode: sProg[next_slot] (0) holds the next item's chain progress
                          // (-1: not needed, -2: not read)
     uint32_t it = 0;  // items done by this CTA (mbarrier phase)
     Cur cur = split(first);
@@ -745,52 +817,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
                          : 0.f;
     }
 
-    // ---- cumulative decay: thread = (channel, 16-token tile), in place over g --------
-    {
-        float a[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) {  // rows past the chunk: g = 0
-            const int t = 16 * ti4 + r;
-            const float gv = gpc ? *reinterpret_cast<const float *>(smem + kOffAcum + a_off(t, ch))
-                             : pa.gs_tma ? reinterpret_cast<const float *>(smem + kOffAcum)[4 * t + (h & 3)]
-                                         : reinterpret_cast<const float *>(smem + kOffGs)[t];
-            a[r] = t < L ? clamp_g(gv) : 0.f;
-        }
-#pragma unroll
-        for (int r = 1; r < 16; ++r) a[r] += a[r - 1];
-        sQsum[ti4 * 128 + ch] = a[15];
-        __syncthreads();
-        float rr[5];  // r_0 .. r_3, and r_4 = a_C
-        rr[0] = 0.f;
-#pragma unroll
-        for (int i2 = 0; i2 < 4; ++i2) rr[i2 + 1] = rr[i2] + sQsum[i2 * 128 + ch];
-        float off = rr[0];
-#pragma unroll
-        for (int i2 = 1; i2 < 4; ++i2) off = ti4 == i2 ? rr[i2] : off;
-        sRef[ti4 * 128 + ch] = off;  // cumulative decay just before tile ti4
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            *reinterpret_cast<float *>(smem + kOffAcum + a_off(16 * ti4 + r, ch)) = a[r] + off;
-        if (!gpc && ch == 0) {  // one decay per token: a_t kept for the Gram read-back
-#pragma unroll
-            for (int r = 0; r < 16; ++r)
-                reinterpret_cast<float *>(smem + kOffGs)[16 * ti4 + r] = a[r] + off;
-        }
-        float *tab = reinterpret_cast<float *>(smem + kOffTab);
-        const float rnext = ti4 == 3 ? rr[4] : (ti4 == 2 ? rr[3] : (ti4 == 1 ? rr[2] : rr[1]));
-        tab[(kTabEr + ti4) * 128 + ch] = __expf(off);
-        tab[(kTabEd + ti4) * 128 + ch] = __expf(rnext - off);   // >= e^-80
-        tab[(kTabEc + ti4) * 128 + ch] = __expf(rr[4] - rnext); // <= 1
-        if (ti4 == 0) {
-            tab[kTabE21 * 128 + ch] = __expf(rr[2] - rr[1]);
-            tab[kTabE31 * 128 + ch] = __expf(rr[3] - rr[1]);
-            tab[kTabE32 * 128 + ch] = __expf(rr[3] - rr[2]);
-        }
-        if (ti4 == 3) {
-            sAcT[ch] = rr[4];
-            reinterpret_cast<float *>(smem + kOffGamS)[ch] = __expf(rr[4]);
-        }
-    }
+    // ---- cumulative decay (unless the previous item's T phase did it) ---------------
+    if (decayed != item) cum_decay(std::integral_constant<int, 1>(), tid, L, h, (int)(it & 1u));
     // this item's q, k, v: out of the staging area before it is overwritten
     uint4 uq[2], uk[2], uv[2];
 #pragma unroll
@@ -1075,19 +1103,15 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     }
 
     // ---- T = (I + A)^{-1}: 16x16 diagonal blocks in fp32, the rest on tensor cores --
-    // Without rings: warps 0..14 only (named barrier 1), so that the last warp
-    // publishes the previous block meanwhile (its release store waits ~1,500
-    // cycles for the ordering of prior writes) and rejoins at the full barrier
-    // before the W / U~ products. (barrier.sync, the form that lets a warp's lanes
-    // arrive apart.) In ring mode all warps take part: measured faster there.
-    constexpr bool kTOff15 = !kRingMode;
+    // Warps 0..3 only (named barrier 1). Meanwhile warps 4..11 form the next
+    // item's cumulative decay (its g was staged after this item's operand phase),
+    // and the last warp publishes the previous block (its release store waits
+    // ~1,500 cycles for the ordering of prior writes); all rejoin at the full
+    // barrier before the W / U~ products. (barrier.sync, the form that lets a
+    // warp's lanes arrive apart.)
+    const bool early = has_next && (gpc || pa.gs_tma);  // (the next g is in shared memory)
     auto tsync = [&]() {
-        if (kTOff15) {
-            if (warp < kPrepWarps - 1)
-                asm volatile("barrier.sync 1, %0;\n" ::"n"(kPrepThreads - 32) : "memory");
-        } else {
-            __syncthreads();
-        }
+        if (warp < 4) asm volatile("barrier.sync 1, 128;\n" ::: "memory");
     };
     const uint32_t aT = sbase + kOffT, aAh = sbase + kOffAh;
     if (tid < 64) {
@@ -1113,16 +1137,21 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         }
 #pragma unroll
         for (int r = 0; r < 16; ++r) store_h(smem + kOffT, off_k64(16 * b + r, 16 * b + cc), x[r]);
-    } else if (!kTOff15 || warp < kPrepWarps - 1) {
+    } else if (warp < 4) {
         // blocks above the diagonal of T: zero
-        for (int idx = tid - 64; idx < 6 * 128; idx += kPrepThreads - (kTOff15 ? 96 : 64)) {
+        for (int idx = tid - 64; idx < 6 * 128; idx += 64) {
             const int b_ = idx >> 7, e = idx & 127;
             const int bi = b_ < 3 ? 0 : (b_ < 5 ? 1 : 2);
             const int bj = b_ < 3 ? b_ + 1 : (b_ < 5 ? b_ - 1 : 3);
             const int t = 16 * bi + (e >> 3), s2 = 16 * bj + 2 * (e & 7);
             *reinterpret_cast<uint32_t *>(smem + kOffT + off_k64(t, s2)) = 0u;
         }
+    } else if (early && warp < 12) {
+        // (every thread of the group reaches the group's barrier, failed or not)
+        if (!failed && !tc::mbar_wait(bInG, (it + 1u) & 1u, kPrepWaitLimit)) failed = true;
+        cum_decay(std::integral_constant<int, 2>(), tid - 128, nL, nh, (int)((it + 1u) & 1u));
     }
+    decayed = early ? nitem : -1;
     tsync();
     {
         // Below the diagonal blocks, in two rounds (16x16 tiles, fp16 tensor cores):
@@ -1233,7 +1262,8 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
         *reinterpret_cast<uint4 *>(su + ut_off(jj, t0 >> 3)) = pack8_f16_u(&ru[0][0]);
         *reinterpret_cast<uint4 *>(su + ut_off(jj, (t0 >> 3) + 1)) = pack8_f16_u(&ru[0][8]);
         if (tid < 128)
-            reinterpret_cast<float *>(su + kGam)[tid] = reinterpret_cast<const float *>(smem + kOffGamS)[tid];
+            reinterpret_cast<float *>(su + kGam)[tid] =
+                reinterpret_cast<const float *>(smem + kOffGamS)[(it & 1u) * 128 + tid];
         if (tid == 0) {  // the block's scale; a fresh maximum for the next item
             *reinterpret_cast<int *>(su + kNu) = nu;
             sVexp = -127;
@@ -1254,9 +1284,9 @@ __device__ __forceinline__ void prep_loop(const PrepArgs &pa, int first, int str
     if (ring && has_next && nx.c >= RG && tid == kStager) {  // 16 bytes through L2
         asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n"
                      "cp.async.commit_group;\n" ::"r"(smem_u32(sProg)),
-                     "l"(pa.progress + (nx.gi & ~3))
+                     "l"(pa.progress + (size_t)nx.gi * kLineInts)
                      : "memory");
-        next_slot = nx.gi & 3;
+        next_slot = 0;
     }
     if (ready) {
         if (it == 0) {  // the chains wait for the first blocks: publish this one at once
@@ -1342,10 +1372,10 @@ struct RecArgs {
     float *fin;
     float *snaps;  // [N][snap_max][H][128][128], or null
     int snap_interval, snap_max;
-    int ring;        // ring > 0: blocks (gi ring + c % ring), flags ready[gi ring + c % ring] = c + 1;
+    int ring;        // ring > 0: blocks (gi ring + c % ring), flags ready[32 gi + c % ring] = c + 1;
                      // ring = 0: blocks (slot H + h), flags ready[h nslots + slot] = c + 1
     int nslots;
-    int *progress;   // ring > 0: progress[gi] = chunks of this chain loaded
+    int *progress;   // ring > 0: progress[32 gi] = chunks of this chain loaded
     uint32_t *status;
     unsigned long long wait_ns;  // bound on every wait of a chain (ns)
 };
@@ -1364,8 +1394,8 @@ __device__ __forceinline__ uint4 flags4_acquire(const int *f) {
 // K2 for one chain (sequence n, head h). Split schedule (`ready` null): the
 // blocks of all chunks are in place. Fused: chunk c's block is loaded once its
 // ready flag = c + 1; in ring mode this chain is number gi of its group, chunk
-// c's block and flag are ring entry (gi ring + c % ring), and progress[gi]
-// tells the producers which entries may be overwritten.
+// c's block is ring entry (gi ring + c % ring), its flag ready[32 gi + c % ring],
+// and progress[32 gi] tells the producers which entries may be overwritten.
 template <bool kRingMode>
 __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi, const int *ready) {
     const int32_t *__restrict__ cu = ra.cu;
@@ -1449,7 +1479,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
         int y0;
         if (RG > 0) {
             const int sx = x % RG;
-            base = (size_t)gi * RG + (sx & ~3);
+            base = (size_t)gi * kLineInts + (sx & ~3);
             y0 = x - (sx & 3);
         } else {
             const size_t a = (size_t)h * ra.nslots + fc + x;
@@ -1597,7 +1627,7 @@ __device__ __forceinline__ void recur_chain(const RecArgs &ra, int chain, int gi
             // the ring entry of chunk c may be reused: its load has completed (the
             // wait above saw it), so a plain store that follows it is enough
             if (ready && RG > 0 && tid == kLoader && !failed)
-                asm volatile("st.relaxed.gpu.global.u32 [%0], %1;\n" ::"l"(ra.progress + gi),
+                asm volatile("st.relaxed.gpu.global.u32 [%0], %1;\n" ::"l"(ra.progress + (size_t)gi * kLineInts),
                              "r"(c + 1)
                              : "memory");
             // this chunk's values may need a larger scale (rare: v grew)
@@ -1810,7 +1840,8 @@ inline const void *fused_fn(bool ring, bool channel_decay) {
 // then by schedule (each region 256-byte padded):
 //   split:        one block per (chunk slot, head);
 //   fused:        ready flags [H][slots] | one block per (chunk slot, head);
-//   fused, ring:  ready flags [G][R] and progress [G] | rings, G R blocks
+//   fused, ring:  ready flags [G][32] (R used) and progress [G][32] (1 used):
+//                 a 128-byte line each | rings, G R blocks
 //                 (G = the most chains of one group, R = the ring length):
 //                 bounded by the group, not by the sequence length.
 // kda_prefill runs the fastest plan that its workspace holds.
@@ -1930,7 +1961,7 @@ bool ring_plan(const PlanSizes &z, long long G, PrefillPlan &p) {
     p.ring = kRing;
     p.lead_items = 0;
     p.groups = (int)((z.nchains + G - 1) / G);
-    p.bytes = z.base + pad256((size_t)G * (p.ring + 1) * 4) + (size_t)G * p.ring * pf::kBlock;
+    p.bytes = z.base + (size_t)G * 2 * pf::kLineInts * 4 + (size_t)G * p.ring * pf::kBlock;
     return true;
 }
 }  // namespace
@@ -2147,8 +2178,8 @@ cudaError_t launch_prefill_tc(const void *q, const void *k, const void *v, const
     if (fused) {
         ready = reinterpret_cast<int *>(ws + off);
         if (plan.ring > 0) {
-            progress = ready + (size_t)plan.group_chains * plan.ring;
-            flag_bytes = pad256((size_t)plan.group_chains * (plan.ring + 1) * 4);
+            progress = ready + (size_t)plan.group_chains * pf::kLineInts;
+            flag_bytes = (size_t)plan.group_chains * 2 * pf::kLineInts * 4;
         } else {
             flag_bytes = pad256((size_t)nitems * 4);
         }

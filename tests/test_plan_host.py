@@ -124,7 +124,8 @@ def test_ring_plan_does_not_grow_with_the_length(plan):
         rc, p = plan(1, T, 32, kind=2)
         assert rc == kda.KDA_OK and p.ring == 16 and p.group_chains == 32 and p.groups == 1
         sizes.add(p.bytes)
-    assert sizes == {256 + pad256(32 * 17 * 4) + 32 * 16 * BLOCK}
+    # per chain: its ring flags and its progress counter, a 128-byte line each
+    assert sizes == {256 + 32 * 2 * 128 + 32 * 16 * BLOCK}
 
 
 def test_group_model_many_chains(plan):
@@ -140,7 +141,7 @@ def test_smallest_plan_is_one_chain_per_group(plan):
     rc, p = plan(2, 8192, 8, kind=3)
     assert rc == kda.KDA_OK
     assert p.group_chains == 1 and p.groups == 16 and p.ring == 16
-    assert p.bytes == 256 + 256 + 16 * BLOCK
+    assert p.bytes == 256 + 2 * 128 + 16 * BLOCK
 
 
 def test_budget_selects_the_plan(plan):
