@@ -21,7 +21,9 @@ namespace kda {
 constexpr int kLayerRowsPerCta = 8;  // one warp per row
 constexpr float kL2Eps = 1e-6f, kRmsEps = 1e-6f;
 
-__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + __expf(-x)); }
+// (the fast reciprocal division: a denominator above 2^126, x below about -87,
+// gives 0, which is the value to fp32 precision)
+__device__ __forceinline__ float sigmoidf_(float x) { return __fdividef(1.f, 1.f + __expf(-x)); }
 
 template <typename IO>
 __device__ __forceinline__ void load4(const IO *p, float *x);
