@@ -583,7 +583,9 @@ def test_append_prefill_full_size():
 @pytest.mark.slow
 def test_varlen_full_size():
     """64 sequences, lengths ~U[1024, 32768], H=32, g near the floor, random
-    initial states; 6 chains sampled (incl. the longest and shortest)."""
+    initial states; 6 chains sampled, incl. the longest sequence (first wave
+    of the longest-first recurrence order) and the shortest (its last wave:
+    2,048 chains on 152 SMs)."""
     w = inputs.WORKLOADS["varlen64_h32_floor"]
     lens = inputs.varlen_lengths(w["n_seqs"], w["lo"], w["hi"], seed=w["seed"])
     x = inputs.prefill_inputs(lens, H=w["H"], io="bf16", seed=w["seed"], g_mode="floor",

@@ -136,16 +136,20 @@ def test_lead_plan_agrees_with_split_and_oracle(case):
     args = (x.q.to(DEV), x.k.to(DEV), x.v.to(DEV), g.to(DEV), x.beta.to(DEV), x.scale)
     cu = x.cu_seqlens.to(DEV) if packed else None
     res = {}
+    S = L // 256  # snapshots every 256 tokens: 8, 2 and 3 of them
     for mode in (None, "split"):
         with prefill_schedule(mode):
             ws = kda.prefill_workspace(args[0], cu, N=N, T=L, chunk=64)
+            snaps = torch.full((N, S, H, 128, 128), 7.0, dtype=torch.float32, device=DEV)
             out, fin = kda.kda_prefill(*args, init_state=x.init_state.to(DEV), cu_seqlens=cu,
-                                       chunk=64, workspace=ws, N=N, T=L)
+                                       chunk=64, workspace=ws, N=N, T=L, snapshot_interval=256,
+                                       snapshots=snaps)
             assert kda.kda_workspace_status(ws) == kda.KDA_OK
             torch.cuda.synchronize()
-            res[mode] = (out, fin)
-    assert torch.equal(res[None][0], res["split"][0])
-    assert torch.equal(res[None][1], res["split"][1])
+            res[mode] = (out, fin, snaps)
+    for a_, b_ in zip(res[None], res["split"]):  # outputs, final states, snapshots
+        assert torch.equal(a_, b_)
+    assert not torch.equal(res[None][2], torch.full_like(res[None][2], 7.0))
     if per_head:
         x.g = x.g[..., :1].expand_as(x.g).contiguous()
     ro, rf = oracle_prefill(x)
