@@ -159,6 +159,10 @@ int kda_prefill_plan(int32_t N, int32_t T, int32_t H, int32_t D, int32_t chunk, 
  * they do for the L2-normalised keys and queries of a KDA layer. If an fp16
  * value overflows anyway, the final state comes out non-finite and
  * kda_workspace_status() reports KDA_ERR_RANGE (never silently).
+ * Accuracy (bf16 I/O): outputs and final states within 2e-2 of an fp64
+ * recurrence (largest error / RMS) on the workloads tested; inputs whose
+ * chunks repeat one key with beta = 1 and almost no decay reach 2.5-4e-2 (the
+ * shared fp16 rounding of the UT inverse's subdiagonal, on rank-one results).
  * Returns KDA_OK after enqueueing the work on `stream`.
  */
 int kda_prefill(const void *q, const void *k, const void *v, const float *g, const void *beta,

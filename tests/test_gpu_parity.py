@@ -599,6 +599,49 @@ def test_varlen_full_size():
     sampled_chain_check(x, out, fin, lens, chains, x.init_state.cpu(), TOL_BF16)
 
 
+# ------------------------------------------------------ degenerate chunk matrices
+# Bound for identical keys with beta = 1 and (nearly) no decay, outside the
+# 2e-2 of the other tests: a documented precision limit of the fp16 state path.
+# Each chunk's A is then the strictly lower all-ones matrix (times |k|^2 =
+# 1 - delta), T's subdiagonal is -(1 + delta), and fp16 rounds every one of
+# those entries the same way; the state and outputs are rank-one and peaked,
+# so the coherent ~1e-3 relative rounding reaches 2.5-4e-2 of their RMS (max
+# over entries). A CPU emulation of the same roundings gives 2-3.5e-2.
+TOL_IDENTICAL_KEYS = 5e-2
+
+
+def _identical_keys_case(lens, H, beta, gval, seed=61):
+    x = inputs.prefill_inputs(lens, H=H, io="bf16", seed=seed, init="normal")
+    gen = torch.Generator().manual_seed(seed + 1)
+    key = torch.randn(H, 128, generator=gen)
+    key = key / key.norm(dim=-1, keepdim=True)
+    x.k = key.to(torch.bfloat16).unsqueeze(0).expand_as(x.k).contiguous()
+    x.beta = torch.full_like(x.beta, beta)
+    x.g = torch.full_like(x.g, gval)
+    return x
+
+
+@pytest.mark.parametrize("mode", [None, "split"])
+@pytest.mark.parametrize("beta,gval,tol", [(0.5, 0.0, TOL_BF16), (1.0, -1.0, TOL_BF16),
+                                           (1.0, 0.0, TOL_IDENTICAL_KEYS),
+                                           (1.0, -0.05, TOL_IDENTICAL_KEYS)])
+def test_identical_keys(mode, beta, gval, tol):
+    """Every token of a head has the same unit key: each chunk's A is a
+    constant times the strictly lower all-ones matrix. T = (I + A)^-1 stays
+    tame (for beta = 1, g = 0 the identity minus the subdiagonal, entries -1,
+    0, 1) while the powers of A that a product form of the inverse would
+    multiply grow like binomial coefficients (A^8 ~5e8 at C = 64, ~3e3 in a
+    16 x 16 tile): the forward substitution in fp32 handles it. With beta = 1
+    and no decay the fp16 state path is at its documented limit (see the
+    bound above); with beta = 1/2 or a decay the usual bf16 tolerance holds."""
+    x = _identical_keys_case([200, 77], 2, beta, gval)
+    with prefill_schedule(mode):
+        out, fin = run_gpu_prefill(x, 64)
+    ro, rf = oracle_prefill(x)
+    eo, ef = out_err(out, ro), rel_err(fin.cpu().numpy(), rf)
+    assert eo <= tol and ef <= tol, (eo, ef)
+
+
 # ---------------------------------------------------------------- schedules
 @pytest.mark.parametrize("lens,H", [([1000], 3), ([5, 0, 129, 1], 2), ([64] * 40, 2)])
 def test_bf16_split_and_fused_schedules_agree(lens, H):
