@@ -1857,12 +1857,14 @@ constexpr int kRing = pf::kRingLen;  // blocks per chain in flight in ring mode 
 // Chains per fused launch when they are many (groups run one after the other):
 // the G that minimises the modelled time of all groups, a group of x chains of L
 // chunks taking max(L t_chain, x L t_block / (SMs - x)) with the measured paces
-// t_chain ~ 1.6 us per chunk of a chain and t_block ~ 6.8 us per block of a
+// t_chain ~ 1.83 us per chunk of a chain and t_block ~ 6.3 us per block of a
 // producer SM; L is the chunks per sequence (the mean for packed sequences).
 int group_chains(long long nchains, long long chunks_per_chain, int nsm) {
     if (nchains <= 0) return 1;
     if (3 * nchains <= nsm) return (int)nchains;  // one group
-    const double tc = 1.6, tp = 6.8, L = (double)(chunks_per_chain > 0 ? chunks_per_chain : 1);
+    // (with 256 chains of 128 chunks: groups of 37 chains, 2.09 ms; the 29 that
+    // paces of 1.6 / 6.8 gave, 2.29 ms)
+    const double tc = 1.83, tp = 6.3, L = (double)(chunks_per_chain > 0 ? chunks_per_chain : 1);
     auto f = [&](long long x) { return std::max(L * tc, x * L * tp / (double)(nsm - x)); };
     long long best = 1;
     double best_t = 1e300;

@@ -130,10 +130,10 @@ def test_ring_plan_does_not_grow_with_the_length(plan):
 
 def test_group_model_many_chains(plan):
     """2,048 chains of equal length: groups of the modelled best size, about
-    SMs x 1.6 / (1.6 + 6.8) ~ 29 chains, every chain in exactly one group."""
+    SMs x 1.83 / (1.83 + 6.3) ~ 34 chains, every chain in exactly one group."""
     rc, p = plan(64, 16384, 32, kind=2)
     assert rc == kda.KDA_OK
-    assert 25 <= p.group_chains <= 33
+    assert 30 <= p.group_chains <= 38
     assert (p.groups - 1) * p.group_chains < 64 * 32 <= p.groups * p.group_chains
 
 
