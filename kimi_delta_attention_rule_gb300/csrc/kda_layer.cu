@@ -70,6 +70,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 // tokens, so a CTA reads whole [H, D] rows. The window is cleared where a
 // sequence starts.
 constexpr int kProTokens = 32;
+static_assert(kProTokens == 32, "beta takes one token of a run per lane");
 template <typename IO>
 struct ProRing {
     static constexpr int depth = sizeof(IO) == 2 ? 4 : 2;  // 32 KiB per 8-warp CTA either way
@@ -182,7 +183,11 @@ __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
         if (t0 + sl < t1) issue(t0 + sl, sl);
         cp_async_commit();
     }
-    IO nb = lane == 0 ? beta_raw[(size_t)t0 * H + h] : IO();  // beta one token ahead
+    // beta needs no window: lane l takes token t0 + l of the run
+    if (t0 + lane < t1) {
+        const size_t br = (size_t)(t0 + lane) * H + h;
+        beta[br] = from_f32<IO>(sigmoidf_(to_f32(beta_raw[br])));
+    }
     IO *out3[3] = {q, k, v};
     int slot = 0;
 #pragma unroll 1
@@ -191,8 +196,6 @@ __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
         Raw4<IO> cx[3], ca = wr[slot][3][lane];
 #pragma unroll
         for (int m = 0; m < 3; ++m) cx[m] = wr[slot][m][lane];
-        const IO cb = nb;
-        if (lane == 0 && t + 1 < t1) nb = beta_raw[(size_t)(t + 1) * H + h];
         if (cu && t >= next_start) {  // a sequence starts here (empty ones are skipped)
             while (n < N - 1 && cu[n + 1] <= t) ++n;
             next_start = cu[n + 1];
@@ -234,7 +237,6 @@ __global__ void __launch_bounds__(32 * kLayerRowsPerCta)
         *reinterpret_cast<float4 *>(g + o) =
             make_float4(-5.f * sigmoidf_(al[0]), -5.f * sigmoidf_(al[1]), -5.f * sigmoidf_(al[2]),
                         -5.f * sigmoidf_(al[3]));
-        if (lane == 0) beta[(size_t)t * H + h] = from_f32<IO>(sigmoidf_(to_f32(cb)));
         // the slot was read above (its values are in use): token t + RD goes into it
         if (t + RD < t1) issue(t + RD, slot);
         cp_async_commit();
