@@ -423,6 +423,36 @@ def test_multi_token_decode(io, tol, T):
     assert rel_err(st.cpu().numpy(), rf) <= tol
 
 
+@pytest.mark.parametrize("io,tol", [("bf16", TOL_BF16), ("f32", TOL_F32)])
+@pytest.mark.parametrize("T", [1, 3, 4, 7])
+def test_multi_token_decode_identical_keys(io, tol, T):
+    """Every token of a call repeats its head's unit key with beta = 1 and no
+    decay (each delta step then overwrites the key's direction): the
+    token-by-token, chunked (T <= 4) and pipelined (T <= 8) decode kernels
+    hold the usual tolerance (their state path is fp32)."""
+    B, H = 5, 3
+    x = inputs.prefill_inputs([T] * B, H=H, io=io, seed=71)
+    shp = (B, T, H, 128)
+    dt = x.k.dtype
+    gen = torch.Generator().manual_seed(72)
+    key = torch.randn(H, 128, generator=gen)
+    key = (key / key.norm(dim=-1, keepdim=True)).to(dt)
+    q, v = x.q.view(shp), x.v.view(shp)
+    k = key.view(1, 1, H, 128).expand(shp).contiguous()
+    g = torch.zeros(shp, dtype=torch.float32)
+    beta = torch.ones((B, T, H), dtype=dt)
+    pool = 0.02 * torch.randn(B, H, 128, 128, generator=gen)
+    cu = np.arange(0, B * T + 1, T, dtype=np.int32)
+    flat = lambda t: np32(t.reshape(B * T, *t.shape[2:]))
+    ro, rf = oracle.prefill(flat(q), flat(k), flat(v), flat(g), flat(beta), x.scale,
+                            init_state=pool.double().numpy(), cu_seqlens=cu)
+    st = pool.to(DEV)
+    out = kda.kda_decode(q.to(DEV), k.to(DEV), v.to(DEV), g.to(DEV), beta.to(DEV), x.scale, st)
+    torch.cuda.synchronize()
+    assert out_err(out, ro.reshape(B, T, H, 128)) <= tol
+    assert rel_err(st.cpu().numpy(), rf) <= tol
+
+
 @pytest.mark.parametrize("io,tol,T", [("bf16", TOL_BF16, 2), ("bf16", TOL_BF16, 4),
                                       ("bf16", TOL_BF16, 8), ("f32", TOL_F32, 3),
                                       ("f32", TOL_F32, 4)])
